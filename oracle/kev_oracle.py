@@ -1,0 +1,326 @@
+"""CPU float64 oracle for packed, question-isolated attention.
+
+TEST INFRASTRUCTURE ONLY.  Nothing on the product path may import, call or
+link this module: only ``tests/``, ``__graft_entry__.smoke()`` and the CPU
+baseline legs of ``bench.py`` use it.  It shares no code with the CUDA
+library (no kernels, headers, helpers, tables or constants); its only
+common dependency with the GPU side is the seeded input module
+``workloads`` (which draws numbers and holds none of the arithmetic).
+
+What it computes is the plain definition, written out with an explicit
+dense T x T mask, in float64:
+
+* Attention (inference-engine notes, sakurs2.com, §2.1, the Z = softmax(QK^T /
+  sqrt(d_h) + M) V equation and its causal mask M_ij = 0 for j <= i, -inf
+  otherwise); the softmax is taken in its stable form, subtracting the row
+  maximum (same page, §2.4, the p_i = e^{s_i - m} / sum_j e^{s_j - m} equation).
+* Isolation (Kev architecture article, icman.com.cn, §2.1 end and §2.3: each
+  question owns one contiguous interval, the isolation mask is block
+  diagonal and is combined with the causal mask by a logical AND; Kev
+  pipeline article, gsyq.cn, §2.2: attention stays inside the question's
+  visible domain, causal within it, and crosses no boundary).
+* KV slot pool (Kev pipeline article, §2.2: a preallocated pool cut into
+  fixed-size slots, one slot per question).
+* Decode with a cache (inference-engine notes, §2.2: only K/V are cached, the
+  new K/V row is appended and the new query attends to every cached
+  position plus itself, with no mask; the result equals the last row of a
+  full recompute).
+* Early stop (Kev pipeline article, §1.2 and §2.3: a question that has
+  finished takes no further part in attention).
+
+Readings taken where the pages are silent or garbled (each listed in the
+design notes): intervals are half-open [s, e); scale = 1/sqrt(d_h) unless
+given; a q-head h uses kv-head h // (H_q / H_kv); tokens in no interval are
+keys for nobody and their own output row is 0; an empty interval is allowed;
+a decode step attends over lens + 1 positions, the new K/V written first.
+
+Pinned by ``tests/test_oracle.py`` against the pages' worked example, closed
+forms, invariants (a)-(d), a library routine and a pure-Python brute force.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+from workloads import to_float64
+
+# Error kinds, in the order they are checked.
+INTERVALS = "intervals"
+SLOT = "slot"
+SLOT_OVERFLOW = "slot_overflow"
+
+
+# ---------------------------------------------------------------------------
+# mask
+# ---------------------------------------------------------------------------
+
+def segment_ids(intervals, total_tokens: int) -> np.ndarray:
+    """seg[t] = i if t lies in question i's interval [s_i, e_i), else -1."""
+    seg = np.full(int(total_tokens), -1, dtype=np.int64)
+    for i, (s, e) in enumerate(np.asarray(intervals, dtype=np.int64).reshape(-1, 2)):
+        seg[s:e] = i
+    return seg
+
+
+def allowed_mask(intervals, total_tokens: int) -> np.ndarray:
+    """Boolean T x T mask: row t may attend to column u.
+
+    The causal lower triangle (u <= t) AND the block-diagonal isolation
+    mask (same question); a token in no question is allowed nothing.
+    """
+    T = int(total_tokens)
+    causal = np.tril(np.ones((T, T), dtype=bool))
+    iso = np.zeros((T, T), dtype=bool)
+    for s, e in np.asarray(intervals, dtype=np.int64).reshape(-1, 2):
+        iso[s:e, s:e] = True
+    return causal & iso
+
+
+def additive_mask(allowed: np.ndarray) -> np.ndarray:
+    """The additive form of the same mask: 0 where allowed, -inf where blocked."""
+    m = np.full(allowed.shape, -np.inf, dtype=np.float64)
+    m[allowed] = 0.0
+    return m
+
+
+def _check_forms_agree(allowed: np.ndarray, add: np.ndarray) -> None:
+    # A 0/1 mask handed to code that expects an additive mask fails silently
+    # (Kev architecture article, §2.3 end); both forms must say the same.
+    if not np.array_equal(np.isfinite(add), allowed):
+        raise AssertionError("boolean and additive masks disagree")
+
+
+# ---------------------------------------------------------------------------
+# softmax
+# ---------------------------------------------------------------------------
+
+def softmax_rows(scores: np.ndarray) -> np.ndarray:
+    """Row softmax in the stable form exp(s - max) / sum exp(s - max).
+
+    A row whose entries are all -inf (a token that may attend to nothing)
+    gets all-zero weights.
+    """
+    m = np.max(scores, axis=-1, keepdims=True)
+    empty = ~np.isfinite(m)
+    m = np.where(empty, 0.0, m)
+    w = np.exp(scores - m)
+    z = np.sum(w, axis=-1, keepdims=True)
+    z = np.where(empty, 1.0, z)
+    return w / z
+
+
+def online_softmax_row(q_row, k, v, scale: float, block: int):
+    """One query row processed block by block with a running max m, sum l and
+    weighted sum u, each block rescaling the old state by alpha = exp(m_old - m_new)
+    (inference-engine notes, §2.4, online softmax).
+
+    Returns (output, list of alpha values, one per block).  Equal to the
+    plain softmax up to rounding; kept here to pin the kernel's algorithm
+    against the page's worked example.
+    """
+    q_row = np.asarray(q_row, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    m = -np.inf
+    ell = 0.0
+    u = np.zeros(v.shape[-1], dtype=np.float64)
+    alphas = []
+    for start in range(0, k.shape[0], block):
+        s = (k[start:start + block] @ q_row) * scale
+        m_new = max(m, float(np.max(s)))
+        alpha = np.exp(m - m_new)
+        w = np.exp(s - m_new)
+        ell = alpha * ell + float(np.sum(w))
+        u = alpha * u + w @ v[start:start + block]
+        m = m_new
+        alphas.append(float(alpha))
+    return u / ell, alphas
+
+
+# ---------------------------------------------------------------------------
+# prefill
+# ---------------------------------------------------------------------------
+
+def _scale(scale, d):
+    return 1.0 / np.sqrt(d) if (scale is None or scale == 0) else float(scale)
+
+
+def _group(h_q: int, h_kv: int) -> int:
+    if h_kv <= 0 or h_q % h_kv:
+        raise ValueError("H_q must be a multiple of H_kv")
+    return h_q // h_kv
+
+
+def prefill(q, k, v, intervals, scale=None, return_probs: bool = False):
+    """Packed prefill attention, float64.
+
+    q [T, H_q, d], k/v [T, H_kv, d] (float64 values); intervals int [N, 2].
+    Returns out [T, H_q, d]; with ``return_probs`` also the weights
+    P [H_q, T, T].
+    """
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    T, h_q, d = q.shape
+    h_kv = k.shape[1]
+    G = _group(h_q, h_kv)
+    sc = _scale(scale, d)
+    allowed = allowed_mask(intervals, T)
+    M = additive_mask(allowed)
+    _check_forms_agree(allowed, M)
+    out = np.zeros((T, h_q, d), dtype=np.float64)
+    probs = np.zeros((h_q, T, T), dtype=np.float64) if return_probs else None
+    for h in range(h_q):
+        g = h // G
+        S = (q[:, h, :] @ k[:, g, :].T) * sc + M
+        P = softmax_rows(S)
+        out[:, h, :] = P @ v[:, g, :]
+        if return_probs:
+            probs[h] = P
+    if return_probs:
+        return out, probs
+    return out
+
+
+def prefill_rows(q, k, v, intervals, rows, heads=None, scale=None):
+    """The same definition evaluated for selected output rows only.
+
+    Row t of the dense mask is built from the same rule (same question and
+    u <= t) over all T columns.  Returns [len(rows), len(heads), d].
+    ``q``/``k``/``v`` may be stored arrays; pass float64 values.
+    """
+    q = np.asarray(q)
+    k = np.asarray(k)
+    v = np.asarray(v)
+    T, h_q, d = q.shape
+    h_kv = k.shape[1]
+    G = _group(h_q, h_kv)
+    sc = _scale(scale, d)
+    heads = list(range(h_q)) if heads is None else list(heads)
+    seg = segment_ids(intervals, T)
+    cols = np.arange(T)
+    out = np.zeros((len(rows), len(heads), d), dtype=np.float64)
+    for r, t in enumerate(rows):
+        allowed = (seg[t] >= 0) & (seg == seg[t]) & (cols <= t)
+        M = np.where(allowed, 0.0, -np.inf)
+        for j, h in enumerate(heads):
+            g = h // G
+            s = (np.asarray(k[:, g, :], dtype=np.float64) @ np.asarray(q[t, h, :], dtype=np.float64)) * sc + M
+            p = softmax_rows(s[None, :])[0]
+            out[r, j] = p @ np.asarray(v[:, g, :], dtype=np.float64)
+    return out
+
+
+# ---------------------------------------------------------------------------
+# KV slot pool
+# ---------------------------------------------------------------------------
+
+def validate_prefill(intervals, total_tokens, slot_ids=None, n_slots=0, cap=0):
+    """Return None if the call is valid, else the error kind.
+
+    Intervals lie in [0, T] with s <= e and non-empty ones do not overlap.
+    With a slot write: every slot id is in [0, n_slots), every question fits
+    (L_i <= cap) and the slots of non-empty questions are distinct (two live
+    questions sharing one cache is the shared-state bug of the KV-cache
+    isolation article, hnwysp.cn, §2.3 and §6.1).
+    """
+    iv = np.asarray(intervals, dtype=np.int64).reshape(-1, 2)
+    T = int(total_tokens)
+    for s, e in iv:
+        if not (0 <= s <= e <= T):
+            return INTERVALS
+    ne = iv[iv[:, 1] > iv[:, 0]]
+    order = np.argsort(ne[:, 0], kind="stable")
+    ne = ne[order]
+    for a in range(1, len(ne)):
+        if ne[a, 0] < ne[a - 1, 1]:
+            return INTERVALS
+    if slot_ids is None:
+        return None
+    sl = np.asarray(slot_ids, dtype=np.int64)
+    if np.any((sl < 0) | (sl >= n_slots)):
+        return SLOT
+    L = iv[:, 1] - iv[:, 0]
+    if np.any(L > cap):
+        return SLOT_OVERFLOW
+    used = sl[L > 0]
+    if len(np.unique(used)) != len(used):
+        return SLOT
+    return None
+
+
+def slot_write(pool_k, pool_v, k, v, intervals, slot_ids):
+    """pool[slot_i, g, j, :] = k/v[s_i + j, g, :] for j < L_i (a bit copy).
+
+    Works on the stored arrays (any dtype); positions >= L_i and slots no
+    question uses keep their previous contents.  Returns new arrays.
+    """
+    pk = np.array(pool_k, copy=True)
+    pv = np.array(pool_v, copy=True)
+    for (s, e), slot in zip(np.asarray(intervals).reshape(-1, 2), np.asarray(slot_ids)):
+        n = int(e - s)
+        if n <= 0:
+            continue
+        pk[slot, :, :n, :] = np.swapaxes(np.asarray(k)[s:e], 0, 1)
+        pv[slot, :, :n, :] = np.swapaxes(np.asarray(v)[s:e], 0, 1)
+    return pk, pv
+
+
+# ---------------------------------------------------------------------------
+# decode
+# ---------------------------------------------------------------------------
+
+def validate_decode(slot_ids, lens, active, n_slots, cap):
+    """Return None if the step is valid, else the error kind.
+
+    Only live questions are checked: a dropped question's slot may already
+    be back in the pool.  A live question needs a slot in [0, n_slots),
+    0 <= lens_i and room for the new row (lens_i < cap), and live slots are
+    distinct.
+    """
+    sl = np.asarray(slot_ids, dtype=np.int64)
+    ln = np.asarray(lens, dtype=np.int64)
+    live = np.asarray(active).astype(bool)
+    if np.any(live & ((sl < 0) | (sl >= n_slots))):
+        return SLOT
+    if np.any(live & ((ln < 0) | (ln >= cap))):
+        return SLOT_OVERFLOW
+    used = sl[live]
+    if len(np.unique(used)) != len(used):
+        return SLOT
+    return None
+
+
+def decode(q_new, k_new, v_new, pool_k, pool_v, slot_ids, lens, active, dtype: str,
+           scale=None, inplace: bool = False):
+    """One decode step over the slot pool.
+
+    For every live question i with n = lens_i: first the new K/V row is
+    written at position n of its slot, then for every q-head h (kv-head
+    g = h // G) o_new[i, h] = softmax(scale * q_new[i, h] . K[0..n]) V[0..n].
+    Dropped questions are skipped: no output, no write.
+
+    ``pool_k``/``pool_v``/``k_new``/``v_new``/``q_new`` are stored arrays of
+    ``dtype`` ('bf16' bits or 'fp32').  Returns (o_new [N, H_q, d] float64
+    with NaN rows for dropped questions, pool_k', pool_v').
+    """
+    pk = pool_k if inplace else np.array(pool_k, copy=True)
+    pv = pool_v if inplace else np.array(pool_v, copy=True)
+    N, h_q, d = np.asarray(q_new).shape
+    h_kv = np.asarray(k_new).shape[1]
+    G = _group(h_q, h_kv)
+    sc = _scale(scale, d)
+    o = np.full((N, h_q, d), np.nan, dtype=np.float64)
+    for i in range(N):
+        if not active[i]:
+            continue
+        slot, n = int(slot_ids[i]), int(lens[i])
+        pk[slot, :, n, :] = k_new[i]
+        pv[slot, :, n, :] = v_new[i]
+        for h in range(h_q):
+            g = h // G
+            K = to_float64(pk[slot, g, :n + 1, :], dtype)
+            V = to_float64(pv[slot, g, :n + 1, :], dtype)
+            qv = to_float64(np.asarray(q_new)[i, h], dtype)
+            p = softmax_rows(((K @ qv) * sc)[None, :])[0]
+            o[i, h] = p @ V
+    return o, pk, pv

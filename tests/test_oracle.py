@@ -1,0 +1,403 @@
+"""Pins of the CPU oracle against what the pages and mathematics fix.
+
+Each test ties the oracle to something other than itself: the pages' worked
+examples (fixtures under tests/golden/, each with its citation), closed
+forms, the invariants (a)-(d), a library routine (torch's scaled dot-product
+attention in float64) and a separate pure-Python brute force.  The
+``test_planted_*`` tests plant plausible mistakes into a copy of the oracle
+and check that at least one pin catches each of them.
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from oracle import brute
+from oracle import kev_oracle as O
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _golden(name):
+    vals = {}
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if not line:
+                continue
+            if "->" in line:
+                k, v = line.split("->")
+                vals[k.strip()] = float(v)
+            elif "=" in line:
+                k, v = line.split("=", 1)
+                vals[k.strip()] = [float(x) for x in v.split()]
+    return vals
+
+
+def _f64(w, name):
+    return W.to_float64(getattr(w, name), w.dtype)
+
+
+# ---------------------------------------------------------------------------
+# worked examples printed on the pages
+# ---------------------------------------------------------------------------
+
+def test_worked_example_online_softmax():
+    g = _golden("online_softmax_worked_example.txt")
+    k = np.array(g["k"]).reshape(4, 1, 1)
+    v = np.array(g["v"]).reshape(4, 1, 1)
+    q = np.full((4, 1, 1), g["q"][0])
+    out = O.prefill(q, k, v, [(0, 4)], scale=g["scale"][0])
+    # the last token sees all four keys: the page's single query row
+    assert round(float(out[3, 0, 0]), int(g["decimals"][0])) == pytest.approx(g["output"][0], abs=0)
+    o_online, alphas = O.online_softmax_row(q[3, 0], k[:, 0], v[:, 0], g["scale"][0], int(g["block"][0]))
+    assert round(float(o_online[0]), 6) == g["output"][0]
+    assert abs(o_online[0] - out[3, 0, 0]) < 1e-12
+    assert round(100 * alphas[1], 1) == g["second_block_rescale_percent"][0]
+    bf = brute.prefill(q.tolist(), k.tolist(), v.tolist(), [(0, 4)], 1.0)
+    assert abs(bf[3][0][0] - out[3, 0, 0]) < 1e-12
+
+
+def test_worked_example_arithmetic_intensity():
+    from packed_question_isolated_gb300.roofline import projection_intensity
+    g = _golden("arithmetic_intensity.txt")
+    d, b = int(g["d"][0]), int(g["bytes_per_value"][0])
+    assert round(projection_intensity(1, d, b), 2) == g["n=1"]
+    assert round(projection_intensity(1024, d, b), 2) == g["n=1024"]
+
+
+def test_kv_cache_demo_shapes_and_last_row():
+    g = _golden("kv_cache_demo.txt")
+    T, dh = int(g["T"][0]), int(g["d_h"][0])
+    rng = np.random.default_rng(7)
+    x = rng.standard_normal((T + 1, 1, dh))
+    k = rng.standard_normal((T + 1, 1, dh))
+    v = rng.standard_normal((T + 1, 1, dh))
+    full, P = O.prefill(x, k, v, [(0, T + 1)], return_probs=True)
+    assert float(np.abs(np.triu(P[0], 1)).max()) == g["future_weight_max"][0]
+    pool_k = np.zeros((1, 1, T + 1, dh))
+    pool_v = np.zeros((1, 1, T + 1, dh))
+    pool_k[0, 0, :T] = k[:T, 0]
+    pool_v[0, 0, :T] = v[:T, 0]
+    o, pk, _ = O.decode(x[T:T + 1].astype(np.float32), k[T:T + 1].astype(np.float32),
+                        v[T:T + 1].astype(np.float32), pool_k.astype(np.float32),
+                        pool_v.astype(np.float32), [0], [T], [1], "fp32")
+    assert pk[0, 0, :T + 1].shape == tuple(int(x) for x in g["k_cache_after_step"])
+    assert o[0].shape == tuple(int(x) for x in g["z_cached"])
+    # same values rounded to fp32 on both sides
+    x32 = x.astype(np.float32).astype(np.float64)
+    k32 = k.astype(np.float32).astype(np.float64)
+    v32 = v.astype(np.float32).astype(np.float64)
+    full32 = O.prefill(x32, k32, v32, [(0, T + 1)])
+    assert np.max(np.abs(o[0] - full32[T])) < 1e-12
+
+
+# ---------------------------------------------------------------------------
+# closed forms
+# ---------------------------------------------------------------------------
+
+def test_closed_form_zero_keys_give_prefix_mean():
+    rng = np.random.default_rng(11)
+    lengths = [5, 9, 1, 7]
+    iv = W.pack_intervals(lengths, gaps=[0, 2, 1, 3])
+    T = int(iv[:, 1].max()) + 2
+    q = rng.standard_normal((T, 4, 8))
+    k = np.zeros((T, 2, 8))
+    v = rng.standard_normal((T, 2, 8))
+    out = O.prefill(q, k, v, iv)
+    for s, e in iv:
+        for t in range(s, e):
+            for h in range(4):
+                expect = v[s:t + 1, h // 2].mean(axis=0)
+                assert np.max(np.abs(out[t, h] - expect)) < 1e-12
+
+
+def test_closed_form_single_token_question_copies_v():
+    rng = np.random.default_rng(12)
+    iv = np.array([[0, 3], [3, 4], [4, 9]])
+    q = rng.standard_normal((9, 2, 16))
+    k = rng.standard_normal((9, 1, 16))
+    v = rng.standard_normal((9, 1, 16))
+    out = O.prefill(q, k, v, iv)
+    assert np.array_equal(out[3, 0], v[3, 0]) and np.array_equal(out[3, 1], v[3, 0])
+    assert np.array_equal(out[0, 0], v[0, 0])
+
+
+def test_closed_form_dominant_key_selects_its_value():
+    rng = np.random.default_rng(13)
+    T, d = 12, 4
+    q = np.zeros((T, 1, d))
+    q[:, 0, 0] = 1.0
+    k = rng.standard_normal((T, 1, d)) * 0.01
+    k[5, 0, 0] = 80.0  # score 40 above the rest at scale 1/2
+    v = rng.standard_normal((T, 1, d))
+    out = O.prefill(q, k, v, [(0, T)])
+    for t in range(5, T):
+        assert np.max(np.abs(out[t, 0] - v[5, 0])) < 1e-12
+    # before the key is visible it has no effect
+    assert np.max(np.abs(out[4, 0] - v[5, 0])) > 1e-3
+
+
+# ---------------------------------------------------------------------------
+# invariants (a)-(d)
+# ---------------------------------------------------------------------------
+
+def test_invariant_a_future_and_cross_question_weights_are_exactly_zero():
+    w = W.random_case(21, [6, 1, 9, 4], 4, 2, 8, "fp32", gaps=[1, 0, 2, 3], tail=2)
+    _, P = O.prefill(_f64(w, "q"), _f64(w, "k"), _f64(w, "v"), w.intervals, return_probs=True)
+    seg = O.segment_ids(w.intervals, w.total_tokens)
+    T = w.total_tokens
+    for t in range(T):
+        for u in range(T):
+            if u > t or seg[t] < 0 or seg[u] != seg[t]:
+                assert (P[:, t, u] == 0.0).all()
+    for t in range(T):
+        row = P[:, t, :].sum(-1)
+        if seg[t] >= 0:
+            assert np.max(np.abs(row - 1.0)) < 1e-12
+        else:
+            assert (row == 0.0).all()
+
+
+@pytest.mark.parametrize("seed", [31, 32])
+def test_invariant_b_packed_equals_alone(seed):
+    w = W.random_case(seed, [17, 3, 29, 1, 12], 6, 2, 16, "fp32", gaps=[0, 4, 1, 2, 0], tail=3,
+                      order=[2, 0, 4, 1, 3])
+    q, k, v = _f64(w, "q"), _f64(w, "k"), _f64(w, "v")
+    packed = O.prefill(q, k, v, w.intervals)
+    for s, e in w.intervals:
+        alone = O.prefill(q[s:e], k[s:e], v[s:e], [(0, e - s)])
+        assert np.max(np.abs(packed[s:e] - alone)) <= 1e-12
+    # rows of tokens that belong to no question are zero
+    seg = O.segment_ids(w.intervals, w.total_tokens)
+    assert (packed[seg < 0] == 0).all()
+
+
+def test_invariant_c_decode_equals_last_row_of_recompute():
+    w = W.random_case(41, [5, 11, 8], 4, 2, 8, "fp32")
+    q, k, v = _f64(w, "q"), _f64(w, "k"), _f64(w, "v")
+    cap = 16
+    pool_k = np.zeros((3, 2, cap, 8), np.float32)
+    pool_v = np.zeros((3, 2, cap, 8), np.float32)
+    pool_k, pool_v = O.slot_write(pool_k, pool_v, w.k, w.v, w.intervals, w.slot_ids)
+    lens = w.lengths.copy()
+    active = np.array([1, 0, 1], np.uint8)
+    o, pk, pv = O.decode(w.q_new, w.k_new, w.v_new, pool_k, pool_v, w.slot_ids, lens, active, "fp32")
+    assert np.isnan(o[1]).all()
+    for i, (s, e) in enumerate(w.intervals):
+        if not active[i]:
+            continue
+        qe = np.concatenate([q[s:e], _f64(w, "q_new")[i:i + 1]])
+        ke = np.concatenate([k[s:e], _f64(w, "k_new")[i:i + 1]])
+        ve = np.concatenate([v[s:e], _f64(w, "v_new")[i:i + 1]])
+        full = O.prefill(qe, ke, ve, [(0, e - s + 1)])
+        assert np.max(np.abs(o[i] - full[-1])) <= 1e-12
+        assert np.array_equal(pk[w.slot_ids[i], :, e - s], w.k_new[i])
+    # the dropped question's slot is untouched
+    assert np.array_equal(pk[w.slot_ids[1]], pool_k[w.slot_ids[1]])
+
+
+def _nested(a):
+    return a.tolist()
+
+
+def test_invariant_d_brute_force_tiny_fp32_config():
+    w = W.tiny_fp32()
+    q, k, v = _f64(w, "q"), _f64(w, "k"), _f64(w, "v")
+    out = O.prefill(q, k, v, w.intervals)
+    bf = np.array(brute.prefill(_nested(q), _nested(k), _nested(v), w.intervals.tolist(),
+                                1.0 / math.sqrt(w.d)))
+    assert np.max(np.abs(out - bf)) <= 1e-12
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_invariant_d_brute_force_random_tiny(seed):
+    rng = np.random.default_rng(100 + seed)
+    n = int(rng.integers(1, 5))
+    lengths = rng.integers(0, 9, size=n)
+    h_kv = int(rng.integers(1, 3))
+    G = int(rng.integers(1, 4))
+    w = W.random_case(200 + seed, lengths, h_kv * G, h_kv, 4, "fp32",
+                      gaps=rng.integers(0, 3, size=n), tail=int(rng.integers(0, 3)))
+    if w.total_tokens == 0:
+        return
+    q, k, v = _f64(w, "q"), _f64(w, "k"), _f64(w, "v")
+    out = O.prefill(q, k, v, w.intervals)
+    bf = np.array(brute.prefill(_nested(q), _nested(k), _nested(v), w.intervals.tolist(), 0.5))
+    assert np.max(np.abs(out - bf)) <= 1e-12
+    rows = list(range(w.total_tokens))
+    pr = O.prefill_rows(q, k, v, w.intervals, rows)
+    assert np.max(np.abs(pr - out)) <= 1e-12
+
+
+def test_brute_force_decode_one_matches_oracle_decode():
+    rng = np.random.default_rng(5)
+    pk = rng.standard_normal((2, 1, 8, 4)).astype(np.float32)
+    pv = rng.standard_normal((2, 1, 8, 4)).astype(np.float32)
+    qn = rng.standard_normal((1, 2, 4)).astype(np.float32)
+    kn = rng.standard_normal((1, 1, 4)).astype(np.float32)
+    vn = rng.standard_normal((1, 1, 4)).astype(np.float32)
+    o, pk2, pv2 = O.decode(qn, kn, vn, pk, pv, [1], [5], [1], "fp32")
+    kr = pk2[1, 0, :6].astype(np.float64).tolist()
+    vr = pv2[1, 0, :6].astype(np.float64).tolist()
+    for h in range(2):
+        ref = brute.decode_one(qn[0, h].astype(np.float64).tolist(), kr, vr, 0.5)
+        assert np.max(np.abs(np.array(ref) - o[0, h])) <= 1e-12
+
+
+# ---------------------------------------------------------------------------
+# a library routine: torch scaled-dot-product attention in float64
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("h_q,h_kv", [(4, 4), (8, 2), (7, 1)])
+def test_single_question_matches_torch_sdpa(h_q, h_kv):
+    rng = np.random.default_rng(h_q * 10 + h_kv)
+    T, d = 23, 16
+    q = rng.standard_normal((T, h_q, d))
+    k = rng.standard_normal((T, h_kv, d))
+    v = rng.standard_normal((T, h_kv, d))
+    out = O.prefill(q, k, v, [(0, T)])
+    tq = torch.from_numpy(q).permute(1, 0, 2)[None]
+    tk = torch.from_numpy(k).permute(1, 0, 2)[None]
+    tv = torch.from_numpy(v).permute(1, 0, 2)[None]
+    ref = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, is_causal=True,
+                                                          enable_gqa=(h_q != h_kv))
+    ref = ref[0].permute(1, 0, 2).numpy()
+    assert np.max(np.abs(out - ref)) < 1e-12
+
+
+def test_packed_matches_torch_sdpa_with_block_mask():
+    w = W.random_case(51, [7, 13, 5], 4, 2, 8, "fp32", gaps=[1, 0, 2])
+    q, k, v = _f64(w, "q"), _f64(w, "k"), _f64(w, "v")
+    out = O.prefill(q, k, v, w.intervals)
+    for s, e in w.intervals:
+        tq = torch.from_numpy(q[s:e]).permute(1, 0, 2)[None]
+        tk = torch.from_numpy(k[s:e]).permute(1, 0, 2)[None]
+        tv = torch.from_numpy(v[s:e]).permute(1, 0, 2)[None]
+        ref = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, is_causal=True,
+                                                              enable_gqa=True)
+        assert np.max(np.abs(out[s:e] - ref[0].permute(1, 0, 2).numpy())) < 1e-12
+
+
+# ---------------------------------------------------------------------------
+# slot pool and validation
+# ---------------------------------------------------------------------------
+
+def test_slot_write_is_bit_copy_and_keeps_sentinels():
+    w = W.random_case(61, [3, 0, 5], 2, 2, 8, "bf16", n_slots=5, permute_slots=True, cap=6)
+    sent = np.uint16(0x7FC1)
+    pk = np.full((5, 2, 6, 8), sent, np.uint16)
+    pv = np.full((5, 2, 6, 8), sent, np.uint16)
+    nk, nv = O.slot_write(pk, pv, w.k, w.v, w.intervals, w.slot_ids)
+    for (s, e), slot in zip(w.intervals, w.slot_ids):
+        n = e - s
+        assert np.array_equal(nk[slot, :, :n], np.swapaxes(w.k[s:e], 0, 1))
+        assert np.array_equal(nv[slot, :, :n], np.swapaxes(w.v[s:e], 0, 1))
+        assert (nk[slot, :, n:] == sent).all() and (nv[slot, :, n:] == sent).all()
+    unused = sorted(set(range(5)) - set(int(x) for x, (s, e) in zip(w.slot_ids, w.intervals) if e > s))
+    for slot in unused:
+        assert (nk[slot] == sent).all()
+
+
+def test_validate_prefill_cases():
+    V = O.validate_prefill
+    assert V([(0, 3), (3, 5)], 5) is None
+    assert V([(0, 3), (2, 5)], 5) == O.INTERVALS          # overlap
+    assert V([(0, 6)], 5) == O.INTERVALS                   # past T
+    assert V([(3, 2)], 5) == O.INTERVALS                   # reversed
+    assert V([(-1, 2)], 5) == O.INTERVALS
+    assert V([(2, 2), (0, 5)], 5) is None                  # empty interval overlaps nothing
+    assert V([(0, 3), (3, 5)], 5, [0, 2], 2, 4) == O.SLOT  # slot out of range
+    assert V([(0, 3), (3, 5)], 5, [1, 1], 2, 4) == O.SLOT  # shared slot
+    assert V([(0, 3), (3, 3)], 5, [1, 1], 2, 4) is None    # empty question's slot may repeat
+    assert V([(0, 5)], 5, [0], 1, 4) == O.SLOT_OVERFLOW    # L > cap
+    assert V([(0, 4)], 5, [0], 1, 4) is None               # L == cap fits exactly
+
+
+def test_validate_decode_cases():
+    V = O.validate_decode
+    assert V([0, 1], [3, 3], [1, 1], 2, 4) is None
+    assert V([0, 1], [4, 3], [1, 1], 2, 4) == O.SLOT_OVERFLOW   # no room for the new row
+    assert V([0, 1], [4, 3], [0, 1], 2, 4) is None              # dropped question not checked
+    assert V([1, 1], [1, 1], [1, 1], 2, 4) == O.SLOT
+    assert V([1, 1], [1, 1], [1, 0], 2, 4) is None
+    assert V([0, 5], [1, 1], [1, 1], 2, 4) == O.SLOT
+    assert V([0, 1], [0, 0], [0, 0], 2, 4) is None              # every question dropped
+
+
+def test_config_realisations():
+    """The seeded procedure gives the workloads quoted in the design notes."""
+    w2 = W.qwen25_7b_prefill()
+    assert w2.lengths.tolist() == [1757, 725, 451, 791, 997, 1715, 1065, 420]
+    assert w2.total_tokens == 7921
+    rng = np.random.default_rng(3)
+    L3 = np.clip(np.rint(np.exp(rng.normal(np.log(512.0), 0.8, size=32))), 1, 4096)
+    assert int(L3.sum()) == 24100 and int(L3.max()) == 4096 and int(L3.min()) == 66
+    s = W.stress()
+    assert s.prefill.total_tokens == 19483
+    assert int((s.n_decoded > 0).sum()) == 256 and int(s.n_decoded.max()) == 116
+
+
+# ---------------------------------------------------------------------------
+# planted mistakes: each must be caught by a pin above
+# ---------------------------------------------------------------------------
+
+def _pins_pass(prefill_fn):
+    """Re-run a representative subset of the pins against a replacement prefill."""
+    ok = []
+    g = _golden("online_softmax_worked_example.txt")
+    k = np.array(g["k"]).reshape(4, 1, 1)
+    v = np.array(g["v"]).reshape(4, 1, 1)
+    q = np.ones((4, 1, 1))
+    ok.append(round(float(prefill_fn(q, k, v, [(0, 4)], 1.0)[3, 0, 0]), 6) == g["output"][0])
+    w = W.random_case(31, [17, 3, 29, 1, 12], 6, 2, 16, "fp32", gaps=[0, 4, 1, 2, 0], tail=3)
+    qq, kk, vv = _f64(w, "q"), _f64(w, "k"), _f64(w, "v")
+    packed = prefill_fn(qq, kk, vv, w.intervals, None)
+    good = True
+    for s, e in w.intervals:
+        alone = prefill_fn(qq[s:e], kk[s:e], vv[s:e], [(0, e - s)], None)
+        good &= bool(np.max(np.abs(packed[s:e] - alone)) <= 1e-12)
+    ok.append(good)
+    bf = np.array(brute.prefill(_nested(qq), _nested(kk), _nested(vv), w.intervals.tolist(), 0.25))
+    ok.append(bool(np.max(np.abs(packed - bf)) <= 1e-12))
+    return all(ok)
+
+
+def test_planted_mistakes_are_caught(monkeypatch):
+    assert _pins_pass(lambda q, k, v, iv, sc: O.prefill(q, k, v, iv, scale=sc))
+
+    def future_mask(intervals, T):          # causal direction reversed
+        return np.triu(np.ones((T, T), bool)) & _iso(intervals, T)
+
+    def no_isolation(intervals, T):          # isolation dropped
+        return np.tril(np.ones((T, T), bool)) & (O.segment_ids(intervals, T)[:, None] >= 0)
+
+    def _iso(intervals, T):
+        m = np.zeros((T, T), bool)
+        for s, e in intervals:
+            m[s:e, s:e] = True
+        return m
+
+    for bad in (future_mask, no_isolation):
+        monkeypatch.setattr(O, "allowed_mask", bad)
+        assert not _pins_pass(lambda q, k, v, iv, sc: O.prefill(q, k, v, iv, scale=sc))
+        monkeypatch.undo()
+
+    def wrong_gqa(q, k, v, iv, sc):          # h % H_kv instead of h // G
+        kk = np.tile(k, (1, q.shape[1] // k.shape[1], 1))
+        vv = np.tile(v, (1, q.shape[1] // v.shape[1], 1))
+        return O.prefill(q, kk, vv, iv, scale=sc)
+    assert not _pins_pass(wrong_gqa)
+
+    # the 1/sqrt(d_h) factor dropped when no scale is given
+    assert not _pins_pass(lambda q, k, v, iv, sc: O.prefill(q, k, v, iv, scale=sc or 1.0))
+
+    plain_softmax = O.softmax_rows
+
+    def transposed_pv(scores):               # weights normalised over the wrong axis
+        return plain_softmax(scores.T).T
+    monkeypatch.setattr(O, "softmax_rows", transposed_pv)
+    assert not _pins_pass(lambda q, k, v, iv, sc: O.prefill(q, k, v, iv, scale=sc))
