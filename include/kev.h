@@ -1,0 +1,197 @@
+/*
+ * kev.h -- C ABI of libkev: packed, question-isolated attention on one GB300 (sm_103a).
+ *
+ * N questions are packed into one token sequence of T tokens.  Question i owns the
+ * half-open interval [begin_i, end_i) of packed positions.  Prefill attention is causal
+ * AND block diagonal: token t of question i attends to token u iff u lies in the same
+ * interval and u <= t (Kev architecture article, icman.com.cn news 75864, §2.1 end and
+ * §2.3; Kev pipeline article, gsyq.cn news 368355, §2.2 "visible domain").  Each
+ * question's K/V rows go into its own slot of a preallocated pool (Kev pipeline article,
+ * §2.2 "KV cache slot pool").  A decode step appends one K/V row per live question and
+ * attends over its whole slot (inference-engine notes, sakurs2.com, §2.2); questions that
+ * stopped early are dropped from the step (Kev pipeline article, §1.2, §2.3).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Every tensor pointer is caller-owned DEVICE memory, contiguous, 16-byte aligned.
+ *    The library allocates nothing and keeps no mutable global state, so calls on
+ *    different streams with different buffers are independent.  The cache is passed in
+ *    and out as an argument, never held by the library (KV-cache isolation article,
+ *    hnwysp.cn news 130224, §3.3 and §4.3).
+ *  - Everything is enqueued on `stream`; no entry point synchronises the host except
+ *    kev_read_status.
+ *  - Layouts (row-major, last index fastest):
+ *        q        [T, H_q, d]          out  [T, H_q, d]
+ *        k, v     [T, H_kv, d]
+ *        pool_k, pool_v  [n_slots, H_kv, slot_cap, d]
+ *        q_new [N, H_q, d], k_new/v_new [N, H_kv, d], decode out [N, H_q, d]
+ *    q-head h reads kv-head h / (H_q / H_kv) (grouped-query attention).
+ *  - Element type: KEV_BF16 (bf16 storage, fp32 accumulation, bf16 output rounded to
+ *    nearest even) or KEV_FP32 (fp32 storage and arithmetic, no TF32).
+ *    Supported head dims: d in {64, 128}; H_q must be a multiple of H_kv, G = H_q/H_kv <= 16.
+ *  - Errors.  Arguments the host can check (null or misaligned pointers, negative sizes,
+ *    unsupported shapes, too small a workspace) are returned at once and nothing is
+ *    launched.  Data-dependent errors (intervals, slot ids, lengths) are found on the
+ *    device before anything is written: the call's kernels then write nothing, and the
+ *    code is stored in *dev_status (if dev_status is not NULL) in stream order.
+ *    kev_read_status turns it into a kev_status.
+ *  - Scale: kev_attn_shape.scale == 0 means 1/sqrt(d).
+ */
+#ifndef KEV_H
+#define KEV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* kev_stream_t; /* same type as cudaStream_t; NULL = legacy default stream */
+
+typedef enum {
+  KEV_OK = 0,
+  KEV_ERR_INVALID_ARG = 1,   /* null / misaligned pointer, negative size, workspace too small */
+  KEV_ERR_UNSUPPORTED = 2,   /* dtype, head dim or group size this library does not implement */
+  KEV_ERR_INTERVALS = 3,     /* (device) an interval is reversed, outside [0,T] or overlaps another */
+  KEV_ERR_SLOT = 4,          /* (device) slot id outside [0,n_slots) or shared by two live questions */
+  KEV_ERR_SLOT_OVERFLOW = 5, /* (device) a question longer than slot_cap, or no room for a decode row */
+  KEV_ERR_TIMEOUT = 6,       /* (device) a bounded wait inside a kernel gave up; outputs are invalid */
+  KEV_ERR_CUDA = 7           /* a CUDA runtime call failed (launch error, no device, ...) */
+} kev_status;
+
+typedef enum { KEV_BF16 = 0, KEV_FP32 = 1 } kev_dtype;
+
+/* Half-open interval [begin, end) of packed-token indices owned by one question. */
+typedef struct {
+  int32_t begin;
+  int32_t end;
+} kev_interval;
+
+typedef struct {
+  int32_t h_q;   /* query heads */
+  int32_t h_kv;  /* key/value heads; h_q % h_kv == 0 */
+  int32_t d_h;   /* head dimension: 64 or 128 */
+  int32_t dtype; /* kev_dtype */
+  float scale;   /* softmax scale; 0 => 1/sqrt(d_h) */
+} kev_attn_shape;
+
+/* ---------------------------------------------------------------------------------------
+ * Prefill
+ * ------------------------------------------------------------------------------------- */
+
+/* Bytes of device workspace kev_prefill_attn / kev_build_segments / kev_kv_write need for
+ * at most `n_questions` questions packed into `total_tokens` tokens.  0 on bad arguments. */
+size_t kev_prefill_workspace_size(int32_t n_questions, int32_t total_tokens, const kev_attn_shape* shape);
+
+/* Segment descriptors (step 1 of prefill; exported for tests and debugging).
+ *
+ * Validates the intervals (0 <= begin <= end <= T; non-empty intervals pairwise disjoint)
+ * and, if slot_ids != NULL, the slots (every id in [0, n_slots); every length <= slot_cap;
+ * non-empty questions on distinct slots -- two live questions sharing one cache is the
+ * shared-state bug of the KV-cache isolation article, §2.3, §6.1).  Then writes into
+ * `workspace`: the status word, cu_seqlens[N+1] (prefix sums of the lengths in interval
+ * order, the varlen form of the block-diagonal mask, Kev architecture article §5.2, §6.4)
+ * and the prefill work list: one item per (question, 128-row query tile, query head),
+ * covering key tiles [0, m] of its own question only, so no tile that is masked across
+ * questions or above the causal diagonal is ever scheduled.  Items are ordered longest
+ * first.  Interval order is free and intervals need not cover [0, T): tokens in no
+ * interval are keys for nobody and their output rows are written as 0.
+ *   intervals  device kev_interval[n_questions]
+ *   slot_ids   device int32[n_questions] or NULL (no slot checks)
+ *   workspace  device, kev_prefill_workspace_size(...) bytes, 256-byte aligned */
+kev_status kev_build_segments(const kev_interval* intervals, int32_t n_questions, int32_t total_tokens,
+                              const int32_t* slot_ids, int32_t n_slots, int32_t slot_cap,
+                              const kev_attn_shape* shape, void* workspace, size_t workspace_bytes,
+                              int32_t* dev_status, kev_stream_t stream);
+
+/* Host copy of the work list built by kev_build_segments (synchronises `stream`).
+ * Each item is {question, q_row_begin, q_rows, head}; returns the item count, or -1 on
+ * error.  Writes at most `max_items` items to `items_out` (host int32[4*max_items]). */
+int32_t kev_read_work_list(const void* workspace, size_t workspace_bytes, int32_t* items_out,
+                           int32_t max_items, kev_stream_t stream);
+
+/* Attention over a work list already built in `workspace` by kev_build_segments with the
+ * same intervals/slots (step 2 of prefill), plus the slot write when slot_ids != NULL:
+ *   out[t, h, :] = softmax_u(scale q[t,h].k[u,g] over allowed u) v[u,g]    (g = h / G)
+ *   pool_{k,v}[slot_i, g, j, :] = {k,v}[begin_i + j, g, :]   for j < L_i   (bit copy)
+ * Rows of tokens in no interval are written as zeros.  Pool positions >= L_i and slots no
+ * question uses are not touched. */
+kev_status kev_prefill_from_segments(const void* q, const void* k, const void* v, int32_t total_tokens,
+                                     const kev_interval* intervals, int32_t n_questions,
+                                     const int32_t* slot_ids, void* pool_k, void* pool_v,
+                                     int32_t n_slots, int32_t slot_cap, void* out,
+                                     const kev_attn_shape* shape, void* workspace, size_t workspace_bytes,
+                                     int32_t* dev_status, kev_stream_t stream);
+
+/* Full prefill: kev_build_segments followed by kev_prefill_from_segments.
+ * Pass slot_ids = NULL (and NULL pools) to skip the slot write. */
+kev_status kev_prefill_attn(const void* q, const void* k, const void* v, int32_t total_tokens,
+                            const kev_interval* intervals, int32_t n_questions,
+                            const int32_t* slot_ids, void* pool_k, void* pool_v,
+                            int32_t n_slots, int32_t slot_cap, void* out,
+                            const kev_attn_shape* shape, void* workspace, size_t workspace_bytes,
+                            int32_t* dev_status, kev_stream_t stream);
+
+/* Slot write alone (validation of kev_build_segments, then the bit copy above).
+ * Uses the same workspace as prefill. */
+kev_status kev_kv_write(const void* k, const void* v, int32_t total_tokens, const kev_interval* intervals,
+                        int32_t n_questions, const int32_t* slot_ids, void* pool_k, void* pool_v,
+                        int32_t n_slots, int32_t slot_cap, const kev_attn_shape* shape,
+                        void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                        kev_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------
+ * Decode
+ * ------------------------------------------------------------------------------------- */
+
+/* Bytes of decode workspace for up to `n_questions` questions in slots of `slot_cap`.
+ * The workspace must be zero-filled once before its first use (e.g. cudaMemsetAsync);
+ * every call leaves its counters at zero again.  Two calls in flight at the same time
+ * must not share one workspace. */
+size_t kev_decode_workspace_size(int32_t n_questions, int32_t slot_cap, const kev_attn_shape* shape);
+
+/* One decode step over the slot pool (inference-engine notes §2.2; Kev pipeline article
+ * §2.2-§2.3).  For every live question i (active[i] != 0), with n = lens[i]:
+ *   pool_{k,v}[slot_ids[i], g, n, :] = {k,v}_new[i, g, :]                (append first)
+ *   out[i, h, :] = softmax_j(scale q_new[i,h] . pool_k[slot, g, j]) pool_v[slot, g, j],
+ *                  j = 0..n  (n + 1 positions; no mask: every cached position is visible)
+ * Dropped questions (active[i] == 0) take no part: nothing is read or written for them,
+ * their out rows keep their contents and their slot ids are not checked.
+ * `lens` is read, never written (see kev_decode_advance).
+ * Device-detected errors: KEV_ERR_SLOT (live slot id out of range or shared by two live
+ * questions), KEV_ERR_SLOT_OVERFLOW (lens[i] < 0 or lens[i] >= slot_cap for a live i).
+ *   slot_ids, lens   device int32[n_questions];  active  device uint8[n_questions] */
+kev_status kev_decode_attn(const void* q_new, const void* k_new, const void* v_new,
+                           void* pool_k, void* pool_v, int32_t n_slots, int32_t slot_cap,
+                           const int32_t* slot_ids, const int32_t* lens, const uint8_t* active,
+                           int32_t n_questions, void* out, const kev_attn_shape* shape,
+                           void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                           kev_stream_t stream);
+
+/* lens[i] += (active[i] != 0) for i < n, on the device (no host synchronisation), so a
+ * decode loop can be captured in a CUDA graph. */
+kev_status kev_decode_advance(int32_t* lens, const uint8_t* active, int32_t n, kev_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------
+ * Status
+ * ------------------------------------------------------------------------------------- */
+
+/* Synchronises `stream`, reads the device status word and returns it (KEV_OK if no
+ * device-side error), or KEV_ERR_CUDA if the stream itself reports an error. */
+kev_status kev_read_status(const int32_t* dev_status, kev_stream_t stream);
+
+/* Static, NUL-terminated description of a status code. */
+const char* kev_status_string(kev_status status);
+
+/* Number of kernel launches the most recent successful call of each entry point enqueues
+ * (a constant per entry point, for launch accounting): 0 = prefill_attn,
+ * 1 = prefill_from_segments, 2 = build_segments, 3 = kv_write, 4 = decode_attn,
+ * 5 = decode_advance.  -1 for an unknown id. */
+int32_t kev_launch_count(int32_t entry_point);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KEV_H */

@@ -1,0 +1,317 @@
+// Host side of the C ABI declared in include/kev.h: argument checks and launches.
+// No entry point allocates memory or synchronises, except kev_read_status / kev_read_work_list.
+#include <math.h>
+#include <string.h>
+
+#include "kev_internal.cuh"
+
+using namespace kev;
+
+namespace {
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+int num_sms_of_current_device() {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return sms;
+}
+
+kev_status check_shape(const kev_attn_shape* s) {
+  if (!s) return KEV_ERR_INVALID_ARG;
+  if (s->h_q <= 0 || s->h_kv <= 0) return KEV_ERR_INVALID_ARG;
+  if (s->h_q % s->h_kv) return KEV_ERR_UNSUPPORTED;
+  if (s->h_q / s->h_kv > 16) return KEV_ERR_UNSUPPORTED;
+  if (s->d_h != 64 && s->d_h != 128) return KEV_ERR_UNSUPPORTED;
+  if (s->dtype != KEV_BF16 && s->dtype != KEV_FP32) return KEV_ERR_UNSUPPORTED;
+  if (!(s->scale >= 0.f) || isinf(s->scale)) return KEV_ERR_INVALID_ARG;
+  return KEV_OK;
+}
+
+float effective_scale(const kev_attn_shape* s) {
+  return s->scale == 0.f ? 1.0f / sqrtf((float)s->d_h) : s->scale;
+}
+
+int elem_size(const kev_attn_shape* s) { return s->dtype == KEV_BF16 ? 2 : 4; }
+
+kev_status from_cuda(cudaError_t e) { return e == cudaSuccess ? KEV_OK : KEV_ERR_CUDA; }
+
+kev_status check_prefill_common(int32_t T, const kev_interval* intervals, int32_t n, const kev_attn_shape* shape,
+                                void* ws, size_t ws_bytes) {
+  kev_status st = check_shape(shape);
+  if (st != KEV_OK) return st;
+  if (T < 0 || n < 0) return KEV_ERR_INVALID_ARG;
+  if (n > kMaxQuestions) return KEV_ERR_UNSUPPORTED;
+  if (n > 0 && (!intervals || ((uintptr_t)intervals & 7u))) return KEV_ERR_INVALID_ARG;
+  if (!ws || ((uintptr_t)ws & 255u)) return KEV_ERR_INVALID_ARG;
+  if (ws_bytes < prefill_layout(n, T, shape->h_q).total) return KEV_ERR_INVALID_ARG;
+  return KEV_OK;
+}
+
+kev_status check_slots(const int32_t* slot_ids, void* pool_k, void* pool_v, int32_t n_slots, int32_t cap, int32_t n) {
+  if (!slot_ids) return KEV_OK;
+  if (((uintptr_t)slot_ids & 3u) || !pool_k || !pool_v || !aligned16(pool_k) || !aligned16(pool_v))
+    return KEV_ERR_INVALID_ARG;
+  if (n_slots <= 0 || cap <= 0) return KEV_ERR_INVALID_ARG;
+  (void)n;
+  return KEV_OK;
+}
+
+SegmentsArgs segments_args(const kev_interval* intervals, int32_t n, int32_t T, const int32_t* slot_ids,
+                           int32_t n_slots, int32_t cap, const kev_attn_shape* shape, void* ws,
+                           int32_t* dev_status) {
+  SegmentsArgs a;
+  a.intervals = intervals;
+  a.slot_ids = slot_ids;
+  a.n = n;
+  a.T = T;
+  a.n_slots = n_slots;
+  a.cap = cap;
+  a.h_q = shape->h_q;
+  a.ws = static_cast<char*>(ws);
+  a.layout = prefill_layout(n, T, shape->h_q);
+  a.dev_status = dev_status;
+  return a;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t kev_prefill_workspace_size(int32_t n_questions, int32_t total_tokens, const kev_attn_shape* shape) {
+  if (check_shape(shape) != KEV_OK || n_questions < 0 || total_tokens < 0 || n_questions > kMaxQuestions) return 0;
+  return prefill_layout(n_questions, total_tokens, shape->h_q).total;
+}
+
+kev_status kev_build_segments(const kev_interval* intervals, int32_t n_questions, int32_t total_tokens,
+                              const int32_t* slot_ids, int32_t n_slots, int32_t slot_cap,
+                              const kev_attn_shape* shape, void* workspace, size_t workspace_bytes,
+                              int32_t* dev_status, kev_stream_t stream) {
+  kev_status st = check_prefill_common(total_tokens, intervals, n_questions, shape, workspace, workspace_bytes);
+  if (st != KEV_OK) return st;
+  if (slot_ids && (((uintptr_t)slot_ids & 3u) || n_slots <= 0 || slot_cap <= 0)) return KEV_ERR_INVALID_ARG;
+  if (dev_status && ((uintptr_t)dev_status & 3u)) return KEV_ERR_INVALID_ARG;
+  SegmentsArgs a = segments_args(intervals, n_questions, total_tokens, slot_ids, n_slots, slot_cap, shape,
+                                 workspace, dev_status);
+  return from_cuda(launch_segments(a, (cudaStream_t)stream));
+}
+
+int32_t kev_read_work_list(const void* workspace, size_t workspace_bytes, int32_t* items_out, int32_t max_items,
+                           kev_stream_t stream) {
+  if (!workspace || workspace_bytes < sizeof(PrefillHeader) || max_items < 0) return -1;
+  if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return -1;
+  PrefillHeader h;
+  if (cudaMemcpy(&h, workspace, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) return -1;
+  if (h.status != ST_OK) return -1;
+  const PrefillLayout L = prefill_layout(h.n_questions, h.total_tokens, h.h_q);
+  if (workspace_bytes < L.total) return -1;
+  const int32_t cnt = h.n_items < max_items ? h.n_items : max_items;
+  if (cnt > 0 && items_out) {
+    if (cudaMemcpy(items_out, static_cast<const char*>(workspace) + L.items, sizeof(int4) * (size_t)cnt,
+                   cudaMemcpyDeviceToHost) != cudaSuccess)
+      return -1;
+  }
+  return h.n_items;
+}
+
+kev_status kev_prefill_from_segments(const void* q, const void* k, const void* v, int32_t total_tokens,
+                                     const kev_interval* intervals, int32_t n_questions, const int32_t* slot_ids,
+                                     void* pool_k, void* pool_v, int32_t n_slots, int32_t slot_cap, void* out,
+                                     const kev_attn_shape* shape, void* workspace, size_t workspace_bytes,
+                                     int32_t* dev_status, kev_stream_t stream) {
+  kev_status st = check_prefill_common(total_tokens, intervals, n_questions, shape, workspace, workspace_bytes);
+  if (st != KEV_OK) return st;
+  if (total_tokens > 0 && (!q || !k || !v || !out || !aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)))
+    return KEV_ERR_INVALID_ARG;
+  st = check_slots(slot_ids, pool_k, pool_v, n_slots, slot_cap, n_questions);
+  if (st != KEV_OK) return st;
+  const int sms = num_sms_of_current_device();
+  if (sms <= 0) return KEV_ERR_CUDA;
+  const cudaStream_t s = (cudaStream_t)stream;
+  const PrefillLayout layout = prefill_layout(n_questions, total_tokens, shape->h_q);
+
+  PrefillArgs p;
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.out = out;
+  p.intervals = intervals;
+  p.T = total_tokens;
+  p.n = n_questions;
+  p.h_q = shape->h_q;
+  p.h_kv = shape->h_kv;
+  p.group = shape->h_q / shape->h_kv;
+  p.scale = effective_scale(shape);
+  p.ws = static_cast<const char*>(workspace);
+  p.layout = layout;
+  p.dev_status = dev_status;
+  cudaError_t e = launch_prefill_simt(p, shape->d_h, (kev_dtype)shape->dtype, sms, s);
+  if (e != cudaSuccess) return KEV_ERR_CUDA;
+
+  AuxArgs x;
+  x.k = k;
+  x.v = v;
+  x.out = out;
+  x.intervals = intervals;
+  x.slot_ids = slot_ids;
+  x.pool_k = pool_k;
+  x.pool_v = pool_v;
+  x.n = n_questions;
+  x.T = total_tokens;
+  x.h_q = shape->h_q;
+  x.h_kv = shape->h_kv;
+  x.cap = slot_cap;
+  x.row_bytes = shape->d_h * elem_size(shape);
+  x.ws = static_cast<const char*>(workspace);
+  x.layout = layout;
+  return from_cuda(launch_aux(x, sms, s));
+}
+
+kev_status kev_prefill_attn(const void* q, const void* k, const void* v, int32_t total_tokens,
+                            const kev_interval* intervals, int32_t n_questions, const int32_t* slot_ids,
+                            void* pool_k, void* pool_v, int32_t n_slots, int32_t slot_cap, void* out,
+                            const kev_attn_shape* shape, void* workspace, size_t workspace_bytes,
+                            int32_t* dev_status, kev_stream_t stream) {
+  // full argument check before the first launch, so an invalid call enqueues nothing
+  kev_status st = check_prefill_common(total_tokens, intervals, n_questions, shape, workspace, workspace_bytes);
+  if (st != KEV_OK) return st;
+  if (total_tokens > 0 && (!q || !k || !v || !out || !aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)))
+    return KEV_ERR_INVALID_ARG;
+  st = check_slots(slot_ids, pool_k, pool_v, n_slots, slot_cap, n_questions);
+  if (st != KEV_OK) return st;
+  if (dev_status && ((uintptr_t)dev_status & 3u)) return KEV_ERR_INVALID_ARG;
+  st = kev_build_segments(intervals, n_questions, total_tokens, slot_ids, n_slots, slot_cap, shape, workspace,
+                          workspace_bytes, dev_status, stream);
+  if (st != KEV_OK) return st;
+  return kev_prefill_from_segments(q, k, v, total_tokens, intervals, n_questions, slot_ids, pool_k, pool_v, n_slots,
+                                   slot_cap, out, shape, workspace, workspace_bytes, dev_status, stream);
+}
+
+kev_status kev_kv_write(const void* k, const void* v, int32_t total_tokens, const kev_interval* intervals,
+                        int32_t n_questions, const int32_t* slot_ids, void* pool_k, void* pool_v, int32_t n_slots,
+                        int32_t slot_cap, const kev_attn_shape* shape, void* workspace, size_t workspace_bytes,
+                        int32_t* dev_status, kev_stream_t stream) {
+  kev_status st = check_prefill_common(total_tokens, intervals, n_questions, shape, workspace, workspace_bytes);
+  if (st != KEV_OK) return st;
+  if (!slot_ids) return KEV_ERR_INVALID_ARG;
+  if (total_tokens > 0 && (!k || !v || !aligned16(k) || !aligned16(v))) return KEV_ERR_INVALID_ARG;
+  st = check_slots(slot_ids, pool_k, pool_v, n_slots, slot_cap, n_questions);
+  if (st != KEV_OK) return st;
+  const int sms = num_sms_of_current_device();
+  if (sms <= 0) return KEV_ERR_CUDA;
+  st = kev_build_segments(intervals, n_questions, total_tokens, slot_ids, n_slots, slot_cap, shape, workspace,
+                          workspace_bytes, dev_status, stream);
+  if (st != KEV_OK) return st;
+  AuxArgs x;
+  x.k = k;
+  x.v = v;
+  x.out = nullptr;
+  x.intervals = intervals;
+  x.slot_ids = slot_ids;
+  x.pool_k = pool_k;
+  x.pool_v = pool_v;
+  x.n = n_questions;
+  x.T = total_tokens;
+  x.h_q = shape->h_q;
+  x.h_kv = shape->h_kv;
+  x.cap = slot_cap;
+  x.row_bytes = shape->d_h * elem_size(shape);
+  x.ws = static_cast<const char*>(workspace);
+  x.layout = prefill_layout(n_questions, total_tokens, shape->h_q);
+  return from_cuda(launch_aux(x, sms, (cudaStream_t)stream));
+}
+
+size_t kev_decode_workspace_size(int32_t n_questions, int32_t slot_cap, const kev_attn_shape* shape) {
+  if (check_shape(shape) != KEV_OK || n_questions < 0 || slot_cap <= 0 || n_questions > kMaxQuestions) return 0;
+  return decode_layout(n_questions, slot_cap, shape->h_q, shape->h_kv, shape->d_h).total;
+}
+
+kev_status kev_decode_attn(const void* q_new, const void* k_new, const void* v_new, void* pool_k, void* pool_v,
+                           int32_t n_slots, int32_t slot_cap, const int32_t* slot_ids, const int32_t* lens,
+                           const uint8_t* active, int32_t n_questions, void* out, const kev_attn_shape* shape,
+                           void* workspace, size_t workspace_bytes, int32_t* dev_status, kev_stream_t stream) {
+  kev_status st = check_shape(shape);
+  if (st != KEV_OK) return st;
+  if (n_questions < 0 || n_slots <= 0 || slot_cap <= 0) return KEV_ERR_INVALID_ARG;
+  if (n_questions > kMaxQuestions) return KEV_ERR_UNSUPPORTED;
+  if (dev_status && ((uintptr_t)dev_status & 3u)) return KEV_ERR_INVALID_ARG;
+  if (n_questions == 0) {
+    if (dev_status) return from_cuda(cudaMemsetAsync(dev_status, 0, sizeof(int32_t), (cudaStream_t)stream));
+    return KEV_OK;
+  }
+  if (!q_new || !k_new || !v_new || !pool_k || !pool_v || !out || !slot_ids || !lens || !active)
+    return KEV_ERR_INVALID_ARG;
+  if (!aligned16(q_new) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(pool_k) || !aligned16(pool_v) ||
+      !aligned16(out) || ((uintptr_t)slot_ids & 3u) || ((uintptr_t)lens & 3u))
+    return KEV_ERR_INVALID_ARG;
+  const DecodeLayout layout = decode_layout(n_questions, slot_cap, shape->h_q, shape->h_kv, shape->d_h);
+  if (!workspace || ((uintptr_t)workspace & 255u) || workspace_bytes < layout.total) return KEV_ERR_INVALID_ARG;
+  const int sms = num_sms_of_current_device();
+  if (sms <= 0) return KEV_ERR_CUDA;
+  DecodeArgs a;
+  a.q_new = q_new;
+  a.k_new = k_new;
+  a.v_new = v_new;
+  a.pool_k = pool_k;
+  a.pool_v = pool_v;
+  a.slot_ids = slot_ids;
+  a.lens = lens;
+  a.active = active;
+  a.out = out;
+  a.n = n_questions;
+  a.n_slots = n_slots;
+  a.cap = slot_cap;
+  a.h_q = shape->h_q;
+  a.h_kv = shape->h_kv;
+  a.group = shape->h_q / shape->h_kv;
+  a.scale = effective_scale(shape);
+  a.ws = static_cast<char*>(workspace);
+  a.layout = layout;
+  a.dev_status = dev_status;
+  return from_cuda(launch_decode(a, shape->d_h, (kev_dtype)shape->dtype, sms, (cudaStream_t)stream));
+}
+
+kev_status kev_decode_advance(int32_t* lens, const uint8_t* active, int32_t n, kev_stream_t stream) {
+  if (n < 0) return KEV_ERR_INVALID_ARG;
+  if (n == 0) return KEV_OK;
+  if (!lens || !active || ((uintptr_t)lens & 3u)) return KEV_ERR_INVALID_ARG;
+  return from_cuda(launch_advance(lens, active, n, (cudaStream_t)stream));
+}
+
+kev_status kev_read_status(const int32_t* dev_status, kev_stream_t stream) {
+  if (!dev_status) return KEV_ERR_INVALID_ARG;
+  if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return KEV_ERR_CUDA;
+  int32_t h = 0;
+  if (cudaMemcpy(&h, dev_status, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) return KEV_ERR_CUDA;
+  if (h < KEV_OK || h > KEV_ERR_CUDA) return KEV_ERR_CUDA;
+  return (kev_status)h;
+}
+
+const char* kev_status_string(kev_status s) {
+  switch (s) {
+    case KEV_OK: return "ok";
+    case KEV_ERR_INVALID_ARG: return "invalid argument (null/misaligned pointer, bad size or workspace too small)";
+    case KEV_ERR_UNSUPPORTED: return "unsupported dtype, head dim or group size";
+    case KEV_ERR_INTERVALS: return "intervals reversed, outside [0,T] or overlapping";
+    case KEV_ERR_SLOT: return "slot id out of range or shared by two live questions";
+    case KEV_ERR_SLOT_OVERFLOW: return "question longer than slot capacity or no room for the decode row";
+    case KEV_ERR_TIMEOUT: return "a bounded device wait gave up";
+    case KEV_ERR_CUDA: return "CUDA runtime error";
+  }
+  return "unknown status";
+}
+
+int32_t kev_launch_count(int32_t entry_point) {
+  switch (entry_point) {
+    case 0: return 3;  // segments, attention, slot write / gap zero
+    case 1: return 2;  // attention, slot write / gap zero
+    case 2: return 1;
+    case 3: return 2;  // segments, slot write
+    case 4: return 1;
+    case 5: return 1;
+  }
+  return -1;
+}
+
+}  // extern "C"

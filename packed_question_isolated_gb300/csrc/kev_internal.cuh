@@ -1,0 +1,204 @@
+// Internal declarations shared by the translation units of libkev (not part of the ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "../../include/kev.h"
+
+namespace kev {
+
+// Query rows (and key rows) per prefill tile.  Tiles are laid out per question starting at
+// the question's first token, so every key tile of a query tile lies inside its question.
+constexpr int kTileM = 128;
+// Upper bound on questions per call (the segment builder keeps them in shared memory).
+constexpr int kMaxQuestions = 4096;
+// Cost bins of the longest-first ordering: tile m (m+1 key tiles) goes to bin min(m, 63).
+constexpr int kCostBins = 64;
+// Positions per decode work item (split-K chunk).
+constexpr int kDecodeChunk = 256;
+
+// Device status codes: same values as kev_status.
+enum : int32_t {
+  ST_OK = 0,
+  ST_INTERVALS = KEV_ERR_INTERVALS,
+  ST_SLOT = KEV_ERR_SLOT,
+  ST_OVERFLOW = KEV_ERR_SLOT_OVERFLOW,
+  ST_TIMEOUT = KEV_ERR_TIMEOUT,
+};
+
+// ---------------------------------------------------------------------------------------
+// prefill workspace
+// ---------------------------------------------------------------------------------------
+struct PrefillHeader {
+  int32_t status;       // result of validation (and of bounded waits, if any gave up)
+  int32_t n_items;      // work items emitted
+  int32_t n_tiles;      // query tiles emitted
+  int32_t n_gaps;       // ranges of tokens that belong to no question
+  int32_t sched;        // dynamic-scheduling counter (reset by the segment builder)
+  int32_t n_questions;
+  int32_t total_tokens;
+  int32_t h_q;
+};
+
+struct PrefillLayout {
+  size_t cu_seqlens;  // int32[N+1]
+  size_t tiles;       // int2[max_tiles]  {question, m}
+  size_t items;       // int4[max_items]  {question, row_begin, rows, head}
+  size_t gaps;        // int2[N+1]        [begin, end)
+  size_t total;
+  int64_t max_tiles;
+  int64_t max_items;
+};
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+inline PrefillLayout prefill_layout(int32_t n, int32_t T, int32_t h_q) {
+  PrefillLayout L;
+  size_t off = align_up(sizeof(PrefillHeader), 256);
+  L.max_tiles = (int64_t)((T + kTileM - 1) / kTileM) + n;
+  L.max_items = L.max_tiles * (int64_t)h_q;
+  L.cu_seqlens = off;
+  off = align_up(off + sizeof(int32_t) * (size_t)(n + 1), 256);
+  L.tiles = off;
+  off = align_up(off + sizeof(int2) * (size_t)L.max_tiles, 256);
+  L.items = off;
+  off = align_up(off + sizeof(int4) * (size_t)L.max_items, 256);
+  L.gaps = off;
+  off = align_up(off + sizeof(int2) * (size_t)(n + 1), 256);
+  L.total = off;
+  return L;
+}
+
+// ---------------------------------------------------------------------------------------
+// decode workspace
+// ---------------------------------------------------------------------------------------
+struct DecodeLayout {
+  size_t counters;  // int32[N * H_kv]  arrivals per (question, kv head); left at zero
+  size_t partials;  // float[N * H_kv * max_chunks * G * (d + 2)]
+  size_t total;
+  int32_t max_chunks;
+};
+
+inline DecodeLayout decode_layout(int32_t n, int32_t cap, int32_t h_q, int32_t h_kv, int32_t d) {
+  DecodeLayout L;
+  L.max_chunks = (cap + kDecodeChunk - 1) / kDecodeChunk;
+  const int32_t G = h_q / h_kv;
+  size_t off = 0;
+  L.counters = off;
+  off = align_up(off + sizeof(int32_t) * (size_t)n * h_kv, 256);
+  L.partials = off;
+  off = align_up(off + sizeof(float) * (size_t)n * h_kv * L.max_chunks * G * (d + 2), 256);
+  L.total = off;
+  return L;
+}
+
+// ---------------------------------------------------------------------------------------
+// launch argument blocks
+// ---------------------------------------------------------------------------------------
+struct SegmentsArgs {
+  const kev_interval* intervals;
+  const int32_t* slot_ids;  // may be null
+  int32_t n;
+  int32_t T;
+  int32_t n_slots;
+  int32_t cap;
+  int32_t h_q;
+  char* ws;
+  PrefillLayout layout;
+  int32_t* dev_status;  // may be null
+};
+
+struct PrefillArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  void* out;
+  const kev_interval* intervals;
+  int32_t T;
+  int32_t n;
+  int32_t h_q;
+  int32_t h_kv;
+  int32_t group;  // h_q / h_kv
+  float scale;
+  const char* ws;
+  PrefillLayout layout;
+  int32_t* dev_status;
+};
+
+struct AuxArgs {  // slot write + zero rows of tokens in no question
+  const void* k;
+  const void* v;
+  void* out;  // may be null (slot write only)
+  const kev_interval* intervals;
+  const int32_t* slot_ids;  // may be null (gap zeroing only)
+  void* pool_k;
+  void* pool_v;
+  int32_t n;
+  int32_t T;
+  int32_t h_q;
+  int32_t h_kv;
+  int32_t cap;
+  int32_t row_bytes;  // d * element size
+  const char* ws;
+  PrefillLayout layout;
+};
+
+struct DecodeArgs {
+  const void* q_new;
+  const void* k_new;
+  const void* v_new;
+  void* pool_k;
+  void* pool_v;
+  const int32_t* slot_ids;
+  const int32_t* lens;
+  const uint8_t* active;
+  void* out;
+  int32_t n;
+  int32_t n_slots;
+  int32_t cap;
+  int32_t h_q;
+  int32_t h_kv;
+  int32_t group;
+  float scale;
+  char* ws;
+  DecodeLayout layout;
+  int32_t* dev_status;
+};
+
+// Host-side launchers (each returns the launch's cudaError_t).
+cudaError_t launch_segments(const SegmentsArgs& a, cudaStream_t s);
+cudaError_t launch_prefill_simt(const PrefillArgs& a, int d, kev_dtype dt, int num_sms, cudaStream_t s);
+cudaError_t launch_aux(const AuxArgs& a, int num_sms, cudaStream_t s);
+cudaError_t launch_decode(const DecodeArgs& a, int d, kev_dtype dt, int num_sms, cudaStream_t s);
+cudaError_t launch_advance(int32_t* lens, const uint8_t* active, int32_t n, cudaStream_t s);
+
+// ---------------------------------------------------------------------------------------
+// device helpers
+// ---------------------------------------------------------------------------------------
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+template <typename T> __device__ __forceinline__ T from_f32(float x);
+template <> __device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
+  return __float2bfloat16_rn(x);
+}
+
+__device__ __forceinline__ float warp_max(float x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+  return x;
+}
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+  return x;
+}
+
+// First error wins; later kernels of the call read the word and write nothing.
+__device__ __forceinline__ void set_status(int32_t* word, int32_t code) {
+  if (word) atomicCAS(word, 0, code);
+}
+
+}  // namespace kev

@@ -1,0 +1,96 @@
+// Packed prefill attention on the CUDA cores (float32 path).
+//
+// Exact attention, Z = softmax(QK^T / sqrt(d_h) + M) V (inference-engine notes,
+// sakurs2.com, §2.1), with M the causal AND block-diagonal mask of the Kev articles
+// (icman.com.cn §2.3, gsyq.cn §2.2) applied as a key range: row t of question i reads keys
+// [begin_i, t] only.  Keys are taken 32 at a time with the online softmax of the notes'
+// §2.4 (running max m, sum l, rescale alpha = exp(m_old - m_new)).
+//
+// Work: one CTA of 4 warps per item of the segment builder's list (question, 128-row tile,
+// q-head); warp w takes rows w, w+4, ...  Inside a 32-key block lane j owns key j for the
+// score and dims [j*D/32, (j+1)*D/32) for the output accumulator.
+#include "kev_internal.cuh"
+
+namespace kev {
+namespace {
+
+constexpr int kWarps = 4;
+
+template <typename T, int D>
+__global__ void __launch_bounds__(kWarps * 32) prefill_simt_kernel(PrefillArgs a) {
+  constexpr int PER = D / 32;
+  __shared__ float q_s[kWarps][D];
+  const PrefillHeader* hdr = reinterpret_cast<const PrefillHeader*>(a.ws);
+  if (hdr->status != ST_OK) return;
+  const int n_items = hdr->n_items;
+  const int4* items = reinterpret_cast<const int4*>(a.ws + a.layout.items);
+  const T* __restrict__ Q = static_cast<const T*>(a.q);
+  const T* __restrict__ K = static_cast<const T*>(a.k);
+  const T* __restrict__ V = static_cast<const T*>(a.v);
+  T* __restrict__ O = static_cast<T*>(a.out);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t q_row = (int64_t)a.h_q * D, kv_row = (int64_t)a.h_kv * D;
+
+  for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
+    const int4 item = items[it];
+    const int seg_begin = a.intervals[item.x].begin;
+    const int h = item.w, g = h / a.group;
+    for (int r = warp; r < item.z; r += kWarps) {
+      const int t = item.y + r;
+      __syncwarp();
+      for (int c = lane; c < D; c += 32) q_s[warp][c] = to_f32(Q[(int64_t)t * q_row + (int64_t)h * D + c]);
+      __syncwarp();
+      float m = -INFINITY, l = 0.f;
+      float acc[PER];
+#pragma unroll
+      for (int e = 0; e < PER; ++e) acc[e] = 0.f;
+      for (int kb = seg_begin; kb <= t; kb += 32) {
+        const int key = kb + lane;
+        float s = -INFINITY;
+        if (key <= t) {
+          const T* kr = K + (int64_t)key * kv_row + (int64_t)g * D;
+          float dot = 0.f;
+#pragma unroll 8
+          for (int c = 0; c < D; ++c) dot = fmaf(q_s[warp][c], to_f32(kr[c]), dot);
+          s = dot * a.scale;
+        }
+        const float m_new = fmaxf(m, warp_max(s));
+        const float alpha = expf(m - m_new);  // m = -inf on the first block gives 0
+        const float p = (key <= t) ? expf(s - m_new) : 0.f;
+        l = l * alpha + warp_sum(p);
+#pragma unroll
+        for (int e = 0; e < PER; ++e) acc[e] *= alpha;
+        const int nk = min(32, t - kb + 1);
+        for (int j = 0; j < nk; ++j) {
+          const float pj = __shfl_sync(0xffffffffu, p, j);
+          const T* vr = V + (int64_t)(kb + j) * kv_row + (int64_t)g * D + lane * PER;
+#pragma unroll
+          for (int e = 0; e < PER; ++e) acc[e] = fmaf(pj, to_f32(vr[e]), acc[e]);
+        }
+        m = m_new;
+      }
+      const float inv = 1.f / l;
+      T* orow = O + (int64_t)t * q_row + (int64_t)h * D + lane * PER;
+#pragma unroll
+      for (int e = 0; e < PER; ++e) orow[e] = from_f32<T>(acc[e] * inv);
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_prefill_simt(const PrefillArgs& a, int d, kev_dtype dt, int num_sms, cudaStream_t s) {
+  const int64_t max_items = a.layout.max_items;
+  if (max_items == 0) return cudaSuccess;
+  const int grid = (int)(max_items < (int64_t)num_sms * 16 ? max_items : (int64_t)num_sms * 16);
+  if (dt == KEV_FP32) {
+    if (d == 64) prefill_simt_kernel<float, 64><<<grid, kWarps * 32, 0, s>>>(a);
+    else prefill_simt_kernel<float, 128><<<grid, kWarps * 32, 0, s>>>(a);
+  } else {
+    if (d == 64) prefill_simt_kernel<__nv_bfloat16, 64><<<grid, kWarps * 32, 0, s>>>(a);
+    else prefill_simt_kernel<__nv_bfloat16, 128><<<grid, kWarps * 32, 0, s>>>(a);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace kev

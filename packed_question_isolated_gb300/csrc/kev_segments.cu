@@ -1,0 +1,252 @@
+// Segment descriptors: validation, cu_seqlens, gap list and the longest-first work list.
+//
+// The block-diagonal mask of the Kev architecture article (icman.com.cn news 75864, §2.1,
+// §2.3) is never materialised: a question's intervals become tiles of 128 query rows, and
+// tile m of a question is paired only with key tiles 0..m of the same question (the causal
+// lower triangle of its own diagonal block).  This is the varlen "cu_seqlens" form the
+// article moves to for long inputs (§5.2, §6.4), extended to a tile work list.
+//
+// One CTA of 1024 threads; at most kMaxQuestions questions.
+#include "kev_internal.cuh"
+
+namespace kev {
+namespace {
+
+constexpr int kThreads = 1024;
+
+// In-place ascending bitonic sort of `n2` (power of two) keys in shared memory.
+__device__ void bitonic_sort(unsigned long long* key, int n2) {
+  for (int k = 2; k <= n2; k <<= 1) {
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      for (int i = threadIdx.x; i < n2; i += blockDim.x) {
+        const int p = i ^ j;
+        if (p > i) {
+          const bool up = (i & k) == 0;
+          const unsigned long long a = key[i], b = key[p];
+          if ((a > b) == up) {
+            key[i] = b;
+            key[p] = a;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  }
+}
+
+__device__ int block_exclusive_scan(int v, int* tmp /* [kThreads/32 + 1] */, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) tmp[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    const int nw = blockDim.x >> 5;
+    int w = lane < nw ? tmp[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    if (lane < nw) tmp[lane] = w;  // inclusive warp totals
+  }
+  __syncthreads();
+  const int base = warp > 0 ? tmp[warp - 1] : 0;
+  const int r = base + x - v;
+  if (total) *total = tmp[(blockDim.x >> 5) - 1];
+  __syncthreads();
+  return r;
+}
+
+__global__ void __launch_bounds__(kThreads) segments_kernel(SegmentsArgs a) {
+  __shared__ unsigned long long keys[kMaxQuestions];
+  __shared__ int s_flags;  // bit 0 intervals, bit 1 slot range, bit 2 overflow, bit 3 duplicate slot
+  __shared__ int scan_tmp[kThreads / 32 + 1];
+  __shared__ int bin_count[kCostBins];
+  __shared__ int bin_cursor[kCostBins];
+  __shared__ int s_ngaps;
+
+  PrefillHeader* hdr = reinterpret_cast<PrefillHeader*>(a.ws);
+  int32_t* cu = reinterpret_cast<int32_t*>(a.ws + a.layout.cu_seqlens);
+  int2* tiles = reinterpret_cast<int2*>(a.ws + a.layout.tiles);
+  int4* items = reinterpret_cast<int4*>(a.ws + a.layout.items);
+  int2* gaps = reinterpret_cast<int2*>(a.ws + a.layout.gaps);
+
+  const int n = a.n;
+  const int tid = threadIdx.x;
+  if (tid == 0) s_flags = 0;
+  if (tid < kCostBins) bin_count[tid] = 0;
+  __syncthreads();
+
+  // 1. per-question range checks
+  for (int i = tid; i < n; i += blockDim.x) {
+    const kev_interval iv = a.intervals[i];
+    if (!(iv.begin >= 0 && iv.begin <= iv.end && iv.end <= a.T)) atomicOr(&s_flags, 1);
+    if (a.slot_ids) {
+      const int s = a.slot_ids[i];
+      if (s < 0 || s >= a.n_slots) atomicOr(&s_flags, 2);
+      if (iv.end - iv.begin > a.cap) atomicOr(&s_flags, 4);
+    }
+  }
+  __syncthreads();
+
+  int n2 = 1;
+  while (n2 < n) n2 <<= 1;
+
+  // 2. overlap: sort non-empty intervals by begin, neighbours must not intersect
+  if ((s_flags & 1) == 0 && n > 1) {
+    for (int i = tid; i < n2; i += blockDim.x) {
+      unsigned long long kk = ~0ull;
+      if (i < n) {
+        const kev_interval iv = a.intervals[i];
+        if (iv.end > iv.begin) kk = ((unsigned long long)(unsigned)iv.begin << 32) | (unsigned)iv.end;
+      }
+      keys[i] = kk;
+    }
+    __syncthreads();
+    bitonic_sort(keys, n2);
+    for (int i = tid + 1; i < n; i += blockDim.x) {
+      const unsigned long long cur = keys[i], prev = keys[i - 1];
+      if (cur != ~0ull && prev != ~0ull) {
+        if ((unsigned)(cur >> 32) < (unsigned)(prev & 0xffffffffu)) atomicOr(&s_flags, 1);
+      }
+    }
+    __syncthreads();
+  } else {
+    for (int i = tid; i < n2; i += blockDim.x) {
+      unsigned long long kk = ~0ull;
+      if (i < n) {
+        const kev_interval iv = a.intervals[i];
+        if (iv.end > iv.begin) kk = ((unsigned long long)(unsigned)iv.begin << 32) | (unsigned)iv.end;
+      }
+      keys[i] = kk;
+    }
+    __syncthreads();
+  }
+
+  // 3. gaps: tokens in no interval, from the begin-sorted intervals
+  if ((s_flags & 1) == 0 && tid == 0) {
+    int ng = 0;
+    int pos = 0;
+    for (int i = 0; i < n; ++i) {
+      const unsigned long long kk = keys[i];
+      if (kk == ~0ull) break;
+      const int b = (int)(kk >> 32), e = (int)(kk & 0xffffffffu);
+      if (b > pos) gaps[ng++] = make_int2(pos, b);
+      pos = e;
+    }
+    if (pos < a.T) gaps[ng++] = make_int2(pos, a.T);
+    s_ngaps = ng;
+  }
+  __syncthreads();
+
+  // 4. duplicate slots among non-empty questions
+  if (a.slot_ids && s_flags == 0 && n > 1) {
+    for (int i = tid; i < n2; i += blockDim.x) {
+      unsigned long long kk = ~0ull;
+      if (i < n) {
+        const kev_interval iv = a.intervals[i];
+        if (iv.end > iv.begin) kk = (unsigned long long)(unsigned)a.slot_ids[i];
+      }
+      keys[i] = kk;
+    }
+    __syncthreads();
+    bitonic_sort(keys, n2);
+    for (int i = tid + 1; i < n; i += blockDim.x) {
+      if (keys[i] != ~0ull && keys[i] == keys[i - 1]) atomicOr(&s_flags, 8);
+    }
+    __syncthreads();
+  }
+
+  const int f = s_flags;
+  const int code = (f & 1) ? ST_INTERVALS : (f & 2) ? ST_SLOT : (f & 4) ? ST_OVERFLOW : (f & 8) ? ST_SLOT : ST_OK;
+  if (code != ST_OK) {
+    if (tid == 0) {
+      hdr->status = code;
+      hdr->n_items = 0;
+      hdr->n_tiles = 0;
+      hdr->n_gaps = 0;
+      hdr->sched = 0;
+      hdr->n_questions = n;
+      hdr->total_tokens = a.T;
+      hdr->h_q = a.h_q;
+      if (a.dev_status) *a.dev_status = code;
+    }
+    return;
+  }
+
+  // 5. cu_seqlens (lengths in interval order) and per-question tile counts
+  int total_len = 0;
+  for (int base = 0; base < n; base += blockDim.x) {
+    const int i = base + tid;
+    const int L = i < n ? a.intervals[i].end - a.intervals[i].begin : 0;
+    int blk_total;
+    const int off = block_exclusive_scan(L, scan_tmp, &blk_total);
+    if (i < n) cu[i] = total_len + off;
+    total_len += blk_total;
+  }
+  if (tid == 0) cu[n] = total_len;
+
+  // 6. tile histogram over cost bins, then longest-first placement
+  for (int i = tid; i < n; i += blockDim.x) {
+    const int L = a.intervals[i].end - a.intervals[i].begin;
+    const int nt = (L + kTileM - 1) / kTileM;
+    for (int m = 0; m < nt; ++m) atomicAdd(&bin_count[m < kCostBins ? m : kCostBins - 1], 1);
+  }
+  __syncthreads();
+  if (tid == 0) {
+    int acc = 0;
+    for (int b = kCostBins - 1; b >= 0; --b) {
+      bin_cursor[b] = acc;
+      acc += bin_count[b];
+    }
+    hdr->n_tiles = acc;
+    hdr->n_items = acc * a.h_q;
+  }
+  __syncthreads();
+  for (int i = tid; i < n; i += blockDim.x) {
+    const int L = a.intervals[i].end - a.intervals[i].begin;
+    const int nt = (L + kTileM - 1) / kTileM;
+    for (int m = nt - 1; m >= 0; --m) {
+      const int pos = atomicAdd(&bin_cursor[m < kCostBins ? m : kCostBins - 1], 1);
+      tiles[pos] = make_int2(i, m);
+    }
+  }
+  __syncthreads();
+
+  // 7. expand tiles into (tile, head) items; the heads of one tile stay adjacent so the
+  //    q-heads that share a kv-head run close together in time (L2 reuse of K/V tiles).
+  const int n_tiles = hdr->n_tiles;
+  const long long n_items = (long long)n_tiles * a.h_q;
+  for (long long k = tid; k < n_items; k += blockDim.x) {
+    const int t = (int)(k / a.h_q);
+    const int h = (int)(k % a.h_q);
+    const int2 tl = tiles[t];
+    const kev_interval iv = a.intervals[tl.x];
+    const int r0 = iv.begin + tl.y * kTileM;
+    const int rows = min(kTileM, iv.end - r0);
+    items[k] = make_int4(tl.x, r0, rows, h);
+  }
+  if (tid == 0) {
+    hdr->status = ST_OK;
+    hdr->n_gaps = s_ngaps;
+    hdr->sched = 0;
+    hdr->n_questions = n;
+    hdr->total_tokens = a.T;
+    hdr->h_q = a.h_q;
+    if (a.dev_status) *a.dev_status = ST_OK;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_segments(const SegmentsArgs& a, cudaStream_t s) {
+  segments_kernel<<<1, kThreads, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace kev

@@ -1,0 +1,70 @@
+"""CPU checks of the C ABI: the library loads, exports every declared symbol, and host-side
+argument checks answer without a GPU (no compute call is made here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from packed_question_isolated_gb300 import build
+    build.build()
+    import packed_question_isolated_gb300 as kev
+    return kev
+
+
+def _declared():
+    text = open(os.path.join(ROOT, "include", "kev.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(kev_[a-z_]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    so = ctypes.CDLL(lib.library_path())
+    declared = _declared()
+    assert len(declared) >= 12
+    for name in declared:
+        assert hasattr(so, name), f"{name} declared in kev.h but not exported"
+    assert set(declared) == set(lib.binding.EXPORTED)
+
+
+def test_status_strings_and_launch_counts(lib):
+    for code in range(8):
+        assert lib.kev_status_string(code)
+    assert lib.kev_status_string(99) == "unknown status"
+    assert lib.kev_launch_count(0) == 3 and lib.kev_launch_count(4) == 1 and lib.kev_launch_count(9) == -1
+
+
+def test_workspace_sizes(lib):
+    s = lib.make_shape(28, 4, 128, "bf16")
+    n, T = 8, 7921
+    sz = lib.kev_prefill_workspace_size(n, T, s)
+    max_tiles = (T + 127) // 128 + n
+    assert sz >= max_tiles * 28 * 16 + max_tiles * 8 + (n + 1) * 4
+    assert lib.kev_prefill_workspace_size(n, T, lib.make_shape(28, 5, 128)) == 0   # H_q % H_kv
+    assert lib.kev_prefill_workspace_size(n, T, lib.make_shape(28, 4, 96)) == 0    # d_h
+    assert lib.kev_prefill_workspace_size(5000, T, s) == 0                          # too many questions
+    d = lib.kev_decode_workspace_size(64, 2458, lib.make_shape(32, 8, 128))
+    assert d >= 64 * 8 * 4 + 64 * 8 * ((2458 + 255) // 256) * 4 * 130 * 4
+
+
+def test_host_argument_errors_without_gpu(lib):
+    b = lib.binding
+    s = lib.make_shape(4, 2, 64, "bf16")
+    # null workspace / misaligned pointers / bad shape are refused before any CUDA call
+    assert lib.kev_build_segments(None, 1, 10, None, 0, 0, s, None, 0, None, stream=0, check=False) == \
+        b.KEV_ERR_INVALID_ARG
+    assert lib.kev_prefill_attn(0x1000, 0x1000, 0x1000, 10, 0x1000, 1, None, None, None, 0, 0, 0x1000,
+                                lib.make_shape(4, 3, 64), 0x1000, 1 << 20, None, stream=0, check=False) == \
+        b.KEV_ERR_UNSUPPORTED
+    assert lib.kev_prefill_attn(0x1000, 0x1000, 0x1000, 10, 0x1000, 1, None, None, None, 0, 0, 0x1000,
+                                s, 0x1010, 1 << 20, None, stream=0, check=False) == b.KEV_ERR_INVALID_ARG
+    assert lib.kev_decode_attn(0x1000, 0x1000, 0x1000, 0x1000, 0x1000, 1, 0, 0x1000, 0x1000, 0x1000, 1, 0x1000,
+                               s, 0x1000, 1 << 20, None, stream=0, check=False) == b.KEV_ERR_INVALID_ARG
+    assert lib.kev_decode_advance(None, None, -1, stream=0, check=False) == b.KEV_ERR_INVALID_ARG
+    with pytest.raises(b.KevError):
+        lib.kev_decode_advance(None, None, -1, stream=0)

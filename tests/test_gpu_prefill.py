@@ -1,0 +1,158 @@
+"""GPU parity of prefill (segments, attention, slot write) against the CPU oracle."""
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from oracle import kev_oracle as O
+
+from kev_harness import PrefillRun, compare, f64, host
+
+pytestmark = pytest.mark.gpu
+
+
+def _oracle_out(w):
+    return O.prefill(W.to_float64(w.q, w.dtype), W.to_float64(w.k, w.dtype), W.to_float64(w.v, w.dtype),
+                     w.intervals, scale=w.scale or None)
+
+
+def _check_pools(run, w):
+    pk0, pv0 = host(run.pool_k0), host(run.pool_v0)
+    ek, ev = O.slot_write(pk0, pv0, w.k, w.v, w.intervals, w.slot_ids)
+    assert np.array_equal(host(run.pool_k), ek), "pool_k differs from the oracle's bit copy"
+    assert np.array_equal(host(run.pool_v), ev), "pool_v differs from the oracle's bit copy"
+
+
+def test_tiny_fp32_config_full_parity():
+    w = W.tiny_fp32()
+    run = PrefillRun(w)
+    run.run()
+    assert run.device_status() == 0
+    compare(f64(run.out, w.dtype), _oracle_out(w), w.dtype, "tiny fp32 prefill")
+    _check_pools(run, w)
+
+
+CASES = [
+    # lengths, h_q, h_kv, d, dtype, gaps, tail
+    ([300, 129, 1, 0, 517], 8, 2, 128, "bf16", [0, 3, 0, 5, 1], 7),
+    ([128, 256, 127, 383], 4, 4, 128, "bf16", None, 0),
+    ([200, 77, 640], 7, 1, 128, "bf16", [2, 0, 1], 3),
+    ([65, 190, 3, 129], 8, 2, 64, "bf16", [1, 1, 1, 1], 1),
+    ([40, 7, 130], 4, 2, 64, "fp32", [0, 2, 1], 2),
+    ([256, 5], 2, 1, 128, "fp32", None, 0),
+]
+
+
+@pytest.mark.parametrize("case", range(len(CASES)))
+def test_random_cases_full_parity(case):
+    lengths, h_q, h_kv, d, dtype, gaps, tail = CASES[case]
+    w = W.random_case(300 + case, lengths, h_q, h_kv, d, dtype, gaps=gaps, tail=tail, permute_slots=True,
+                      n_slots=len(lengths) + 2)
+    run = PrefillRun(w)
+    run.run()
+    assert run.device_status() == 0
+    ref = _oracle_out(w)
+    got = f64(run.out, w.dtype)[:w.total_tokens]
+    compare(got, ref, dtype, f"case {case}")
+    seg = O.segment_ids(w.intervals, w.total_tokens)
+    assert (got[seg < 0] == 0).all(), "rows of tokens in no question must be 0"
+    _check_pools(run, w)
+
+
+def test_unsorted_interval_order_and_no_slot_write():
+    w = W.random_case(77, [90, 300, 12, 150], 8, 2, 128, "bf16", gaps=[3, 0, 2, 0], order=[2, 0, 3, 1])
+    run = PrefillRun(w, slots=False)
+    run.run()
+    assert run.device_status() == 0
+    compare(f64(run.out, w.dtype), _oracle_out(w), w.dtype, "unsorted")
+
+
+def test_qwen25_7b_config_every_question_against_oracle():
+    w = W.qwen25_7b_prefill()
+    run = PrefillRun(w)
+    run.run()
+    assert run.device_status() == 0
+    got = f64(run.out, w.dtype)
+    q, k, v = (W.to_float64(x, w.dtype) for x in (w.q, w.k, w.v))
+    for (s, e) in w.intervals:
+        # invariant (b) of the oracle: the packed rows of a question equal the question alone
+        ref = O.prefill(q[s:e], k[s:e], v[s:e], [(0, e - s)])
+        compare(got[s:e], ref, w.dtype, f"question [{s},{e})")
+    _check_pools(run, w)
+
+
+def test_qwen3_8b_config_sampled_rows_and_pools():
+    w = W.qwen3_8b_prefill()
+    run = PrefillRun(w)
+    run.run()
+    assert run.device_status() == 0
+    got = f64(run.out, w.dtype)
+    q, k, v = (W.to_float64(x, w.dtype) for x in (w.q, w.k, w.v))
+    rng = np.random.default_rng(0)
+    rows = set(rng.choice(w.total_tokens, 40, replace=False).tolist())
+    for s, e in w.intervals:           # first, last and a tile-boundary row of each question
+        rows.update({int(s), int(e - 1), int(min(e - 1, s + 128))})
+    rows = sorted(rows)
+    ref = O.prefill_rows(q, k, v, w.intervals, rows)
+    compare(got[rows], ref, w.dtype, "sampled rows")
+    # whole short questions
+    for s, e in w.intervals:
+        if e - s <= 300:
+            ref = O.prefill(q[s:e], k[s:e], v[s:e], [(0, e - s)])
+            compare(got[s:e], ref, w.dtype, f"question [{s},{e})")
+    _check_pools(run, w)
+
+
+def test_deterministic_and_isolated_bitwise():
+    """Same call twice gives identical bits; a question's rows do not depend on its neighbours
+    or on where it sits in the packed sequence (segment-local tiling)."""
+    w = W.random_case(88, [150, 260, 33, 129], 8, 2, 128, "bf16", gaps=[0, 1, 0, 2])
+    a = PrefillRun(w, slots=False)
+    a.run()
+    first = host(a.out).copy()
+    a.run()
+    assert np.array_equal(first, host(a.out))
+    for i, (s, e) in enumerate(w.intervals):
+        alone = W.Workload(name="alone", seed=0, dtype=w.dtype, h_q=w.h_q, h_kv=w.h_kv, d=w.d,
+                           lengths=np.array([e - s], np.int32), intervals=np.array([[5, 5 + e - s]], np.int32),
+                           total_tokens=int(e - s + 9), q=np.concatenate([w.q[:5], w.q[s:e], w.q[:4]]),
+                           k=np.concatenate([w.k[:5], w.k[s:e], w.k[:4]]),
+                           v=np.concatenate([w.v[:5], w.v[s:e], w.v[:4]]),
+                           slot_ids=np.array([0], np.int32), n_slots=1, cap=int(e - s))
+        b = PrefillRun(alone, slots=False)
+        b.run()
+        assert np.array_equal(host(b.out)[5:5 + e - s], first[s:e]), f"question {i} not bitwise isolated"
+
+
+def test_work_list_covers_exactly_the_allowed_tiles():
+    import packed_question_isolated_gb300 as kev
+    w = W.random_case(99, [300, 1, 0, 129, 128, 257], 4, 2, 64, "bf16", gaps=[0, 2, 1, 0, 3, 1], tail=5)
+    run = PrefillRun(w)
+    run.run()
+    items, n = kev.kev_read_work_list(run.ws, run.ws_bytes, 100000)
+    assert n == len(items)
+    T = w.total_tokens
+    allowed = O.allowed_mask(w.intervals, T)
+    covered = np.zeros((w.h_q, T, T), dtype=np.int32)
+    costs = []
+    for (qi, r0, rows, h) in items:
+        s, e = w.intervals[qi]
+        assert s <= r0 and r0 + rows <= e and 0 < rows <= 128 and (r0 - s) % 128 == 0
+        # key range of the item: [s, r0 + rows)
+        blk = allowed[r0:r0 + rows, s:r0 + rows]
+        assert blk.any(), "an item with no allowed entry was scheduled"
+        covered[h, r0:r0 + rows, s:r0 + rows] += 1
+        costs.append((r0 - s) // 128 + 1)
+    for h in range(w.h_q):
+        assert (covered[h][allowed] == 1).all(), "allowed entry not covered exactly once"
+        assert (covered[h] <= 1).all()
+    assert costs == sorted(costs, reverse=True), "items are not ordered longest first"
+
+
+def test_empty_batch_and_all_empty_questions():
+    w = W.random_case(5, [0, 0], 4, 2, 64, "bf16", gaps=[3, 2], tail=1)
+    run = PrefillRun(w)
+    run.run()
+    assert run.device_status() == 0
+    assert (f64(run.out, w.dtype)[:w.total_tokens] == 0).all()
+    _check_pools(run, w)
