@@ -1,0 +1,401 @@
+"""Benchmark of the packed, question-isolated attention hot path on GB300.
+
+One step = the whole hot path over one batch of 8 Qwen2.5-7B-shaped questions
+(lengths U{256..2048}, T = 7921, H_q 28 / H_kv 4, d 128, bf16, slot cap 2458):
+segment build + prefill attention + slot write + one decode step of every
+question, all through the C ABI of libkev.  The headline value is useful
+prefill TFLOP/s over the whole step (sum_i 2 d H_q L_i (L_i + 1) per step).
+Decode GB/s is measured on its own workload (64-slot pool of cap 2458, 32 of
+64 questions live) and reported in the same JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+With torchrun, every rank runs its own batch (questions are independent:
+weak scaling, no collective on the data path); rank 0 prints one JSON line.
+``--impl reference`` times the CPU oracle (dense-mask fp64 attention) on a
+bounded sample of the same workload on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+from packed_question_isolated_gb300 import roofline as RL  # noqa: E402
+
+METRIC = "prefill useful TFLOP/s & decode HBM GB/s vs GB300 roofline, 1 GPU"
+WORKLOAD = ("qwen25_7b_prefill: 8 questions, lengths U{256..2048} seed 2 (T=7921), H_q 28, H_kv 4, d 128, bf16, "
+            "slot cap 2458; step = segment build + prefill attention + slot write + 1 decode step per question")
+DECODE_WORKLOAD = ("qwen3_8b_decode: [64, 8, 2458, 128] bf16 pools, lens U{64..2400} seed 4, 32 of 64 questions "
+                   "live, 1 new token each")
+FLUSH_BYTES = 512 << 20   # > 2 x L2 (129 MB)
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), float(p.get("bf16_tflops_sustained", 0)), "measured"
+    except Exception:
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def _traffic(kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel source is unchanged."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    for line in open(path):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        fields = dict(kv.split("=", 1) for kv in line.split() if "=" in kv)
+        if fields.get("kernel") != kernel:
+            continue
+        src = os.path.join(ROOT, "packed_question_isolated_gb300", "csrc", fields.get("source", ""))
+        if not os.path.exists(src):
+            return None
+        h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        if h != fields.get("sha"):
+            return None
+        return float(fields["bytes_per_launch"])
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled in the background."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"kev_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                                          "-i", str(self.gpu), "-lms", "100"], stdout=open(self.path, "w"),
+                                         stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        time.sleep(0.2)
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        mx = max(r[1] for r in rows)
+        load = [r for r in rows if r[0] > 0.5 * mx] or rows
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[j] for r in load for j, v in enumerate(r[2]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in load), "sm_max_mhz": mx, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------------------
+# CPU oracle legs (bounded samples)
+# ---------------------------------------------------------------------------------------
+
+_W_CACHE = {}
+
+
+def _oracle_sample(heads):
+    """Time the oracle's dense-mask prefill for the given q-heads over the whole packed batch."""
+    from oracle import kev_oracle as O
+    if "w" not in _W_CACHE:
+        _W_CACHE["w"] = W.qwen25_7b_prefill()
+    w = _W_CACHE["w"]
+    G = w.h_q // w.h_kv
+    kv_heads = sorted({h // G for h in heads})
+    q = W.to_float64(w.q[:, heads], "bf16")
+    k = W.to_float64(w.k[:, kv_heads], "bf16")
+    v = W.to_float64(w.v[:, kv_heads], "bf16")
+    # keep the GQA mapping of the sampled heads: a sample of G' q-heads per kv head
+    t0 = time.perf_counter()
+    O.prefill(q, k, v, w.intervals)
+    dt = time.perf_counter() - t0
+    flops = RL.prefill_useful_flops(w.lengths, len(heads), w.d)
+    return flops, dt
+
+
+def cpu_baseline(heads=(0, 1, 2, 3)):
+    heads = list(heads)
+    flops, dt = _oracle_sample(heads)
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"oracle dense-mask fp64 prefill of q-heads {heads[0]}-{heads[-1]} (of 28, kv-head 0) "
+                      f"over the full 8-question packed batch (T=7921); {dt:.2f} s"}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    heads = [0]
+    for _ in range(args.warmup):
+        _oracle_sample(heads)
+    times = []
+    flops = 0.0
+    for _ in range(args.steps):
+        f, dt = _oracle_sample(heads)
+        flops += f
+        times.append(dt)
+    total = sum(times)
+    value = flops / total / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "sample": "q-head 0 of 28 per step"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+                         "sample": "oracle dense-mask fp64 prefill of q-head 0 over the full packed batch "
+                                   "(T=7921), one per step"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------------------
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="kev", choices=["kev", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import torch
+    import torch.distributed as dist
+    import packed_question_isolated_gb300 as kev
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream()
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    def tdev(a):
+        t = torch.from_numpy(np.ascontiguousarray(a))
+        return (t.view(torch.bfloat16) if a.dtype == np.uint16 else t).to(dev)
+
+    # ---- main workload -----------------------------------------------------------------
+    w = W.qwen25_7b_prefill()
+    shape = kev.make_shape(w.h_q, w.h_kv, w.d, "bf16")
+    N, T = w.n_questions, w.total_tokens
+    q, k, v = tdev(w.q), tdev(w.k), tdev(w.v)
+    iv = tdev(w.intervals)
+    slots = tdev(w.slot_ids)
+    out = torch.empty((T, w.h_q, w.d), dtype=torch.bfloat16, device=dev)
+    pool_k = torch.zeros((w.n_slots, w.h_kv, w.cap, w.d), dtype=torch.bfloat16, device=dev)
+    pool_v = torch.zeros_like(pool_k)
+    ws_bytes = kev.kev_prefill_workspace_size(N, T, shape)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    q_new, k_new, v_new = tdev(w.q_new), tdev(w.k_new), tdev(w.v_new)
+    lens = tdev(w.lengths)
+    active = torch.ones(N, dtype=torch.uint8, device=dev)
+    o_new = torch.empty((N, w.h_q, w.d), dtype=torch.bfloat16, device=dev)
+    dws_bytes = kev.kev_decode_workspace_size(N, w.cap, shape)
+    dws = torch.zeros(dws_bytes, dtype=torch.uint8, device=dev)
+    dstatus = torch.zeros(1, dtype=torch.int32, device=dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    launches_per_step = kev.kev_launch_count(2) + kev.kev_launch_count(1) + kev.kev_launch_count(4)
+
+    def step(ev_a=None, ev_b=None, bufs=None):
+        qq, kk, vv, ivv, sl, qn, kn, vn, ln, act, oo, on = bufs or (q, k, v, iv, slots, q_new, k_new, v_new, lens,
+                                                                  active, out, o_new)
+        kev.kev_build_segments(ivv, N, T, sl, w.n_slots, w.cap, shape, ws, ws_bytes, status)
+        if ev_a is not None:
+            ev_a.record()
+        kev.kev_prefill_from_segments(qq, kk, vv, T, ivv, N, sl, pool_k, pool_v, w.n_slots, w.cap, oo, shape, ws,
+                                      ws_bytes, status)
+        if ev_b is not None:
+            ev_b.record()
+        kev.kev_decode_attn(qn, kn, vn, pool_k, pool_v, w.n_slots, w.cap, sl, ln, act, N, on, shape, dws,
+                            dws_bytes, dstatus)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    assert kev.kev_read_status(status) == 0 and kev.kev_read_status(dstatus) == 0
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    torch.cuda.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        for s in range(K):
+            flush.zero_()
+            ev[s][0].record()
+            step(ev[s][1], ev[s][2])
+            ev[s][3].record()
+        torch.cuda.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    step_ms = [ev[s][0].elapsed_time(ev[s][3]) for s in range(K)]
+    attn_ms = [ev[s][1].elapsed_time(ev[s][2]) for s in range(K)]
+    total_ms = float(sum(step_ms))
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    useful = RL.prefill_useful_flops(w.lengths, w.h_q, w.d)
+    value = useful * K * world / (total_ms * 1e-3) / 1e12
+    hbm_peak, tf_peak, tf_sust, peak_src = _peaks()
+    attn_avg_ms = statistics.mean(attn_ms)
+    achieved = useful / (attn_avg_ms * 1e-3) / 1e12
+    traffic = _traffic("prefill")
+
+    # ---- e2e: host buffers, copies inside the timed region ------------------------------
+    def pinned(t):
+        return t.cpu().pin_memory()
+    h_in = [pinned(x) for x in (q, k, v, iv, slots, q_new, k_new, v_new, lens, active)]
+    d_in = [torch.empty_like(x) for x in (q, k, v, iv, slots, q_new, k_new, v_new, lens, active)]
+    h_out = [torch.empty(out.shape, dtype=out.dtype, pin_memory=True),
+             torch.empty(o_new.shape, dtype=o_new.dtype, pin_memory=True)]
+    d_out = [torch.empty_like(out), torch.empty_like(o_new)]
+    h2d = sum(x.numel() * x.element_size() for x in h_in)
+    d2h = sum(x.numel() * x.element_size() for x in h_out)
+
+    def e2e_step():
+        for hd, dd in zip(h_in, d_in):
+            dd.copy_(hd, non_blocking=True)
+        step(bufs=(*d_in, *d_out))
+        for hd, dd in zip(h_out, d_out):
+            hd.copy_(dd, non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e_step()
+    torch.cuda.synchronize()
+    Ke = max(5, K // 2)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    e0.record()
+    for _ in range(Ke):
+        e2e_step()
+    e1.record()
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_value = useful * Ke * world / (e2e_ms * 1e-3) / 1e12
+
+    # ---- decode workload ----------------------------------------------------------------
+    dwl = W.qwen3_8b_decode()
+    dshape = kev.make_shape(dwl.h_q, dwl.h_kv, dwl.d, "bf16")
+    dpk, dpv = tdev(dwl.pool_k), tdev(dwl.pool_v)
+    dsl, dln, dact = tdev(dwl.slot_ids), tdev(dwl.lens), tdev(dwl.active)
+    dq, dk, dv = tdev(dwl.q_new), tdev(dwl.k_new), tdev(dwl.v_new)
+    dout = torch.empty((dwl.n_questions, dwl.h_q, dwl.d), dtype=torch.bfloat16, device=dev)
+    d_bytes = kev.kev_decode_workspace_size(dwl.n_questions, dwl.cap, dshape)
+    d_ws = torch.zeros(d_bytes, dtype=torch.uint8, device=dev)
+
+    def dstep():
+        kev.kev_decode_attn(dq, dk, dv, dpk, dpv, dwl.n_slots, dwl.cap, dsl, dln, dact, dwl.n_questions, dout,
+                            dshape, d_ws, d_bytes, dstatus)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        dstep()
+    torch.cuda.synchronize()
+    assert kev.kev_read_status(dstatus) == 0
+    Kd = max(10, K)
+    dev_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(Kd)]
+    for s in range(Kd):
+        flush.zero_()
+        dev_ev[s][0].record()
+        dstep()
+        dev_ev[s][1].record()
+    torch.cuda.synchronize()
+    dec_ms = statistics.mean(a.elapsed_time(b) for a, b in dev_ev)
+    dec_bytes = RL.decode_bytes(dwl.lens, dwl.active, dwl.h_q, dwl.h_kv, dwl.d, 2)
+    dec_gbs = dec_bytes / (dec_ms * 1e-3) / 1e9
+    dec_traffic = _traffic("decode")
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline()
+
+    if rank == 0:
+        clocks = clk.summary()
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": K,
+            "warmup": args.warmup, "ms_per_step": total_ms / K, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "questions_per_gpu": N, "total_tokens_per_gpu": T,
+                       "useful_gflop_per_step": useful / 1e9, "l2": "flushed (512 MB write) before every step",
+                       "parallelism": f"replicas x{world} (independent question batches)"},
+            "clocks": clocks,
+            "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "ms_per_step": e2e_ms / Ke},
+            "gpu_launches": launches_per_step * K,
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": tf_peak, "unit": "TFLOP/s",
+                         "frac": achieved / tf_peak, "traffic": traffic,
+                         "kernel": "prefill attention (kev_prefill_from_segments)",
+                         "peak_source": f"bf16_tflops burst, {peak_src}", "launch_ms": attn_avg_ms},
+            "decode": {"workload": DECODE_WORKLOAD, "value": dec_gbs, "unit": "GB/s", "ms_per_step": dec_ms,
+                       "roofline": {"bound": "hbm", "achieved": dec_gbs, "peak": hbm_peak, "unit": "GB/s",
+                                    "frac": dec_gbs / hbm_peak, "traffic": dec_traffic,
+                                    "algorithmic_bytes": dec_bytes, "peak_source": f"hbm_gbs, {peak_src}"}},
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
