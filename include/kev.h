@@ -14,8 +14,9 @@
  * Conventions shared by every entry point
  * ---------------------------------------
  *  - Every tensor pointer is caller-owned DEVICE memory, contiguous, 16-byte aligned.
- *    The library allocates nothing and keeps no mutable global state, so calls on
- *    different streams with different buffers are independent.  The cache is passed in
+ *    The library allocates nothing and keeps no mutable global state (the one exception is
+ *    the fixed scratch of kev_decode_attn_static, below), so calls on different streams
+ *    with different buffers are independent.  The cache is passed in
  *    and out as an argument, never held by the library (KV-cache isolation article,
  *    hnwysp.cn news 130224, §3.3 and §4.3).
  *  - Everything is enqueued on `stream`; no entry point synchronises the host except
@@ -168,6 +169,27 @@ kev_status kev_decode_attn(const void* q_new, const void* k_new, const void* v_n
                            int32_t n_questions, void* out, const kev_attn_shape* shape,
                            void* workspace, size_t workspace_bytes, int32_t* dev_status,
                            kev_stream_t stream);
+
+/* Size of the scratch area compiled into the library for kev_decode_attn_static (16 MiB). */
+#define KEV_STATIC_SCRATCH_BYTES (16u << 20)
+
+/* kev_decode_attn without a caller-provided workspace.  The pages have no counterpart: this is
+ * a library-level convenience for callers that cannot allocate device memory (a plugin inside a
+ * framework that owns the whole device-memory budget and hands out no allocator, or a
+ * latency-critical path where cudaMalloc/cudaFree and their device synchronisation are not
+ * allowed).  Same arguments, results and errors as kev_decode_attn, minus the workspace.
+ * Scratch: a fixed device array of KEV_STATIC_SCRATCH_BYTES inside the library, held by every
+ * GPU that loads it until the process exits.  Calls needing more scratch than that
+ * (kev_decode_workspace_size(...) > KEV_STATIC_SCRATCH_BYTES) return KEV_ERR_UNSUPPORTED and
+ * launch nothing.  The first call on a device looks up the array's device address and clears
+ * it (in stream order), so make that first call before any stream capture.  Every call shares
+ * the array: calls that overlap on the GPU race on it and give wrong results.  Allocates
+ * nothing (no cudaMalloc/cudaFree, no allocating library routine). */
+kev_status kev_decode_attn_static(const void* q_new, const void* k_new, const void* v_new,
+                                  void* pool_k, void* pool_v, int32_t n_slots, int32_t slot_cap,
+                                  const int32_t* slot_ids, const int32_t* lens, const uint8_t* active,
+                                  int32_t n_questions, void* out, const kev_attn_shape* shape,
+                                  int32_t* dev_status, kev_stream_t stream);
 
 /* lens[i] += (active[i] != 0) for i < n, on the device (no host synchronisation), so a
  * decode loop can be captured in a CUDA graph. */

@@ -43,7 +43,7 @@ EXPORTED = [
     "kev_prefill_workspace_size", "kev_build_segments", "kev_read_work_list",
     "kev_prefill_from_segments", "kev_prefill_attn", "kev_kv_write",
     "kev_decode_workspace_size", "kev_decode_attn", "kev_decode_advance",
-    "kev_read_status", "kev_status_string", "kev_launch_count",
+    "kev_read_status", "kev_status_string", "kev_launch_count", "kev_decode_attn_static",
 ]
 
 
@@ -84,6 +84,8 @@ _c = {
     "kev_decode_workspace_size": _sig("kev_decode_workspace_size", _Z, _I, _I, _S),
     "kev_decode_attn": _sig("kev_decode_attn", _I, _P, _P, _P, _P, _P, _I, _I, _P, _P, _P, _I, _P, _S,
                             _P, _Z, _P, _P),
+    "kev_decode_attn_static": _sig("kev_decode_attn_static", _I, _P, _P, _P, _P, _P, _I, _I, _P, _P, _P, _I,
+                                   _P, _S, _P, _P),
     "kev_decode_advance": _sig("kev_decode_advance", _I, _P, _P, _I, _P),
     "kev_read_status": _sig("kev_read_status", _I, _P, _P),
     "kev_status_string": _sig("kev_status_string", ctypes.c_char_p, _I),
@@ -210,6 +212,21 @@ def kev_decode_attn(q_new, k_new, v_new, pool_k, pool_v, n_slots, slot_cap, slot
                                _ptr(out), ctypes.byref(s), _ptr(workspace), int(workspace_bytes),
                                _ptr(dev_status), _stream(stream))
     return _check(st, "kev_decode_attn", check)
+
+
+KEV_STATIC_SCRATCH_BYTES = 16 << 20
+
+
+def kev_decode_attn_static(q_new, k_new, v_new, pool_k, pool_v, n_slots, slot_cap, slot_ids, lens, active,
+                           n_questions, out, shape, dev_status=None, stream=None, check=True) -> int:
+    """kev_decode_attn with the library's fixed scratch instead of a caller workspace (for
+    callers that cannot allocate device memory); calls that overlap on the GPU race."""
+    s = _shape(shape)
+    st = _c["kev_decode_attn_static"](_ptr(q_new), _ptr(k_new), _ptr(v_new), _ptr(pool_k), _ptr(pool_v),
+                                      int(n_slots), int(slot_cap), _ptr(slot_ids), _ptr(lens), _ptr(active),
+                                      int(n_questions), _ptr(out), ctypes.byref(s), _ptr(dev_status),
+                                      _stream(stream))
+    return _check(st, "kev_decode_attn_static", check)
 
 
 def kev_decode_advance(lens, active, n, stream=None, check=True) -> int:
