@@ -146,7 +146,8 @@ kev_status kev_prefill_from_segments(const void* q, const void* k, const void* v
   p.ws = static_cast<const char*>(workspace);
   p.layout = layout;
   p.dev_status = dev_status;
-  cudaError_t e = launch_prefill_simt(p, shape->d_h, (kev_dtype)shape->dtype, sms, s);
+  cudaError_t e = shape->dtype == KEV_BF16 ? launch_prefill_tc(p, shape->d_h, sms, s)
+                                            : launch_prefill_simt(p, shape->d_h, sms, s);
   if (e != cudaSuccess) return KEV_ERR_CUDA;
 
   AuxArgs x;

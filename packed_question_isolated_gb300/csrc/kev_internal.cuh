@@ -169,7 +169,8 @@ struct DecodeArgs {
 
 // Host-side launchers (each returns the launch's cudaError_t).
 cudaError_t launch_segments(const SegmentsArgs& a, cudaStream_t s);
-cudaError_t launch_prefill_simt(const PrefillArgs& a, int d, kev_dtype dt, int num_sms, cudaStream_t s);
+cudaError_t launch_prefill_simt(const PrefillArgs& a, int d, int num_sms, cudaStream_t s);  // fp32
+cudaError_t launch_prefill_tc(const PrefillArgs& a, int d, int num_sms, cudaStream_t s);    // bf16
 cudaError_t launch_aux(const AuxArgs& a, int num_sms, cudaStream_t s);
 cudaError_t launch_decode(const DecodeArgs& a, int d, kev_dtype dt, int num_sms, cudaStream_t s);
 cudaError_t launch_advance(int32_t* lens, const uint8_t* active, int32_t n, cudaStream_t s);

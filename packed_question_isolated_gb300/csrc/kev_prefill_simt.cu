@@ -1,4 +1,4 @@
-// Packed prefill attention on the CUDA cores (float32 path).
+// Packed prefill attention on the CUDA cores (the float32 path: true fp32 FMA, no TF32).
 //
 // Exact attention, Z = softmax(QK^T / sqrt(d_h) + M) V (inference-engine notes,
 // sakurs2.com, §2.1), with M the causal AND block-diagonal mask of the Kev articles
@@ -79,17 +79,12 @@ __global__ void __launch_bounds__(kWarps * 32) prefill_simt_kernel(PrefillArgs a
 
 }  // namespace
 
-cudaError_t launch_prefill_simt(const PrefillArgs& a, int d, kev_dtype dt, int num_sms, cudaStream_t s) {
+cudaError_t launch_prefill_simt(const PrefillArgs& a, int d, int num_sms, cudaStream_t s) {
   const int64_t max_items = a.layout.max_items;
   if (max_items == 0) return cudaSuccess;
   const int grid = (int)(max_items < (int64_t)num_sms * 16 ? max_items : (int64_t)num_sms * 16);
-  if (dt == KEV_FP32) {
-    if (d == 64) prefill_simt_kernel<float, 64><<<grid, kWarps * 32, 0, s>>>(a);
-    else prefill_simt_kernel<float, 128><<<grid, kWarps * 32, 0, s>>>(a);
-  } else {
-    if (d == 64) prefill_simt_kernel<__nv_bfloat16, 64><<<grid, kWarps * 32, 0, s>>>(a);
-    else prefill_simt_kernel<__nv_bfloat16, 128><<<grid, kWarps * 32, 0, s>>>(a);
-  }
+  if (d == 64) prefill_simt_kernel<float, 64><<<grid, kWarps * 32, 0, s>>>(a);
+  else prefill_simt_kernel<float, 128><<<grid, kWarps * 32, 0, s>>>(a);
   return cudaGetLastError();
 }
 
