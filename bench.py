@@ -192,6 +192,26 @@ def run_reference(args):
 # GPU arm
 # ---------------------------------------------------------------------------------------
 
+def _decode_only(args, kev, torch, dev, tdev, flush):
+    """Warm-up and timed loop of the decode workload alone (profiling aid)."""
+    dwl = W.qwen3_8b_decode()
+    dshape = kev.make_shape(dwl.h_q, dwl.h_kv, dwl.d, "bf16")
+    dpk, dpv = tdev(dwl.pool_k), tdev(dwl.pool_v)
+    dsl, dln, dact = tdev(dwl.slot_ids), tdev(dwl.lens), tdev(dwl.active)
+    dq, dk, dv = tdev(dwl.q_new), tdev(dwl.k_new), tdev(dwl.v_new)
+    dout = torch.empty((dwl.n_questions, dwl.h_q, dwl.d), dtype=torch.bfloat16, device=dev)
+    d_bytes = kev.kev_decode_workspace_size(dwl.n_questions, dwl.cap, dshape)
+    d_ws = torch.zeros(d_bytes, dtype=torch.uint8, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    for _ in range(args.warmup + args.steps):
+        flush.zero_()
+        kev.kev_decode_attn(dq, dk, dv, dpk, dpv, dwl.n_slots, dwl.cap, dsl, dln, dact, dwl.n_questions, dout,
+                            dshape, d_ws, d_bytes, st)
+    torch.cuda.synchronize()
+    assert kev.kev_read_status(st) == 0
+    return None
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -199,6 +219,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="kev", choices=["kev", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", choices=["step", "decode"], default=None,
+                    help="run only one workload's warm-up and timed loop (for profiling); prints no JSON line")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
@@ -262,11 +284,19 @@ def main(argv=None):
         kev.kev_decode_attn(qn, kn, vn, pool_k, pool_v, w.n_slots, w.cap, sl, ln, act, N, on, shape, dws,
                             dws_bytes, dstatus)
 
+    if args.only == "decode":
+        return _decode_only(args, kev, torch, dev, tdev, flush)
     for _ in range(args.warmup):
         flush.zero_()
         step()
     torch.cuda.synchronize()
     assert kev.kev_read_status(status) == 0 and kev.kev_read_status(dstatus) == 0
+    if args.only == "step":
+        for _ in range(args.steps):
+            flush.zero_()
+            step()
+        torch.cuda.synchronize()
+        return None
 
     K = args.steps
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]

@@ -6,36 +6,141 @@
 // a question with active[i] == 0 is removed from the step -- it contributes no work item,
 // so its slot is neither read nor written.
 //
-// One launch.  Every CTA first runs the same prologue over the N questions (validation,
-// per-question chunk counts, prefix sum of work items: the compacted list of live
-// (question, kv-head, chunk) items), so no second launch or grid-wide wait is needed.
-// Items are chunks of kDecodeChunk positions of one (question, kv head); a CTA computes
-// the partial (m, l, o) of all G q-heads of the group for its chunk.  When a (question,
-// kv head) has several chunks, the CTA that arrives last (atomic counter) merges the
-// partials in chunk order, so the result does not depend on timing.
+// One launch, one persistent CTA per SM.  Every CTA first runs the same prologue over the N
+// questions: validation of the live questions and a prefix sum of their work items, which
+// is the compacted list of live (question, kv head, head block, chunk) items -- so no second
+// launch or grid-wide wait is needed.  A chunk is kChunk consecutive positions of one slot;
+// its K rows and its V rows are each one contiguous range of the pool and are streamed into
+// shared memory with single bulk copies (TMA, 1-D), double buffered: while the eight warps
+// work on chunk x, the copies of chunk x+1 are in flight.
+//
+// Eight compute warps per CTA, for the G q-heads that share the kv head (up to 8 per item):
+//   scores   half a warp per K row, lane l holding 8 dims of the row and the same 8 dims of
+//            every query in registers; the 16 partial dot products of 4 rows are combined
+//            with a shuffle reduce-scatter (5 shuffles per head for 4 rows);
+//   softmax  one warp per head: max, exp2 and sum over the chunk's rows;
+//   PV       16 lanes across the 128 dims x 16 row groups; packed fp32x2 FMAs; the row
+//            groups are summed with shuffles and one pass through shared memory.
+// When a (question, kv head) has several chunks, the CTA that finishes last (arrival
+// counter) merges the chunk results in chunk order, so the output does not depend on timing.
 #include "kev_internal.cuh"
+#include "kev_sm100.cuh"
 
 namespace kev {
 namespace {
 
-constexpr int kWarps = 4;
-constexpr int kThreads = kWarps * 32;
-constexpr int kGMax = 16;
+using namespace sm100;
 
-struct DecodeSmem {
-  int item_base[kMaxQuestions + 1];  // prefix of work items over questions (dropped: 0 items)
-  int hash[2 * kMaxQuestions];       // live slot ids, open addressing
-  float q[kGMax][128];               // the group's queries in fp32
-  float wm[kWarps][kGMax];
-  float wl[kWarps][kGMax];
-  float wo[kWarps][kGMax][128];
+constexpr int kComputeWarps = 8;
+constexpr int kComputeThreads = kComputeWarps * 32;
+constexpr int kThreads = kComputeThreads;  // thread 0 also issues the bulk copies
+constexpr int kChunk = kDecodeChunk;            // rows per work item
+constexpr int kMaxStages = 3;
+constexpr int kHB = 8;                          // q-heads per item at most
+constexpr long long kDrainBudget = 4000000000ll;
+
+template <int D, int EB, int GT, int NS>
+struct DSmem {
+  static constexpr int kRowBytes = D * EB;
+  static constexpr int kQBytes = kHB * kRowBytes;                       // the item's queries
+  static constexpr int kStageBytes = 2 * kChunk * kRowBytes + kQBytes;  // K rows, V rows, queries
+  static constexpr int kStages = NS;                                    // stage ring depth
+  static constexpr int kStage = 0;
+  static constexpr int kS = kStage + kStages * kStageBytes;   // float [GT][kChunk]  scores
+  static constexpr int kP = kS + GT * kChunk * 4;             // float [kChunk][GT]  weights
+  static constexpr int kRed = kP + kChunk * GT * 4;           // float [4][GT][D]    cross-warp sums
+  static constexpr int kStat = kRed + 4 * GT * D * 4;         // float m[kHB], l[kHB], alpha[kHB]
+  static constexpr int kBar = kStat + 3 * kHB * 4;            // DBars
+  static constexpr int kBase = kBar + 128;                    // int item_base[N + 1], then int2 meta[N]
+  // total for N questions
+  static __host__ __device__ constexpr int bytes(int n) { return kBase + ((n + 2) / 2) * 8 + n * 8; }
+  static __host__ __device__ constexpr int meta_off(int n) { return kBase + ((n + 2) / 2) * 8; }
+};
+
+struct DBars {
+  uint64_t full[kMaxStages];
   int flags;
-  int scan_tmp[kWarps + 1];
   int last;
+  int abort;
+  int never;
+  int scan_tmp[(kThreads + 31) / 32];
+};
+
+__device__ __forceinline__ void named_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kComputeThreads) : "memory");
+}
+// Barrier over the compute warps that also ANDs a flag across them (a uniform decision).
+__device__ __forceinline__ bool named_sync_and(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, 1, %2, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)v), "n"(kComputeThreads)
+      : "memory");
+  return r != 0;
+}
+
+__device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ unsigned long long f2pack(float a, float b) {
+  return (unsigned long long)__float_as_uint(a) | ((unsigned long long)__float_as_uint(b) << 32);
+}
+__device__ __forceinline__ float2 unpack2(unsigned long long v) {
+  return make_float2(__uint_as_float((uint32_t)v), __uint_as_float((uint32_t)(v >> 32)));
+}
+__device__ __forceinline__ unsigned long long fma2(unsigned long long a, unsigned long long b, unsigned long long c) {
+  unsigned long long d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+// bf16 pair (low element first) -> packed fp32 pair, exact
+__device__ __forceinline__ unsigned long long bf2_to_f2(uint32_t w) {
+  return (unsigned long long)(w << 16) | ((unsigned long long)(w & 0xffff0000u) << 32);
+}
+
+// Element access for both storage types: 8 consecutive elements as 4 packed fp32 pairs.
+template <typename T> struct Elem;
+template <> struct Elem<__nv_bfloat16> {
+  static constexpr int kBytes = 2;
+  __device__ static __forceinline__ void load8(const unsigned char* p, unsigned long long (&o)[4]) {
+    const uint4 w = *reinterpret_cast<const uint4*>(p);
+    o[0] = bf2_to_f2(w.x);
+    o[1] = bf2_to_f2(w.y);
+    o[2] = bf2_to_f2(w.z);
+    o[3] = bf2_to_f2(w.w);
+  }
+  __device__ static __forceinline__ void store(void* base, int64_t idx, float v) {
+    static_cast<__nv_bfloat16*>(base)[idx] = __float2bfloat16_rn(v);
+  }
+  __device__ static __forceinline__ float load(const void* base, int64_t idx) {
+    return __bfloat162float(static_cast<const __nv_bfloat16*>(base)[idx]);
+  }
+};
+template <> struct Elem<float> {
+  static constexpr int kBytes = 4;
+  __device__ static __forceinline__ void load8(const unsigned char* p, unsigned long long (&o)[4]) {
+    const uint4 a = *reinterpret_cast<const uint4*>(p);
+    const uint4 b = *reinterpret_cast<const uint4*>(p + 16);
+    o[0] = (unsigned long long)a.x | ((unsigned long long)a.y << 32);
+    o[1] = (unsigned long long)a.z | ((unsigned long long)a.w << 32);
+    o[2] = (unsigned long long)b.x | ((unsigned long long)b.y << 32);
+    o[3] = (unsigned long long)b.z | ((unsigned long long)b.w << 32);
+  }
+  __device__ static __forceinline__ void store(void* base, int64_t idx, float v) { static_cast<float*>(base)[idx] = v; }
+  __device__ static __forceinline__ float load(const void* base, int64_t idx) { return static_cast<const float*>(base)[idx]; }
 };
 
 __device__ int block_exclusive_scan(int v, int* tmp, int* total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  constexpr int nw = kThreads / 32;
   int x = v;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -46,7 +151,7 @@ __device__ int block_exclusive_scan(int v, int* tmp, int* total) {
   __syncthreads();
   int base = 0, tot = 0;
 #pragma unroll
-  for (int w = 0; w < kWarps; ++w) {
+  for (int w = 0; w < nw; ++w) {
     if (w < warp) base += tmp[w];
     tot += tmp[w];
   }
@@ -55,212 +160,455 @@ __device__ int block_exclusive_scan(int v, int* tmp, int* total) {
   return base + x - v;
 }
 
-template <typename T>
-__device__ __forceinline__ const T* kv_row_ptr(const DecodeArgs& a, const void* pool, const void* fresh, int slot,
-                                               int g, int pos, int n, int i, int D) {
-  if (pos == n) return static_cast<const T*>(fresh) + ((int64_t)i * a.h_kv + g) * D;
-  return static_cast<const T*>(pool) + (((int64_t)slot * a.h_kv + g) * a.cap + pos) * D;
+struct ItemInfo {
+  int i, g, hb, c, len, slot, nch, p0, p1, h0, nh;
+};
+
+// Decodes work chunk `x` (item_base: prefix over questions of H_kv * n_hblocks * n_chunks;
+// meta: {len, slot} per question, both in shared memory).
+__device__ __forceinline__ ItemInfo decode_item(const DecodeArgs& a, const int* item_base, const int2* meta, int x,
+                                                int n_hblocks) {
+  int lo = 0, hi = a.n;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (item_base[mid] <= x) lo = mid; else hi = mid;
+  }
+  ItemInfo f;
+  f.i = lo;
+  const int2 m = meta[lo];
+  f.len = m.x;
+  f.slot = m.y;
+  f.nch = (f.len + 1 + kChunk - 1) / kChunk;
+  const int r = x - item_base[lo];
+  f.c = r % f.nch;
+  const int gh = r / f.nch;
+  f.hb = gh % n_hblocks;
+  f.g = gh / n_hblocks;
+  f.p0 = f.c * kChunk;
+  f.p1 = min(f.p0 + kChunk, f.len + 1);
+  f.h0 = f.g * a.group + f.hb * kHB;
+  f.nh = min(kHB, a.group - f.hb * kHB);
+  return f;
 }
 
-template <typename T, int D>
-__global__ void __launch_bounds__(kThreads) decode_kernel(DecodeArgs a) {
-  constexpr int PER = D / 32;
-  extern __shared__ __align__(16) unsigned char smem_raw[];
-  DecodeSmem& S = *reinterpret_cast<DecodeSmem*>(smem_raw);
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int n = a.n, G = a.group;
+// Static split of the chunk space [0, total) into one contiguous range per CTA.
+__device__ __forceinline__ int range_start(int b, int total, int nb) { return (int)((int64_t)b * total / nb); }
+__device__ __forceinline__ int range_owner(int x, int total, int nb) {
+  return (int)((((int64_t)x + 1) * nb - 1) / total);
+}
 
-  // ---- prologue: validation (live questions only) ------------------------------------
+template <typename T, int D, int GT, int NS>
+__global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
+  using E = Elem<T>;
+  constexpr int EB = E::kBytes;
+  using L = DSmem<D, EB, GT, NS>;
+  constexpr int kRow = D * EB;  // bytes of one stored row
+  extern __shared__ __align__(128) unsigned char smem[];
+  DBars* bars = reinterpret_cast<DBars*>(smem + L::kBar);
+  int* item_base = reinterpret_cast<int*>(smem + L::kBase);
+  int2* meta = reinterpret_cast<int2*>(smem + L::meta_off(a.n));
+  int* hash = reinterpret_cast<int*>(smem + L::kStage);
+  float* sc = reinterpret_cast<float*>(smem + L::kS);
+  float* pw = reinterpret_cast<float*>(smem + L::kP);
+  float* red = reinterpret_cast<float*>(smem + L::kRed);
+  float* st_m = reinterpret_cast<float*>(smem + L::kStat);
+  float* st_l = st_m + kHB;
+  float* st_a = st_l + kHB;
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int n = a.n;
+  const int n_hblocks = (a.group + kHB - 1) / kHB;
+
+  // ---- prologue: validation of live questions -----------------------------------------
   int hs = 1;
   while (hs < 2 * n) hs <<= 1;
-  if (tid == 0) S.flags = 0;
-  for (int j = tid; j < hs; j += kThreads) S.hash[j] = -1;
+  if (tid == 0) {
+    bars->flags = 0;
+    bars->abort = 0;
+    bars->never = 0;
+  }
+  for (int j = tid; j < hs; j += kThreads) hash[j] = -1;
   __syncthreads();
   for (int i = tid; i < n; i += kThreads) {
-    if (!a.active[i]) continue;
+    const int live = a.active[i];
     const int slot = a.slot_ids[i];
     const int len = a.lens[i];
-    if (slot < 0 || slot >= a.n_slots) { atomicOr(&S.flags, 1); continue; }
-    if (len < 0 || len >= a.cap) atomicOr(&S.flags, 2);
+    meta[i] = make_int2(len, slot);
+    if (!live) continue;
+    if (slot < 0 || slot >= a.n_slots) {
+      atomicOr(&bars->flags, 1);
+      continue;
+    }
+    if (len < 0 || len >= a.cap) atomicOr(&bars->flags, 2);
     unsigned h = ((unsigned)slot * 2654435761u) & (unsigned)(hs - 1);
     for (int probe = 0; probe < hs; ++probe) {
-      const int prev = atomicCAS(&S.hash[h], -1, slot);
+      const int prev = atomicCAS(&hash[h], -1, slot);
       if (prev == -1) break;
-      if (prev == slot) { atomicOr(&S.flags, 4); break; }
+      if (prev == slot) {
+        atomicOr(&bars->flags, 4);
+        break;
+      }
       h = (h + 1) & (unsigned)(hs - 1);
     }
   }
   __syncthreads();
-  const int f = S.flags;
+  const int f = bars->flags;
   const int code = (f & 1) ? ST_SLOT : (f & 2) ? ST_OVERFLOW : (f & 4) ? ST_SLOT : ST_OK;
   if (blockIdx.x == 0 && tid == 0 && a.dev_status) *a.dev_status = code;
   if (code != ST_OK) return;
 
-  // ---- compacted work list: items of live questions only -----------------------------
+  // ---- compacted work list: chunks of live questions only ------------------------------
   int running = 0;
   for (int base = 0; base < n; base += kThreads) {
     const int i = base + tid;
     int cnt = 0;
-    if (i < n && a.active[i]) cnt = a.h_kv * ((a.lens[i] + 1 + kDecodeChunk - 1) / kDecodeChunk);
+    if (i < n && a.active[i]) cnt = a.h_kv * n_hblocks * ((meta[i].x + 1 + kChunk - 1) / kChunk);
     int tot;
-    const int off = block_exclusive_scan(cnt, S.scan_tmp, &tot);
-    if (i < n) S.item_base[i] = running + off;
+    const int off = block_exclusive_scan(cnt, bars->scan_tmp, &tot);
+    if (i < n) item_base[i] = running + off;
     running += tot;
   }
-  if (tid == 0) S.item_base[n] = running;
-  __syncthreads();
-  const int total_items = running;
+  if (tid == 0) {
+    item_base[n] = running;
+    for (int s = 0; s < L::kStages; ++s) {
+      mbar_init(&bars->full[s], 1);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();  // the hash is dead from here on: the stages may be written
+  const int total = running;
+  // at most one CTA per chunk, so that every CTA's range is non-empty and the CTAs that
+  // touch a (question, kv head) are exactly the owners of its first..last chunk
+  const int nb = min((int)gridDim.x, total);
+  if ((int)blockIdx.x >= nb) return;
+  const int x_begin = range_start(blockIdx.x, total, nb);
+  const int x_end = range_start(blockIdx.x + 1, total, nb);
+  volatile int* abort_flag = &bars->abort;
+  const volatile int* never = &bars->never;
+  const long long budget = 4000000000ll;
 
+  // Thread 0 issues the bulk copies of a chunk: K rows, V rows (positions already in the
+  // pool) and the item's queries, all counted on the stage's mbarrier.
+  uint32_t issued[kMaxStages] = {0, 0, 0};
+  auto issue = [&](int xx, int stage) {
+    const ItemInfo fi = decode_item(a, item_base, meta, xx, n_hblocks);
+    const int rows = min(fi.p1, fi.len) - fi.p0;  // the new row is not in the pool yet
+    const uint32_t bytes = (uint32_t)rows * kRow;
+    const uint32_t qbytes = (uint32_t)fi.nh * kRow;
+    unsigned char* dst = smem + L::kStage + stage * L::kStageBytes;
+    mbar_arrive_expect_tx(&bars->full[stage], 2 * bytes + qbytes);
+    if (rows > 0) {
+      const int64_t row0 = ((int64_t)fi.slot * a.h_kv + fi.g) * a.cap + fi.p0;
+      bulk_copy_g2s(dst, static_cast<const unsigned char*>(a.pool_k) + row0 * kRow, bytes, &bars->full[stage]);
+      bulk_copy_g2s(dst + kChunk * kRow, static_cast<const unsigned char*>(a.pool_v) + row0 * kRow, bytes,
+                    &bars->full[stage]);
+    }
+    bulk_copy_g2s(dst + 2 * kChunk * kRow,
+                  static_cast<const unsigned char*>(a.q_new) + ((int64_t)fi.i * a.h_q + fi.h0) * kRow, qbytes,
+                  &bars->full[stage]);
+    ++issued[stage];
+  };
+  if (L::kStages > 1 && tid == 0)
+    for (int k = 0; k < L::kStages - 1 && x_begin + k < x_end; ++k) issue(x_begin + k, k);
+
+  // ------------------------------------------------------------------ compute warps
   int* counters = reinterpret_cast<int*>(a.ws + a.layout.counters);
   float* partials = reinterpret_cast<float*>(a.ws + a.layout.partials);
-  const int pstride = G * (D + 2);
+  const int pstride = GT * (D + 2);
+  const int half = lane >> 4, hl = lane & 15;  // half-warp and lane inside it
+  constexpr int kDimL = D / 16;                // dims per lane in the score phase (8 or 4)
+  constexpr int kDG = D / 8;                   // 8-dim groups per row in the PV phase (16 or 8)
+  constexpr int kRG = kComputeThreads / kDG;   // PV row groups (16 or 32)
+  const int dg = tid % kDG, rg = tid / kDG;
+  unsigned long long o2[GT][4];               // this thread's share of the running output
+  uint32_t iter = 0;
 
-  for (int it = blockIdx.x; it < total_items; it += gridDim.x) {
-    // question owning item `it`: item_base[i] <= it < item_base[i+1]
-    int lo = 0, hi = n;
-    while (hi - lo > 1) {
-      const int mid = (lo + hi) >> 1;
-      if (S.item_base[mid] <= it) lo = mid; else hi = mid;
+  for (int x = x_begin; x < x_end; ++x, ++iter) {
+    const ItemInfo fi = decode_item(a, item_base, meta, x, n_hblocks);
+    if (L::kStages == 1) {  // single stage: refill it once every thread is done with it
+      named_sync();
+      if (tid == 0) issue(x, 0);
     }
-    const int i = lo;
-    const int len = a.lens[i];
-    const int slot = a.slot_ids[i];
-    const int nch = (len + 1 + kDecodeChunk - 1) / kDecodeChunk;
-    const int r = it - S.item_base[i];
-    const int g = r / nch, c = r % nch;
-    const int p0 = c * kDecodeChunk, p1 = min(p0 + kDecodeChunk, len + 1);
+    const int s = iter % L::kStages;
+    const uint32_t round = iter / L::kStages;
+    unsigned char* kst = smem + L::kStage + s * L::kStageBytes;
+    unsigned char* vst = kst + kChunk * kRow;
+    const unsigned char* qst = kst + 2 * kChunk * kRow;
+    const int nr = fi.p1 - fi.p0;  // rows of this chunk, the new row included
+    const bool piece_first = (x == x_begin) || fi.c == 0;
+    const bool piece_last = (x == x_end - 1) || fi.c == fi.nch - 1;
+    if (piece_first) {
+#pragma unroll
+      for (int g = 0; g < GT; ++g)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) o2[g][e] = 0ull;
+    }
 
-    // queries of the group's q-heads, fp32
-    const T* qsrc = static_cast<const T*>(a.q_new) + ((int64_t)i * a.h_q + (int64_t)g * G) * D;
-    for (int e = tid; e < G * D; e += kThreads) S.q[e / D][e % D] = to_f32(qsrc[e]);
-    // append the new row (only the chunk that holds position len does it)
-    if (p0 <= len && len < p1) {
-      const int64_t dst = (((int64_t)slot * a.h_kv + g) * a.cap + len) * D;
-      const int64_t src = ((int64_t)i * a.h_kv + g) * D;
-      for (int e = tid; e < D; e += kThreads) {
-        static_cast<T*>(a.pool_k)[dst + e] = static_cast<const T*>(a.k_new)[src + e];
-        static_cast<T*>(a.pool_v)[dst + e] = static_cast<const T*>(a.v_new)[src + e];
-      }
-    }
-    __syncthreads();
-
-    float m[kGMax], l[kGMax], acc[kGMax][PER];
-#pragma unroll
-    for (int gg = 0; gg < kGMax; ++gg) {
-      m[gg] = -INFINITY;
-      l[gg] = 0.f;
-#pragma unroll
-      for (int e = 0; e < PER; ++e) acc[gg][e] = 0.f;
-    }
-    for (int b0 = p0 + warp * 32; b0 < p1; b0 += kWarps * 32) {
-      const int pos = b0 + lane;
-      const bool valid = pos < p1;
-      float s[kGMax];
-#pragma unroll
-      for (int gg = 0; gg < kGMax; ++gg) s[gg] = 0.f;
-      if (valid) {
-        const T* kr = kv_row_ptr<T>(a, a.pool_k, a.k_new, slot, g, pos, len, i, D);
-        for (int cidx = 0; cidx < D; ++cidx) {
-          const float kv = to_f32(kr[cidx]);
-#pragma unroll
-          for (int gg = 0; gg < kGMax; ++gg)
-            if (gg < G) s[gg] = fmaf(S.q[gg][cidx], kv, s[gg]);
-        }
-      }
-      float p[kGMax];
-#pragma unroll
-      for (int gg = 0; gg < kGMax; ++gg) {
-        if (gg < G) {
-          const float sc = valid ? s[gg] * a.scale : -INFINITY;
-          const float m_new = fmaxf(m[gg], warp_max(sc));
-          const float alpha = expf(m[gg] - m_new);
-          p[gg] = valid ? expf(sc - m_new) : 0.f;
-          l[gg] = l[gg] * alpha + warp_sum(p[gg]);
-#pragma unroll
-          for (int e = 0; e < PER; ++e) acc[gg][e] *= alpha;
-          m[gg] = m_new;
-        }
-      }
-      const int nk = min(32, p1 - b0);
-      for (int j = 0; j < nk; ++j) {
-        const T* vr = kv_row_ptr<T>(a, a.pool_v, a.v_new, slot, g, b0 + j, len, i, D) + lane * PER;
-        float vv[PER];
-#pragma unroll
-        for (int e = 0; e < PER; ++e) vv[e] = to_f32(vr[e]);
-#pragma unroll
-        for (int gg = 0; gg < kGMax; ++gg) {
-          if (gg < G) {
-            const float pj = __shfl_sync(0xffffffffu, p[gg], j);
-#pragma unroll
-            for (int e = 0; e < PER; ++e) acc[gg][e] = fmaf(pj, vv[e], acc[gg][e]);
-          }
-        }
-      }
-    }
-    // combine the warps of the CTA
-#pragma unroll
-    for (int gg = 0; gg < kGMax; ++gg) {
-      if (gg < G) {
-        if (lane == 0) {
-          S.wm[warp][gg] = m[gg];
-          S.wl[warp][gg] = l[gg];
-        }
-#pragma unroll
-        for (int e = 0; e < PER; ++e) S.wo[warp][gg][lane * PER + e] = acc[gg][e];
-      }
-    }
-    __syncthreads();
-    float* part = partials + (((int64_t)i * a.h_kv + g) * a.layout.max_chunks + c) * pstride;
-    for (int e = tid; e < G * D; e += kThreads) {
-      const int gg = e / D, dd = e % D;
-      float M = -INFINITY;
-#pragma unroll
-      for (int w = 0; w < kWarps; ++w) M = fmaxf(M, S.wm[w][gg]);
-      float L = 0.f, O = 0.f;
-#pragma unroll
-      for (int w = 0; w < kWarps; ++w) {
-        const float sc = expf(S.wm[w][gg] - M);  // warps that saw no position: exp(-inf) = 0
-        L += S.wl[w][gg] * sc;
-        O += S.wo[w][gg][dd] * sc;
-      }
-      if (nch == 1) {
-        static_cast<T*>(a.out)[((int64_t)i * a.h_q + (int64_t)g * G + gg) * D + dd] = from_f32<T>(O / L);
-      } else {
-        part[gg * D + dd] = O;
-        if (dd == 0) {
-          part[G * D + gg] = M;
-          part[G * D + G + gg] = L;
-        }
-      }
-    }
-    if (nch > 1) {
-      __threadfence();
-      __syncthreads();
+    const bool landed = mbar_wait(&bars->full[s], round & 1, abort_flag, budget);
+    if (!named_sync_and(landed)) {
       if (tid == 0) {
-        const int prev = atomicAdd(&counters[i * a.h_kv + g], 1);
-        S.last = (prev == nch - 1);
+        set_status(a.dev_status, ST_TIMEOUT);
+        *abort_flag = 1;
       }
-      __syncthreads();
-      if (S.last) {
-        __threadfence();
-        const float* base = partials + ((int64_t)i * a.h_kv + g) * a.layout.max_chunks * pstride;
-        for (int e = tid; e < G * D; e += kThreads) {
-          const int gg = e / D, dd = e % D;
-          float M = -INFINITY;
-          for (int cc = 0; cc < nch; ++cc) M = fmaxf(M, __ldcg(base + cc * pstride + G * D + gg));
-          float L = 0.f, O = 0.f;
-          for (int cc = 0; cc < nch; ++cc) {
-            const float* pc = base + cc * pstride;
-            const float sc = expf(__ldcg(pc + G * D + gg) - M);
-            L += __ldcg(pc + G * D + G + gg) * sc;
-            O += __ldcg(pc + gg * D + dd) * sc;
-          }
-          static_cast<T*>(a.out)[((int64_t)i * a.h_q + (int64_t)g * G + gg) * D + dd] = from_f32<T>(O / L);
+      break;
+    }
+    // every thread is past chunk x-1: its stage takes chunk x + kStages - 1
+    if (L::kStages > 1 && tid == 0 && x + L::kStages - 1 < x_end)
+      issue(x + L::kStages - 1, (iter + L::kStages - 1) % L::kStages);
+    // the new row: into this chunk's shared rows and, once per (question, kv head), the pool
+    if (fi.len < fi.p1) {
+      const int r = fi.len - fi.p0;
+      const int64_t src = ((int64_t)fi.i * a.h_kv + fi.g) * kRow;
+      const int64_t dst = (((int64_t)fi.slot * a.h_kv + fi.g) * a.cap + fi.len) * kRow;
+      for (int e = tid; e < kRow / 16; e += kComputeThreads) {
+        const uint4 kw = *reinterpret_cast<const uint4*>(static_cast<const unsigned char*>(a.k_new) + src + 16 * e);
+        const uint4 vw = *reinterpret_cast<const uint4*>(static_cast<const unsigned char*>(a.v_new) + src + 16 * e);
+        *reinterpret_cast<uint4*>(kst + r * kRow + 16 * e) = kw;
+        *reinterpret_cast<uint4*>(vst + r * kRow + 16 * e) = vw;
+        if (fi.hb == 0) {
+          *reinterpret_cast<uint4*>(static_cast<unsigned char*>(a.pool_k) + dst + 16 * e) = kw;
+          *reinterpret_cast<uint4*>(static_cast<unsigned char*>(a.pool_v) + dst + 16 * e) = vw;
         }
-        if (tid == 0) counters[i * a.h_kv + g] = 0;
+      }
+      named_sync();
+    }
+
+    // ---- scores: half-warp per row, 4 rows per block, 16 rows per warp ----------------
+    {
+      unsigned long long q2[GT][kDimL / 2];
+#pragma unroll
+      for (int g = 0; g < GT; ++g) {
+        if (g < fi.nh) {
+          if (kDimL == 8) {
+            unsigned long long t[4];
+            E::load8(qst + g * kRow + hl * kDimL * EB, t);
+#pragma unroll
+            for (int e = 0; e < kDimL / 2; ++e) q2[g][e] = t[e];
+          } else {
+            const unsigned char* qp = qst + g * kRow + hl * kDimL * EB;
+            if (EB == 2) {
+              const uint2 w = *reinterpret_cast<const uint2*>(qp);
+              q2[g][0] = bf2_to_f2(w.x);
+              q2[g][1 % (kDimL / 2)] = bf2_to_f2(w.y);
+            } else {
+              const uint4 w = *reinterpret_cast<const uint4*>(qp);
+              q2[g][0] = (unsigned long long)w.x | ((unsigned long long)w.y << 32);
+              q2[g][1 % (kDimL / 2)] = (unsigned long long)w.z | ((unsigned long long)w.w << 32);
+            }
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < kDimL / 2; ++e) q2[g][e] = 0ull;
+        }
+      }
+      const float sl2 = a.scale * 1.4426950408889634f;
+#pragma unroll
+      for (int blk = 0; blk < 2; ++blk) {
+        const int rbase = warp * 16 + half * 8 + blk * 4;
+        float acc[4][GT];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int r = rbase + k;
+          unsigned long long kv[4] = {0ull, 0ull, 0ull, 0ull};
+          if (r < nr) {
+            const unsigned char* kp = kst + r * kRow + hl * kDimL * EB;
+            if (kDimL == 8) {
+              E::load8(kp, kv);
+            } else if (EB == 2) {
+              const uint2 w = *reinterpret_cast<const uint2*>(kp);
+              kv[0] = bf2_to_f2(w.x);
+              kv[1] = bf2_to_f2(w.y);
+            } else {
+              const uint4 w = *reinterpret_cast<const uint4*>(kp);
+              kv[0] = (unsigned long long)w.x | ((unsigned long long)w.y << 32);
+              kv[1] = (unsigned long long)w.z | ((unsigned long long)w.w << 32);
+            }
+          }
+#pragma unroll
+          for (int g = 0; g < GT; ++g) {
+            unsigned long long p2 = 0ull;
+#pragma unroll
+            for (int e = 0; e < kDimL / 2; ++e) p2 = fma2(q2[g][e], kv[e], p2);
+            const float2 pf = unpack2(p2);
+            acc[k][g] = pf.x + pf.y;
+          }
+        }
+        // reduce-scatter over the 16 lanes of the half-warp
+        float b[2][GT];
+        const bool up8 = hl & 8, up4 = hl & 4;
+#pragma unroll
+        for (int g = 0; g < GT; ++g) {
+#pragma unroll
+          for (int kk = 0; kk < 2; ++kk) {
+            const float send = up8 ? acc[kk][g] : acc[kk + 2][g];
+            const float keep = up8 ? acc[kk + 2][g] : acc[kk][g];
+            b[kk][g] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+          }
+        }
+        const int r = rbase + (up8 ? 2 : 0) + (up4 ? 1 : 0);
+#pragma unroll
+        for (int g = 0; g < GT; ++g) {
+          const float send = up4 ? b[0][g] : b[1][g];
+          const float keep = up4 ? b[1][g] : b[0][g];
+          float c = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+          c += __shfl_xor_sync(0xffffffffu, c, 2);
+          c += __shfl_xor_sync(0xffffffffu, c, 1);
+          if ((hl & 3) == 0) sc[g * kChunk + r] = r < nr ? c * sl2 : -INFINITY;
+        }
       }
     }
-    __syncthreads();
+    named_sync();
+
+    // ---- online softmax over the piece: one warp per head --------------------------------
+    if (warp < GT) {
+      const int g = warp;
+      float v[kChunk / 32];
+      float mc = -INFINITY;
+#pragma unroll
+      for (int k = 0; k < kChunk / 32; ++k) {
+        v[k] = sc[g * kChunk + lane + 32 * k];
+        mc = fmaxf(mc, v[k]);
+      }
+      mc = warp_max(mc);
+      const float m_old = piece_first ? -INFINITY : st_m[g];
+      const float l_old = piece_first ? 0.f : st_l[g];
+      const float m_new = fmaxf(m_old, mc);  // finite: every chunk holds at least one row
+      float l = 0.f;
+#pragma unroll
+      for (int k = 0; k < kChunk / 32; ++k) {
+        const float pv = ex2_approx(v[k] - m_new);  // rows past the chunk: exp2(-inf) = 0
+        pw[(lane + 32 * k) * GT + g] = pv;
+        l += pv;
+      }
+      l = warp_sum(l);
+      __syncwarp();
+      if (lane == 0) {
+        const float alpha = ex2_approx(m_old - m_new);  // first chunk of a piece: exp2(-inf) = 0
+        st_a[g] = alpha;
+        st_m[g] = m_new;
+        st_l[g] = l_old * alpha + l;
+      }
+    }
+    named_sync();
+
+    // ---- PV: lanes across dims, row groups; running output rescaled by alpha ------------
+    {
+#pragma unroll
+      for (int g = 0; g < GT; ++g) {
+        const float al = st_a[g];
+        const unsigned long long aa = f2pack(al, al);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) o2[g][e] = fma2(aa, o2[g][e], 0ull);
+      }
+      for (int r = rg; r < nr; r += kRG) {
+        unsigned long long vv[4];
+        E::load8(vst + r * kRow + dg * 8 * EB, vv);
+#pragma unroll
+        for (int g = 0; g < GT; ++g) {
+          const float pr = pw[r * GT + g];
+          const unsigned long long pp = f2pack(pr, pr);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) o2[g][e] = fma2(pp, vv[e], o2[g][e]);
+        }
+      }
+      // rows are read; order these reads before the bulk copy that refills the stage
+      fence_proxy_async_smem();
+    }
+    if (!piece_last) continue;
+
+    // ---- end of a piece: sum the row groups, then output or partial + ordered merge -----
+    {
+      float o[GT][8];
+#pragma unroll
+      for (int g = 0; g < GT; ++g)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 t = unpack2(o2[g][e]);
+          o[g][2 * e] = t.x;
+          o[g][2 * e + 1] = t.y;
+        }
+#pragma unroll
+      for (int off = kDG; off < 32; off <<= 1)
+#pragma unroll
+        for (int g = 0; g < GT; ++g)
+#pragma unroll
+          for (int e = 0; e < 8; ++e) o[g][e] += __shfl_xor_sync(0xffffffffu, o[g][e], off);
+      // warps 4-7 hand their sums to warps 0-3 (fixed order: the result is deterministic)
+      if (warp >= 4 && lane < kDG) {
+#pragma unroll
+        for (int g = 0; g < GT; ++g)
+#pragma unroll
+          for (int e = 0; e < 8; ++e) red[((warp - 4) * GT + g) * D + dg * 8 + e] = o[g][e];
+      }
+      named_sync();
+      if (warp < 4 && lane < kDG) {
+#pragma unroll
+        for (int g = 0; g < GT; ++g)
+#pragma unroll
+          for (int e = 0; e < 8; ++e) red[(warp * GT + g) * D + dg * 8 + e] += o[g][e];
+      }
+    }
+    named_sync();
+    const int x0 = x - fi.c;                         // first chunk of this (question, kv head, block)
+    const int c_start = max(x_begin, x0) - x0;       // first chunk of this piece
+    const bool whole = (c_start == 0) && (fi.c == fi.nch - 1);
+    const int cidx = (fi.i * a.h_kv + fi.g) * n_hblocks + fi.hb;
+    float* part = partials + ((int64_t)cidx * a.layout.max_chunks + c_start) * pstride;
+    for (int e = tid; e < GT * D; e += kComputeThreads) {
+      const int g = e / D, dd = e % D;
+      float acc = 0.f;
+#pragma unroll
+      for (int w = 0; w < 4; ++w) acc += red[(w * GT + g) * D + dd];
+      if (g >= fi.nh) continue;
+      if (whole) {
+        E::store(a.out, ((int64_t)fi.i * a.h_q + fi.h0 + g) * D + dd, acc / st_l[g]);
+      } else {
+        part[g * D + dd] = acc;
+        if (dd == 0) {
+          part[GT * D + g] = st_m[g];
+          part[GT * D + GT + g] = st_l[g];
+        }
+      }
+    }
+    if (!whole) {
+      __threadfence();  // this CTA's partial is visible before its arrival is counted
+      named_sync();
+      if (tid == 0) {
+        const int b_first = range_owner(x0, total, nb), b_last = range_owner(x0 + fi.nch - 1, total, nb);
+        bars->last = (atomicAdd(&counters[cidx], 1) == b_last - b_first);
+      }
+      named_sync();
+      if (bars->last) {
+        __threadfence();
+        const int b_first = range_owner(x0, total, nb), b_last = range_owner(x0 + fi.nch - 1, total, nb);
+        const float* base = partials + (int64_t)cidx * a.layout.max_chunks * pstride;
+        for (int e = tid; e < GT * D; e += kComputeThreads) {
+          const int g = e / D, dd = e % D;
+          if (g >= fi.nh) continue;
+          float M = -INFINITY;
+          for (int b = b_first; b <= b_last; ++b) {
+            const int cs = max(range_start(b, total, nb), x0) - x0;
+            M = fmaxf(M, __ldcg(base + cs * pstride + GT * D + g));
+          }
+          float Lsum = 0.f, O = 0.f;
+          for (int b = b_first; b <= b_last; ++b) {
+            const int cs = max(range_start(b, total, nb), x0) - x0;
+            const float* pc = base + cs * pstride;
+            const float w = ex2_approx(__ldcg(pc + GT * D + g) - M);
+            Lsum += __ldcg(pc + GT * D + GT + g) * w;
+            O += __ldcg(pc + g * D + dd) * w;
+          }
+          E::store(a.out, ((int64_t)fi.i * a.h_q + fi.h0 + g) * D + dd, O / Lsum);
+        }
+        if (tid == 0) counters[cidx] = 0;
+      }
+    }
+    named_sync();
+  }
+  // every copy lands before the CTA leaves
+  if (tid == 0) {
+    for (int st = 0; st < L::kStages; ++st)
+      if (issued[st]) mbar_wait(&bars->full[st], (issued[st] - 1) & 1, never, kDrainBudget);
   }
 }
 
@@ -269,31 +617,40 @@ __global__ void advance_kernel(int32_t* lens, const uint8_t* active, int32_t n) 
   if (i < n && active[i]) lens[i] += 1;
 }
 
+template <typename T, int D, int GT, int NS>
+cudaError_t launch_stages(const DecodeArgs& a, int num_sms, cudaStream_t s) {
+  using L = DSmem<D, (int)sizeof(T), GT, NS>;
+  static_assert(L::kStages * L::kStageBytes >= 2 * kMaxQuestions * 4, "the validation hash lives in the stages");
+  const int smem = L::bytes(a.n);
+  cudaError_t e = cudaFuncSetAttribute(decode_kernel<T, D, GT, NS>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  decode_kernel<T, D, GT, NS><<<num_sms, kThreads, smem, s>>>(a);
+  return cudaGetLastError();
+}
+
+// Deepest stage ring that fits the shared-memory budget for this many questions.
+template <typename T, int D, int GT>
+cudaError_t launch_one(const DecodeArgs& a, int num_sms, cudaStream_t s) {
+  constexpr int kMaxSmem = 232448;
+  if (DSmem<D, (int)sizeof(T), GT, 3>::bytes(a.n) <= kMaxSmem) return launch_stages<T, D, GT, 3>(a, num_sms, s);
+  if (DSmem<D, (int)sizeof(T), GT, 2>::bytes(a.n) <= kMaxSmem) return launch_stages<T, D, GT, 2>(a, num_sms, s);
+  return launch_stages<T, D, GT, 1>(a, num_sms, s);
+}
+
+template <typename T, int D>
+cudaError_t launch_d(const DecodeArgs& a, int num_sms, cudaStream_t s) {
+  const int g = a.group < kHB ? a.group : kHB;
+  if (g <= 1) return launch_one<T, D, 1>(a, num_sms, s);
+  if (g <= 2) return launch_one<T, D, 2>(a, num_sms, s);
+  if (g <= 4) return launch_one<T, D, 4>(a, num_sms, s);
+  return launch_one<T, D, 8>(a, num_sms, s);
+}
+
 }  // namespace
 
 cudaError_t launch_decode(const DecodeArgs& a, int d, kev_dtype dt, int num_sms, cudaStream_t s) {
-  const size_t smem = sizeof(DecodeSmem);
-  const int grid = num_sms * 2;
-  cudaError_t e = cudaSuccess;
-  if (dt == KEV_FP32) {
-    if (d == 64) {
-      e = cudaFuncSetAttribute(decode_kernel<float, 64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      if (e == cudaSuccess) decode_kernel<float, 64><<<grid, kThreads, smem, s>>>(a);
-    } else {
-      e = cudaFuncSetAttribute(decode_kernel<float, 128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      if (e == cudaSuccess) decode_kernel<float, 128><<<grid, kThreads, smem, s>>>(a);
-    }
-  } else {
-    if (d == 64) {
-      e = cudaFuncSetAttribute(decode_kernel<__nv_bfloat16, 64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      if (e == cudaSuccess) decode_kernel<__nv_bfloat16, 64><<<grid, kThreads, smem, s>>>(a);
-    } else {
-      e = cudaFuncSetAttribute(decode_kernel<__nv_bfloat16, 128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      if (e == cudaSuccess) decode_kernel<__nv_bfloat16, 128><<<grid, kThreads, smem, s>>>(a);
-    }
-  }
-  if (e != cudaSuccess) return e;
-  return cudaGetLastError();
+  if (dt == KEV_FP32) return d == 64 ? launch_d<float, 64>(a, num_sms, s) : launch_d<float, 128>(a, num_sms, s);
+  return d == 64 ? launch_d<__nv_bfloat16, 64>(a, num_sms, s) : launch_d<__nv_bfloat16, 128>(a, num_sms, s);
 }
 
 cudaError_t launch_advance(int32_t* lens, const uint8_t* active, int32_t n, cudaStream_t s) {

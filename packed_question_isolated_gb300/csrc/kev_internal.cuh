@@ -17,7 +17,7 @@ constexpr int kMaxQuestions = 4096;
 // Cost bins of the longest-first ordering: tile m (m+1 key tiles) goes to bin min(m, 63).
 constexpr int kCostBins = 64;
 // Positions per decode work item (split-K chunk).
-constexpr int kDecodeChunk = 256;
+constexpr int kDecodeChunk = 128;
 
 // Device status codes: same values as kev_status.
 enum : int32_t {
@@ -75,21 +75,30 @@ inline PrefillLayout prefill_layout(int32_t n, int32_t T, int32_t h_q) {
 // decode workspace
 // ---------------------------------------------------------------------------------------
 struct DecodeLayout {
-  size_t counters;  // int32[N * H_kv]  arrivals per (question, kv head); left at zero
-  size_t partials;  // float[N * H_kv * max_chunks * G * (d + 2)]
+  size_t counters;  // int32[N * H_kv * n_hblocks]  arrivals per (question, kv head, head block); left at zero
+  size_t partials;  // float[N * H_kv * n_hblocks * max_chunks * GT * (d + 2)]
   size_t total;
   int32_t max_chunks;
 };
+
+// q-heads of one decode item: the group padded to a power of two, at most 8 (larger groups
+// are split into blocks of 8).
+inline int decode_head_block_size(int group) {
+  const int g = group < 8 ? group : 8;
+  return g <= 1 ? 1 : g <= 2 ? 2 : g <= 4 ? 4 : 8;
+}
 
 inline DecodeLayout decode_layout(int32_t n, int32_t cap, int32_t h_q, int32_t h_kv, int32_t d) {
   DecodeLayout L;
   L.max_chunks = (cap + kDecodeChunk - 1) / kDecodeChunk;
   const int32_t G = h_q / h_kv;
+  const int32_t nhb = (G + 7) / 8;
+  const int32_t GT = decode_head_block_size(G);
   size_t off = 0;
   L.counters = off;
-  off = align_up(off + sizeof(int32_t) * (size_t)n * h_kv, 256);
+  off = align_up(off + sizeof(int32_t) * (size_t)n * h_kv * nhb, 256);
   L.partials = off;
-  off = align_up(off + sizeof(float) * (size_t)n * h_kv * L.max_chunks * G * (d + 2), 256);
+  off = align_up(off + sizeof(float) * (size_t)n * h_kv * nhb * L.max_chunks * GT * (d + 2), 256);
   L.total = off;
   return L;
 }
