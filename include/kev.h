@@ -93,7 +93,7 @@ size_t kev_prefill_workspace_size(int32_t n_questions, int32_t total_tokens, con
  * shared-state bug of the KV-cache isolation article, §2.3, §6.1).  Then writes into
  * `workspace`: the status word, cu_seqlens[N+1] (prefix sums of the lengths in interval
  * order, the varlen form of the block-diagonal mask, Kev architecture article §5.2, §6.4)
- * and the prefill work list: one item per (question, 128-row query tile, query head),
+ * and the prefill work list: one item per (question, 128-row query tile, q-head block),
  * covering key tiles [0, m] of its own question only, so no tile that is masked across
  * questions or above the causal diagonal is ever scheduled.  Items are ordered longest
  * first.  Interval order is free and intervals need not cover [0, T): tokens in no
@@ -107,8 +107,10 @@ kev_status kev_build_segments(const kev_interval* intervals, int32_t n_questions
                               int32_t* dev_status, kev_stream_t stream);
 
 /* Host copy of the work list built by kev_build_segments (synchronises `stream`).
- * Each item is {question, q_row_begin, q_rows, head}; returns the item count, or -1 on
- * error.  Writes at most `max_items` items to `items_out` (host int32[4*max_items]). */
+ * Each item is {question, q_row_begin, q_rows, first_head | (n_heads << 16)}: n_heads
+ * consecutive q-heads of one kv group (2 for bf16, whose kernel runs two query tiles that
+ * share every K/V tile; 1 for fp32).  Returns the item count, or -1 on error.  Writes at
+ * most `max_items` items to `items_out` (host int32[4*max_items]). */
 int32_t kev_read_work_list(const void* workspace, size_t workspace_bytes, int32_t* items_out,
                            int32_t max_items, kev_stream_t stream);
 

@@ -162,7 +162,7 @@ def kev_build_segments(intervals, n_questions, total_tokens, slot_ids, n_slots, 
 
 
 def kev_read_work_list(workspace, workspace_bytes, max_items: int, stream=None):
-    """Returns the work list as a list of (question, q_row_begin, q_rows, head) tuples."""
+    """Returns the work list as (question, q_row_begin, q_rows, first_head | n_heads << 16) tuples."""
     buf = (ctypes.c_int32 * (4 * max(int(max_items), 1)))()
     n = int(_c["kev_read_work_list"](_ptr(workspace), int(workspace_bytes), buf, int(max_items),
                                      _stream(stream)))

@@ -69,6 +69,9 @@ SegmentsArgs segments_args(const kev_interval* intervals, int32_t n, int32_t T, 
   a.n_slots = n_slots;
   a.cap = cap;
   a.h_q = shape->h_q;
+  a.group = shape->h_q / shape->h_kv;
+  // the tensor-core kernel takes two q-heads of a kv group per item, the fp32 kernel one
+  a.heads_per_item = shape->dtype == KEV_BF16 ? 2 : 1;
   a.ws = static_cast<char*>(ws);
   a.layout = prefill_layout(n, T, shape->h_q);
   a.dev_status = dev_status;

@@ -90,17 +90,6 @@ __device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32
       : "memory");
 }
 
-__device__ __forceinline__ unsigned long long f2pack(float a, float b) {
-  return (unsigned long long)__float_as_uint(a) | ((unsigned long long)__float_as_uint(b) << 32);
-}
-__device__ __forceinline__ float2 unpack2(unsigned long long v) {
-  return make_float2(__uint_as_float((uint32_t)v), __uint_as_float((uint32_t)(v >> 32)));
-}
-__device__ __forceinline__ unsigned long long fma2(unsigned long long a, unsigned long long b, unsigned long long c) {
-  unsigned long long d;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-  return d;
-}
 // bf16 pair (low element first) -> packed fp32 pair, exact
 __device__ __forceinline__ unsigned long long bf2_to_f2(uint32_t w) {
   return (unsigned long long)(w << 16) | ((unsigned long long)(w & 0xffff0000u) << 32);

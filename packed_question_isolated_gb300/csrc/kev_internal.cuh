@@ -33,7 +33,7 @@ enum : int32_t {
 // ---------------------------------------------------------------------------------------
 struct PrefillHeader {
   int32_t status;       // result of validation (and of bounded waits, if any gave up)
-  int32_t n_items;      // work items emitted
+  int32_t n_items;      // work items emitted: {question, row_begin, rows, first_head | n_heads << 16}
   int32_t n_tiles;      // query tiles emitted
   int32_t n_gaps;       // ranges of tokens that belong to no question
   int32_t sched;        // dynamic-scheduling counter (reset by the segment builder)
@@ -45,7 +45,7 @@ struct PrefillHeader {
 struct PrefillLayout {
   size_t cu_seqlens;  // int32[N+1]
   size_t tiles;       // int2[max_tiles]  {question, m}
-  size_t items;       // int4[max_items]  {question, row_begin, rows, head}
+  size_t items;       // int4[max_items]  {question, row_begin, rows, first_head | n_heads << 16}
   size_t gaps;        // int2[N+1]        [begin, end)
   size_t total;
   int64_t max_tiles;
@@ -114,6 +114,8 @@ struct SegmentsArgs {
   int32_t n_slots;
   int32_t cap;
   int32_t h_q;
+  int32_t group;           // h_q / h_kv
+  int32_t heads_per_item;  // consecutive q-heads of one kv group per work item (1 or 2)
   char* ws;
   PrefillLayout layout;
   int32_t* dev_status;  // may be null

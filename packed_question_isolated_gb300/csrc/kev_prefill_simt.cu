@@ -34,7 +34,7 @@ __global__ void __launch_bounds__(kWarps * 32) prefill_simt_kernel(PrefillArgs a
   for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
     const int4 item = items[it];
     const int seg_begin = a.intervals[item.x].begin;
-    const int h = item.w, g = h / a.group;
+    const int h = item.w & 0xffff, g = h / a.group;  // one head per item on this path
     for (int r = warp; r < item.z; r += kWarps) {
       const int t = item.y + r;
       __syncwarp();

@@ -1,28 +1,32 @@
 // Packed prefill attention on the 5th-generation tensor cores (bf16 in, fp32 accumulate).
 //
-// Computes, for every work item (question i, 128-row query tile m, q-head h) of the segment
-// builder's list, the exact attention of the inference-engine notes (sakurs2.com, §2.1,
-// Z = softmax(QK^T / sqrt(d_h) + M) V) restricted by the causal AND block-diagonal mask of
-// the Kev articles (icman.com.cn §2.3, gsyq.cn §2.2): the tile's rows read key tiles
-// 0..m of their own question only, and only the diagonal tile m needs the element mask
-// (key <= row).  Tiles are FlashAttention-style (notes §2.4): the T x T score matrix never
-// leaves the chip, and the softmax is the online form with a running max m, sum l and a
-// rescale of the accumulator when the max moves.
+// Computes, for every work item of the segment builder's list -- (question i, 128-row query
+// tile m, one or two q-heads of one kv group) -- the exact attention of the inference-engine
+// notes (sakurs2.com, §2.1, Z = softmax(QK^T / sqrt(d_h) + M) V) restricted by the causal AND
+// block-diagonal mask of the Kev articles (icman.com.cn §2.3, gsyq.cn §2.2): the tile's rows
+// read key tiles 0..m of their own question only, and only the diagonal tile m needs the
+// element mask (key <= row).  Tiles are FlashAttention-style (notes §2.4): the T x T score
+// matrix never leaves the chip, and the softmax is the online form with a running max m, sum
+// l and a rescale of the accumulator when the max moves.
 //
-// GB300 mapping (one persistent CTA per SM, 192 threads):
-//   warp 0     TMA producer: Q tile (128 x d) once per item, then K/V tiles (128 x d) into a
-//              2-stage ring; 128-byte swizzled boxes, completion counted on mbarriers.
-//   warp 1     MMA issuer: S = Q K^T into one of two TMEM buffers (128 x 128 fp32), then
-//              O += P V into a TMEM accumulator (128 x d fp32) with tcgen05.mma, and
-//              tcgen05.commit to release stages and signal the softmax warps.
-//   warps 2-5  softmax: each thread owns one query row (its TMEM lane), reads its S row
-//              with tcgen05.ld, applies the diagonal mask, updates m and l, writes P as
-//              bf16 into a swizzled shared-memory tile for the PV MMA, and rescales its O
-//              row in TMEM only when its running max grew by more than 2^8 (exact: O and l
-//              always share the same reference max).  The epilogue divides by l and
-//              stores bf16 rows; rows past the question's end are not stored.
-// Every wait is bounded; a wait that gives up sets KEV_ERR_TIMEOUT and raises the CTA's
-// abort flag, and the CTA drains its own copies and MMAs before freeing TMEM and exiting.
+// GB300 mapping (one persistent CTA per SM, 384 threads = 3 warpgroups):
+//   warp 8      TMA producer: the item's query tiles (one per q-head, 128 x d each), then
+//               K/V tiles (128 x d) of the shared kv head into a 2-stage ring; 128-byte
+//               swizzled boxes, completion counted on mbarriers.
+//   warp 9      MMA issuer, ping-pong over the two query tiles A and B: S_t = Q_t K^T into
+//               TMEM (128 x 128 fp32 per tile), then O_t += P_t V with P_t read from TMEM
+//               (it overwrites S_t as bf16) and V from shared memory; tcgen05.commit
+//               releases stages and signals the softmax warps.  While softmax A works on
+//               its tile, the tensor core runs tile B's MMAs, and the other way round.
+//   warps 0-3   softmax of tile A, warps 4-7 softmax of tile B: each thread owns one query
+//               row (its TMEM lane): tcgen05.ld of S, diagonal mask, row max on the raw
+//               scores, exp2 of one fused multiply-add per element (scale * log2 e folded),
+//               packed fp32x2 sums, P as bf16 back into TMEM, and an O rescale in TMEM only
+//               when the row's running max grew by more than 2^8 (exact: O and l always
+//               share one reference max).  The epilogue divides by l and stores bf16 rows;
+//               rows past the question's end are not stored.
+// Every wait is bounded; a wait that gives up sets KEV_ERR_TIMEOUT and raises the CTA's abort
+// flag, and the CTA drains its own copies and MMAs before freeing TMEM and exiting.
 #include <cuda.h>
 #include <stdlib.h>
 
@@ -37,11 +41,12 @@ using namespace sm100;
 constexpr int kBM = 128;            // query rows per tile
 constexpr int kBN = 128;            // keys per tile
 constexpr int kStages = 2;          // K/V ring depth
-constexpr int kThreads = 192;
+constexpr int kThreads = 384;       // 3 warpgroups
+constexpr int kProducerWarp = 8;    // warpgroup 2: TMA producer, MMA issuer, two idle warps
+constexpr int kMmaWarp = 9;
 constexpr uint32_t kTmemCols = 512;
-constexpr float kRescaleThreshold = 8.0f;      // log2 units: rescale O when the max grows by > 2^8
+constexpr float kRescaleThreshold = 8.0f;         // log2 units: rescale O when the max grows by > 2^8
 constexpr long long kDrainBudget = 4000000000ll;  // cycles to wait for in-flight work on abort
-constexpr int kPSub = kBM * 128;               // bytes of one 64-key column block of P
 
 struct TcParams {
   char* ws;
@@ -60,11 +65,10 @@ struct Smem {
   static constexpr int kSub = D / 64;             // 64-column (128-byte) sub-tiles per row
   static constexpr int kSubBytes = kBM * 128;     // one 128-row x 128-byte sub-tile
   static constexpr int kTileBytes = kBM * D * 2;  // one Q/K/V tile
-  static constexpr int kQ = 0;
-  static constexpr int kK = kQ + kTileBytes;
+  static constexpr int kQ = 0;                    // two query tiles
+  static constexpr int kK = kQ + 2 * kTileBytes;
   static constexpr int kV = kK + kStages * kTileBytes;
-  static constexpr int kP = kV + kStages * kTileBytes;
-  static constexpr int kBar = kP + kBM * kBN * 2;
+  static constexpr int kBar = kV + kStages * kTileBytes;
   static constexpr int kBytes = kBar + 1024;
   static constexpr int kLaunchBytes = kBytes + 1024;  // slack for 1024-byte alignment
 };
@@ -72,8 +76,8 @@ struct Smem {
 struct Bars {
   uint64_t q_full, q_empty;
   uint64_t k_full[kStages], v_full[kStages], kv_empty[kStages];
-  uint64_t s_full[2], s_free[2];
-  uint64_t p_full, o_done, o_free, drain;
+  uint64_t s_full[2], p_full[2], o_done[2], o_free[2];
+  uint64_t drain;
   uint32_t tmem_base;
   int abort;
   int never;  // stays 0: abort flag for waits that must not give up early
@@ -91,6 +95,22 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const 
                                           long long budget) {
   const bool ok = mbar_wait(bar, parity, abort_flag, budget);
   return __all_sync(0xffffffffu, ok);
+}
+
+struct Item {
+  int q, row0, rows, h0, nh, seg_begin, nkv;
+};
+__device__ __forceinline__ Item load_item(const int4* items, const kev_interval* iv, int it) {
+  const int4 w = items[it];
+  Item x;
+  x.q = w.x;
+  x.row0 = w.y;
+  x.rows = w.z;
+  x.h0 = w.w & 0xffff;
+  x.nh = w.w >> 16;
+  x.seg_begin = iv[w.x].begin;
+  x.nkv = (w.y - x.seg_begin) / kBM + 1;
+  return x;
 }
 
 template <int D>
@@ -118,24 +138,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars->v_full[s], 1);
       mbar_init(&bars->kv_empty[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&bars->s_full[b], 1);
-      mbar_init(&bars->s_free[b], 128);
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&bars->s_full[t], 1);
+      mbar_init(&bars->p_full[t], 128);
+      mbar_init(&bars->o_done[t], 1);
+      mbar_init(&bars->o_free[t], 128);
     }
-    mbar_init(&bars->p_full, 128);
-    mbar_init(&bars->o_done, 1);
-    mbar_init(&bars->o_free, 128);
     mbar_init(&bars->drain, 1);
     bars->abort = 0;
     bars->never = 0;
     fence_mbar_init();
   }
-  if (warp == 0 && lane == 0) {
+  if (warp == kProducerWarp && lane == 0) {
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
   }
-  if (warp == 1) {
+  if (warp == kMmaWarp) {
     tmem_alloc(&bars->tmem_base, kTmemCols);
     tmem_relinquish();
   }
@@ -143,38 +162,38 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
-  const uint32_t tm_o = tmem + 2u * kBN;
+  // TMEM columns: S_A [0,128), S_B [128,256), O_A [256,256+D), O_B [256+D, 256+2D)
   volatile int* abort_flag = &bars->abort;
   const volatile int* never = &bars->never;
   const long long budget = p.wait_budget;
 
-  if (warp == 0) {
+  if (warp == kProducerWarp) {
     // ------------------------------------------------------------------ TMA producer
     if (lane == 0) {
       uint32_t kv_iter = 0, n = 0, q_loads = 0;
       uint32_t kv_loads[kStages] = {0, 0};
       bool ok = true;
       for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, ++n) {
-        const int4 item = items[it];
-        const int seg_begin = p.intervals[item.x].begin;
-        const int nkv = (item.y - seg_begin) / kBM + 1;
-        const int g = item.w / p.group;
+        const Item x = load_item(items, p.intervals, it);
+        const int g = x.h0 / p.group;
         if (n > 0 && !mbar_wait(&bars->q_empty, (n - 1) & 1, abort_flag, budget)) {
           ok = false;
           break;
         }
-        mbar_arrive_expect_tx(&bars->q_full, L::kTileBytes);
-        for (int c = 0; c < L::kSub; ++c)
-          tma_load_2d(smem + L::kQ + c * L::kSubBytes, &tm_q, item.w * D + c * 64, item.y, &bars->q_full);
+        mbar_arrive_expect_tx(&bars->q_full, x.nh * L::kTileBytes);
+        for (int t = 0; t < x.nh; ++t)
+          for (int c = 0; c < L::kSub; ++c)
+            tma_load_2d(smem + L::kQ + t * L::kTileBytes + c * L::kSubBytes, &tm_q, (x.h0 + t) * D + c * 64, x.row0,
+                        &bars->q_full);
         ++q_loads;
-        for (int j = 0; j < nkv; ++j, ++kv_iter) {
+        for (int j = 0; j < x.nkv; ++j, ++kv_iter) {
           const int s = kv_iter % kStages;
           const uint32_t round = kv_iter / kStages;
           if (round > 0 && !mbar_wait(&bars->kv_empty[s], (round - 1) & 1, abort_flag, budget)) {
             ok = false;
             break;
           }
-          const int key0 = seg_begin + j * kBN;
+          const int key0 = x.seg_begin + j * kBN;
           mbar_arrive_expect_tx(&bars->k_full[s], L::kTileBytes);
           for (int c = 0; c < L::kSub; ++c)
             tma_load_2d(smem + L::kK + s * L::kTileBytes + c * L::kSubBytes, &tm_k, g * D + c * 64, key0,
@@ -198,129 +217,136 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-  } else if (warp == 1) {
+  } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_bf16(kBM, kBN, false, false);
       constexpr uint32_t idesc_o = idesc_bf16(kBM, D, false, true);
-      const uint32_t q_addr = smem_u32(smem + L::kQ);
-      const uint32_t p_addr = smem_u32(smem + L::kP);
-      uint32_t kv_iter = 0, s_iter = 0, p_iter = 0, n = 0;
+      uint32_t kv_iter = 0, n = 0;
+      uint32_t p_cnt[2] = {0, 0}, items_done[2] = {0, 0};
       bool ok = true;
 
-      auto issue_s = [&](uint32_t kvi) -> bool {
-        const int s = kvi % kStages;
-        const uint32_t round = kvi / kStages;
-        if (!mbar_wait(&bars->k_full[s], round & 1, abort_flag, budget)) return false;
-        const int sb = s_iter & 1;
-        const uint32_t sround = s_iter >> 1;
-        if (sround > 0 && !mbar_wait(&bars->s_free[sb], (sround - 1) & 1, abort_flag, budget)) return false;
-        tc_fence_after();
-        const uint32_t k_addr = smem_u32(smem + L::kK + s * L::kTileBytes);
+      auto issue_s = [&](int t, int stage) {
+        const uint32_t q_addr = smem_u32(smem + L::kQ + t * L::kTileBytes);
+        const uint32_t k_addr = smem_u32(smem + L::kK + stage * L::kTileBytes);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * L::kSubBytes + (kk & 3) * 32;
-          umma_bf16(tmem + sb * kBN, sdesc_sw128(q_addr + off, 16, 1024), sdesc_sw128(k_addr + off, 16, 1024),
-                    idesc_s, kk > 0);
+          umma_bf16(tmem + t * kBN, sdesc_sw128(q_addr + off, 16, 1024), sdesc_sw128(k_addr + off, 16, 1024), idesc_s,
+                    kk > 0);
         }
-        umma_commit(&bars->s_full[sb]);
-        ++s_iter;
-        return true;
+        umma_commit(&bars->s_full[t]);
+      };
+      auto issue_pv = [&](int t, int stage, bool accumulate) {
+        const uint32_t v_addr = smem_u32(smem + L::kV + stage * L::kTileBytes);
+#pragma unroll
+        for (int kk = 0; kk < kBN / 16; ++kk) {
+          const uint64_t b = sdesc_sw128(v_addr + kk * 16 * 128, L::kSubBytes, 1024);
+          umma_bf16_ts(tmem + 256 + t * D, tmem + t * kBN + kk * 8, b, idesc_o, (accumulate || kk > 0) ? 1u : 0u);
+        }
       };
 
       for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, ++n) {
-        const int4 item = items[it];
-        const int seg_begin = p.intervals[item.x].begin;
-        const int nkv = (item.y - seg_begin) / kBM + 1;
-        if (!mbar_wait(&bars->q_full, n & 1, abort_flag, budget) || !issue_s(kv_iter)) {
-          ok = false;
-          break;
-        }
-        if (nkv == 1) umma_commit(&bars->q_empty);
-        for (int j = 0; j < nkv; ++j) {
-          if (j + 1 < nkv) {
-            if (!issue_s(kv_iter + j + 1)) {
-              ok = false;
-              break;
-            }
-            if (j + 1 == nkv - 1) umma_commit(&bars->q_empty);  // last use of this Q tile issued
-          }
-          const int s = (kv_iter + j) % kStages;
-          const uint32_t round = (kv_iter + j) / kStages;
-          if (!mbar_wait(&bars->p_full, p_iter & 1, abort_flag, budget) ||
-              !mbar_wait(&bars->v_full[s], round & 1, abort_flag, budget) ||
-              (j == 0 && n > 0 && !mbar_wait(&bars->o_free, (n - 1) & 1, abort_flag, budget))) {
+        const Item x = load_item(items, p.intervals, it);
+        {
+          const int s0 = kv_iter % kStages;
+          if (!mbar_wait(&bars->q_full, n & 1, abort_flag, budget) ||
+              !mbar_wait(&bars->k_full[s0], (kv_iter / kStages) & 1, abort_flag, budget)) {
             ok = false;
             break;
           }
-          ++p_iter;
           tc_fence_after();
-          const uint32_t v_addr = smem_u32(smem + L::kV + s * L::kTileBytes);
-#pragma unroll
-          for (int kk = 0; kk < kBN / 16; ++kk) {
-            const uint64_t a = sdesc_sw128(p_addr + (kk >> 2) * kPSub + (kk & 3) * 32, 16, 1024);
-            const uint64_t b = sdesc_sw128(v_addr + kk * 16 * 128, L::kSubBytes, 1024);
-            umma_bf16(tm_o, a, b, idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
-          }
-          umma_commit(&bars->kv_empty[s]);
-          umma_commit(&bars->o_done);
+          for (int t = 0; t < x.nh; ++t) issue_s(t, s0);
+          if (x.nkv == 1) umma_commit(&bars->q_empty);
         }
-        kv_iter += nkv;
+        for (int j = 0; j < x.nkv && ok; ++j) {
+          const uint32_t ki = kv_iter + j;
+          const int st = ki % kStages;
+          const bool has_next = j + 1 < x.nkv;
+          const int stn = (ki + 1) % kStages;
+          if (!mbar_wait(&bars->v_full[st], (ki / kStages) & 1, abort_flag, budget) ||
+              (has_next && !mbar_wait(&bars->k_full[stn], ((ki + 1) / kStages) & 1, abort_flag, budget))) {
+            ok = false;
+            break;
+          }
+          for (int t = 0; t < x.nh; ++t) {
+            if (!mbar_wait(&bars->p_full[t], p_cnt[t] & 1, abort_flag, budget) ||
+                (j == 0 && items_done[t] > 0 &&
+                 !mbar_wait(&bars->o_free[t], (items_done[t] - 1) & 1, abort_flag, budget))) {
+              ok = false;
+              break;
+            }
+            ++p_cnt[t];
+            tc_fence_after();
+            issue_pv(t, st, j > 0);
+            if (has_next) {
+              issue_s(t, stn);  // overwrites S_t / P_t after the PV above has read it (in order)
+            } else {
+              umma_commit(&bars->o_done[t]);
+            }
+          }
+          if (!ok) break;
+          if (has_next && j + 1 == x.nkv - 1) umma_commit(&bars->q_empty);  // last use of the Q tiles issued
+          umma_commit(&bars->kv_empty[st]);
+        }
+        for (int t = 0; t < x.nh; ++t) ++items_done[t];
+        kv_iter += x.nkv;
       }
       if (!ok) raise_timeout(p, bars);
       // every MMA this thread issued is complete before TMEM is freed
       umma_commit(&bars->drain);
       mbar_wait(&bars->drain, 0, never, kDrainBudget);
     }
-  } else {
+  } else if (warp < kProducerWarp) {
     // ------------------------------------------------------------------ softmax warps
-    const int quarter = warp & 3;  // a warp may only touch TMEM lanes [32*(warp%4), +32)
+    const int t = warp >> 2;        // query tile of this warpgroup
+    const int quarter = warp & 3;   // a warp may only touch TMEM lanes [32*(warp%4), +32)
     const int r = quarter * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    const uint32_t p_addr = smem_u32(smem + L::kP);
+    const uint32_t tm_s = tmem + t * kBN + lane_off;
+    const uint32_t tm_o = tmem + 256 + t * D + lane_off;
     const float sl2 = p.scale_log2;
-    uint32_t s_iter = 0, o_iter = 0;
+    const unsigned long long sl2x2 = f2pack(sl2, sl2);
+    uint32_t s_cnt = 0, o_cnt = 0;
     bool ok = true;
     __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
 
     for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
-      const int4 item = items[it];
-      const int seg_begin = p.intervals[item.x].begin;
-      const int nkv = (item.y - seg_begin) / kBM + 1;
+      const Item x = load_item(items, p.intervals, it);
+      if (t >= x.nh) continue;
       float m_run = -INFINITY, l_run = 0.f;
 
-      for (int j = 0; j < nkv; ++j) {
-        const int sb = s_iter & 1;
-        const uint32_t sround = s_iter >> 1;
-        if (!warp_wait(&bars->s_full[sb], sround & 1, abort_flag, budget)) {
+      for (int j = 0; j < x.nkv; ++j) {
+        if (!warp_wait(&bars->s_full[t], s_cnt & 1, abort_flag, budget)) {
           ok = false;
           break;
         }
+        ++s_cnt;
         tc_fence_after();
-        float t[kBN];
-        {
-          uint32_t sr[4][32];
+        // pass 1: row max over the raw scores, 64 columns at a time (the element mask is
+        // applied on the diagonal tile only)
+        const bool diag = (j == x.nkv - 1);  // diagonal tile: key k is visible to row r iff k <= r
+        float mt = -INFINITY;
+#pragma unroll 1
+        for (int hh = 0; hh < 2; ++hh) {
+          uint32_t sr[2][32];
+          tmem_ld32(tm_s + hh * 64, sr[0]);
+          tmem_ld32(tm_s + hh * 64 + 32, sr[1]);
+          tmem_ld_wait(sr[0]);
+          tmem_ld_wait(sr[1]);
+          if (diag) {
 #pragma unroll
-          for (int c = 0; c < 4; ++c) tmem_ld32(tmem + sb * kBN + lane_off + c * 32, sr[c]);
+            for (int c = 0; c < 2; ++c)
 #pragma unroll
-          for (int c = 0; c < 4; ++c) tmem_ld_wait(sr[c]);
+              for (int e = 0; e < 32; ++e)
+                if (hh * 64 + c * 32 + e > r) sr[c][e] = __float_as_uint(-INFINITY);
+          }
 #pragma unroll
-          for (int c = 0; c < 4; ++c)
+          for (int c = 0; c < 2; ++c)
 #pragma unroll
-            for (int e = 0; e < 32; ++e) t[c * 32 + e] = __uint_as_float(sr[c][e]) * sl2;
+            for (int e = 0; e < 32; e += 2) mt = fmax3(mt, __uint_as_float(sr[c][e]), __uint_as_float(sr[c][e + 1]));
         }
-        tc_fence_before();
-        mbar_arrive(&bars->s_free[sb]);
-        ++s_iter;
-
-        if (j == nkv - 1) {  // diagonal tile: key x is visible to row r iff x <= r
-#pragma unroll
-          for (int x = 0; x < kBN; ++x)
-            if (x > r) t[x] = -INFINITY;
-        }
-        float mt = t[0];
-#pragma unroll
-        for (int x = 1; x < kBN; ++x) mt = fmaxf(mt, t[x]);
+        mt *= sl2;  // the scale is positive: max of scaled = scaled max
         float alpha = 1.f;
         bool rescale = false;
         if (j == 0) {
@@ -331,62 +357,73 @@ __global__ void __launch_bounds__(kThreads, 1)
           l_run *= alpha;
           rescale = true;
         }
-        uint32_t pk[kBN / 2];
-        float rs = 0.f;
+        // pass 2: P = exp2(s * scale * log2e - m) as bf16 pairs into the first 64 columns of
+        // S_t (half hh of S is read before the P columns that overlap it are written); the PV
+        // MMA reads P from there
+        const unsigned long long negm = f2pack(-m_run, -m_run);
+        unsigned long long acc2 = 0ull;
+#pragma unroll 1
+        for (int hh = 0; hh < 2; ++hh) {
+          uint32_t sr[2][32];
+          tmem_ld32(tm_s + hh * 64, sr[0]);
+          tmem_ld32(tm_s + hh * 64 + 32, sr[1]);
+          tmem_ld_wait(sr[0]);
+          tmem_ld_wait(sr[1]);
+          if (diag) {
 #pragma unroll
-        for (int x = 0; x < kBN; x += 2) {
-          const float a = ex2_approx(t[x] - m_run);
-          const float b = ex2_approx(t[x + 1] - m_run);
-          rs += a + b;
-          pk[x >> 1] = pack_bf16x2(a, b);
-        }
-        l_run += rs;
-
-        if (j > 0) {  // PV of the previous tile must be done: it reads P and accumulates O
-          if (!warp_wait(&bars->o_done, o_iter & 1, abort_flag, budget)) {
-            ok = false;
-            break;
+            for (int c = 0; c < 2; ++c)
+#pragma unroll
+              for (int e = 0; e < 32; ++e)
+                if (hh * 64 + c * 32 + e > r) sr[c][e] = __float_as_uint(-INFINITY);
           }
-          ++o_iter;
-          tc_fence_after();
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              const unsigned long long sv =
+                  (unsigned long long)sr[c][2 * e] | ((unsigned long long)sr[c][2 * e + 1] << 32);
+              const float2 a = unpack2(fma2(sv, sl2x2, negm));
+              const float p0 = ex2_approx(a.x), p1 = ex2_approx(a.y);
+              acc2 = add2(acc2, f2pack(p0, p1));
+              pk[e] = pack_bf16x2(p0, p1);
+            }
+            tmem_st16(tm_s + hh * 32 + c * 16, pk);
+          }
         }
-        if (__any_sync(0xffffffffu, rescale)) {
+        const float2 acc = unpack2(acc2);
+        l_run += acc.x + acc.y;
+        if (__any_sync(0xffffffffu, rescale)) {  // PV of the previous tile is complete (S_t came after it)
 #pragma unroll
           for (int c = 0; c < D / 32; ++c) {
             uint32_t o[32];
-            tmem_ld32(tm_o + lane_off + c * 32, o);
+            tmem_ld32(tm_o + c * 32, o);
             tmem_ld_wait(o);
 #pragma unroll
             for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-            tmem_st32(tm_o + lane_off + c * 32, o);
+            tmem_st32(tm_o + c * 32, o);
           }
-          tmem_st_wait();
         }
-#pragma unroll
-        for (int ch = 0; ch < kBN / 8; ++ch) {
-          const uint32_t addr = p_addr + (ch >> 3) * kPSub + r * 128 + (((ch & 7) ^ (r & 7)) << 4);
-          st_shared_v4(addr, pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
-        }
-        fence_proxy_async_smem();
+        tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(&bars->p_full);
+        mbar_arrive(&bars->p_full[t]);
       }
       if (!ok) break;
 
       // epilogue: O / l -> bf16 rows of this item
-      if (!warp_wait(&bars->o_done, o_iter & 1, abort_flag, budget)) {
+      if (!warp_wait(&bars->o_done[t], o_cnt & 1, abort_flag, budget)) {
         ok = false;
         break;
       }
-      ++o_iter;
+      ++o_cnt;
       tc_fence_after();
       const float inv = 1.f / l_run;
-      const bool valid = r < item.z;
-      __nv_bfloat16* orow = out + ((int64_t)(item.y + r) * p.h_q + item.w) * D;
+      const bool valid = r < x.rows;
+      __nv_bfloat16* orow = out + ((int64_t)(x.row0 + r) * p.h_q + x.h0 + t) * D;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t o[32];
-        tmem_ld32(tm_o + lane_off + c * 32, o);
+        tmem_ld32(tm_o + c * 32, o);
         tmem_ld_wait(o);
         if (valid) {
           uint32_t w[16];
@@ -399,14 +436,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       tc_fence_before();
-      mbar_arrive(&bars->o_free);
+      mbar_arrive(&bars->o_free[t]);
     }
     if (!ok && lane == 0) raise_timeout(p, bars);
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }

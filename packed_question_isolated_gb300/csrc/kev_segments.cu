@@ -205,7 +205,7 @@ __global__ void __launch_bounds__(kThreads) segments_kernel(SegmentsArgs a) {
       acc += bin_count[b];
     }
     hdr->n_tiles = acc;
-    hdr->n_items = acc * a.h_q;
+    hdr->n_items = acc * (a.h_q / a.group) * ((a.group + a.heads_per_item - 1) / a.heads_per_item);
   }
   __syncthreads();
   for (int i = tid; i < n; i += blockDim.x) {
@@ -218,18 +218,24 @@ __global__ void __launch_bounds__(kThreads) segments_kernel(SegmentsArgs a) {
   }
   __syncthreads();
 
-  // 7. expand tiles into (tile, head) items; the heads of one tile stay adjacent so the
-  //    q-heads that share a kv-head run close together in time (L2 reuse of K/V tiles).
+  // 7. expand tiles into (tile, head block) items: a block is heads_per_item consecutive
+  //    q-heads of one kv group (they share every K/V tile); the blocks of one tile stay
+  //    adjacent so the q-heads that share a kv-head run close together (L2 reuse).
   const int n_tiles = hdr->n_tiles;
-  const long long n_items = (long long)n_tiles * a.h_q;
+  const int per_group = (a.group + a.heads_per_item - 1) / a.heads_per_item;
+  const int per_tile = (a.h_q / a.group) * per_group;
+  const long long n_items = (long long)n_tiles * per_tile;
   for (long long k = tid; k < n_items; k += blockDim.x) {
-    const int t = (int)(k / a.h_q);
-    const int h = (int)(k % a.h_q);
+    const int t = (int)(k / per_tile);
+    const int r = (int)(k % per_tile);
+    const int g = r / per_group, b = r % per_group;
+    const int h0 = g * a.group + b * a.heads_per_item;
+    const int nh = min(a.heads_per_item, a.group - b * a.heads_per_item);
     const int2 tl = tiles[t];
     const kev_interval iv = a.intervals[tl.x];
     const int r0 = iv.begin + tl.y * kTileM;
     const int rows = min(kTileM, iv.end - r0);
-    items[k] = make_int4(tl.x, r0, rows, h);
+    items[k] = make_int4(tl.x, r0, rows, h0 | (nh << 16));
   }
   if (tid == 0) {
     hdr->status = ST_OK;

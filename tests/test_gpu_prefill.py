@@ -135,13 +135,17 @@ def test_work_list_covers_exactly_the_allowed_tiles():
     allowed = O.allowed_mask(w.intervals, T)
     covered = np.zeros((w.h_q, T, T), dtype=np.int32)
     costs = []
-    for (qi, r0, rows, h) in items:
+    G = w.h_q // w.h_kv
+    for (qi, r0, rows, hw) in items:
+        h0, nh = hw & 0xffff, hw >> 16
+        assert 1 <= nh <= 2 and h0 // G == (h0 + nh - 1) // G, "an item's heads share one kv head"
         s, e = w.intervals[qi]
         assert s <= r0 and r0 + rows <= e and 0 < rows <= 128 and (r0 - s) % 128 == 0
         # key range of the item: [s, r0 + rows)
         blk = allowed[r0:r0 + rows, s:r0 + rows]
         assert blk.any(), "an item with no allowed entry was scheduled"
-        covered[h, r0:r0 + rows, s:r0 + rows] += 1
+        for h in range(h0, h0 + nh):
+            covered[h, r0:r0 + rows, s:r0 + rows] += 1
         costs.append((r0 - s) // 128 + 1)
     for h in range(w.h_q):
         assert (covered[h][allowed] == 1).all(), "allowed entry not covered exactly once"
