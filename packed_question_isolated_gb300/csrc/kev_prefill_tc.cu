@@ -10,9 +10,11 @@
 // l and a rescale of the accumulator when the max moves.
 //
 // GB300 mapping (one persistent CTA per SM, 384 threads = 3 warpgroups):
-//   warp 8      TMA producer: the item's query tiles (one per q-head, 128 x d each), then
-//               K/V tiles (128 x d) of the shared kv head into a 2-stage ring; 128-byte
-//               swizzled boxes, completion counted on mbarriers.
+//   warp 8      TMA producer of the item's query tiles (one per q-head, 128 x d each) and of
+//               the K tiles (128 x d) of the shared kv head into a 3-stage ring; warp 10
+//               produces the V tiles into a 2-stage ring.  A K tile is released as soon as
+//               both S MMAs have used it, a V tile after both PV MMAs, so the next tiles'
+//               loads start early.  128-byte swizzled boxes, completion on mbarriers.
 //   warp 9      MMA issuer, ping-pong over the two query tiles A and B: S_t = Q_t K^T into
 //               TMEM (128 x 128 fp32 per tile), then O_t += P_t V with P_t read from TMEM
 //               (it overwrites S_t as bf16) and V from shared memory; tcgen05.commit
@@ -25,6 +27,8 @@
 //               when the row's running max grew by more than 2^8 (exact: O and l always
 //               share one reference max).  The epilogue divides by l and stores bf16 rows;
 //               rows past the question's end are not stored.
+//   The control warpgroup (warps 8-11) hands registers to the softmax warpgroups (setmaxnreg),
+//   so a softmax thread holds its whole 128-wide score row in registers.
 // Every wait is bounded; a wait that gives up sets KEV_ERR_TIMEOUT and raises the CTA's abort
 // flag, and the CTA drains its own copies and MMAs before freeing TMEM and exiting.
 #include <cuda.h>
@@ -40,10 +44,17 @@ using namespace sm100;
 
 constexpr int kBM = 128;            // query rows per tile
 constexpr int kBN = 128;            // keys per tile
-constexpr int kStages = 2;          // K/V ring depth
+constexpr int kKStages = 3;         // K ring depth (a K tile is free once both S MMAs used it)
+constexpr int kVStages = 2;         // V ring depth (a V tile is free once both PV MMAs used it)
 constexpr int kThreads = 384;       // 3 warpgroups
-constexpr int kProducerWarp = 8;    // warpgroup 2: TMA producer, MMA issuer, two idle warps
+constexpr int kProducerWarp = 8;    // warpgroup 2: Q/K producer, MMA issuer, V producer, idle
 constexpr int kMmaWarp = 9;
+constexpr int kVProducerWarp = 10;
+// Register split: the kernel is launched at <= 168 registers per thread (384 x 168 = 64512);
+// the control warpgroup drops to 80 and the two softmax warpgroups rise to 208:
+// 128 x 80 + 256 x 208 = 63488 <= 64512, so the increase can always be granted.
+constexpr int kRegsControl = 80;
+constexpr int kRegsSoftmax = 208;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;         // log2 units: rescale O when the max grows by > 2^8
 constexpr long long kDrainBudget = 4000000000ll;  // cycles to wait for in-flight work on abort
@@ -67,15 +78,15 @@ struct Smem {
   static constexpr int kTileBytes = kBM * D * 2;  // one Q/K/V tile
   static constexpr int kQ = 0;                    // two query tiles
   static constexpr int kK = kQ + 2 * kTileBytes;
-  static constexpr int kV = kK + kStages * kTileBytes;
-  static constexpr int kBar = kV + kStages * kTileBytes;
+  static constexpr int kV = kK + kKStages * kTileBytes;
+  static constexpr int kBar = kV + kVStages * kTileBytes;
   static constexpr int kBytes = kBar + 1024;
   static constexpr int kLaunchBytes = kBytes + 1024;  // slack for 1024-byte alignment
 };
 
 struct Bars {
   uint64_t q_full, q_empty;
-  uint64_t k_full[kStages], v_full[kStages], kv_empty[kStages];
+  uint64_t k_full[kKStages], k_empty[kKStages], v_full[kVStages], v_empty[kVStages];
   uint64_t s_full[2], p_full[2], o_done[2], o_free[2];
   uint64_t drain;
   uint32_t tmem_base;
@@ -133,10 +144,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(&bars->q_full, 1);
     mbar_init(&bars->q_empty, 1);
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < kKStages; ++s) {
       mbar_init(&bars->k_full[s], 1);
+      mbar_init(&bars->k_empty[s], 1);
+    }
+    for (int s = 0; s < kVStages; ++s) {
       mbar_init(&bars->v_full[s], 1);
-      mbar_init(&bars->kv_empty[s], 1);
+      mbar_init(&bars->v_empty[s], 1);
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&bars->s_full[t], 1);
@@ -167,14 +181,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   const volatile int* never = &bars->never;
   const long long budget = p.wait_budget;
 
+  if (warp >= kProducerWarp) {
+  regs_dec<kRegsControl>();
   if (warp == kProducerWarp) {
-    // ------------------------------------------------------------------ TMA producer
+    // ------------------------------------------------------------------ Q and K producer
     if (lane == 0) {
-      uint32_t kv_iter = 0, n = 0, q_loads = 0;
-      uint32_t kv_loads[kStages] = {0, 0};
+      uint32_t k_iter = 0, n = 0, q_loads = 0;
+      uint32_t k_loads[kKStages] = {0, 0, 0};
       bool ok = true;
+      Item x_next = load_item(items, p.intervals, blockIdx.x);
       for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, ++n) {
-        const Item x = load_item(items, p.intervals, it);
+        const Item x = x_next;  // loaded one item ahead: its latency hides behind this item
+        if (it + (int)gridDim.x < n_items) x_next = load_item(items, p.intervals, it + gridDim.x);
         const int g = x.h0 / p.group;
         if (n > 0 && !mbar_wait(&bars->q_empty, (n - 1) & 1, abort_flag, budget)) {
           ok = false;
@@ -186,35 +204,70 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_2d(smem + L::kQ + t * L::kTileBytes + c * L::kSubBytes, &tm_q, (x.h0 + t) * D + c * 64, x.row0,
                         &bars->q_full);
         ++q_loads;
-        for (int j = 0; j < x.nkv; ++j, ++kv_iter) {
-          const int s = kv_iter % kStages;
-          const uint32_t round = kv_iter / kStages;
-          if (round > 0 && !mbar_wait(&bars->kv_empty[s], (round - 1) & 1, abort_flag, budget)) {
+        // warm L2 (and the address translation) for the next item's query tiles and first
+        // K/V tile while this item runs: its Q load is issued only when this item's last S
+        // MMA has read the Q buffer
+        if (it + (int)gridDim.x < n_items) {
+          const Item& nx = x_next;
+          const int ng = nx.h0 / p.group;
+          for (int t = 0; t < nx.nh; ++t)
+            for (int c = 0; c < L::kSub; ++c) tma_prefetch_l2_2d(&tm_q, (nx.h0 + t) * D + c * 64, nx.row0);
+          for (int c = 0; c < L::kSub; ++c) {
+            tma_prefetch_l2_2d(&tm_k, ng * D + c * 64, nx.seg_begin);
+            tma_prefetch_l2_2d(&tm_v, ng * D + c * 64, nx.seg_begin);
+          }
+        }
+        for (int j = 0; j < x.nkv; ++j, ++k_iter) {
+          const int s = k_iter % kKStages;
+          const uint32_t round = k_iter / kKStages;
+          if (round > 0 && !mbar_wait(&bars->k_empty[s], (round - 1) & 1, abort_flag, budget)) {
             ok = false;
             break;
           }
-          const int key0 = x.seg_begin + j * kBN;
           mbar_arrive_expect_tx(&bars->k_full[s], L::kTileBytes);
           for (int c = 0; c < L::kSub; ++c)
-            tma_load_2d(smem + L::kK + s * L::kTileBytes + c * L::kSubBytes, &tm_k, g * D + c * 64, key0,
-                        &bars->k_full[s]);
-          mbar_arrive_expect_tx(&bars->v_full[s], L::kTileBytes);
-          for (int c = 0; c < L::kSub; ++c)
-            tma_load_2d(smem + L::kV + s * L::kTileBytes + c * L::kSubBytes, &tm_v, g * D + c * 64, key0,
-                        &bars->v_full[s]);
-          ++kv_loads[s];
+            tma_load_2d(smem + L::kK + s * L::kTileBytes + c * L::kSubBytes, &tm_k, g * D + c * 64,
+                        x.seg_begin + j * kBN, &bars->k_full[s]);
+          ++k_loads[s];
         }
       }
       if (!ok) raise_timeout(p, bars);
       if (*abort_flag) {
         // every copy issued by this thread lands before the CTA leaves
         if (q_loads) mbar_wait(&bars->q_full, (q_loads - 1) & 1, never, kDrainBudget);
-        for (int s = 0; s < kStages; ++s) {
-          if (kv_loads[s]) {
-            mbar_wait(&bars->k_full[s], (kv_loads[s] - 1) & 1, never, kDrainBudget);
-            mbar_wait(&bars->v_full[s], (kv_loads[s] - 1) & 1, never, kDrainBudget);
+        for (int s = 0; s < kKStages; ++s)
+          if (k_loads[s]) mbar_wait(&bars->k_full[s], (k_loads[s] - 1) & 1, never, kDrainBudget);
+      }
+    }
+  } else if (warp == kVProducerWarp) {
+    // ------------------------------------------------------------------ V producer
+    if (lane == 0) {
+      uint32_t v_iter = 0;
+      uint32_t v_loads[kVStages] = {0, 0};
+      bool ok = true;
+      Item x_next = load_item(items, p.intervals, blockIdx.x);
+      for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+        const Item x = x_next;  // loaded one item ahead: its latency hides behind this item
+        if (it + (int)gridDim.x < n_items) x_next = load_item(items, p.intervals, it + gridDim.x);
+        const int g = x.h0 / p.group;
+        for (int j = 0; j < x.nkv; ++j, ++v_iter) {
+          const int s = v_iter % kVStages;
+          const uint32_t round = v_iter / kVStages;
+          if (round > 0 && !mbar_wait(&bars->v_empty[s], (round - 1) & 1, abort_flag, budget)) {
+            ok = false;
+            break;
           }
+          mbar_arrive_expect_tx(&bars->v_full[s], L::kTileBytes);
+          for (int c = 0; c < L::kSub; ++c)
+            tma_load_2d(smem + L::kV + s * L::kTileBytes + c * L::kSubBytes, &tm_v, g * D + c * 64,
+                        x.seg_begin + j * kBN, &bars->v_full[s]);
+          ++v_loads[s];
         }
+      }
+      if (!ok) raise_timeout(p, bars);
+      if (*abort_flag) {
+        for (int s = 0; s < kVStages; ++s)
+          if (v_loads[s]) mbar_wait(&bars->v_full[s], (v_loads[s] - 1) & 1, never, kDrainBudget);
       }
     }
   } else if (warp == kMmaWarp) {
@@ -228,7 +281,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       auto issue_s = [&](int t, int stage) {
         const uint32_t q_addr = smem_u32(smem + L::kQ + t * L::kTileBytes);
-        const uint32_t k_addr = smem_u32(smem + L::kK + stage * L::kTileBytes);
+        const uint32_t k_addr = smem_u32(smem + L::kK + stage * L::kTileBytes);  // K ring stage
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * L::kSubBytes + (kk & 3) * 32;
@@ -246,26 +299,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       };
 
+      Item x_next = load_item(items, p.intervals, blockIdx.x);
       for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, ++n) {
-        const Item x = load_item(items, p.intervals, it);
+        const Item x = x_next;  // loaded one item ahead: its latency hides behind this item
+        if (it + (int)gridDim.x < n_items) x_next = load_item(items, p.intervals, it + gridDim.x);
         {
-          const int s0 = kv_iter % kStages;
+          const int k0 = kv_iter % kKStages;
           if (!mbar_wait(&bars->q_full, n & 1, abort_flag, budget) ||
-              !mbar_wait(&bars->k_full[s0], (kv_iter / kStages) & 1, abort_flag, budget)) {
+              !mbar_wait(&bars->k_full[k0], (kv_iter / kKStages) & 1, abort_flag, budget)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          for (int t = 0; t < x.nh; ++t) issue_s(t, s0);
+          for (int t = 0; t < x.nh; ++t) issue_s(t, k0);
+          umma_commit(&bars->k_empty[k0]);
           if (x.nkv == 1) umma_commit(&bars->q_empty);
         }
         for (int j = 0; j < x.nkv && ok; ++j) {
           const uint32_t ki = kv_iter + j;
-          const int st = ki % kStages;
+          const int vs = ki % kVStages;
           const bool has_next = j + 1 < x.nkv;
-          const int stn = (ki + 1) % kStages;
-          if (!mbar_wait(&bars->v_full[st], (ki / kStages) & 1, abort_flag, budget) ||
-              (has_next && !mbar_wait(&bars->k_full[stn], ((ki + 1) / kStages) & 1, abort_flag, budget))) {
+          const int kn = (ki + 1) % kKStages;
+          if (!mbar_wait(&bars->v_full[vs], (ki / kVStages) & 1, abort_flag, budget) ||
+              (has_next && !mbar_wait(&bars->k_full[kn], ((ki + 1) / kKStages) & 1, abort_flag, budget))) {
             ok = false;
             break;
           }
@@ -278,16 +334,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             ++p_cnt[t];
             tc_fence_after();
-            issue_pv(t, st, j > 0);
+            issue_pv(t, vs, j > 0);
             if (has_next) {
-              issue_s(t, stn);  // overwrites S_t / P_t after the PV above has read it (in order)
+              issue_s(t, kn);  // overwrites S_t / P_t after the PV above has read it (in order)
             } else {
               umma_commit(&bars->o_done[t]);
             }
           }
           if (!ok) break;
-          if (has_next && j + 1 == x.nkv - 1) umma_commit(&bars->q_empty);  // last use of the Q tiles issued
-          umma_commit(&bars->kv_empty[st]);
+          umma_commit(&bars->v_empty[vs]);
+          if (has_next) {
+            umma_commit(&bars->k_empty[kn]);
+            if (j + 1 == x.nkv - 1) umma_commit(&bars->q_empty);  // last use of the Q tiles issued
+          }
         }
         for (int t = 0; t < x.nh; ++t) ++items_done[t];
         kv_iter += x.nkv;
@@ -297,7 +356,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       umma_commit(&bars->drain);
       mbar_wait(&bars->drain, 0, never, kDrainBudget);
     }
-  } else if (warp < kProducerWarp) {
+  }
+  } else {
+    regs_inc<kRegsSoftmax>();
     // ------------------------------------------------------------------ softmax warps
     const int t = warp >> 2;        // query tile of this warpgroup
     const int quarter = warp & 3;   // a warp may only touch TMEM lanes [32*(warp%4), +32)
@@ -310,9 +371,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t s_cnt = 0, o_cnt = 0;
     bool ok = true;
     __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
+    const bool out32 = (reinterpret_cast<uintptr_t>(p.out) & 31) == 0;
 
+    Item x_next = load_item(items, p.intervals, blockIdx.x);
     for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
-      const Item x = load_item(items, p.intervals, it);
+      const Item x = x_next;  // loaded one item ahead: its latency hides behind this item
+      if (it + (int)gridDim.x < n_items) x_next = load_item(items, p.intervals, it + gridDim.x);
       if (t >= x.nh) continue;
       float m_run = -INFINITY, l_run = 0.f;
 
@@ -323,29 +387,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         ++s_cnt;
         tc_fence_after();
-        // pass 1: row max over the raw scores, 64 columns at a time (the element mask is
-        // applied on the diagonal tile only)
-        const bool diag = (j == x.nkv - 1);  // diagonal tile: key k is visible to row r iff k <= r
-        float mt = -INFINITY;
-#pragma unroll 1
-        for (int hh = 0; hh < 2; ++hh) {
-          uint32_t sr[2][32];
-          tmem_ld32(tm_s + hh * 64, sr[0]);
-          tmem_ld32(tm_s + hh * 64 + 32, sr[1]);
-          tmem_ld_wait(sr[0]);
-          tmem_ld_wait(sr[1]);
-          if (diag) {
+        // the whole 128-wide score row of this thread, one load round trip
+        uint32_t sr[4][32];
 #pragma unroll
-            for (int c = 0; c < 2; ++c)
+        for (int c = 0; c < 4; ++c) tmem_ld32(tm_s + c * 32, sr[c]);
 #pragma unroll
-              for (int e = 0; e < 32; ++e)
-                if (hh * 64 + c * 32 + e > r) sr[c][e] = __float_as_uint(-INFINITY);
-          }
+        for (int c = 0; c < 4; ++c) tmem_ld_wait(sr[c]);
+        if (j == x.nkv - 1) {  // diagonal tile: key k is visible to row r iff k <= r
 #pragma unroll
-          for (int c = 0; c < 2; ++c)
+          for (int c = 0; c < 4; ++c)
 #pragma unroll
-            for (int e = 0; e < 32; e += 2) mt = fmax3(mt, __uint_as_float(sr[c][e]), __uint_as_float(sr[c][e + 1]));
+            for (int e = 0; e < 32; ++e)
+              if (c * 32 + e > r) sr[c][e] = __float_as_uint(-INFINITY);
         }
+        float mt = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) mt = fmax3(mt, __uint_as_float(sr[c][e]), __uint_as_float(sr[c][e + 1]));
         mt *= sl2;  // the scale is positive: max of scaled = scaled max
         float alpha = 1.f;
         bool rescale = false;
@@ -357,39 +416,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           l_run *= alpha;
           rescale = true;
         }
-        // pass 2: P = exp2(s * scale * log2e - m) as bf16 pairs into the first 64 columns of
-        // S_t (half hh of S is read before the P columns that overlap it are written); the PV
-        // MMA reads P from there
+        // P = exp2(s * scale * log2e - m) as bf16 pairs into the first 64 columns of S_t
+        // (S is already in registers); the PV MMA reads P from there
         const unsigned long long negm = f2pack(-m_run, -m_run);
         unsigned long long acc2 = 0ull;
-#pragma unroll 1
-        for (int hh = 0; hh < 2; ++hh) {
-          uint32_t sr[2][32];
-          tmem_ld32(tm_s + hh * 64, sr[0]);
-          tmem_ld32(tm_s + hh * 64 + 32, sr[1]);
-          tmem_ld_wait(sr[0]);
-          tmem_ld_wait(sr[1]);
-          if (diag) {
 #pragma unroll
-            for (int c = 0; c < 2; ++c)
+        for (int c = 0; c < 4; ++c) {
+          uint32_t pk[16];
 #pragma unroll
-              for (int e = 0; e < 32; ++e)
-                if (hh * 64 + c * 32 + e > r) sr[c][e] = __float_as_uint(-INFINITY);
+          for (int e = 0; e < 16; ++e) {
+            const unsigned long long sv = (unsigned long long)sr[c][2 * e] | ((unsigned long long)sr[c][2 * e + 1] << 32);
+            const float2 a = unpack2(fma2(sv, sl2x2, negm));
+            const float p0 = ex2_approx(a.x), p1 = ex2_approx(a.y);
+            acc2 = add2(acc2, f2pack(p0, p1));
+            pk[e] = pack_bf16x2(p0, p1);
           }
-#pragma unroll
-          for (int c = 0; c < 2; ++c) {
-            uint32_t pk[16];
-#pragma unroll
-            for (int e = 0; e < 16; ++e) {
-              const unsigned long long sv =
-                  (unsigned long long)sr[c][2 * e] | ((unsigned long long)sr[c][2 * e + 1] << 32);
-              const float2 a = unpack2(fma2(sv, sl2x2, negm));
-              const float p0 = ex2_approx(a.x), p1 = ex2_approx(a.y);
-              acc2 = add2(acc2, f2pack(p0, p1));
-              pk[e] = pack_bf16x2(p0, p1);
-            }
-            tmem_st16(tm_s + hh * 32 + c * 16, pk);
-          }
+          tmem_st16(tm_s + c * 16, pk);
         }
         const float2 acc = unpack2(acc2);
         l_run += acc.x + acc.y;
@@ -420,19 +462,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float inv = 1.f / l_run;
       const bool valid = r < x.rows;
       __nv_bfloat16* orow = out + ((int64_t)(x.row0 + r) * p.h_q + x.h0 + t) * D;
+      {
+        uint32_t o[D / 32][32];
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t o[32];
-        tmem_ld32(tm_o + c * 32, o);
-        tmem_ld_wait(o);
+        for (int c = 0; c < D / 32; ++c) tmem_ld32(tm_o + c * 32, o[c]);
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) tmem_ld_wait(o[c]);
         if (valid) {
-          uint32_t w[16];
 #pragma unroll
-          for (int e = 0; e < 16; ++e)
-            w[e] = pack_bf16x2(__uint_as_float(o[2 * e]) * inv, __uint_as_float(o[2 * e + 1]) * inv);
-          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t w[16];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) dst[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+            for (int e = 0; e < 16; ++e)
+              w[e] = pack_bf16x2(__uint_as_float(o[c][2 * e]) * inv, __uint_as_float(o[c][2 * e + 1]) * inv);
+            if (out32) {  // 32-byte stores when the output allows them (the ABI promises 16)
+              st_global_v8(orow + c * 32, w);
+              st_global_v8(orow + c * 32 + 16, w + 8);
+            } else {
+              uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+              for (int e = 0; e < 4; ++e) dst[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+            }
+          }
         }
       }
       tc_fence_before();
