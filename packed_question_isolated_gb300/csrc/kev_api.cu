@@ -35,6 +35,9 @@ float effective_scale(const kev_attn_shape* s) {
 
 int elem_size(const kev_attn_shape* s) { return s->dtype == KEV_BF16 ? 2 : 4; }
 
+// bf16 with d = 128 decodes on the tensor cores; fp32 (no TF32) and d = 64 on the CUDA cores.
+bool decode_on_tensor_cores(const kev_attn_shape* s) { return s->dtype == KEV_BF16 && s->d_h == 128; }
+
 kev_status from_cuda(cudaError_t e) { return e == cudaSuccess ? KEV_OK : KEV_ERR_CUDA; }
 
 kev_status check_prefill_common(int32_t T, const kev_interval* intervals, int32_t n, const kev_attn_shape* shape,
@@ -228,7 +231,7 @@ kev_status kev_kv_write(const void* k, const void* v, int32_t total_tokens, cons
 
 size_t kev_decode_workspace_size(int32_t n_questions, int32_t slot_cap, const kev_attn_shape* shape) {
   if (check_shape(shape) != KEV_OK || n_questions < 0 || slot_cap <= 0 || n_questions > kMaxQuestions) return 0;
-  return decode_layout(n_questions, slot_cap, shape->h_q, shape->h_kv, shape->d_h).total;
+  return decode_layout(n_questions, slot_cap, shape->h_q, shape->h_kv, shape->d_h, decode_on_tensor_cores(shape)).total;
 }
 
 kev_status kev_decode_attn(const void* q_new, const void* k_new, const void* v_new, void* pool_k, void* pool_v,
@@ -249,7 +252,8 @@ kev_status kev_decode_attn(const void* q_new, const void* k_new, const void* v_n
   if (!aligned16(q_new) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(pool_k) || !aligned16(pool_v) ||
       !aligned16(out) || ((uintptr_t)slot_ids & 3u) || ((uintptr_t)lens & 3u))
     return KEV_ERR_INVALID_ARG;
-  const DecodeLayout layout = decode_layout(n_questions, slot_cap, shape->h_q, shape->h_kv, shape->d_h);
+  const DecodeLayout layout =
+      decode_layout(n_questions, slot_cap, shape->h_q, shape->h_kv, shape->d_h, decode_on_tensor_cores(shape));
   if (!workspace || ((uintptr_t)workspace & 255u) || workspace_bytes < layout.total) return KEV_ERR_INVALID_ARG;
   const int sms = num_sms_of_current_device();
   if (sms <= 0) return KEV_ERR_CUDA;
@@ -273,6 +277,7 @@ kev_status kev_decode_attn(const void* q_new, const void* k_new, const void* v_n
   a.ws = static_cast<char*>(workspace);
   a.layout = layout;
   a.dev_status = dev_status;
+  if (decode_on_tensor_cores(shape)) return from_cuda(launch_decode_tc(a, sms, (cudaStream_t)stream));
   return from_cuda(launch_decode(a, shape->d_h, (kev_dtype)shape->dtype, sms, (cudaStream_t)stream));
 }
 

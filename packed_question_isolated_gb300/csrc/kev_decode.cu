@@ -23,6 +23,7 @@
 //            groups are summed with shuffles and one pass through shared memory.
 // When a (question, kv head) has several chunks, the CTA that finishes last (arrival
 // counter) merges the chunk results in chunk order, so the output does not depend on timing.
+#include "kev_decode_common.cuh"
 #include "kev_internal.cuh"
 #include "kev_sm100.cuh"
 
@@ -30,6 +31,9 @@ namespace kev {
 namespace {
 
 using namespace sm100;
+using dec::ItemInfo;
+using dec::range_owner;
+using dec::range_start;
 
 constexpr int kComputeWarps = 8;
 constexpr int kComputeThreads = kComputeWarps * 32;
@@ -127,65 +131,6 @@ template <> struct Elem<float> {
   __device__ static __forceinline__ float load(const void* base, int64_t idx) { return static_cast<const float*>(base)[idx]; }
 };
 
-__device__ int block_exclusive_scan(int v, int* tmp, int* total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  constexpr int nw = kThreads / 32;
-  int x = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, x, o);
-    if (lane >= o) x += y;
-  }
-  if (lane == 31) tmp[warp] = x;
-  __syncthreads();
-  int base = 0, tot = 0;
-#pragma unroll
-  for (int w = 0; w < nw; ++w) {
-    if (w < warp) base += tmp[w];
-    tot += tmp[w];
-  }
-  __syncthreads();
-  *total = tot;
-  return base + x - v;
-}
-
-struct ItemInfo {
-  int i, g, hb, c, len, slot, nch, p0, p1, h0, nh;
-};
-
-// Decodes work chunk `x` (item_base: prefix over questions of H_kv * n_hblocks * n_chunks;
-// meta: {len, slot} per question, both in shared memory).
-__device__ __forceinline__ ItemInfo decode_item(const DecodeArgs& a, const int* item_base, const int2* meta, int x,
-                                                int n_hblocks) {
-  int lo = 0, hi = a.n;
-  while (hi - lo > 1) {
-    const int mid = (lo + hi) >> 1;
-    if (item_base[mid] <= x) lo = mid; else hi = mid;
-  }
-  ItemInfo f;
-  f.i = lo;
-  const int2 m = meta[lo];
-  f.len = m.x;
-  f.slot = m.y;
-  f.nch = (f.len + 1 + kChunk - 1) / kChunk;
-  const int r = x - item_base[lo];
-  f.c = r % f.nch;
-  const int gh = r / f.nch;
-  f.hb = gh % n_hblocks;
-  f.g = gh / n_hblocks;
-  f.p0 = f.c * kChunk;
-  f.p1 = min(f.p0 + kChunk, f.len + 1);
-  f.h0 = f.g * a.group + f.hb * kHB;
-  f.nh = min(kHB, a.group - f.hb * kHB);
-  return f;
-}
-
-// Static split of the chunk space [0, total) into one contiguous range per CTA.
-__device__ __forceinline__ int range_start(int b, int total, int nb) { return (int)((int64_t)b * total / nb); }
-__device__ __forceinline__ int range_owner(int x, int total, int nb) {
-  return (int)((((int64_t)x + 1) * nb - 1) / total);
-}
-
 template <typename T, int D, int GT, int NS>
 __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
   using E = Elem<T>;
@@ -208,60 +153,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
   const int n = a.n;
   const int n_hblocks = (a.group + kHB - 1) / kHB;
 
-  // ---- prologue: validation of live questions -----------------------------------------
-  int hs = 1;
-  while (hs < 2 * n) hs <<= 1;
+  // ---- prologue: validation of live questions, compacted work list --------------------
   if (tid == 0) {
-    bars->flags = 0;
     bars->abort = 0;
     bars->never = 0;
   }
-  for (int j = tid; j < hs; j += kThreads) hash[j] = -1;
-  __syncthreads();
-  for (int i = tid; i < n; i += kThreads) {
-    const int live = a.active[i];
-    const int slot = a.slot_ids[i];
-    const int len = a.lens[i];
-    meta[i] = make_int2(len, slot);
-    if (!live) continue;
-    if (slot < 0 || slot >= a.n_slots) {
-      atomicOr(&bars->flags, 1);
-      continue;
-    }
-    if (len < 0 || len >= a.cap) atomicOr(&bars->flags, 2);
-    unsigned h = ((unsigned)slot * 2654435761u) & (unsigned)(hs - 1);
-    for (int probe = 0; probe < hs; ++probe) {
-      const int prev = atomicCAS(&hash[h], -1, slot);
-      if (prev == -1) break;
-      if (prev == slot) {
-        atomicOr(&bars->flags, 4);
-        break;
-      }
-      h = (h + 1) & (unsigned)(hs - 1);
-    }
-  }
-  __syncthreads();
-  const int f = bars->flags;
-  const int code = (f & 1) ? ST_SLOT : (f & 2) ? ST_OVERFLOW : (f & 4) ? ST_SLOT : ST_OK;
-  if (blockIdx.x == 0 && tid == 0 && a.dev_status) *a.dev_status = code;
-  if (code != ST_OK) return;
-
-  // ---- compacted work list: chunks of live questions only ------------------------------
-  int running = 0;
-  for (int base = 0; base < n; base += kThreads) {
-    const int i = base + tid;
-    int cnt = 0;
-    if (i < n && a.active[i]) cnt = a.h_kv * n_hblocks * ((meta[i].x + 1 + kChunk - 1) / kChunk);
-    int tot;
-    const int off = block_exclusive_scan(cnt, bars->scan_tmp, &tot);
-    if (i < n) item_base[i] = running + off;
-    running += tot;
-  }
+  const int running = dec::prologue<kThreads>(a, n_hblocks, item_base, meta, hash, &bars->flags, bars->scan_tmp);
+  if (running < 0) return;
   if (tid == 0) {
-    item_base[n] = running;
-    for (int s = 0; s < L::kStages; ++s) {
-      mbar_init(&bars->full[s], 1);
-    }
+    for (int s = 0; s < L::kStages; ++s) mbar_init(&bars->full[s], 1);
     fence_mbar_init();
   }
   __syncthreads();  // the hash is dead from here on: the stages may be written
@@ -280,7 +180,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
   // pool) and the item's queries, all counted on the stage's mbarrier.
   uint32_t issued[kMaxStages] = {0, 0, 0};
   auto issue = [&](int xx, int stage) {
-    const ItemInfo fi = decode_item(a, item_base, meta, xx, n_hblocks);
+    const ItemInfo fi = dec::decode_item<kHB>(a, item_base, meta, xx, n_hblocks);
     const int rows = min(fi.p1, fi.len) - fi.p0;  // the new row is not in the pool yet
     const uint32_t bytes = (uint32_t)rows * kRow;
     const uint32_t qbytes = (uint32_t)fi.nh * kRow;
@@ -313,7 +213,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
   uint32_t iter = 0;
 
   for (int x = x_begin; x < x_end; ++x, ++iter) {
-    const ItemInfo fi = decode_item(a, item_base, meta, x, n_hblocks);
+    const ItemInfo fi = dec::decode_item<kHB>(a, item_base, meta, x, n_hblocks);
     if (L::kStages == 1) {  // single stage: refill it once every thread is done with it
       named_sync();
       if (tid == 0) issue(x, 0);

@@ -88,12 +88,14 @@ inline int decode_head_block_size(int group) {
   return g <= 1 ? 1 : g <= 2 ? 2 : g <= 4 ? 4 : 8;
 }
 
-inline DecodeLayout decode_layout(int32_t n, int32_t cap, int32_t h_q, int32_t h_kv, int32_t d) {
+// `tc`: the tensor-core kernel (bf16, d = 128) takes the whole group (up to 16 q-heads, padded
+// to 16) per item; the CUDA-core kernel takes blocks of up to 8.
+inline DecodeLayout decode_layout(int32_t n, int32_t cap, int32_t h_q, int32_t h_kv, int32_t d, bool tc) {
   DecodeLayout L;
   L.max_chunks = (cap + kDecodeChunk - 1) / kDecodeChunk;
   const int32_t G = h_q / h_kv;
-  const int32_t nhb = (G + 7) / 8;
-  const int32_t GT = decode_head_block_size(G);
+  const int32_t nhb = tc ? 1 : (G + 7) / 8;
+  const int32_t GT = tc ? 16 : decode_head_block_size(G);
   size_t off = 0;
   L.counters = off;
   off = align_up(off + sizeof(int32_t) * (size_t)n * h_kv * nhb, 256);
@@ -183,7 +185,8 @@ cudaError_t launch_segments(const SegmentsArgs& a, cudaStream_t s);
 cudaError_t launch_prefill_simt(const PrefillArgs& a, int d, int num_sms, cudaStream_t s);  // fp32
 cudaError_t launch_prefill_tc(const PrefillArgs& a, int d, int num_sms, cudaStream_t s);    // bf16
 cudaError_t launch_aux(const AuxArgs& a, int num_sms, cudaStream_t s);
-cudaError_t launch_decode(const DecodeArgs& a, int d, kev_dtype dt, int num_sms, cudaStream_t s);
+cudaError_t launch_decode(const DecodeArgs& a, int d, kev_dtype dt, int num_sms, cudaStream_t s);     // CUDA cores
+cudaError_t launch_decode_tc(const DecodeArgs& a, int num_sms, cudaStream_t s);                       // bf16, d = 128
 cudaError_t launch_advance(int32_t* lens, const uint8_t* active, int32_t n, cudaStream_t s);
 
 // ---------------------------------------------------------------------------------------

@@ -22,10 +22,11 @@
 //               its tile, the tensor core runs tile B's MMAs, and the other way round.
 //   warps 0-3   softmax of tile A, warps 4-7 softmax of tile B: each thread owns one query
 //               row (its TMEM lane): tcgen05.ld of S, diagonal mask, row max on the raw
-//               scores, exp2 of one fused multiply-add per element (scale * log2 e folded),
-//               packed fp32x2 sums, P as bf16 back into TMEM, and an O rescale in TMEM only
-//               when the row's running max grew by more than 2^8 (exact: O and l always
-//               share one reference max).  The epilogue divides by l and stores bf16 rows;
+//               scores on an item's first tile only, exp2 of one fused multiply-add per
+//               element (scale * log2 e folded), packed fp32x2 sums, P as bf16 back into
+//               TMEM; a later tile recomputes the max and rescales O in TMEM only if its
+//               exponentials approach the fp32 range (exact: O and l always share one
+//               reference max).  The epilogue divides by l and stores bf16 rows;
 //               rows past the question's end are not stored.
 //   The control warpgroup (warps 8-11) hands registers to the softmax warpgroups (setmaxnreg),
 //   so a softmax thread holds its whole 128-wide score row in registers.
@@ -56,7 +57,7 @@ constexpr int kVProducerWarp = 10;
 constexpr int kRegsControl = 80;
 constexpr int kRegsSoftmax = 208;
 constexpr uint32_t kTmemCols = 512;
-constexpr float kRescaleThreshold = 8.0f;         // log2 units: rescale O when the max grows by > 2^8
+constexpr float kOverflowSum = 1.8446744e19f;      // 2^64: a tile sum above it triggers the exact path
 constexpr long long kDrainBudget = 4000000000ll;  // cycles to wait for in-flight work on abort
 
 struct TcParams {
@@ -400,42 +401,63 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int e = 0; e < 32; ++e)
               if (c * 32 + e > r) sr[c][e] = __float_as_uint(-INFINITY);
         }
-        float mt = -INFINITY;
+        // Row max (8 independent partial maxima, then combined), in scaled log2 units.
+        auto row_max = [&]() -> float {
+          float mp[8];
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
+          for (int q = 0; q < 8; ++q)
+            mp[q] = fmax3(__uint_as_float(sr[q >> 1][(q & 1) * 16]), __uint_as_float(sr[q >> 1][(q & 1) * 16 + 1]),
+                          __uint_as_float(sr[q >> 1][(q & 1) * 16 + 2]));
 #pragma unroll
-          for (int e = 0; e < 32; e += 2) mt = fmax3(mt, __uint_as_float(sr[c][e]), __uint_as_float(sr[c][e + 1]));
-        mt *= sl2;  // the scale is positive: max of scaled = scaled max
-        float alpha = 1.f;
-        bool rescale = false;
-        if (j == 0) {
-          m_run = mt;
-        } else if (mt > m_run + kRescaleThreshold) {
-          alpha = ex2_approx(m_run - mt);
-          m_run = mt;
-          l_run *= alpha;
-          rescale = true;
-        }
-        // P = exp2(s * scale * log2e - m) as bf16 pairs into the first 64 columns of S_t
-        // (S is already in registers); the PV MMA reads P from there
-        const unsigned long long negm = f2pack(-m_run, -m_run);
-        unsigned long long acc2 = 0ull;
+          for (int e = 3; e < 15; e += 2)
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t pk[16];
+            for (int q = 0; q < 8; ++q)
+              mp[q] = fmax3(mp[q], __uint_as_float(sr[q >> 1][(q & 1) * 16 + e]),
+                            __uint_as_float(sr[q >> 1][(q & 1) * 16 + e + 1]));
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const unsigned long long sv = (unsigned long long)sr[c][2 * e] | ((unsigned long long)sr[c][2 * e + 1] << 32);
-            const float2 a = unpack2(fma2(sv, sl2x2, negm));
-            const float p0 = ex2_approx(a.x), p1 = ex2_approx(a.y);
-            acc2 = add2(acc2, f2pack(p0, p1));
-            pk[e] = pack_bf16x2(p0, p1);
+          for (int q = 0; q < 8; ++q) mp[q] = fmaxf(mp[q], __uint_as_float(sr[q >> 1][(q & 1) * 16 + 15]));
+          return fmax3(fmax3(mp[0], mp[1], mp[2]), fmax3(mp[3], mp[4], mp[5]), fmaxf(mp[6], mp[7])) * sl2;
+        };
+        // P = exp2(s * scale * log2e - m) as bf16 pairs into the first 64 columns of S_t (S is
+        // already in registers; the PV MMA reads P from there); returns the row's sum of P.
+        auto exp_tile = [&](float m) -> float {
+          const unsigned long long negm = f2pack(-m, -m);
+          unsigned long long accs[4] = {0ull, 0ull, 0ull, 0ull};  // independent partial sums
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              const unsigned long long sv =
+                  (unsigned long long)sr[c][2 * e] | ((unsigned long long)sr[c][2 * e + 1] << 32);
+              const float2 a = unpack2(fma2(sv, sl2x2, negm));
+              const float p0 = ex2_approx(a.x), p1 = ex2_approx(a.y);
+              accs[e & 3] = add2(accs[e & 3], f2pack(p0, p1));
+              pk[e] = pack_bf16x2(p0, p1);
+            }
+            tmem_st16(tm_s + c * 16, pk);
           }
-          tmem_st16(tm_s + c * 16, pk);
-        }
-        const float2 acc = unpack2(acc2);
-        l_run += acc.x + acc.y;
-        if (__any_sync(0xffffffffu, rescale)) {  // PV of the previous tile is complete (S_t came after it)
+          const float2 acc = unpack2(add2(add2(accs[0], accs[1]), add2(accs[2], accs[3])));
+          return acc.x + acc.y;
+        };
+        // The reference max only guards the exponentials against overflow (P is bf16 and O, l
+        // accumulate in fp32: their precision is relative, whatever the reference).  So the
+        // first tile of an item sets it, later tiles reuse it, and only a tile whose sum
+        // signals overflow risk (its scores grew by ~2^60 over the reference) pays for a row
+        // max, rescales O and l, and recomputes P: exact in every case.
+        if (j == 0) m_run = row_max();
+        float lt = exp_tile(m_run);
+        const bool big = !(lt <= kOverflowSum);
+        float alpha = 1.f;
+        if (__any_sync(0xffffffffu, big)) {
+          if (big) {
+            const float mt = fmaxf(row_max(), m_run);
+            alpha = ex2_approx(m_run - mt);
+            m_run = mt;
+            l_run *= alpha;
+          }
+          lt = exp_tile(m_run);
+          // PV of the previous tile is complete (S_t came after it): rescale O
 #pragma unroll
           for (int c = 0; c < D / 32; ++c) {
             uint32_t o[32];
@@ -446,6 +468,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_st32(tm_o + c * 32, o);
           }
         }
+        l_run += lt;
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(&bars->p_full[t]);
