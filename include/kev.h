@@ -150,7 +150,8 @@ kev_status kev_kv_write(const void* k, const void* v, int32_t total_tokens, cons
 
 /* Bytes of decode workspace for up to `n_questions` questions in slots of `slot_cap`.
  * The workspace must be zero-filled once before its first use (e.g. cudaMemsetAsync);
- * every call leaves its counters at zero again.  Two calls in flight at the same time
+ * every call that ends in KEV_OK leaves its counters at zero again (after a call whose
+ * device status is KEV_ERR_TIMEOUT, zero it again).  Two calls in flight at the same time
  * must not share one workspace. */
 size_t kev_decode_workspace_size(int32_t n_questions, int32_t slot_cap, const kev_attn_shape* shape);
 

@@ -36,7 +36,9 @@ float effective_scale(const kev_attn_shape* s) {
 int elem_size(const kev_attn_shape* s) { return s->dtype == KEV_BF16 ? 2 : 4; }
 
 // bf16 with d = 128 decodes on the tensor cores; fp32 (no TF32) and d = 64 on the CUDA cores.
-bool decode_on_tensor_cores(const kev_attn_shape* s) { return s->dtype == KEV_BF16 && s->d_h == 128; }
+bool decode_on_tensor_cores(const kev_attn_shape* s) {
+  return s->dtype == KEV_BF16 && s->d_h == 128 && s->h_q / s->h_kv <= kDecodeTcMaxGroup;
+}
 
 kev_status from_cuda(cudaError_t e) { return e == cudaSuccess ? KEV_OK : KEV_ERR_CUDA; }
 

@@ -13,11 +13,13 @@
 // so the CUDA cores only run the softmax over 128 x 16 scores per chunk and the kernel is a
 // TMA stream of K/V tiles: decode is HBM-bound, and this keeps its instruction count tiny.
 //
-// Roles (192 threads): warp 0 issues the TMA loads (K, V tiles of 128 rows, the 16 query rows)
-// into a ring of stages; warp 1 issues the MMAs without blocking on either kind (a stage is
-// released as soon as its PV is issued and done); warps 2-5 (one thread per key row for S^T,
-// one thread per head dimension for O^T): per-head column max and sum over the chunk with
-// warp shuffles and a 4-warp exchange, the online rescale of O^T in TMEM, P^T into shared
+// Roles (224 threads): warp 0 issues the TMA loads (K, V tiles of 128 rows, the 16 query rows)
+// into a ring of stages, records each chunk's position in the stage, and pulls the K/V tiles
+// of the chunk kAhead places ahead into L2, so more of the HBM stream is in flight than the
+// stages alone hold; warp 1 issues the S MMAs, warp 6 the PV MMAs (each on its own thread, so
+// neither waits behind the other; a stage is released when its PV completes); warps 2-5 (one
+// thread per key row for S^T, one thread per head dimension for O^T): the softmax over the
+// group's heads only, with a reference max per piece and per-thread sums, P^T into shared
 // memory, the new K/V row and the zeroing of V rows past the question's length (fix-ups of
 // the chunk that holds position n), and the output / split-K partials.  Consecutive chunks of
 // one (question, kv head) in a CTA accumulate in TMEM; the pieces of one (question, kv head)
@@ -38,17 +40,29 @@ using dec::range_owner;
 using dec::range_start;
 
 constexpr int kD = 128;
-constexpr int kN = 16;             // q-heads per item (MMA N)
+constexpr int kN = 16;             // MMA N: q-heads of one group, padded to 16
 constexpr int kC = dec::kChunk;    // 128 keys per chunk
-constexpr int kThreads = 192;
+constexpr int kThreads = 224;
 constexpr int kSoftmax = 128;      // threads of warps 2-5
+constexpr int kAhead = 4;          // chunks the producer pulls into L2 ahead of their TMA load
 constexpr long long kDrainBudget = 4000000000ll;
 constexpr uint32_t kTmemCols = 64; // S^T x2 (16 cols each) + O^T (16 cols)
+// A chunk whose scores exceed the piece's reference max by more than this (log2 units) takes
+// the exact rescaling path: below it, P < 2^64 and the fp32 sums cannot overflow.
+constexpr float kLog2Guard = 64.f;
 
 struct DTcParams {
   DecodeArgs a;
   long long wait_budget;
 };
+
+// What the producer knows about the chunk in a stage: the consumers read it from here
+// instead of decoding the chunk index again.
+struct StageInfo {
+  int i, g, c, nch, len, slot, flags;  // flags: 1 first of a piece, 2 last of a piece, 4 holds position n
+  int pad;
+};
+constexpr int kFirst = 1, kLast = 2, kFix = 4;
 
 template <int NS>
 struct TSmem {
@@ -58,8 +72,10 @@ struct TSmem {
   static constexpr int kStage = 0;
   static constexpr int kPBytes = kN * kC * 2;          // P^T: 2 sub-tiles of 16 rows x 128 B
   static constexpr int kP = kStage + NS * kStageBytes;  // two P^T buffers (chunk parity)
-  static constexpr int kRed = kP + 2 * kPBytes;         // float red_m[4][16], red_l[2][4][16]
-  static constexpr int kBar = kRed + 3 * 4 * kN * 4;
+  static constexpr int kRed = kP + 2 * kPBytes;         // float red_m[4][16], red_l[4][16]
+  static constexpr int kMerge = kRed + 2 * 4 * kN * 4;  // float mm[128], ll[128]; int off[128]
+  static constexpr int kInfo = kMerge + 3 * 128 * 4;    // StageInfo[NS]
+  static constexpr int kBar = kInfo + NS * (int)sizeof(StageInfo);
   static constexpr int kBase = kBar + 512;              // int item_base[N+1], then int2 meta[N]
   static __host__ __device__ constexpr int meta_off(int n) { return kBase + ((n + 2) / 2) * 8; }
   static __host__ __device__ constexpr int bytes(int n) { return meta_off(n) + n * 8 + 1024; }
@@ -67,7 +83,7 @@ struct TSmem {
 
 struct TBars {
   uint64_t full[3], empty[3];
-  uint64_t fixed, s_full[2], s_free[2], p_full[2], o_done[2], o_free, drain;
+  uint64_t fixed, s_full[2], s_free[2], p_full[2], o_done[2], o_free, drain_s, drain_p;
   uint32_t tmem_base;
   int flags, last, abort, never;
   int scan_tmp[8];
@@ -75,6 +91,19 @@ struct TBars {
 
 __device__ __forceinline__ void named_sync_sm() {
   asm volatile("bar.sync 1, %0;" ::"n"(kSoftmax) : "memory");
+}
+// OR of a predicate over the softmax threads (named barrier 1).
+__device__ __forceinline__ bool named_or_sm(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 q, %1, 0;\n\t"
+      "bar.red.or.pred p, 1, %2, q;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)v), "n"(kSoftmax)
+      : "memory");
+  return r != 0;
 }
 
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const volatile int* abort_flag,
@@ -88,42 +117,67 @@ __device__ __forceinline__ void raise_timeout(const DecodeArgs& a, TBars* b) {
   *reinterpret_cast<volatile int*>(&b->abort) = 1;
 }
 
-// Reduce 16 per-lane values over the warp (max or sum).  Reduce-scatter: after the steps,
-// lane l holds the warp result for head H(l) = 8 b4 + 4 b3 + 2 b2 + b1 (bits of l), and lanes
-// l, l ^ 1 hold the same head.
-template <bool MAX>
-__device__ __forceinline__ float warp_reduce16(float (&v)[kN], int lane) {
+// Reduce NH per-lane values over the warp (max or sum).  Reduce-scatter halving steps over
+// lane bits 16, 8, ... leave each lane with the partial of one head, the remaining butterfly
+// steps finish it; lane l then holds the warp result for head reduce_head<NH>(l).
+template <int NH, bool MAX>
+__device__ __forceinline__ float warp_reduce(const float (&v)[NH], int lane) {
   auto op = [](float x, float y) { return MAX ? fmaxf(x, y) : x + y; };
-  float a8[8], a4[4], a2[2];
-  const bool u16 = lane & 16, u8 = lane & 8, u4 = lane & 4, u2 = lane & 2;
+  float a[NH];
 #pragma unroll
-  for (int k = 0; k < 8; ++k) {
-    const float send = u16 ? v[k] : v[k + 8];
-    const float keep = u16 ? v[k + 8] : v[k];
-    a8[k] = op(keep, __shfl_xor_sync(0xffffffffu, send, 16));
+  for (int h = 0; h < NH; ++h) a[h] = v[h];
+#pragma unroll
+  for (int half = NH / 2, bit = 16; half >= 1; half >>= 1, bit >>= 1) {
+    const bool up = lane & bit;
+#pragma unroll
+    for (int k = 0; k < half; ++k) {
+      const float send = up ? a[k] : a[k + half];
+      const float keep = up ? a[k + half] : a[k];
+      a[k] = op(keep, __shfl_xor_sync(0xffffffffu, send, bit));
+    }
   }
 #pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const float send = u8 ? a8[k] : a8[k + 4];
-    const float keep = u8 ? a8[k + 4] : a8[k];
-    a4[k] = op(keep, __shfl_xor_sync(0xffffffffu, send, 8));
-  }
-#pragma unroll
-  for (int k = 0; k < 2; ++k) {
-    const float send = u4 ? a4[k] : a4[k + 2];
-    const float keep = u4 ? a4[k + 2] : a4[k];
-    a2[k] = op(keep, __shfl_xor_sync(0xffffffffu, send, 4));
-  }
-  const float send = u2 ? a2[0] : a2[1];
-  const float keep = u2 ? a2[1] : a2[0];
-  float r = op(keep, __shfl_xor_sync(0xffffffffu, send, 2));
-  return op(r, __shfl_xor_sync(0xffffffffu, r, 1));
+  for (int bit = 16 / NH; bit >= 1; bit >>= 1) a[0] = op(a[0], __shfl_xor_sync(0xffffffffu, a[0], bit));
+  return a[0];
 }
-__device__ __forceinline__ int reduce16_head(int lane) {
-  return ((lane >> 4) & 1) * 8 + ((lane >> 3) & 1) * 4 + ((lane >> 2) & 1) * 2 + ((lane >> 1) & 1);
+template <int NH>
+__device__ __forceinline__ int reduce_head(int lane) {
+  int h = 0;
+#pragma unroll
+  for (int half = NH / 2, bit = 16; half >= 1; half >>= 1, bit >>= 1) h += (lane & bit) ? half : 0;
+  return h;
+}
+// one lane per head writes the warp result
+template <int NH>
+__device__ __forceinline__ bool reduce_writer(int lane) {
+  return (lane & (32 / NH - 1)) == 0;
 }
 
-template <int NS>
+// Sequential walk over the compacted chunk list (the producer's view): the chunk after
+// (i, g, c) is (i, g, c + 1), else (i, g + 1, 0), else chunk 0 of the next live question.
+struct Cursor {
+  int i, g, c, nch, len, slot;
+};
+__device__ __forceinline__ Cursor cursor_at(const DecodeArgs& a, const int* item_base, const int2* meta, int x) {
+  const ItemInfo f = dec::decode_item<kN>(a, item_base, meta, x, 1);
+  return Cursor{f.i, f.g, f.c, f.nch, f.len, f.slot};
+}
+__device__ __forceinline__ void cursor_next(Cursor& u, const DecodeArgs& a, const int* item_base, const int2* meta) {
+  if (++u.c < u.nch) return;
+  u.c = 0;
+  if (++u.g < a.h_kv) return;
+  u.g = 0;
+  int j = u.i + 1;
+  while (j < a.n && item_base[j + 1] == item_base[j]) ++j;  // dropped questions have no chunk
+  u.i = j;
+  if (j >= a.n) return;  // past the last chunk: not used
+  const int2 m = meta[j];
+  u.len = m.x;
+  u.slot = m.y;
+  u.nch = (u.len + 1 + kC - 1) / kC;
+}
+
+template <int NS, int NH>
 __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
                                                                const __grid_constant__ CUtensorMap tm_v,
                                                                const __grid_constant__ CUtensorMap tm_q,
@@ -134,11 +188,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
   unsigned char* smem =
       reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   TBars* bars = reinterpret_cast<TBars*>(smem + L::kBar);
+  StageInfo* info = reinterpret_cast<StageInfo*>(smem + L::kInfo);
   int* item_base = reinterpret_cast<int*>(smem + L::kBase);
   int2* meta = reinterpret_cast<int2*>(smem + L::meta_off(a.n));
   int* hash = reinterpret_cast<int*>(smem + L::kStage);
   float* red_m = reinterpret_cast<float*>(smem + L::kRed);
   float* red_l = red_m + 4 * kN;
+  float* mg_m = reinterpret_cast<float*>(smem + L::kMerge);
+  float* mg_l = mg_m + 128;
+  int* mg_off = reinterpret_cast<int*>(mg_l + 128);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   if (tid == 0) {
@@ -151,6 +209,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
   if ((int)blockIdx.x >= nb) return;
   const int x_begin = range_start(blockIdx.x, total, nb);
   const int x_end = range_start(blockIdx.x + 1, total, nb);
+  const int count = x_end - x_begin;
 
   if (tid == 0) {
     for (int s = 0; s < NS; ++s) {
@@ -161,13 +220,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
     for (int b = 0; b < 2; ++b) {
       mbar_init(&bars->s_full[b], 1);
       mbar_init(&bars->s_free[b], kSoftmax);
+      mbar_init(&bars->p_full[b], kSoftmax);
+      mbar_init(&bars->o_done[b], 1);
     }
-    mbar_init(&bars->p_full[0], kSoftmax);
-    mbar_init(&bars->p_full[1], kSoftmax);
-    mbar_init(&bars->o_done[0], 1);
-    mbar_init(&bars->o_done[1], 1);
     mbar_init(&bars->o_free, kSoftmax);
-    mbar_init(&bars->drain, 1);
+    mbar_init(&bars->drain_s, 1);
+    mbar_init(&bars->drain_p, 1);
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
@@ -193,103 +251,116 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
     if (lane == 0) {
       uint32_t issued[3] = {0, 0, 0};
       bool ok = true;
-      uint32_t it = 0;
-      for (int x = x_begin; x < x_end; ++x, ++it) {
-        const ItemInfo fi = dec::decode_item<kN>(a, item_base, meta, x, 1);
-        const int s = it % NS;
-        const uint32_t round = it / NS;
+      Cursor ld = cursor_at(a, item_base, meta, x_begin);
+      // L2 prefetch cursor: chunks [NS, kAhead) now, then chunk k + kAhead with the load of k
+      Cursor pf = ld;
+      int pf_k = 0;
+      auto prefetch_next = [&]() {
+        const int row0 = (pf.slot * a.h_kv + pf.g) * a.cap + pf.c * kC;
+        for (int c = 0; c < 2; ++c) {
+          tma_prefetch_l2_2d(&tm_k, c * 64, row0);
+          tma_prefetch_l2_2d(&tm_v, c * 64, row0);
+        }
+        cursor_next(pf, a, item_base, meta);
+        ++pf_k;
+      };
+      while (pf_k < NS && pf_k < count) {
+        cursor_next(pf, a, item_base, meta);
+        ++pf_k;
+      }
+      while (pf_k < kAhead && pf_k < count) prefetch_next();
+      for (int k = 0; k < count; ++k) {
+        const int s = k % NS;
+        const uint32_t round = k / NS;
         if (round > 0 && !mbar_wait(&bars->empty[s], (round - 1) & 1, abort_flag, budget)) {
           ok = false;
           break;
         }
+        int flags = 0;
+        if (k == 0 || ld.c == 0) flags |= kFirst;
+        if (k == count - 1 || ld.c == ld.nch - 1) flags |= kLast;
+        if (ld.c == ld.nch - 1) flags |= kFix;
+        info[s] = StageInfo{ld.i, ld.g, ld.c, ld.nch, ld.len, ld.slot, flags, 0};
         unsigned char* st = smem + L::kStage + s * L::kStageBytes;
-        const int row0 = (fi.slot * a.h_kv + fi.g) * a.cap + fi.p0;
-        mbar_arrive_expect_tx(&bars->full[s], L::kStageBytes);
+        const int row0 = (ld.slot * a.h_kv + ld.g) * a.cap + ld.c * kC;
+        const int qrow = ld.i * a.h_q + ld.g * a.group;
+        mbar_arrive_expect_tx(&bars->full[s], L::kStageBytes);  // release: info[s] is visible with the phase
         for (int c = 0; c < 2; ++c) {
           tma_load_2d(st + c * (kC * 128), &tm_k, c * 64, row0, &bars->full[s]);
           tma_load_2d(st + L::kKBytes + c * (kC * 128), &tm_v, c * 64, row0, &bars->full[s]);
-          tma_load_2d(st + 2 * L::kKBytes + c * (kN * 128), &tm_q, c * 64, fi.i * a.h_q + fi.h0, &bars->full[s]);
+          tma_load_2d(st + 2 * L::kKBytes + c * (kN * 128), &tm_q, c * 64, qrow, &bars->full[s]);
         }
         ++issued[s];
+        if (pf_k < count) prefetch_next();
+        cursor_next(ld, a, item_base, meta);
       }
       if (!ok) raise_timeout(a, bars);
       for (int s = 0; s < NS; ++s)  // every copy lands before the CTA leaves
         if (issued[s]) mbar_wait(&bars->full[s], (issued[s] - 1) & 1, never, kDrainBudget);
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------------ MMA issuer
+    // ------------------------------------------------------------------ S issuer
     if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_bf16(128, kN, false, false);  // K (K-major) x Q^T
-      constexpr uint32_t idesc_o = idesc_bf16(128, kN, true, false);   // V^T (MN-major) x P^T
-      const uint32_t p_addr = smem_u32(smem + L::kP);
-      // Non-blocking issue loop: S of the next chunk as soon as its tiles (and fix-ups) are in
-      // and an S buffer is free, PV of the next chunk as soon as its P is written.  Neither
-      // waits behind the other, so a stage is released right after its PV.
-      const int count = x_end - x_begin;
-      int ns = 0, np = 0;  // next chunk for S, for PV
-      uint32_t fix_cnt = 0, pieces = 0;
+      uint32_t fix_cnt = 0;
       bool ok = true;
-      long long t_last = clock64();
-      while (np < count) {
-        bool progressed = false;
-        if (ns < count) {
-          const ItemInfo fi = dec::decode_item<kN>(a, item_base, meta, x_begin + ns, 1);
-          const int s = ns % NS, sb = ns & 1;
-          const bool fix = fi.c == fi.nch - 1;  // the chunk with the new row is fixed up first
-          if (mbar_test(&bars->full[s], (ns / NS) & 1) && (!fix || mbar_test(&bars->fixed, fix_cnt & 1)) &&
-              (ns < 2 || mbar_test(&bars->s_free[sb], ((ns >> 1) - 1) & 1))) {
-            tc_fence_after();
-            const uint32_t k_addr = smem_u32(smem + L::kStage + s * L::kStageBytes);
-            const uint32_t q_addr = k_addr + 2 * L::kKBytes;
+      for (int k = 0; k < count; ++k) {
+        const int s = k % NS, sb = k & 1;
+        if (!mbar_wait(&bars->full[s], (k / NS) & 1, abort_flag, budget)) { ok = false; break; }
+        if (info[s].flags & kFix) {  // the new row is written into the tiles first
+          if (!mbar_wait(&bars->fixed, fix_cnt & 1, abort_flag, budget)) { ok = false; break; }
+          ++fix_cnt;
+        }
+        if (k >= 2 && !mbar_wait(&bars->s_free[sb], ((k >> 1) - 1) & 1, abort_flag, budget)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t k_addr = smem_u32(smem + L::kStage + s * L::kStageBytes);
+        const uint32_t q_addr = k_addr + 2 * L::kKBytes;
 #pragma unroll
-            for (int kk = 0; kk < kD / 16; ++kk) {
-              const uint64_t ak = sdesc_sw128(k_addr + (kk >> 2) * (kC * 128) + (kk & 3) * 32, 16, 1024);
-              const uint64_t bq = sdesc_sw128(q_addr + (kk >> 2) * (kN * 128) + (kk & 3) * 32, 16, 1024);
-              umma_bf16(tmem + sb * kN, ak, bq, idesc_s, kk > 0 ? 1u : 0u);
-            }
-            umma_commit(&bars->s_full[sb]);
-            if (fix) ++fix_cnt;
-            ++ns;
-            progressed = true;
-          }
+        for (int kk = 0; kk < kD / 16; ++kk) {
+          const uint64_t ak = sdesc_sw128(k_addr + (kk >> 2) * (kC * 128) + (kk & 3) * 32, 16, 1024);
+          const uint64_t bq = sdesc_sw128(q_addr + (kk >> 2) * (kN * 128) + (kk & 3) * 32, 16, 1024);
+          umma_bf16(tmem + sb * kN, ak, bq, idesc_s, kk > 0 ? 1u : 0u);
         }
-        if (np < ns) {
-          const int x = x_begin + np;
-          const ItemInfo fi = dec::decode_item<kN>(a, item_base, meta, x, 1);
-          const bool first = (x == x_begin) || fi.c == 0;
-          const bool last = (x == x_end - 1) || fi.c == fi.nch - 1;
-          if (mbar_test(&bars->p_full[np & 1], (np >> 1) & 1) &&
-              (!first || pieces == 0 || mbar_test(&bars->o_free, (pieces - 1) & 1))) {
-            tc_fence_after();
-            const int s = np % NS;
-            const uint32_t v_addr = smem_u32(smem + L::kStage + s * L::kStageBytes + L::kKBytes);
-#pragma unroll
-            for (int kk = 0; kk < kC / 16; ++kk) {
-              const uint64_t av = sdesc_sw128(v_addr + kk * 16 * 128, kC * 128, 1024);
-              const uint64_t bp =
-                  sdesc_sw128(p_addr + (np & 1) * L::kPBytes + (kk >> 2) * (kN * 128) + (kk & 3) * 32, 16, 1024);
-              umma_bf16(tm_o, av, bp, idesc_o, (first && kk == 0) ? 0u : 1u);
-            }
-            umma_commit(&bars->o_done[np & 1]);
-            umma_commit(&bars->empty[s]);
-            if (last) ++pieces;
-            ++np;
-            progressed = true;
-          }
-        }
-        if (progressed) {
-          t_last = clock64();
-        } else {
-          if (*abort_flag || clock64() - t_last > budget) {
-            ok = false;
-            break;
-          }
-          __nanosleep(32);  // leave the issue slots to the softmax warps
-        }
+        umma_commit(&bars->s_full[sb]);
       }
       if (!ok) raise_timeout(a, bars);
-      umma_commit(&bars->drain);  // every MMA is complete before TMEM is freed
-      mbar_wait(&bars->drain, 0, never, kDrainBudget);
+      umma_commit(&bars->drain_s);  // every MMA of this thread is complete before TMEM is freed
+      mbar_wait(&bars->drain_s, 0, never, kDrainBudget);
+    }
+  } else if (warp == 6) {
+    // ------------------------------------------------------------------ PV issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_o = idesc_bf16(128, kN, true, false);  // V^T (MN-major) x P^T
+      const uint32_t p_addr = smem_u32(smem + L::kP);
+      uint32_t pieces = 0;
+      bool ok = true;
+      for (int k = 0; k < count; ++k) {
+        const int s = k % NS;
+        // full[s] is long complete (S ran on this stage); waiting on it orders the read of info[s]
+        if (!mbar_wait(&bars->full[s], (k / NS) & 1, abort_flag, budget)) { ok = false; break; }
+        const int flags = info[s].flags;
+        const bool first = flags & kFirst;
+        if (!mbar_wait(&bars->p_full[k & 1], (k >> 1) & 1, abort_flag, budget)) { ok = false; break; }
+        if (first && pieces > 0 && !mbar_wait(&bars->o_free, (pieces - 1) & 1, abort_flag, budget)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t v_addr = smem_u32(smem + L::kStage + s * L::kStageBytes + L::kKBytes);
+#pragma unroll
+        for (int kk = 0; kk < kC / 16; ++kk) {
+          const uint64_t av = sdesc_sw128(v_addr + kk * 16 * 128, kC * 128, 1024);
+          const uint64_t bp =
+              sdesc_sw128(p_addr + (k & 1) * L::kPBytes + (kk >> 2) * (kN * 128) + (kk & 3) * 32, 16, 1024);
+          umma_bf16(tm_o, av, bp, idesc_o, (first && kk == 0) ? 0u : 1u);
+        }
+        umma_commit(&bars->o_done[k & 1]);
+        umma_commit(&bars->empty[s]);
+        if (flags & kLast) ++pieces;
+      }
+      if (!ok) raise_timeout(a, bars);
+      umma_commit(&bars->drain_p);
+      mbar_wait(&bars->drain_p, 0, never, kDrainBudget);
     }
   } else {
     // ------------------------------------------------------------------ softmax warps
@@ -302,27 +373,54 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
     float* partials = reinterpret_cast<float*>(a.ws + a.layout.partials);
     constexpr int pstride = kN * (kD + 2);
     unsigned char* pbuf = smem + L::kP;
-    float m_run[kN], l_run[kN];
-    uint32_t obs[2] = {0, 0};  // phases of o_done[0/1] seen
+    float m_ref[NH], l_thr[NH];  // reference max (identical in all threads), this thread's sums
+    uint32_t obs[2] = {0, 0};    // phases of o_done[0/1] seen
+    // A failed (timed-out) wait makes `ok` false and raises the abort flag, so that every other
+    // wait fails fast; the warps keep the same barrier sequence and leave the loop together at
+    // the next vote, so no warp is left waiting at a named barrier.
     bool ok = true;
-    uint32_t it = 0;
-    for (int x = x_begin; x < x_end; ++x, ++it) {
-      const ItemInfo fi = dec::decode_item<kN>(a, item_base, meta, x, 1);
-      const int s = it % NS, sb = it & 1;
-      const bool first = (x == x_begin) || fi.c == 0;
-      const bool last = (x == x_end - 1) || fi.c == fi.nch - 1;
-      const int nr = fi.p1 - fi.p0;  // valid rows, the new one included
+    auto wait_ok = [&](uint64_t* bar, uint32_t parity) {
+      if (!ok) return;
+      ok = warp_wait(bar, parity, abort_flag, budget);
+      if (!ok) *abort_flag = 1;
+    };
+
+    // column max of the scores over the 128 key rows (all softmax threads take part)
+    auto column_max = [&](const float (&t)[NH], float (&cm)[NH]) {
+      const float wm = warp_reduce<NH, true>(t, lane);
+      if (reduce_writer<NH>(lane)) red_m[q4 * kN + reduce_head<NH>(lane)] = wm;
+      named_sync_sm();
+#pragma unroll
+      for (int h = 0; h < NH; ++h)
+        cm[h] = fmaxf(fmaxf(red_m[h], red_m[kN + h]), fmaxf(red_m[2 * kN + h], red_m[3 * kN + h]));
+    };
+    // PV(k) complete?  (o_done[k & 1] completes once per chunk of that parity)
+    auto wait_pv = [&](int k) {
+      const int b = k & 1;
+      const uint32_t ph = (uint32_t)k >> 1;
+      if (obs[b] > ph) return;
+      wait_ok(&bars->o_done[b], ph & 1);
+      obs[b] = ph + 1;
+    };
+
+    for (int k = 0; k < count; ++k) {
+      const int s = k % NS, sb = k & 1;
+      wait_ok(&bars->full[s], (k / NS) & 1);
+      const StageInfo inf = info[s];
+      const bool first = inf.flags & kFirst, last = inf.flags & kLast;
+      const int p0 = inf.c * kC;
+      const int nr = min(kC, inf.len + 1 - p0);  // valid rows, the new one included
+      const int h0 = inf.g * a.group;
       unsigned char* kst = smem + L::kStage + s * L::kStageBytes;
       unsigned char* vst = kst + L::kKBytes;
 
-      if (fi.c == fi.nch - 1) {
+      if (inf.flags & kFix) {
         // fix-ups of the chunk that holds position n = len: the new K/V row goes into the
         // swizzled tiles (and, once, into the pool); V rows past it are zeroed (their P is 0,
         // but stale pool contents could hold NaN bit patterns)
-        if (!warp_wait(&bars->full[s], (it / NS) & 1, abort_flag, budget)) { ok = false; break; }
-        const int rn = fi.len - fi.p0;
-        const int64_t src = ((int64_t)fi.i * a.h_kv + fi.g) * kD * 2;
-        const int64_t dst = (((int64_t)fi.slot * a.h_kv + fi.g) * a.cap + fi.len) * kD * 2;
+        const int rn = inf.len - p0;
+        const int64_t src = ((int64_t)inf.i * a.h_kv + inf.g) * kD * 2;
+        const int64_t dst = (((int64_t)inf.slot * a.h_kv + inf.g) * a.cap + inf.len) * kD * 2;
         if (sid < 32) {
           const int ch = sid & 15;  // 16-byte chunk of the 256-byte row
           const bool isv = sid >= 16;
@@ -330,7 +428,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
                                                           src + ch * 16);
           unsigned char* tile = isv ? vst : kst;
           *reinterpret_cast<uint4*>(tile + (ch >> 3) * (kC * 128) + rn * 128 + (((ch & 7) ^ (rn & 7)) << 4)) = w;
-          *reinterpret_cast<uint4*>(static_cast<unsigned char*>(isv ? a.pool_v : a.pool_k) + dst + ch * 16) = w;
+          if (ok) *reinterpret_cast<uint4*>(static_cast<unsigned char*>(isv ? a.pool_v : a.pool_k) + dst + ch * 16) = w;
         }
         for (int e = (nr * 16) + sid; e < kC * 16; e += kSoftmax) {  // rows nr..127, 16 chunks each
           const int row = e >> 4, ch = e & 15;
@@ -340,172 +438,183 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
         mbar_arrive(&bars->fixed);
       }
 
-      // scores of this thread's key row for the 16 heads
-      if (!warp_wait(&bars->s_full[sb], (it >> 1) & 1, abort_flag, budget)) { ok = false; break; }
+      // scores of this thread's key row for the group's heads
+      wait_ok(&bars->s_full[sb], (k >> 1) & 1);
       tc_fence_after();
-      uint32_t sr[kN];
-      tmem_ld16(tmem + sb * kN + lane_off, sr);
-      tmem_ld_wait16(sr);
+      uint32_t sr[NH];
+      tmem_ld_cols<NH>(tmem + sb * kN + lane_off, sr);
       tc_fence_before();
       mbar_arrive(&bars->s_free[sb]);
-      float t[kN];
+      float t[NH];
       const bool valid = r < nr;
 #pragma unroll
-      for (int h = 0; h < kN; ++h) t[h] = valid ? __uint_as_float(sr[h]) * sl2 : -INFINITY;
+      for (int h = 0; h < NH; ++h) t[h] = valid ? __uint_as_float(sr[h]) * sl2 : -INFINITY;
 
-      auto column_max = [&](float (&cm)[kN]) {
-        float v[kN];
-#pragma unroll
-        for (int h = 0; h < kN; ++h) v[h] = t[h];
-        const float wm = warp_reduce16<true>(v, lane);
-        if ((lane & 1) == 0) red_m[q4 * kN + reduce16_head(lane)] = wm;
-        named_sync_sm();
-#pragma unroll
-        for (int h = 0; h < kN; ++h)
-          cm[h] = fmaxf(fmaxf(red_m[h], red_m[kN + h]), fmaxf(red_m[2 * kN + h], red_m[3 * kN + h]));
-      };
-      auto exp_and_sum = [&](float (&p)[kN], float (&cs)[kN]) {
-        float v[kN];
-#pragma unroll
-        for (int h = 0; h < kN; ++h) v[h] = p[h] = ex2_approx(t[h] - m_run[h]);
-        // exchange buffer by chunk parity: the next chunk writes the other one before any
-        // barrier, while slow threads may still read this one
-        float* rl = red_l + (it & 1) * 4 * kN;
-        const float ws = warp_reduce16<false>(v, lane);
-        if ((lane & 1) == 0) rl[q4 * kN + reduce16_head(lane)] = ws;
-        named_sync_sm();
-#pragma unroll
-        for (int h = 0; h < kN; ++h) cs[h] = (rl[h] + rl[kN + h]) + (rl[2 * kN + h] + rl[3 * kN + h]);
-      };
-      // PV(k) complete?  (o_done[k & 1] completes once per chunk of that parity)
-      auto wait_pv = [&](int k) -> bool {
-        const int b = k & 1;
-        const uint32_t ph = (uint32_t)k >> 1;
-        if (obs[b] > ph) return true;
-        if (!warp_wait(&bars->o_done[b], ph & 1, abort_flag, budget)) return false;
-        obs[b] = ph + 1;
-        return true;
-      };
-
-      // The reference max of each head is fixed at the first chunk of a piece: it only guards
-      // the exponentials against overflow (P is bf16, O and l accumulate in fp32, so their
-      // precision is relative).  A later chunk whose sum signals overflow risk (its scores
-      // grew by ~2^57 over the reference) takes the exact path: new max, O^T and l rescaled.
-      float p[kN], cs[kN];
+      // The reference max of each head is fixed at the first chunk of a piece; it only guards
+      // the exponentials against overflow (P is bf16, O and the sums accumulate in fp32, so
+      // their precision is relative).  A later chunk whose scores exceed it by more than the
+      // guard takes the exact path: new max, O^T and the sums rescaled.
       if (first) {
-        float cm[kN];
-        column_max(cm);
+        column_max(t, m_ref);  // finite: every chunk holds at least one valid row
 #pragma unroll
-        for (int h = 0; h < kN; ++h) {
-          m_run[h] = cm[h];  // finite: every chunk holds at least one row
-          l_run[h] = 0.f;
-        }
+        for (int h = 0; h < NH; ++h) l_thr[h] = 0.f;
       }
-      exp_and_sum(p, cs);
       bool big = false;
 #pragma unroll
-      for (int h = 0; h < kN; ++h) big |= !(cs[h] <= 1.8446744e19f);  // identical in all threads
-      if (big) {
-        float cm[kN], alpha[kN];
-        column_max(cm);
+      for (int h = 0; h < NH; ++h) big |= (t[h] - m_ref[h] > kLog2Guard);
+      if (named_or_sm(big || !ok)) {
+        if (named_or_sm(!ok)) break;  // every softmax thread leaves here together
+        float cm[NH], alpha[NH];
+        column_max(t, cm);
 #pragma unroll
-        for (int h = 0; h < kN; ++h) {
-          const float m_new = fmaxf(m_run[h], cm[h]);
-          alpha[h] = ex2_approx(m_run[h] - m_new);
-          m_run[h] = m_new;
-          l_run[h] *= alpha[h];
+        for (int h = 0; h < NH; ++h) {
+          const float m_new = fmaxf(m_ref[h], cm[h]);
+          alpha[h] = ex2_approx(m_ref[h] - m_new);
+          m_ref[h] = m_new;
+          l_thr[h] *= alpha[h];
         }
-        if (!first) {  // O^T holds the chunks before this one: rescale it once PV(it-1) is done
-          if (!wait_pv((int)it - 1)) { ok = false; break; }
+        if (!first) {  // O^T holds the chunks before this one: rescale it once PV(k-1) is done
+          wait_pv(k - 1);
           tc_fence_after();
-          uint32_t o[16];
-          tmem_ld16(tm_o + lane_off, o);
-          tmem_ld_wait16(o);
+          uint32_t o[NH];
+          tmem_ld_cols<NH>(tm_o + lane_off, o);
 #pragma unroll
-          for (int h = 0; h < kN; ++h) o[h] = __float_as_uint(__uint_as_float(o[h]) * alpha[h]);
-          tmem_st16(tm_o + lane_off, o);
-          tmem_st_wait();
+          for (int h = 0; h < NH; ++h) o[h] = __float_as_uint(__uint_as_float(o[h]) * alpha[h]);
+          tmem_st_cols<NH>(tm_o + lane_off, o);
         }
-        named_sync_sm();  // this chunk's sums are read by every thread before they are rewritten
-        exp_and_sum(p, cs);
       }
+      float p[NH];
 #pragma unroll
-      for (int h = 0; h < kN; ++h) l_run[h] += cs[h];
+      for (int h = 0; h < NH; ++h) {
+        p[h] = ex2_approx(t[h] - m_ref[h]);
+        l_thr[h] += p[h];
+      }
 
-      // P^T buffer it & 1 was last read by PV(it - 2)
-      if (it >= 2 && !wait_pv((int)it - 2)) { ok = false; break; }
-      // P^T: row h = head, column = key r, bf16, 128-byte swizzled (K-major B operand)
+      // P^T buffer k & 1 was last read by PV(k - 2)
+      if (k >= 2) wait_pv(k - 2);
+      // P^T: row h = head, column = key r, bf16, 128-byte swizzled (K-major B operand); rows
+      // NH..15 are never written: they only feed O^T columns that are never read
       {
-        unsigned char* pb = pbuf + (it & 1) * L::kPBytes;
+        unsigned char* pb = pbuf + (k & 1) * L::kPBytes;
         const int sub = r >> 6, kb = (r & 63) * 2;
 #pragma unroll
-        for (int h = 0; h < kN; ++h) {
+        for (int h = 0; h < NH; ++h) {
           const int off = sub * (kN * 128) + h * 128 + ((((kb >> 4) ^ (h & 7))) << 4) + (kb & 15);
           *reinterpret_cast<__nv_bfloat16*>(pb + off) = __float2bfloat16_rn(p[h]);
         }
       }
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(&bars->p_full[it & 1]);
+      mbar_arrive(&bars->p_full[k & 1]);
 
       if (!last) continue;
-      // ---- end of a piece: this thread holds dimension r of O for the 16 heads ----------
-      if (!wait_pv((int)it)) { ok = false; break; }
-      tc_fence_after();
-      float ov[kN];
+      // ---- end of a piece: this thread holds dimension r of O for the group's heads -------
+      float l_sum[NH];
       {
-        uint32_t o[16];
-        tmem_ld16(tm_o + lane_off, o);
-        tmem_ld_wait16(o);
+        const float ws = warp_reduce<NH, false>(l_thr, lane);
+        if (reduce_writer<NH>(lane)) red_l[q4 * kN + reduce_head<NH>(lane)] = ws;
+        named_sync_sm();
 #pragma unroll
-        for (int h = 0; h < kN; ++h) ov[h] = __uint_as_float(o[h]);
+        for (int h = 0; h < NH; ++h) l_sum[h] = (red_l[h] + red_l[kN + h]) + (red_l[2 * kN + h] + red_l[3 * kN + h]);
+      }
+      wait_pv(k);
+      tc_fence_after();
+      float ov[NH];
+      {
+        uint32_t o[NH];
+        tmem_ld_cols<NH>(tm_o + lane_off, o);
+#pragma unroll
+        for (int h = 0; h < NH; ++h) ov[h] = __uint_as_float(o[h]);
       }
       tc_fence_before();
       mbar_arrive(&bars->o_free);
-      const int x0 = x - fi.c;
+      const int nh = a.group;
+      const int x = x_begin + k;
+      const int x0 = x - inf.c;
       const int c_start = max(x_begin, x0) - x0;
-      const bool whole = (c_start == 0) && (fi.c == fi.nch - 1);
-      __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out);
+      const bool whole = (c_start == 0) && (inf.c == inf.nch - 1);
+      __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out) + ((int64_t)inf.i * a.h_q + h0) * kD + r;
       if (whole) {
-        for (int h = 0; h < fi.nh; ++h)
-          out[((int64_t)fi.i * a.h_q + fi.h0 + h) * kD + r] = __float2bfloat16_rn(ov[h] / l_run[h]);
+#pragma unroll
+        for (int h = 0; h < NH; ++h)
+          if (ok && h < nh) out[h * kD] = __float2bfloat16_rn(ov[h] / l_sum[h]);
         continue;
       }
-      const int cidx = fi.i * a.h_kv + fi.g;
+      const int cidx = inf.i * a.h_kv + inf.g;
       float* part = partials + ((int64_t)cidx * a.layout.max_chunks + c_start) * pstride;
 #pragma unroll
-      for (int h = 0; h < kN; ++h) part[h * kD + r] = ov[h];
-      if (sid < kN) {
-        part[kN * kD + sid] = m_run[sid];
-        part[kN * kD + kN + sid] = l_run[sid];
+      for (int h = 0; h < NH; ++h)
+        if (ok) part[h * kD + r] = ov[h];
+      if (ok && sid < NH) {
+        part[kN * kD + sid] = m_ref[sid];
+        part[kN * kD + kN + sid] = l_sum[sid];
       }
       __threadfence();  // this CTA's partial is visible before its arrival is counted
       named_sync_sm();
-      if (sid == 0) {
-        const int b_first = range_owner(x0, total, nb), b_last = range_owner(x0 + fi.nch - 1, total, nb);
-        bars->last = (atomicAdd(&counters[cidx], 1) == b_last - b_first);
-      }
+      const int b_first = range_owner(x0, total, nb), b_last = range_owner(x0 + inf.nch - 1, total, nb);
+      if (sid == 0) bars->last = ok && (atomicAdd(&counters[cidx], 1) == b_last - b_first);
       named_sync_sm();
       if (bars->last) {
+        // fixed-order merge of the pieces b_first..b_last (online over rounds of pieces whose
+        // max and sum are gathered into shared memory by one thread per (piece, head))
         __threadfence();
-        const int b_first = range_owner(x0, total, nb), b_last = range_owner(x0 + fi.nch - 1, total, nb);
         const float* base = partials + (int64_t)cidx * a.layout.max_chunks * pstride;
-        for (int h = 0; h < fi.nh; ++h) {
-          float M = -INFINITY;
-          for (int b = b_first; b <= b_last; ++b) {
-            const int cs = max(range_start(b, total, nb), x0) - x0;
-            M = fmaxf(M, __ldcg(base + cs * pstride + kN * kD + h));
-          }
-          float Lsum = 0.f, O = 0.f;
-          for (int b = b_first; b <= b_last; ++b) {
-            const int cs = max(range_start(b, total, nb), x0) - x0;
-            const float* pc = base + cs * pstride;
-            const float wgt = ex2_approx(__ldcg(pc + kN * kD + h) - M);
-            Lsum += __ldcg(pc + kN * kD + kN + h) * wgt;
-            O += __ldcg(pc + h * kD + r) * wgt;
-          }
-          out[((int64_t)fi.i * a.h_q + fi.h0 + h) * kD + r] = __float2bfloat16_rn(O / Lsum);
+        constexpr int kPer = 128 / NH;  // pieces per round
+        float M[NH], Ls[NH], O[NH];
+#pragma unroll
+        for (int h = 0; h < NH; ++h) {
+          M[h] = -INFINITY;
+          Ls[h] = 0.f;
+          O[h] = 0.f;
         }
+        for (int j0 = b_first; j0 <= b_last; j0 += kPer) {
+          const int jn = min(kPer, b_last - j0 + 1);
+          if (sid < jn * NH) {
+            const int j = sid / NH, h = sid % NH;
+            const int cs = max(range_start(j0 + j, total, nb), x0) - x0;
+            mg_m[sid] = __ldcg(base + cs * pstride + kN * kD + h);
+            mg_l[sid] = __ldcg(base + cs * pstride + kN * kD + kN + h);
+            if (h == 0) mg_off[j] = cs * pstride;
+          }
+          named_sync_sm();
+#pragma unroll
+          for (int h = 0; h < NH; ++h) {
+            float mr = M[h];
+            for (int j = 0; j < jn; ++j) mr = fmaxf(mr, mg_m[j * NH + h]);
+            const float sc = ex2_approx(M[h] - mr);  // 0 on the first round (M = -inf)
+            Ls[h] *= sc;
+            O[h] *= sc;
+            M[h] = mr;
+          }
+          int j = 0;
+          for (; j + 4 <= jn; j += 4) {
+            float ov4[4][NH];
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+#pragma unroll
+              for (int h = 0; h < NH; ++h) ov4[u][h] = __ldcg(base + mg_off[j + u] + h * kD + r);
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+#pragma unroll
+              for (int h = 0; h < NH; ++h) {
+                const float wgt = ex2_approx(mg_m[(j + u) * NH + h] - M[h]);
+                Ls[h] += mg_l[(j + u) * NH + h] * wgt;
+                O[h] += ov4[u][h] * wgt;
+              }
+          }
+          for (; j < jn; ++j) {
+#pragma unroll
+            for (int h = 0; h < NH; ++h) {
+              const float wgt = ex2_approx(mg_m[j * NH + h] - M[h]);
+              Ls[h] += mg_l[j * NH + h] * wgt;
+              O[h] += __ldcg(base + mg_off[j] + h * kD + r) * wgt;
+            }
+          }
+          named_sync_sm();  // the round's gathered values are read before the next round overwrites them
+        }
+#pragma unroll
+        for (int h = 0; h < NH; ++h)
+          if (ok && h < nh) out[h * kD] = __float2bfloat16_rn(O[h] / Ls[h]);
         if (sid == 0) counters[cidx] = 0;
       }
       named_sync_sm();  // `last` is read by every thread before the next piece may set it
@@ -560,30 +669,41 @@ long long wait_budget_cycles() {
   return 4000000000ll;
 }
 
-template <int NS>
+template <int NS, int NH>
 cudaError_t launch_ns(const DecodeArgs& a, int num_sms, cudaStream_t st, const CUtensorMap& mk,
                       const CUtensorMap& mv, const CUtensorMap& mq) {
   const int smem = TSmem<NS>::bytes(a.n);
-  cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<NS>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e =
+      cudaFuncSetAttribute(decode_tc_kernel<NS, NH>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   DTcParams p;
   p.a = a;
   p.wait_budget = wait_budget_cycles();
-  decode_tc_kernel<NS><<<num_sms, kThreads, smem, st>>>(mk, mv, mq, p);
+  decode_tc_kernel<NS, NH><<<num_sms, kThreads, smem, st>>>(mk, mv, mq, p);
   return cudaGetLastError();
+}
+
+template <int NH>
+cudaError_t launch_nh(const DecodeArgs& a, int num_sms, cudaStream_t st, const CUtensorMap& mk,
+                      const CUtensorMap& mv, const CUtensorMap& mq) {
+  constexpr int kMaxSmem = 232448;
+  if (TSmem<3>::bytes(a.n) <= kMaxSmem) return launch_ns<3, NH>(a, num_sms, st, mk, mv, mq);
+  return launch_ns<2, NH>(a, num_sms, st, mk, mv, mq);
 }
 
 }  // namespace
 
 cudaError_t launch_decode_tc(const DecodeArgs& a, int num_sms, cudaStream_t st) {
+  static_assert(kDecodeTcMaxGroup == kN, "one MMA covers the q-heads of a group");
+  if (a.group < 1 || a.group > kDecodeTcMaxGroup) return cudaErrorInvalidValue;
   CUtensorMap mk, mv, mq;
   const uint64_t pool_rows = (uint64_t)a.n_slots * a.h_kv * a.cap;
   if (!make_map(&mk, a.pool_k, pool_rows, kC) || !make_map(&mv, a.pool_v, pool_rows, kC) ||
       !make_map(&mq, a.q_new, (uint64_t)a.n * a.h_q, kN))
     return cudaErrorInvalidValue;
-  constexpr int kMaxSmem = 232448;
-  if (TSmem<3>::bytes(a.n) <= kMaxSmem) return launch_ns<3>(a, num_sms, st, mk, mv, mq);
-  return launch_ns<2>(a, num_sms, st, mk, mv, mq);
+  if (a.group <= 4) return launch_nh<4>(a, num_sms, st, mk, mv, mq);
+  if (a.group <= 8) return launch_nh<8>(a, num_sms, st, mk, mv, mq);
+  return launch_nh<16>(a, num_sms, st, mk, mv, mq);
 }
 
 }  // namespace kev

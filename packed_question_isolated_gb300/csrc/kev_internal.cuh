@@ -18,6 +18,8 @@ constexpr int kMaxQuestions = 4096;
 constexpr int kCostBins = 64;
 // Positions per decode work item (split-K chunk).
 constexpr int kDecodeChunk = 128;
+// Largest q-head group (h_q / h_kv) the tensor-core decode covers with one MMA.
+constexpr int kDecodeTcMaxGroup = 16;
 
 // Device status codes: same values as kev_status.
 enum : int32_t {

@@ -57,7 +57,7 @@ def test_decode_equals_last_row_of_packed_prefill():
         compare(got[i], full[-1], "bf16", f"question {i}")
 
 
-@pytest.mark.parametrize("G", [1, 4, 7])
+@pytest.mark.parametrize("G", [1, 4, 7, 8, 16])
 def test_random_decode_group_sizes(G):
     rng = np.random.default_rng(G)
     h_kv, d, cap, n, n_slots = 2, 128, 700, 9, 12
@@ -80,6 +80,57 @@ def test_random_decode_group_sizes(G):
     run.pool_v.copy_(torch.from_numpy(pool_v).view(torch.bfloat16))
     run.run()
     assert np.array_equal(first, host(run.out))
+
+
+def _ramp_pools(rng, n_slots, h_kv, cap, d, growth):
+    """K rows aligned with a fixed +-1 direction u and growing with position: q = u scores
+    position j at growth * j (log2 units, after the 1/sqrt(d) scale), so later chunks exceed
+    the first chunk of a piece by far more than 2^64 in exp2."""
+    u = np.where(rng.random(d) < 0.5, -1.0, 1.0).astype(np.float32)
+    step = growth / (d / np.sqrt(d) * np.log2(np.e))  # per-position growth of k along u
+    ramp = (np.arange(cap, dtype=np.float32) * step)[None, None, :, None]
+    noise = rng.standard_normal((n_slots, h_kv, cap, d), dtype=np.float32) * 0.05
+    pool_k = W.f32_to_bf16_bits(u[None, None, None, :] * ramp + noise)
+    pool_v = W.f32_to_bf16_bits(rng.standard_normal((n_slots, h_kv, cap, d), dtype=np.float32))
+    return u, pool_k, pool_v
+
+
+def test_decode_scores_growing_past_the_reference_max():
+    rng = np.random.default_rng(21)
+    h_kv, G, d, cap, n = 4, 4, 128, 4096, 8
+    u, pool_k, pool_v = _ramp_pools(rng, n, h_kv, cap, d, growth=0.25)  # ~32 log2 units per chunk
+    slot_ids = rng.permutation(n).astype(np.int32)
+    lens = rng.integers(3000, cap - 1, n).astype(np.int32)
+    active = np.ones(n, np.uint8)
+    q_new = W.f32_to_bf16_bits(np.broadcast_to(u, (n, h_kv * G, d)).copy())
+    k_new = W.f32_to_bf16_bits(rng.standard_normal((n, h_kv, d), dtype=np.float32))
+    v_new = W.f32_to_bf16_bits(rng.standard_normal((n, h_kv, d), dtype=np.float32))
+    run = DecodeRun("bf16", h_kv * G, h_kv, d, pool_k, pool_v, slot_ids, lens, active, q_new, k_new, v_new,
+                    cap, n)
+    run.run()
+    assert run.device_status() == 0
+    _check_decode(run, pool_k, pool_v, slot_ids, lens, active, q_new, k_new, v_new, "bf16")
+
+
+@pytest.mark.parametrize("h_kv,G", [(1, 4), (1, 16)])
+def test_long_context_pieces_merged_across_many_ctas(h_kv, G):
+    """Few (question, kv head) pairs, each far longer than one CTA's share of the chunks: every
+    pair is split over dozens of CTAs and merged in more than one round."""
+    rng = np.random.default_rng(31 + G)
+    d, cap, n = 128, 40000, 2
+    pool_k = W.f32_to_bf16_bits(rng.standard_normal((n, h_kv, cap, d), dtype=np.float32))
+    pool_v = W.f32_to_bf16_bits(rng.standard_normal((n, h_kv, cap, d), dtype=np.float32))
+    slot_ids = np.array([1, 0], np.int32)
+    lens = np.array([cap - 1, 23456], np.int32)
+    active = np.ones(n, np.uint8)
+    q_new = W.f32_to_bf16_bits(rng.standard_normal((n, h_kv * G, d), dtype=np.float32))
+    k_new = W.f32_to_bf16_bits(rng.standard_normal((n, h_kv, d), dtype=np.float32))
+    v_new = W.f32_to_bf16_bits(rng.standard_normal((n, h_kv, d), dtype=np.float32))
+    run = DecodeRun("bf16", h_kv * G, h_kv, d, pool_k, pool_v, slot_ids, lens, active, q_new, k_new, v_new,
+                    cap, n)
+    run.run()
+    assert run.device_status() == 0
+    _check_decode(run, pool_k, pool_v, slot_ids, lens, active, q_new, k_new, v_new, "bf16")
 
 
 def test_qwen3_8b_decode_config():

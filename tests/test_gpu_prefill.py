@@ -153,6 +153,27 @@ def test_work_list_covers_exactly_the_allowed_tiles():
     assert costs == sorted(costs, reverse=True), "items are not ordered longest first"
 
 
+def test_scores_growing_past_the_reference_max():
+    """Keys aligned with the queries and growing along the sequence: later key tiles exceed the
+    first tile of an item by far more than 2^64 in exp2 (the exact rescaling path)."""
+    rng = np.random.default_rng(23)
+    h_q, h_kv, d, L = 4, 2, 128, 900
+    w = W.random_case(23, [L, 130], h_q, h_kv, d, "bf16", gaps=[1, 0], tail=2)
+    u = np.where(rng.random(d) < 0.5, -1.0, 1.0).astype(np.float32)
+    step = 0.25 / (d / np.sqrt(d) * np.log2(np.e))  # ~32 log2 units per 128 keys
+    pos = np.zeros(w.total_tokens, np.float32)
+    for s0, e0 in w.intervals:
+        pos[s0:e0] = np.arange(e0 - s0, dtype=np.float32)
+    k = u[None, None, :] * (pos * step)[:, None, None] + rng.standard_normal(
+        (w.total_tokens, h_kv, d), dtype=np.float32) * 0.05
+    w.k = W.f32_to_bf16_bits(k)
+    w.q = W.f32_to_bf16_bits(np.broadcast_to(u, (w.total_tokens, h_q, d)).copy())
+    run = PrefillRun(w)
+    run.run()
+    assert run.device_status() == 0
+    compare(f64(run.out, w.dtype), _oracle_out(w), w.dtype, "growing scores")
+
+
 def test_empty_batch_and_all_empty_questions():
     w = W.random_case(5, [0, 0], 4, 2, 64, "bf16", gaps=[3, 2], tail=1)
     run = PrefillRun(w)
