@@ -210,9 +210,10 @@ kev_status kev_read_status(const int32_t* dev_status, kev_stream_t stream);
 const char* kev_status_string(kev_status status);
 
 /* Number of kernel launches the most recent successful call of each entry point enqueues
- * (a constant per entry point, for launch accounting): 0 = prefill_attn,
- * 1 = prefill_from_segments, 2 = build_segments, 3 = kv_write, 4 = decode_attn,
- * 5 = decode_advance.  -1 for an unknown id. */
+ * (for launch accounting): 0 = prefill_attn, 1 = prefill_from_segments, 2 = build_segments,
+ * 3 = kv_write, 4 = decode_attn (2 when the last call ran on the tensor cores: bf16 with
+ * d_h = 128, decode and merge kernels; 1 otherwise and before any call), 5 = decode_advance.
+ * -1 for an unknown id. */
 int32_t kev_launch_count(int32_t entry_point);
 
 #ifdef __cplusplus

@@ -3,11 +3,16 @@
 #include <math.h>
 #include <string.h>
 
+#include <atomic>
+
 #include "kev_internal.cuh"
 
 using namespace kev;
 
 namespace {
+
+// kernel launches of the most recent successful kev_decode_attn (2 on the tensor-core path)
+std::atomic<int32_t> g_decode_launches{1};
 
 bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
@@ -279,8 +284,14 @@ kev_status kev_decode_attn(const void* q_new, const void* k_new, const void* v_n
   a.ws = static_cast<char*>(workspace);
   a.layout = layout;
   a.dev_status = dev_status;
-  if (decode_on_tensor_cores(shape)) return from_cuda(launch_decode_tc(a, sms, (cudaStream_t)stream));
-  return from_cuda(launch_decode(a, shape->d_h, (kev_dtype)shape->dtype, sms, (cudaStream_t)stream));
+  if (decode_on_tensor_cores(shape)) {  // decode kernel + merge kernel
+    st = from_cuda(launch_decode_tc(a, sms, (cudaStream_t)stream));
+    if (st == KEV_OK) g_decode_launches.store(2);
+    return st;
+  }
+  st = from_cuda(launch_decode(a, shape->d_h, (kev_dtype)shape->dtype, sms, (cudaStream_t)stream));
+  if (st == KEV_OK) g_decode_launches.store(1);
+  return st;
 }
 
 kev_status kev_decode_advance(int32_t* lens, const uint8_t* active, int32_t n, kev_stream_t stream) {
@@ -319,7 +330,7 @@ int32_t kev_launch_count(int32_t entry_point) {
     case 1: return 2;  // attention, slot write / gap zero
     case 2: return 1;
     case 3: return 2;  // segments, slot write
-    case 4: return 1;
+    case 4: return g_decode_launches.load();
     case 5: return 1;
   }
   return -1;

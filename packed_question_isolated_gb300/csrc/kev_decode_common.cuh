@@ -78,10 +78,11 @@ __device__ __forceinline__ int range_owner(int x, int total, int nb) {
 // questions (slot range, room for the new row, no slot shared by two live questions; a
 // shared-memory hash finds duplicates), and the prefix sum of their chunks into
 // `item_base`.  `hash` (int[2 * kMaxQuestions]) may alias memory the caller uses later.
-// Returns the number of chunks, or -1 when the call is invalid (block 0 stores the status).
+// Returns the number of chunks, or -1 when the call is invalid (block 0 stores the status, and
+// also the validation code into *code_out when that is not null).
 template <int NT>
 __device__ int prologue(const DecodeArgs& a, int n_hblocks, int* item_base, int2* meta, int* hash, int* flags,
-                        int* scan_tmp) {
+                        int* scan_tmp, int* code_out = nullptr) {
   const int tid = threadIdx.x;
   const int n = a.n;
   int hs = 1;
@@ -114,7 +115,10 @@ __device__ int prologue(const DecodeArgs& a, int n_hblocks, int* item_base, int2
   __syncthreads();
   const int f = *flags;
   const int code = (f & 1) ? ST_SLOT : (f & 2) ? ST_OVERFLOW : (f & 4) ? ST_SLOT : ST_OK;
-  if (blockIdx.x == 0 && tid == 0 && a.dev_status) *a.dev_status = code;
+  if (blockIdx.x == 0 && tid == 0) {
+    if (a.dev_status) *a.dev_status = code;
+    if (code_out) *code_out = code;
+  }
   if (code != ST_OK) return -1;
 
   int running = 0;

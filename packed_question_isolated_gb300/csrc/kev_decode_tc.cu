@@ -36,17 +36,15 @@ namespace {
 
 using namespace sm100;
 using dec::ItemInfo;
-using dec::range_owner;
-using dec::range_start;
 
 constexpr int kD = 128;
 constexpr int kN = 16;             // MMA N: q-heads of one group, padded to 16
 constexpr int kC = dec::kChunk;    // 128 keys per chunk
-constexpr int kThreads = 224;
-constexpr int kSoftmax = 128;      // threads of warps 2-5
-constexpr int kAhead = 4;          // chunks the producer pulls into L2 ahead of their TMA load
+constexpr int kBatch = 4;          // consecutive chunks per dynamic grab
+constexpr int kThreads = 352;
+constexpr int kQuad = 128;         // threads of the softmax (warps 2-5) and of the epilogue (warps 7-10)
 constexpr long long kDrainBudget = 4000000000ll;
-constexpr uint32_t kTmemCols = 64; // S^T x2 (16 cols each) + O^T (16 cols)
+constexpr uint32_t kTmemCols = 64; // S^T x2 (cols 0, 16) + O^T x2 (cols 32, 48), 16 cols each
 // A chunk whose scores exceed the piece's reference max by more than this (log2 units) takes
 // the exact rescaling path: below it, P < 2^64 and the fp32 sums cannot overflow.
 constexpr float kLog2Guard = 64.f;
@@ -56,13 +54,21 @@ struct DTcParams {
   long long wait_budget;
 };
 
-// What the producer knows about the chunk in a stage: the consumers read it from here
-// instead of decoding the chunk index again.
+// What the producer knows about the chunk in a stage; the consumers read it from here.
 struct StageInfo {
-  int i, g, c, nch, len, slot, flags;  // flags: 1 first of a piece, 2 last of a piece, 4 holds position n
-  int pad;
+  int i, g, c, nch, len, slot;
+  int xi0;    // global index of chunk 0 of this (question, kv head)
+  int flags;  // kFirst / kLast of a piece, kFix: holds position n, kEnd: no more chunks
 };
-constexpr int kFirst = 1, kLast = 2, kFix = 4;
+constexpr int kFirst = 1, kLast = 2, kFix = 4, kEnd = 8;
+
+// A finished piece, handed from the softmax to the epilogue warps.
+struct PieceInfo {
+  int i, g, c_start, nch, n_in, xi0, flags, pad;  // flags: kWhole, kEnd
+  float m[kN];                                    // reference max per head (log2 units)
+  float l4[4][kN];                                // per-warp partial sums per head
+};
+constexpr int kWhole = 1;
 
 template <int NS>
 struct TSmem {
@@ -70,38 +76,42 @@ struct TSmem {
   static constexpr int kQBytes = kN * kD * 2;        // 4 KB, 2 sub-tiles of 16 rows x 128 B
   static constexpr int kStageBytes = 2 * kKBytes + kQBytes;
   static constexpr int kStage = 0;
-  static constexpr int kPBytes = kN * kC * 2;          // P^T: 2 sub-tiles of 16 rows x 128 B
-  static constexpr int kP = kStage + NS * kStageBytes;  // two P^T buffers (chunk parity)
-  static constexpr int kRed = kP + 2 * kPBytes;         // float red_m[4][16], red_l[4][16]
-  static constexpr int kMerge = kRed + 2 * 4 * kN * 4;  // float mm[128], ll[128]; int off[128]
-  static constexpr int kInfo = kMerge + 3 * 128 * 4;    // StageInfo[NS]
+  static constexpr int kPBytes = kN * kC * 2;           // P^T: 2 sub-tiles of 16 rows x 128 B
+  static constexpr int kP = kStage + NS * kStageBytes;   // two P^T buffers (chunk parity)
+  static constexpr int kRed = kP + 2 * kPBytes;          // float red_m[4][16]
+  static constexpr int kPiece = kRed + 4 * kN * 4;       // PieceInfo[2]
+  static constexpr int kInfo = kPiece + 2 * (int)sizeof(PieceInfo);  // StageInfo[NS]
   static constexpr int kBar = kInfo + NS * (int)sizeof(StageInfo);
-  static constexpr int kBase = kBar + 512;              // int item_base[N+1], then int2 meta[N]
+  static constexpr int kBase = kBar + 512;               // int item_base[N+1], then int2 meta[N]
   static __host__ __device__ constexpr int meta_off(int n) { return kBase + ((n + 2) / 2) * 8; }
   static __host__ __device__ constexpr int bytes(int n) { return meta_off(n) + n * 8 + 1024; }
 };
 
 struct TBars {
   uint64_t full[3], empty[3];
-  uint64_t fixed, s_full[2], s_free[2], p_full[2], o_done[2], o_free, drain_s, drain_p;
+  uint64_t fixed, s_full[2], s_free[2], p_full[2], o_done[2];
+  uint64_t o_full[2], o_free[2], pc_full[2];  // per piece buffer: O^T complete, O^T + info consumed, info written
+  uint64_t drain_s, drain_p;
   uint32_t tmem_base;
   int flags, last, abort, never;
-  int scan_tmp[8];
+  int scan_tmp[11];
 };
 
-__device__ __forceinline__ void named_sync_sm() {
-  asm volatile("bar.sync 1, %0;" ::"n"(kSoftmax) : "memory");
+// named barriers: 1 = softmax warps, 2 = epilogue warps
+template <int ID>
+__device__ __forceinline__ void named_sync() {
+  asm volatile("bar.sync %0, %1;" ::"n"(ID), "n"(kQuad) : "memory");
 }
-// OR of a predicate over the softmax threads (named barrier 1).
-__device__ __forceinline__ bool named_or_sm(bool v) {
+template <int ID>
+__device__ __forceinline__ bool named_or(bool v) {
   uint32_t r;
   asm volatile(
       "{\n\t.reg .pred p, q;\n\t"
       "setp.ne.u32 q, %1, 0;\n\t"
-      "bar.red.or.pred p, 1, %2, q;\n\t"
+      "bar.red.or.pred p, %2, %3, q;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(r)
-      : "r"((uint32_t)v), "n"(kSoftmax)
+      : "r"((uint32_t)v), "n"(ID), "n"(kQuad)
       : "memory");
   return r != 0;
 }
@@ -114,6 +124,7 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const 
 
 __device__ __forceinline__ void raise_timeout(const DecodeArgs& a, TBars* b) {
   set_status(a.dev_status, ST_TIMEOUT);
+  reinterpret_cast<int*>(a.ws + a.layout.sched)[2] = ST_TIMEOUT;  // the merge kernel skips the call
   *reinterpret_cast<volatile int*>(&b->abort) = 1;
 }
 
@@ -153,8 +164,8 @@ __device__ __forceinline__ bool reduce_writer(int lane) {
   return (lane & (32 / NH - 1)) == 0;
 }
 
-// Sequential walk over the compacted chunk list (the producer's view): the chunk after
-// (i, g, c) is (i, g, c + 1), else (i, g + 1, 0), else chunk 0 of the next live question.
+// Sequential walk over the compacted chunk list: the chunk after (i, g, c) is (i, g, c + 1),
+// else (i, g + 1, 0), else chunk 0 of the next live question.
 struct Cursor {
   int i, g, c, nch, len, slot;
 };
@@ -189,444 +200,509 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
       reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   TBars* bars = reinterpret_cast<TBars*>(smem + L::kBar);
   StageInfo* info = reinterpret_cast<StageInfo*>(smem + L::kInfo);
+  PieceInfo* pinfo = reinterpret_cast<PieceInfo*>(smem + L::kPiece);
   int* item_base = reinterpret_cast<int*>(smem + L::kBase);
   int2* meta = reinterpret_cast<int2*>(smem + L::meta_off(a.n));
   int* hash = reinterpret_cast<int*>(smem + L::kStage);
   float* red_m = reinterpret_cast<float*>(smem + L::kRed);
-  float* red_l = red_m + 4 * kN;
-  float* mg_m = reinterpret_cast<float*>(smem + L::kMerge);
-  float* mg_l = mg_m + 128;
-  int* mg_off = reinterpret_cast<int*>(mg_l + 128);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  int* sched = reinterpret_cast<int*>(a.ws + a.layout.sched);
 
+  // the first batch grab goes out now; its latency hides behind the validation (the merge
+  // kernel that follows resets the counter for the next call)
+  int grab = 0;
   if (tid == 0) {
+    grab = atomicAdd(&sched[0], 1);
     bars->abort = 0;
     bars->never = 0;
   }
-  const int total = dec::prologue<kThreads>(a, 1, item_base, meta, hash, &bars->flags, bars->scan_tmp);
-  if (total < 0) return;
-  const int nb = min((int)gridDim.x, total);  // every CTA range non-empty
-  if ((int)blockIdx.x >= nb) return;
-  const int x_begin = range_start(blockIdx.x, total, nb);
-  const int x_end = range_start(blockIdx.x + 1, total, nb);
-  const int count = x_end - x_begin;
+  const int total = dec::prologue<kThreads>(a, 1, item_base, meta, hash, &bars->flags, bars->scan_tmp, &sched[2]);
 
-  if (tid == 0) {
-    for (int s = 0; s < NS; ++s) {
-      mbar_init(&bars->full[s], 1);
-      mbar_init(&bars->empty[s], 1);
+  if (total >= 0) {
+    if (tid == 0) {
+      for (int s = 0; s < NS; ++s) {
+        mbar_init(&bars->full[s], 1);
+        mbar_init(&bars->empty[s], 1);
+      }
+      mbar_init(&bars->fixed, kQuad);
+      for (int b = 0; b < 2; ++b) {
+        mbar_init(&bars->s_full[b], 1);
+        mbar_init(&bars->s_free[b], kQuad);
+        mbar_init(&bars->p_full[b], kQuad);
+        mbar_init(&bars->o_done[b], 1);
+        mbar_init(&bars->o_full[b], 1);
+        mbar_init(&bars->o_free[b], kQuad);
+        mbar_init(&bars->pc_full[b], kQuad);
+      }
+      mbar_init(&bars->drain_s, 1);
+      mbar_init(&bars->drain_p, 1);
+      fence_mbar_init();
     }
-    mbar_init(&bars->fixed, kSoftmax);
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&bars->s_full[b], 1);
-      mbar_init(&bars->s_free[b], kSoftmax);
-      mbar_init(&bars->p_full[b], kSoftmax);
-      mbar_init(&bars->o_done[b], 1);
+    if (warp == 0 && lane == 0) {
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      tma_prefetch_desc(&tm_q);
     }
-    mbar_init(&bars->o_free, kSoftmax);
-    mbar_init(&bars->drain_s, 1);
-    mbar_init(&bars->drain_p, 1);
-    fence_mbar_init();
-  }
-  if (warp == 0 && lane == 0) {
-    tma_prefetch_desc(&tm_k);
-    tma_prefetch_desc(&tm_v);
-    tma_prefetch_desc(&tm_q);
-  }
-  if (warp == 1) {
-    tmem_alloc(&bars->tmem_base, kTmemCols);
-    tmem_relinquish();
-  }
-  tc_fence_before();
-  __syncthreads();  // the hash is dead from here on: the stages may be written
-  tc_fence_after();
-  const uint32_t tmem = bars->tmem_base;
-  const uint32_t tm_o = tmem + 2 * kN;
-  volatile int* abort_flag = &bars->abort;
-  const volatile int* never = &bars->never;
-  const long long budget = prm.wait_budget;
-
-  if (warp == 0) {
-    // ------------------------------------------------------------------ TMA producer
-    if (lane == 0) {
-      uint32_t issued[3] = {0, 0, 0};
-      bool ok = true;
-      Cursor ld = cursor_at(a, item_base, meta, x_begin);
-      // L2 prefetch cursor: chunks [NS, kAhead) now, then chunk k + kAhead with the load of k
-      Cursor pf = ld;
-      int pf_k = 0;
-      auto prefetch_next = [&]() {
-        const int row0 = (pf.slot * a.h_kv + pf.g) * a.cap + pf.c * kC;
-        for (int c = 0; c < 2; ++c) {
-          tma_prefetch_l2_2d(&tm_k, c * 64, row0);
-          tma_prefetch_l2_2d(&tm_v, c * 64, row0);
-        }
-        cursor_next(pf, a, item_base, meta);
-        ++pf_k;
-      };
-      while (pf_k < NS && pf_k < count) {
-        cursor_next(pf, a, item_base, meta);
-        ++pf_k;
-      }
-      while (pf_k < kAhead && pf_k < count) prefetch_next();
-      for (int k = 0; k < count; ++k) {
-        const int s = k % NS;
-        const uint32_t round = k / NS;
-        if (round > 0 && !mbar_wait(&bars->empty[s], (round - 1) & 1, abort_flag, budget)) {
-          ok = false;
-          break;
-        }
-        int flags = 0;
-        if (k == 0 || ld.c == 0) flags |= kFirst;
-        if (k == count - 1 || ld.c == ld.nch - 1) flags |= kLast;
-        if (ld.c == ld.nch - 1) flags |= kFix;
-        info[s] = StageInfo{ld.i, ld.g, ld.c, ld.nch, ld.len, ld.slot, flags, 0};
-        unsigned char* st = smem + L::kStage + s * L::kStageBytes;
-        const int row0 = (ld.slot * a.h_kv + ld.g) * a.cap + ld.c * kC;
-        const int qrow = ld.i * a.h_q + ld.g * a.group;
-        mbar_arrive_expect_tx(&bars->full[s], L::kStageBytes);  // release: info[s] is visible with the phase
-        for (int c = 0; c < 2; ++c) {
-          tma_load_2d(st + c * (kC * 128), &tm_k, c * 64, row0, &bars->full[s]);
-          tma_load_2d(st + L::kKBytes + c * (kC * 128), &tm_v, c * 64, row0, &bars->full[s]);
-          tma_load_2d(st + 2 * L::kKBytes + c * (kN * 128), &tm_q, c * 64, qrow, &bars->full[s]);
-        }
-        ++issued[s];
-        if (pf_k < count) prefetch_next();
-        cursor_next(ld, a, item_base, meta);
-      }
-      if (!ok) raise_timeout(a, bars);
-      for (int s = 0; s < NS; ++s)  // every copy lands before the CTA leaves
-        if (issued[s]) mbar_wait(&bars->full[s], (issued[s] - 1) & 1, never, kDrainBudget);
+    if (warp == 1) {
+      tmem_alloc(&bars->tmem_base, kTmemCols);
+      tmem_relinquish();
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------------ S issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc_s = idesc_bf16(128, kN, false, false);  // K (K-major) x Q^T
-      uint32_t fix_cnt = 0;
-      bool ok = true;
-      for (int k = 0; k < count; ++k) {
-        const int s = k % NS, sb = k & 1;
-        if (!mbar_wait(&bars->full[s], (k / NS) & 1, abort_flag, budget)) { ok = false; break; }
-        if (info[s].flags & kFix) {  // the new row is written into the tiles first
-          if (!mbar_wait(&bars->fixed, fix_cnt & 1, abort_flag, budget)) { ok = false; break; }
-          ++fix_cnt;
+    tc_fence_before();
+    __syncthreads();  // the hash is dead from here on: the stages may be written
+    tc_fence_after();
+    const uint32_t tmem = bars->tmem_base;
+    volatile int* abort_flag = &bars->abort;
+    const volatile int* never = &bars->never;
+    const long long budget = prm.wait_budget;
+
+    if (warp == 0) {
+      // ---------------------------------------------------------------- TMA producer
+      if (lane == 0) {
+        uint32_t issued[3] = {0, 0, 0};
+        bool ok = true;
+        const int nbat = (total + kBatch - 1) / kBatch;
+        int k = 0;  // position in the stage ring
+        int bat = grab;
+        while (ok && bat < nbat) {
+          const int next = atomicAdd(&sched[0], 1);  // used when this batch is issued
+          const int x0 = bat * kBatch, x1 = min(x0 + kBatch, total);
+          Cursor u = cursor_at(a, item_base, meta, x0);
+          for (int x = x0; x < x1; ++x, ++k) {
+            const int s = k % NS;
+            const uint32_t round = k / NS;
+            if (round > 0 && !mbar_wait(&bars->empty[s], (round - 1) & 1, abort_flag, budget)) {
+              ok = false;
+              break;
+            }
+            int flags = 0;
+            if (x == x0 || u.c == 0) flags |= kFirst;
+            if (x == x1 - 1 || u.c == u.nch - 1) flags |= kLast;
+            if (u.c == u.nch - 1) flags |= kFix;
+            info[s] = StageInfo{u.i, u.g, u.c, u.nch, u.len, u.slot, x - u.c, flags};
+            unsigned char* st = smem + L::kStage + s * L::kStageBytes;
+            const int row0 = (u.slot * a.h_kv + u.g) * a.cap + u.c * kC;
+            const int qrow = u.i * a.h_q + u.g * a.group;
+            mbar_arrive_expect_tx(&bars->full[s], L::kStageBytes);  // release: info[s] is visible with the phase
+            for (int c = 0; c < 2; ++c) {
+              tma_load_2d(st + c * (kC * 128), &tm_k, c * 64, row0, &bars->full[s]);
+              tma_load_2d(st + L::kKBytes + c * (kC * 128), &tm_v, c * 64, row0, &bars->full[s]);
+              tma_load_2d(st + 2 * L::kKBytes + c * (kN * 128), &tm_q, c * 64, qrow, &bars->full[s]);
+            }
+            ++issued[s];
+            cursor_next(u, a, item_base, meta);
+          }
+          bat = next;
         }
-        if (k >= 2 && !mbar_wait(&bars->s_free[sb], ((k >> 1) - 1) & 1, abort_flag, budget)) { ok = false; break; }
-        tc_fence_after();
-        const uint32_t k_addr = smem_u32(smem + L::kStage + s * L::kStageBytes);
-        const uint32_t q_addr = k_addr + 2 * L::kKBytes;
-#pragma unroll
-        for (int kk = 0; kk < kD / 16; ++kk) {
-          const uint64_t ak = sdesc_sw128(k_addr + (kk >> 2) * (kC * 128) + (kk & 3) * 32, 16, 1024);
-          const uint64_t bq = sdesc_sw128(q_addr + (kk >> 2) * (kN * 128) + (kk & 3) * 32, 16, 1024);
-          umma_bf16(tmem + sb * kN, ak, bq, idesc_s, kk > 0 ? 1u : 0u);
+        if (ok) {  // end of the stream: a stage whose info says so, completed without copies
+          const int s = k % NS;
+          const uint32_t round = k / NS;
+          if (round > 0 && !mbar_wait(&bars->empty[s], (round - 1) & 1, abort_flag, budget)) {
+            ok = false;
+          } else {
+            info[s].flags = kEnd;
+            mbar_arrive(&bars->full[s]);
+          }
         }
-        umma_commit(&bars->s_full[sb]);
+        if (!ok) {
+          raise_timeout(a, bars);
+          for (int s = 0; s < NS; ++s)  // every copy lands before the CTA leaves
+            if (issued[s]) mbar_wait(&bars->full[s], (issued[s] - 1) & 1, never, kDrainBudget);
+        }
       }
-      if (!ok) raise_timeout(a, bars);
-      umma_commit(&bars->drain_s);  // every MMA of this thread is complete before TMEM is freed
-      mbar_wait(&bars->drain_s, 0, never, kDrainBudget);
-    }
-  } else if (warp == 6) {
-    // ------------------------------------------------------------------ PV issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc_o = idesc_bf16(128, kN, true, false);  // V^T (MN-major) x P^T
-      const uint32_t p_addr = smem_u32(smem + L::kP);
-      uint32_t pieces = 0;
-      bool ok = true;
-      for (int k = 0; k < count; ++k) {
-        const int s = k % NS;
-        // full[s] is long complete (S ran on this stage); waiting on it orders the read of info[s]
-        if (!mbar_wait(&bars->full[s], (k / NS) & 1, abort_flag, budget)) { ok = false; break; }
-        const int flags = info[s].flags;
-        const bool first = flags & kFirst;
-        if (!mbar_wait(&bars->p_full[k & 1], (k >> 1) & 1, abort_flag, budget)) { ok = false; break; }
-        if (first && pieces > 0 && !mbar_wait(&bars->o_free, (pieces - 1) & 1, abort_flag, budget)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t v_addr = smem_u32(smem + L::kStage + s * L::kStageBytes + L::kKBytes);
-#pragma unroll
-        for (int kk = 0; kk < kC / 16; ++kk) {
-          const uint64_t av = sdesc_sw128(v_addr + kk * 16 * 128, kC * 128, 1024);
-          const uint64_t bp =
-              sdesc_sw128(p_addr + (k & 1) * L::kPBytes + (kk >> 2) * (kN * 128) + (kk & 3) * 32, 16, 1024);
-          umma_bf16(tm_o, av, bp, idesc_o, (first && kk == 0) ? 0u : 1u);
-        }
-        umma_commit(&bars->o_done[k & 1]);
-        umma_commit(&bars->empty[s]);
-        if (flags & kLast) ++pieces;
-      }
-      if (!ok) raise_timeout(a, bars);
-      umma_commit(&bars->drain_p);
-      mbar_wait(&bars->drain_p, 0, never, kDrainBudget);
-    }
-  } else {
-    // ------------------------------------------------------------------ softmax warps
-    const int q4 = warp & 3;                 // TMEM lane quarter of this warp
-    const int r = q4 * 32 + lane;            // key row (S^T) and head dimension (O^T) of this thread
-    const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
-    const int sid = tid - 64;                // 0..127 among the softmax threads
-    const float sl2 = a.scale * 1.4426950408889634f;
-    int* counters = reinterpret_cast<int*>(a.ws + a.layout.counters);
-    float* partials = reinterpret_cast<float*>(a.ws + a.layout.partials);
-    constexpr int pstride = kN * (kD + 2);
-    unsigned char* pbuf = smem + L::kP;
-    float m_ref[NH], l_thr[NH];  // reference max (identical in all threads), this thread's sums
-    uint32_t obs[2] = {0, 0};    // phases of o_done[0/1] seen
-    // A failed (timed-out) wait makes `ok` false and raises the abort flag, so that every other
-    // wait fails fast; the warps keep the same barrier sequence and leave the loop together at
-    // the next vote, so no warp is left waiting at a named barrier.
-    bool ok = true;
-    auto wait_ok = [&](uint64_t* bar, uint32_t parity) {
-      if (!ok) return;
-      ok = warp_wait(bar, parity, abort_flag, budget);
-      if (!ok) *abort_flag = 1;
-    };
-
-    // column max of the scores over the 128 key rows (all softmax threads take part)
-    auto column_max = [&](const float (&t)[NH], float (&cm)[NH]) {
-      const float wm = warp_reduce<NH, true>(t, lane);
-      if (reduce_writer<NH>(lane)) red_m[q4 * kN + reduce_head<NH>(lane)] = wm;
-      named_sync_sm();
-#pragma unroll
-      for (int h = 0; h < NH; ++h)
-        cm[h] = fmaxf(fmaxf(red_m[h], red_m[kN + h]), fmaxf(red_m[2 * kN + h], red_m[3 * kN + h]));
-    };
-    // PV(k) complete?  (o_done[k & 1] completes once per chunk of that parity)
-    auto wait_pv = [&](int k) {
-      const int b = k & 1;
-      const uint32_t ph = (uint32_t)k >> 1;
-      if (obs[b] > ph) return;
-      wait_ok(&bars->o_done[b], ph & 1);
-      obs[b] = ph + 1;
-    };
-
-    for (int k = 0; k < count; ++k) {
-      const int s = k % NS, sb = k & 1;
-      wait_ok(&bars->full[s], (k / NS) & 1);
-      const StageInfo inf = info[s];
-      const bool first = inf.flags & kFirst, last = inf.flags & kLast;
-      const int p0 = inf.c * kC;
-      const int nr = min(kC, inf.len + 1 - p0);  // valid rows, the new one included
-      const int h0 = inf.g * a.group;
-      unsigned char* kst = smem + L::kStage + s * L::kStageBytes;
-      unsigned char* vst = kst + L::kKBytes;
-
-      if (inf.flags & kFix) {
-        // fix-ups of the chunk that holds position n = len: the new K/V row goes into the
-        // swizzled tiles (and, once, into the pool); V rows past it are zeroed (their P is 0,
-        // but stale pool contents could hold NaN bit patterns)
-        const int rn = inf.len - p0;
-        const int64_t src = ((int64_t)inf.i * a.h_kv + inf.g) * kD * 2;
-        const int64_t dst = (((int64_t)inf.slot * a.h_kv + inf.g) * a.cap + inf.len) * kD * 2;
-        if (sid < 32) {
-          const int ch = sid & 15;  // 16-byte chunk of the 256-byte row
-          const bool isv = sid >= 16;
-          const uint4 w = *reinterpret_cast<const uint4*>(static_cast<const unsigned char*>(isv ? a.v_new : a.k_new) +
-                                                          src + ch * 16);
-          unsigned char* tile = isv ? vst : kst;
-          *reinterpret_cast<uint4*>(tile + (ch >> 3) * (kC * 128) + rn * 128 + (((ch & 7) ^ (rn & 7)) << 4)) = w;
-          if (ok) *reinterpret_cast<uint4*>(static_cast<unsigned char*>(isv ? a.pool_v : a.pool_k) + dst + ch * 16) = w;
-        }
-        for (int e = (nr * 16) + sid; e < kC * 16; e += kSoftmax) {  // rows nr..127, 16 chunks each
-          const int row = e >> 4, ch = e & 15;
-          *reinterpret_cast<uint4*>(vst + (ch >> 3) * (kC * 128) + row * 128 + (ch & 7) * 16) = make_uint4(0, 0, 0, 0);
-        }
-        fence_proxy_async_smem();
-        mbar_arrive(&bars->fixed);
-      }
-
-      // scores of this thread's key row for the group's heads
-      wait_ok(&bars->s_full[sb], (k >> 1) & 1);
-      tc_fence_after();
-      uint32_t sr[NH];
-      tmem_ld_cols<NH>(tmem + sb * kN + lane_off, sr);
-      tc_fence_before();
-      mbar_arrive(&bars->s_free[sb]);
-      float t[NH];
-      const bool valid = r < nr;
-#pragma unroll
-      for (int h = 0; h < NH; ++h) t[h] = valid ? __uint_as_float(sr[h]) * sl2 : -INFINITY;
-
-      // The reference max of each head is fixed at the first chunk of a piece; it only guards
-      // the exponentials against overflow (P is bf16, O and the sums accumulate in fp32, so
-      // their precision is relative).  A later chunk whose scores exceed it by more than the
-      // guard takes the exact path: new max, O^T and the sums rescaled.
-      if (first) {
-        column_max(t, m_ref);  // finite: every chunk holds at least one valid row
-#pragma unroll
-        for (int h = 0; h < NH; ++h) l_thr[h] = 0.f;
-      }
-      bool big = false;
-#pragma unroll
-      for (int h = 0; h < NH; ++h) big |= (t[h] - m_ref[h] > kLog2Guard);
-      if (named_or_sm(big || !ok)) {
-        if (named_or_sm(!ok)) break;  // every softmax thread leaves here together
-        float cm[NH], alpha[NH];
-        column_max(t, cm);
-#pragma unroll
-        for (int h = 0; h < NH; ++h) {
-          const float m_new = fmaxf(m_ref[h], cm[h]);
-          alpha[h] = ex2_approx(m_ref[h] - m_new);
-          m_ref[h] = m_new;
-          l_thr[h] *= alpha[h];
-        }
-        if (!first) {  // O^T holds the chunks before this one: rescale it once PV(k-1) is done
-          wait_pv(k - 1);
+    } else if (warp == 1) {
+      // ---------------------------------------------------------------- S issuer
+      if (lane == 0) {
+        constexpr uint32_t idesc_s = idesc_bf16(128, kN, false, false);  // K (K-major) x Q^T
+        uint32_t fix_cnt = 0;
+        bool ok = true;
+        for (int k = 0;; ++k) {
+          const int s = k % NS, sb = k & 1;
+          if (!mbar_wait(&bars->full[s], (k / NS) & 1, abort_flag, budget)) { ok = false; break; }
+          const int flags = info[s].flags;
+          if (flags & kEnd) break;
+          if (flags & kFix) {  // the new row is written into the tiles first
+            if (!mbar_wait(&bars->fixed, fix_cnt & 1, abort_flag, budget)) { ok = false; break; }
+            ++fix_cnt;
+          }
+          if (k >= 2 && !mbar_wait(&bars->s_free[sb], ((k >> 1) - 1) & 1, abort_flag, budget)) { ok = false; break; }
           tc_fence_after();
-          uint32_t o[NH];
-          tmem_ld_cols<NH>(tm_o + lane_off, o);
+          const uint32_t k_addr = smem_u32(smem + L::kStage + s * L::kStageBytes);
+          const uint32_t q_addr = k_addr + 2 * L::kKBytes;
 #pragma unroll
-          for (int h = 0; h < NH; ++h) o[h] = __float_as_uint(__uint_as_float(o[h]) * alpha[h]);
-          tmem_st_cols<NH>(tm_o + lane_off, o);
+          for (int kk = 0; kk < kD / 16; ++kk) {
+            const uint64_t ak = sdesc_sw128(k_addr + (kk >> 2) * (kC * 128) + (kk & 3) * 32, 16, 1024);
+            const uint64_t bq = sdesc_sw128(q_addr + (kk >> 2) * (kN * 128) + (kk & 3) * 32, 16, 1024);
+            umma_bf16(tmem + sb * kN, ak, bq, idesc_s, kk > 0 ? 1u : 0u);
+          }
+          umma_commit(&bars->s_full[sb]);
         }
+        if (!ok) raise_timeout(a, bars);
+        umma_commit(&bars->drain_s);  // every MMA of this thread is complete before TMEM is freed
+        mbar_wait(&bars->drain_s, 0, never, kDrainBudget);
       }
-      float p[NH];
+    } else if (warp == 6) {
+      // ---------------------------------------------------------------- PV issuer
+      if (lane == 0) {
+        constexpr uint32_t idesc_o = idesc_bf16(128, kN, true, false);  // V^T (MN-major) x P^T
+        const uint32_t p_addr = smem_u32(smem + L::kP);
+        int pc = 0;  // piece index: O^T buffer pc & 1
+        bool ok = true;
+        for (int k = 0;; ++k) {
+          const int s = k % NS;
+          // full[s] is long complete (S ran on this stage); waiting on it orders the read of info[s]
+          if (!mbar_wait(&bars->full[s], (k / NS) & 1, abort_flag, budget)) { ok = false; break; }
+          const int flags = info[s].flags;
+          if (flags & kEnd) break;
+          const bool first = flags & kFirst;
+          if (!mbar_wait(&bars->p_full[k & 1], (k >> 1) & 1, abort_flag, budget)) { ok = false; break; }
+          if (first && pc >= 2 && !mbar_wait(&bars->o_free[pc & 1], ((pc >> 1) - 1) & 1, abort_flag, budget)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t v_addr = smem_u32(smem + L::kStage + s * L::kStageBytes + L::kKBytes);
+          const uint32_t d_o = tmem + (2 + (pc & 1)) * kN;
 #pragma unroll
-      for (int h = 0; h < NH; ++h) {
-        p[h] = ex2_approx(t[h] - m_ref[h]);
-        l_thr[h] += p[h];
-      }
-
-      // P^T buffer k & 1 was last read by PV(k - 2)
-      if (k >= 2) wait_pv(k - 2);
-      // P^T: row h = head, column = key r, bf16, 128-byte swizzled (K-major B operand); rows
-      // NH..15 are never written: they only feed O^T columns that are never read
-      {
-        unsigned char* pb = pbuf + (k & 1) * L::kPBytes;
-        const int sub = r >> 6, kb = (r & 63) * 2;
-#pragma unroll
-        for (int h = 0; h < NH; ++h) {
-          const int off = sub * (kN * 128) + h * 128 + ((((kb >> 4) ^ (h & 7))) << 4) + (kb & 15);
-          *reinterpret_cast<__nv_bfloat16*>(pb + off) = __float2bfloat16_rn(p[h]);
+          for (int kk = 0; kk < kC / 16; ++kk) {
+            const uint64_t av = sdesc_sw128(v_addr + kk * 16 * 128, kC * 128, 1024);
+            const uint64_t bp =
+                sdesc_sw128(p_addr + (k & 1) * L::kPBytes + (kk >> 2) * (kN * 128) + (kk & 3) * 32, 16, 1024);
+            umma_bf16(d_o, av, bp, idesc_o, (first && kk == 0) ? 0u : 1u);
+          }
+          umma_commit(&bars->o_done[k & 1]);
+          umma_commit(&bars->empty[s]);
+          if (flags & kLast) {
+            umma_commit(&bars->o_full[pc & 1]);
+            ++pc;
+          }
         }
+        if (!ok) raise_timeout(a, bars);
+        umma_commit(&bars->drain_p);
+        mbar_wait(&bars->drain_p, 0, never, kDrainBudget);
       }
-      fence_proxy_async_smem();
-      tc_fence_before();
-      mbar_arrive(&bars->p_full[k & 1]);
-
-      if (!last) continue;
-      // ---- end of a piece: this thread holds dimension r of O for the group's heads -------
-      float l_sum[NH];
-      {
-        const float ws = warp_reduce<NH, false>(l_thr, lane);
-        if (reduce_writer<NH>(lane)) red_l[q4 * kN + reduce_head<NH>(lane)] = ws;
-        named_sync_sm();
-#pragma unroll
-        for (int h = 0; h < NH; ++h) l_sum[h] = (red_l[h] + red_l[kN + h]) + (red_l[2 * kN + h] + red_l[3 * kN + h]);
-      }
-      wait_pv(k);
-      tc_fence_after();
-      float ov[NH];
-      {
-        uint32_t o[NH];
-        tmem_ld_cols<NH>(tm_o + lane_off, o);
-#pragma unroll
-        for (int h = 0; h < NH; ++h) ov[h] = __uint_as_float(o[h]);
-      }
-      tc_fence_before();
-      mbar_arrive(&bars->o_free);
-      const int nh = a.group;
-      const int x = x_begin + k;
-      const int x0 = x - inf.c;
-      const int c_start = max(x_begin, x0) - x0;
-      const bool whole = (c_start == 0) && (inf.c == inf.nch - 1);
-      __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out) + ((int64_t)inf.i * a.h_q + h0) * kD + r;
-      if (whole) {
+    } else if (warp <= 5) {
+      // ---------------------------------------------------------------- softmax warps 2-5
+      const int q4 = warp & 3;                 // TMEM lane quarter of this warp
+      const int r = q4 * 32 + lane;            // key row of S^T owned by this thread
+      const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
+      const int sid = tid - 64;                // 0..127
+      const float sl2 = a.scale * 1.4426950408889634f;
+      unsigned char* pbuf = smem + L::kP;
+      float m_ref[NH], l_thr[NH];  // reference max (identical in all threads), this thread's sums
+      uint32_t obs[2] = {0, 0};    // phases of o_done[0/1] seen
+      int pc = 0, c_start = 0, n_in = 0;
+      // A failed (timed-out) wait makes `ok` false and raises the abort flag, so every other
+      // wait fails fast; the warps keep the same barrier sequence and leave together at a vote.
+      bool ok = true;
+      auto wait_ok = [&](uint64_t* bar, uint32_t parity) {
+        if (!ok) return;
+        ok = warp_wait(bar, parity, abort_flag, budget);
+        if (!ok) *abort_flag = 1;
+      };
+      auto column_max = [&](const float (&t)[NH], float (&cm)[NH]) {
+        const float wm = warp_reduce<NH, true>(t, lane);
+        if (reduce_writer<NH>(lane)) red_m[q4 * kN + reduce_head<NH>(lane)] = wm;
+        named_sync<1>();
 #pragma unroll
         for (int h = 0; h < NH; ++h)
-          if (ok && h < nh) out[h * kD] = __float2bfloat16_rn(ov[h] / l_sum[h]);
-        continue;
-      }
-      const int cidx = inf.i * a.h_kv + inf.g;
-      float* part = partials + ((int64_t)cidx * a.layout.max_chunks + c_start) * pstride;
-#pragma unroll
-      for (int h = 0; h < NH; ++h)
-        if (ok) part[h * kD + r] = ov[h];
-      if (ok && sid < NH) {
-        part[kN * kD + sid] = m_ref[sid];
-        part[kN * kD + kN + sid] = l_sum[sid];
-      }
-      __threadfence();  // this CTA's partial is visible before its arrival is counted
-      named_sync_sm();
-      const int b_first = range_owner(x0, total, nb), b_last = range_owner(x0 + inf.nch - 1, total, nb);
-      if (sid == 0) bars->last = ok && (atomicAdd(&counters[cidx], 1) == b_last - b_first);
-      named_sync_sm();
-      if (bars->last) {
-        // fixed-order merge of the pieces b_first..b_last (online over rounds of pieces whose
-        // max and sum are gathered into shared memory by one thread per (piece, head))
-        __threadfence();
-        const float* base = partials + (int64_t)cidx * a.layout.max_chunks * pstride;
-        constexpr int kPer = 128 / NH;  // pieces per round
-        float M[NH], Ls[NH], O[NH];
-#pragma unroll
-        for (int h = 0; h < NH; ++h) {
-          M[h] = -INFINITY;
-          Ls[h] = 0.f;
-          O[h] = 0.f;
-        }
-        for (int j0 = b_first; j0 <= b_last; j0 += kPer) {
-          const int jn = min(kPer, b_last - j0 + 1);
-          if (sid < jn * NH) {
-            const int j = sid / NH, h = sid % NH;
-            const int cs = max(range_start(j0 + j, total, nb), x0) - x0;
-            mg_m[sid] = __ldcg(base + cs * pstride + kN * kD + h);
-            mg_l[sid] = __ldcg(base + cs * pstride + kN * kD + kN + h);
-            if (h == 0) mg_off[j] = cs * pstride;
+          cm[h] = fmaxf(fmaxf(red_m[h], red_m[kN + h]), fmaxf(red_m[2 * kN + h], red_m[3 * kN + h]));
+      };
+      auto wait_pv = [&](int k) {  // PV(k) complete (o_done[k & 1] completes once per chunk of that parity)
+        const int b = k & 1;
+        const uint32_t ph = (uint32_t)k >> 1;
+        if (obs[b] > ph) return;
+        wait_ok(&bars->o_done[b], ph & 1);
+        obs[b] = ph + 1;
+      };
+      // piece slot pc & 1 is free once the epilogue consumed piece pc - 2
+      auto wait_slot = [&]() {
+        if (pc >= 2) wait_ok(&bars->o_free[pc & 1], ((pc >> 1) - 1) & 1);
+      };
+
+      int k = 0;
+      for (;; ++k) {
+        const int s = k % NS, sb = k & 1;
+        wait_ok(&bars->full[s], (k / NS) & 1);
+        const StageInfo inf = info[s];
+        if (named_or<1>(!ok || (inf.flags & kEnd))) break;  // identical in all threads when ok
+        const bool first = inf.flags & kFirst, last = inf.flags & kLast;
+        const int p0 = inf.c * kC;
+        const int nr = min(kC, inf.len + 1 - p0);  // valid rows, the new one included
+        unsigned char* kst = smem + L::kStage + s * L::kStageBytes;
+        unsigned char* vst = kst + L::kKBytes;
+
+        if (inf.flags & kFix) {
+          // fix-ups of the chunk that holds position n = len: the new K/V row goes into the
+          // swizzled tiles (and, once, into the pool); V rows past it are zeroed (their P is 0,
+          // but stale pool contents could hold NaN bit patterns)
+          const int rn = inf.len - p0;
+          const int64_t src = ((int64_t)inf.i * a.h_kv + inf.g) * kD * 2;
+          const int64_t dst = (((int64_t)inf.slot * a.h_kv + inf.g) * a.cap + inf.len) * kD * 2;
+          if (sid < 32) {
+            const int ch = sid & 15;  // 16-byte chunk of the 256-byte row
+            const bool isv = sid >= 16;
+            const uint4 w = *reinterpret_cast<const uint4*>(
+                static_cast<const unsigned char*>(isv ? a.v_new : a.k_new) + src + ch * 16);
+            unsigned char* tile = isv ? vst : kst;
+            *reinterpret_cast<uint4*>(tile + (ch >> 3) * (kC * 128) + rn * 128 + (((ch & 7) ^ (rn & 7)) << 4)) = w;
+            if (ok)
+              *reinterpret_cast<uint4*>(static_cast<unsigned char*>(isv ? a.pool_v : a.pool_k) + dst + ch * 16) = w;
           }
-          named_sync_sm();
+          for (int e = (nr * 16) + sid; e < kC * 16; e += kQuad) {  // rows nr..127, 16 chunks each
+            const int row = e >> 4, ch = e & 15;
+            *reinterpret_cast<uint4*>(vst + (ch >> 3) * (kC * 128) + row * 128 + (ch & 7) * 16) =
+                make_uint4(0, 0, 0, 0);
+          }
+          fence_proxy_async_smem();
+          mbar_arrive(&bars->fixed);
+        }
+
+        // scores of this thread's key row for the group's heads
+        wait_ok(&bars->s_full[sb], (k >> 1) & 1);
+        tc_fence_after();
+        uint32_t sr[NH];
+        tmem_ld_cols<NH>(tmem + sb * kN + lane_off, sr);
+        tc_fence_before();
+        mbar_arrive(&bars->s_free[sb]);
+        float t[NH];
+        const bool valid = r < nr;
+#pragma unroll
+        for (int h = 0; h < NH; ++h) t[h] = valid ? __uint_as_float(sr[h]) * sl2 : -INFINITY;
+
+        // The reference max of each head is fixed at the first chunk of a piece; it only
+        // guards the exponentials against overflow (P is bf16, O and the sums accumulate in
+        // fp32, so their precision is relative).  A later chunk whose scores exceed it by more
+        // than the guard takes the exact path: new max, O^T and the sums rescaled.
+        if (first) {
+          column_max(t, m_ref);  // finite: every chunk holds at least one valid row
+#pragma unroll
+          for (int h = 0; h < NH; ++h) l_thr[h] = 0.f;
+          c_start = inf.c;
+          n_in = 0;
+        }
+        bool big = false;
+#pragma unroll
+        for (int h = 0; h < NH; ++h) big |= (t[h] - m_ref[h] > kLog2Guard);
+        if (named_or<1>(big || !ok)) {
+          if (named_or<1>(!ok)) break;  // every softmax thread leaves here together
+          float cm[NH], alpha[NH];
+          column_max(t, cm);
 #pragma unroll
           for (int h = 0; h < NH; ++h) {
-            float mr = M[h];
-            for (int j = 0; j < jn; ++j) mr = fmaxf(mr, mg_m[j * NH + h]);
-            const float sc = ex2_approx(M[h] - mr);  // 0 on the first round (M = -inf)
-            Ls[h] *= sc;
-            O[h] *= sc;
-            M[h] = mr;
+            const float m_new = fmaxf(m_ref[h], cm[h]);
+            alpha[h] = ex2_approx(m_ref[h] - m_new);
+            m_ref[h] = m_new;
+            l_thr[h] *= alpha[h];
           }
-          int j = 0;
-          for (; j + 4 <= jn; j += 4) {
-            float ov4[4][NH];
+          if (!first) {  // O^T holds the piece's chunks before this one: rescale once PV(k-1) is done
+            wait_pv(k - 1);
+            tc_fence_after();
+            const uint32_t t_o = tmem + (2 + (pc & 1)) * kN + lane_off;
+            uint32_t o[NH];
+            tmem_ld_cols<NH>(t_o, o);
 #pragma unroll
-            for (int u = 0; u < 4; ++u)
-#pragma unroll
-              for (int h = 0; h < NH; ++h) ov4[u][h] = __ldcg(base + mg_off[j + u] + h * kD + r);
-#pragma unroll
-            for (int u = 0; u < 4; ++u)
-#pragma unroll
-              for (int h = 0; h < NH; ++h) {
-                const float wgt = ex2_approx(mg_m[(j + u) * NH + h] - M[h]);
-                Ls[h] += mg_l[(j + u) * NH + h] * wgt;
-                O[h] += ov4[u][h] * wgt;
-              }
+            for (int h = 0; h < NH; ++h) o[h] = __float_as_uint(__uint_as_float(o[h]) * alpha[h]);
+            tmem_st_cols<NH>(t_o, o);
           }
-          for (; j < jn; ++j) {
-#pragma unroll
-            for (int h = 0; h < NH; ++h) {
-              const float wgt = ex2_approx(mg_m[j * NH + h] - M[h]);
-              Ls[h] += mg_l[j * NH + h] * wgt;
-              O[h] += __ldcg(base + mg_off[j] + h * kD + r) * wgt;
-            }
-          }
-          named_sync_sm();  // the round's gathered values are read before the next round overwrites them
         }
+        float p[NH];
 #pragma unroll
-        for (int h = 0; h < NH; ++h)
-          if (ok && h < nh) out[h * kD] = __float2bfloat16_rn(O[h] / Ls[h]);
-        if (sid == 0) counters[cidx] = 0;
+        for (int h = 0; h < NH; ++h) {
+          p[h] = ex2_approx(t[h] - m_ref[h]);
+          l_thr[h] += p[h];
+        }
+
+        // P^T buffer k & 1 was last read by PV(k - 2)
+        if (k >= 2) wait_pv(k - 2);
+        // P^T: row h = head, column = key r, bf16, 128-byte swizzled (K-major B operand); rows
+        // NH..15 are never written: they only feed O^T columns that are never read
+        {
+          unsigned char* pb = pbuf + (k & 1) * L::kPBytes;
+          const int sub = r >> 6, kb = (r & 63) * 2;
+#pragma unroll
+          for (int h = 0; h < NH; ++h) {
+            const int off = sub * (kN * 128) + h * 128 + ((((kb >> 4) ^ (h & 7))) << 4) + (kb & 15);
+            *reinterpret_cast<__nv_bfloat16*>(pb + off) = __float2bfloat16_rn(p[h]);
+          }
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(&bars->p_full[k & 1]);
+        ++n_in;
+
+        if (last) {  // hand the piece to the epilogue warps
+          wait_slot();
+          PieceInfo& pi = pinfo[pc & 1];
+          const float ws = warp_reduce<NH, false>(l_thr, lane);
+          if (reduce_writer<NH>(lane)) pi.l4[q4][reduce_head<NH>(lane)] = ws;
+          if (sid < NH) pi.m[sid] = m_ref[sid];
+          if (sid == 0) {
+            pi.i = inf.i;
+            pi.g = inf.g;
+            pi.c_start = c_start;
+            pi.nch = inf.nch;
+            pi.n_in = n_in;
+            pi.xi0 = inf.xi0;
+            pi.flags = (c_start == 0 && n_in == inf.nch) ? kWhole : 0;
+          }
+          mbar_arrive(&bars->pc_full[pc & 1]);
+          ++pc;
+        }
       }
-      named_sync_sm();  // `last` is read by every thread before the next piece may set it
+      if (ok) {  // end marker for the epilogue
+        wait_slot();
+        if (ok) {
+          if (sid == 0) pinfo[pc & 1].flags = kEnd;
+          mbar_arrive(&bars->pc_full[pc & 1]);
+        }
+      }
+      if (!ok && lane == 0) raise_timeout(a, bars);
+    } else {
+      // ---------------------------------------------------------------- epilogue warps 7-10
+      // Stores each finished piece: the output rows when the piece is a whole (question, kv
+      // head), else its partial (O rows, reference max, sum) for the merge kernel.  No waiting
+      // on global memory here, so the O^T buffers are released right away.
+      const int q4 = warp & 3;
+      const int r = q4 * 32 + lane;  // head dimension of O^T owned by this thread
+      const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
+      const int eid = tid - 224;     // 0..127
+      float* partials = reinterpret_cast<float*>(a.ws + a.layout.partials);
+      int* item_xi0 = reinterpret_cast<int*>(a.ws + a.layout.xi0);
+      constexpr int pstride = kN * (kD + 2);
+      bool ok = true;
+      for (int pc = 0;; ++pc) {
+        const int b = pc & 1;
+        const uint32_t ph = (pc >> 1) & 1;
+        if (!warp_wait(&bars->pc_full[b], ph, abort_flag, budget)) { ok = false; break; }
+        const PieceInfo& pi = pinfo[b];
+        if (pi.flags & kEnd) break;
+        if (!warp_wait(&bars->o_full[b], ph, abort_flag, budget)) { ok = false; break; }  // last PV complete
+        tc_fence_after();
+        float ov[NH], l_sum[NH], m_p[NH];
+        {
+          uint32_t o[NH];
+          tmem_ld_cols<NH>(tmem + (2 + b) * kN + lane_off, o);
+#pragma unroll
+          for (int h = 0; h < NH; ++h) {
+            ov[h] = __uint_as_float(o[h]);
+            l_sum[h] = (pi.l4[0][h] + pi.l4[1][h]) + (pi.l4[2][h] + pi.l4[3][h]);
+            m_p[h] = pi.m[h];
+          }
+        }
+        const int i = pi.i, g = pi.g, c_start = pi.c_start, xi0 = pi.xi0;
+        const bool whole = pi.flags & kWhole;
+        tc_fence_before();
+        mbar_arrive(&bars->o_free[b]);  // O^T buffer b and piece slot b are free
+
+        const int cidx = i * a.h_kv + g;
+        if (whole) {
+          __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out) + ((int64_t)i * a.h_q + g * a.group) * kD + r;
+#pragma unroll
+          for (int h = 0; h < NH; ++h)
+            if (h < a.group) out[h * kD] = __float2bfloat16_rn(ov[h] / l_sum[h]);
+        } else {
+          float* part = partials + ((int64_t)cidx * a.layout.max_chunks + c_start) * pstride;
+#pragma unroll
+          for (int h = 0; h < NH; ++h) part[h * kD + r] = ov[h];
+          if (eid < NH) {
+            part[kN * kD + eid] = m_p[eid];
+            part[kN * kD + kN + eid] = l_sum[eid];
+          }
+        }
+        if (c_start == 0 && eid == 0) item_xi0[cidx] = xi0;
+      }
+      if (!ok && lane == 0) raise_timeout(a, bars);
     }
-    if (!ok && lane == 0) raise_timeout(a, bars);
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+      tc_fence_after();
+      tmem_dealloc(tmem, kTmemCols);
+    }
   }
 
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 1) {
-    tc_fence_after();
-    tmem_dealloc(tmem, kTmemCols);
+  // the merge kernel may be scheduled as soon as every CTA got here (it still waits for this
+  // grid to complete before it reads anything)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Merge of the pieces of every (question, kv head) that the decode kernel split (one CTA per
+// pair, thread r = head dimension r), in a fixed order: piece 0 starts at chunk 0, piece j > 0
+// at the j-th batch boundary after the pair's first chunk.  Online over rounds of pieces whose
+// reference max and sum are gathered into shared memory while the O rows load.  Block 0 also
+// resets the decode kernel's batch counter for the next call.
+template <int NH>
+__global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeArgs a) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // the decode grid is complete and visible
+  int* sched = reinterpret_cast<int*>(a.ws + a.layout.sched);
+  if (blockIdx.x == 0 && threadIdx.x == 0) sched[0] = 0;
+  if (sched[2] != ST_OK) return;  // invalid call: the decode kernel wrote nothing
+  __shared__ float mg_m[128], mg_l[128];
+  const int r = threadIdx.x;
+  const float* partials = reinterpret_cast<const float*>(a.ws + a.layout.partials);
+  const int* item_xi0 = reinterpret_cast<const int*>(a.ws + a.layout.xi0);
+  constexpr int pstride = kN * (kD + 2);
+  constexpr int kRound = 32 / NH > 8 ? 8 : 32 / NH;  // pieces per round (O loads in flight)
+  for (int cidx = blockIdx.x; cidx < a.n * a.h_kv; cidx += gridDim.x) {
+    const int i = cidx / a.h_kv, g = cidx % a.h_kv;
+    if (!a.active[i]) continue;
+    const int nch = (a.lens[i] + 1 + kC - 1) / kC;
+    const int xi0 = item_xi0[cidx];
+    if (xi0 < 0) continue;  // not a chunk index (never written by a valid decode kernel)
+    const int np = (xi0 + nch - 1) / kBatch - xi0 / kBatch + 1;
+    if (np == 1) continue;  // one piece: the decode kernel wrote the output
+    const float* base = partials + (int64_t)cidx * a.layout.max_chunks * pstride;
+    auto piece_off = [&](int j) { return (j == 0 ? 0 : (xi0 / kBatch + j) * kBatch - xi0) * pstride; };
+    float M[NH], Ls[NH], O[NH];
+#pragma unroll
+    for (int h = 0; h < NH; ++h) {
+      M[h] = -INFINITY;
+      Ls[h] = 0.f;
+      O[h] = 0.f;
+    }
+    for (int j0 = 0; j0 < np; j0 += kRound) {
+      const int jn = min(kRound, np - j0);
+      if (r < jn * NH) {
+        const int j = r / NH, h = r % NH;
+        const int off = piece_off(j0 + j);
+        mg_m[r] = base[off + kN * kD + h];
+        mg_l[r] = base[off + kN * kD + kN + h];
+      }
+      float ovr[kRound][NH];
+#pragma unroll
+      for (int u = 0; u < kRound; ++u) {
+        const int off = piece_off(j0 + u);
+#pragma unroll
+        for (int h = 0; h < NH; ++h) ovr[u][h] = (u < jn) ? base[off + h * kD + r] : 0.f;
+      }
+      __syncthreads();
+#pragma unroll
+      for (int h = 0; h < NH; ++h) {
+        float mr = M[h];
+        for (int j = 0; j < jn; ++j) mr = fmaxf(mr, mg_m[j * NH + h]);
+        const float sc = ex2_approx(M[h] - mr);  // 0 on the first round (M = -inf)
+        Ls[h] *= sc;
+        O[h] *= sc;
+        M[h] = mr;
+      }
+#pragma unroll
+      for (int u = 0; u < kRound; ++u) {
+        if (u < jn) {
+#pragma unroll
+          for (int h = 0; h < NH; ++h) {
+            const float wgt = ex2_approx(mg_m[u * NH + h] - M[h]);
+            Ls[h] += mg_l[u * NH + h] * wgt;
+            O[h] += ovr[u][h] * wgt;
+          }
+        }
+      }
+      __syncthreads();  // the round's gathered values are read before the next round overwrites them
+    }
+    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out) + ((int64_t)i * a.h_q + g * a.group) * kD + r;
+#pragma unroll
+    for (int h = 0; h < NH; ++h)
+      if (h < a.group) out[h * kD] = __float2bfloat16_rn(O[h] / Ls[h]);
   }
 }
 
@@ -680,7 +756,21 @@ cudaError_t launch_ns(const DecodeArgs& a, int num_sms, cudaStream_t st, const C
   p.a = a;
   p.wait_budget = wait_budget_cycles();
   decode_tc_kernel<NS, NH><<<num_sms, kThreads, smem, st>>>(mk, mv, mq, p);
-  return cudaGetLastError();
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  // the merge kernel, programmatically dependent on the decode kernel (its launch overlaps the
+  // decode kernel's end; its griddepcontrol.wait orders every read after the decode grid)
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)min(a.n * a.h_kv, 8 * num_sms));
+  cfg.blockDim = dim3(128);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decode_merge_kernel<NH>, a);
 }
 
 template <int NH>

@@ -77,6 +77,8 @@ inline PrefillLayout prefill_layout(int32_t n, int32_t T, int32_t h_q) {
 // decode workspace
 // ---------------------------------------------------------------------------------------
 struct DecodeLayout {
+  size_t sched;     // int32[4]  tensor-core decode: [0] batch-grab counter (left at zero), [2] validation code
+  size_t xi0;       // int32[N * H_kv]  tensor-core decode: global index of chunk 0 of each (question, kv head)
   size_t counters;  // int32[N * H_kv * n_hblocks]  arrivals per (question, kv head, head block); left at zero
   size_t partials;  // float[N * H_kv * n_hblocks * max_chunks * GT * (d + 2)]
   size_t total;
@@ -99,6 +101,10 @@ inline DecodeLayout decode_layout(int32_t n, int32_t cap, int32_t h_q, int32_t h
   const int32_t nhb = tc ? 1 : (G + 7) / 8;
   const int32_t GT = tc ? 16 : decode_head_block_size(G);
   size_t off = 0;
+  L.sched = off;
+  off = align_up(off + 4 * sizeof(int32_t), 256);
+  L.xi0 = off;
+  off = align_up(off + (tc ? sizeof(int32_t) * (size_t)n * h_kv : 0), 256);
   L.counters = off;
   off = align_up(off + sizeof(int32_t) * (size_t)n * h_kv * nhb, 256);
   L.partials = off;
