@@ -285,7 +285,6 @@ def main(argv=None):
     dws = torch.zeros(dws_bytes, dtype=torch.uint8, device=dev)
     dstatus = torch.zeros(1, dtype=torch.int32, device=dev)
     flush = L2Flush(torch, dev)
-    launches_per_step = kev.kev_launch_count(2) + kev.kev_launch_count(1) + kev.kev_launch_count(4)
 
     def step(ev_a=None, ev_b=None, bufs=None):
         qq, kk, vv, ivv, sl, qn, kn, vn, ln, act, oo, on = bufs or (q, k, v, iv, slots, q_new, k_new, v_new, lens,
@@ -307,6 +306,8 @@ def main(argv=None):
         step()
     torch.cuda.synchronize()
     assert kev.kev_read_status(status) == 0 and kev.kev_read_status(dstatus) == 0
+    # kernels per step, as the library reports them for the calls just made
+    launches_per_step = kev.kev_launch_count(2) + kev.kev_launch_count(1) + kev.kev_launch_count(4)
     if args.only == "step":
         for _ in range(args.steps):
             flush()

@@ -40,7 +40,8 @@ using dec::ItemInfo;
 constexpr int kD = 128;
 constexpr int kN = 16;             // MMA N: q-heads of one group, padded to 16
 constexpr int kC = dec::kChunk;    // 128 keys per chunk
-constexpr int kBatch = 4;          // consecutive chunks per dynamic grab
+constexpr int kBatch = 4;          // consecutive chunks per dynamic grab (before the tail)
+constexpr int kTailPerCta = 0;     // single-chunk grabs at the end, per CTA of the grid (measured: none is best)
 constexpr int kThreads = 352;
 constexpr int kQuad = 128;         // threads of the softmax (warps 2-5) and of the epilogue (warps 7-10)
 constexpr long long kDrainBudget = 4000000000ll;
@@ -164,6 +165,25 @@ __device__ __forceinline__ bool reduce_writer(int lane) {
   return (lane & (32 / NH - 1)) == 0;
 }
 
+// The fixed plan of the dynamic grabs: batches of kBatch chunks over [0, x1), then one batch
+// per chunk over [x1, total) so the last grabs are short and every CTA finishes at about the
+// same time.  Batch boundaries depend on the chunk index only (not on which CTA grabs what),
+// so the pieces, and hence the results, are the same on every run.
+struct BatchPlan {
+  int n1, x1, nbat;
+  __device__ int start(int b) const { return b < n1 ? b * kBatch : x1 + (b - n1); }
+  __device__ int end(int b) const { return b < n1 ? (b + 1) * kBatch : x1 + (b - n1) + 1; }
+  __device__ int of(int x) const { return x < x1 ? x / kBatch : n1 + (x - x1); }
+};
+__device__ __forceinline__ BatchPlan make_plan(int total, int ctas) {
+  const int tail = kTailPerCta * ctas;
+  BatchPlan p;
+  p.n1 = total > tail ? (total - tail) / kBatch : 0;
+  p.x1 = p.n1 * kBatch;
+  p.nbat = p.n1 + (total - p.x1);
+  return p;
+}
+
 // Sequential walk over the compacted chunk list: the chunk after (i, g, c) is (i, g, c + 1),
 // else (i, g + 1, 0), else chunk 0 of the next live question.
 struct Cursor {
@@ -219,6 +239,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
   const int total = dec::prologue<kThreads>(a, 1, item_base, meta, hash, &bars->flags, bars->scan_tmp, &sched[2]);
 
   if (total >= 0) {
+    if (blockIdx.x == 0 && tid == 0) {  // the merge kernel rebuilds the pieces from the plan
+      const BatchPlan plan = make_plan(total, gridDim.x);
+      sched[1] = plan.x1;
+      sched[3] = plan.n1;
+    }
     if (tid == 0) {
       for (int s = 0; s < NS; ++s) {
         mbar_init(&bars->full[s], 1);
@@ -260,12 +285,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
       if (lane == 0) {
         uint32_t issued[3] = {0, 0, 0};
         bool ok = true;
-        const int nbat = (total + kBatch - 1) / kBatch;
+        const BatchPlan plan = make_plan(total, gridDim.x);
         int k = 0;  // position in the stage ring
-        int bat = grab;
-        while (ok && bat < nbat) {
-          const int next = atomicAdd(&sched[0], 1);  // used when this batch is issued
-          const int x0 = bat * kBatch, x1 = min(x0 + kBatch, total);
+        // two grabs stay in flight ahead of the batch being issued (a grab's round trip is
+        // longer than a single-chunk batch)
+        int bat = grab, bat1 = atomicAdd(&sched[0], 1);
+        while (ok && bat < plan.nbat) {
+          const int bat2 = atomicAdd(&sched[0], 1);
+          const int x0 = plan.start(bat), x1 = plan.end(bat);
           Cursor u = cursor_at(a, item_base, meta, x0);
           for (int x = x0; x < x1; ++x, ++k) {
             const int s = k % NS;
@@ -291,8 +318,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
             ++issued[s];
             cursor_next(u, a, item_base, meta);
           }
-          bat = next;
+          bat = bat1;
+          bat1 = bat2;
         }
+        // no more work for this CTA: the merge grid may be launched (it waits for this grid)
+        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
         if (ok) {  // end of the stream: a stage whose info says so, completed without copies
           const int s = k % NS;
           const uint32_t round = k / NS;
@@ -629,7 +659,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
 
 // Merge of the pieces of every (question, kv head) that the decode kernel split (one CTA per
 // pair, thread r = head dimension r), in a fixed order: piece 0 starts at chunk 0, piece j > 0
-// at the j-th batch boundary after the pair's first chunk.  Online over rounds of pieces whose
+// at the j-th batch boundary of the grab plan after the pair's first chunk.  Online over rounds of pieces whose
 // reference max and sum are gathered into shared memory while the O rows load.  Block 0 also
 // resets the decode kernel's batch counter for the next call.
 template <int NH>
@@ -637,7 +667,10 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeArgs a) {
   asm volatile("griddepcontrol.wait;" ::: "memory");  // the decode grid is complete and visible
   int* sched = reinterpret_cast<int*>(a.ws + a.layout.sched);
   if (blockIdx.x == 0 && threadIdx.x == 0) sched[0] = 0;
-  if (sched[2] != ST_OK) return;  // invalid call: the decode kernel wrote nothing
+  if (sched[2] != ST_OK) return;  // invalid call (or timeout): nothing to merge
+  BatchPlan plan;
+  plan.x1 = sched[1];
+  plan.n1 = sched[3];
   __shared__ float mg_m[128], mg_l[128];
   const int r = threadIdx.x;
   const float* partials = reinterpret_cast<const float*>(a.ws + a.layout.partials);
@@ -646,14 +679,15 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeArgs a) {
   constexpr int kRound = 32 / NH > 8 ? 8 : 32 / NH;  // pieces per round (O loads in flight)
   for (int cidx = blockIdx.x; cidx < a.n * a.h_kv; cidx += gridDim.x) {
     const int i = cidx / a.h_kv, g = cidx % a.h_kv;
-    if (!a.active[i]) continue;
-    const int nch = (a.lens[i] + 1 + kC - 1) / kC;
-    const int xi0 = item_xi0[cidx];
-    if (xi0 < 0) continue;  // not a chunk index (never written by a valid decode kernel)
-    const int np = (xi0 + nch - 1) / kBatch - xi0 / kBatch + 1;
+    // three independent loads in one round trip
+    const int live = a.active[i], len = a.lens[i], xi0 = item_xi0[cidx];
+    if (!live || xi0 < 0) continue;  // dropped, or not a chunk index (never written by a valid call)
+    const int nch = (len + 1 + kC - 1) / kC;
+    const int b0 = plan.of(xi0);
+    const int np = plan.of(xi0 + nch - 1) - b0 + 1;
     if (np == 1) continue;  // one piece: the decode kernel wrote the output
     const float* base = partials + (int64_t)cidx * a.layout.max_chunks * pstride;
-    auto piece_off = [&](int j) { return (j == 0 ? 0 : (xi0 / kBatch + j) * kBatch - xi0) * pstride; };
+    auto piece_off = [&](int j) { return (j == 0 ? 0 : plan.start(b0 + j) - xi0) * pstride; };
     float M[NH], Ls[NH], O[NH];
 #pragma unroll
     for (int h = 0; h < NH; ++h) {
