@@ -10,11 +10,12 @@
 // l and a rescale of the accumulator when the max moves.
 //
 // GB300 mapping (one persistent CTA per SM, 384 threads = 3 warpgroups):
-//   warp 8      TMA producer of the item's query tiles (one per q-head, 128 x d each) and of
-//               the K tiles (128 x d) of the shared kv head into a 3-stage ring; warp 10
-//               produces the V tiles into a 2-stage ring.  A K tile is released as soon as
-//               both S MMAs have used it, a V tile after both PV MMAs, so the next tiles'
-//               loads start early.  128-byte swizzled boxes, completion on mbarriers.
+//   warp 8      TMA producer of the K and V tiles (128 x d each) of the shared kv head, in
+//               the order K(0) V(0) K(1) V(1) ... into one 5-slot ring: a K slot is released
+//               when both S MMAs have read it, a V slot after both PV MMAs, and each tile's
+//               load starts 2-3 key steps ahead.  Warp 10 loads the item's query tiles (one per
+//               q-head) once the previous item's last S MMA has read them.  128-byte swizzled
+//               boxes, completion on mbarriers.
 //   warp 9      MMA issuer, ping-pong over the two query tiles A and B: S_t = Q_t K^T into
 //               TMEM (128 x 128 fp32 per tile), then O_t += P_t V with P_t read from TMEM
 //               (it overwrites S_t as bf16) and V from shared memory; tcgen05.commit
@@ -45,12 +46,15 @@ using namespace sm100;
 
 constexpr int kBM = 128;            // query rows per tile
 constexpr int kBN = 128;            // keys per tile
-constexpr int kKStages = 3;         // K ring depth (a K tile is free once both S MMAs used it)
-constexpr int kVStages = 2;         // V ring depth (a V tile is free once both PV MMAs used it)
+// K and V tiles share one ring, in the order K(0) V(0) K(1) V(1) ...: with 5 slots, K(j) reuses
+// the slot of V(j-3) and V(j) that of K(j-2), so each tile's load starts 2-3 key steps before
+// its MMA needs it (a TMA round trip takes ~4700 cycles under load, more than one step).
+constexpr int kRingSlots = 5;
 constexpr int kThreads = 384;       // 3 warpgroups
-constexpr int kProducerWarp = 8;    // warpgroup 2: Q/K producer, MMA issuer, V producer, idle
+constexpr int kProducerWarp = 8;    // warpgroup 2: K/V producer, MMA issuer A, Q producer, MMA issuer B
 constexpr int kMmaWarp = 9;
-constexpr int kVProducerWarp = 10;
+constexpr int kQProducerWarp = 10;
+constexpr int kMmaWarpB = 11;       // MMA issuer of query tile B (warp 9 issues tile A's)
 // Register split: the kernel is launched at <= 168 registers per thread (384 x 168 = 64512);
 // the control warpgroup drops to 80 and the two softmax warpgroups rise to 208:
 // 128 x 80 + 256 x 208 = 63488 <= 64512, so the increase can always be granted.
@@ -78,18 +82,17 @@ struct Smem {
   static constexpr int kSubBytes = kBM * 128;     // one 128-row x 128-byte sub-tile
   static constexpr int kTileBytes = kBM * D * 2;  // one Q/K/V tile
   static constexpr int kQ = 0;                    // two query tiles
-  static constexpr int kK = kQ + 2 * kTileBytes;
-  static constexpr int kV = kK + kKStages * kTileBytes;
-  static constexpr int kBar = kV + kVStages * kTileBytes;
+  static constexpr int kRing = kQ + 2 * kTileBytes;  // K/V ring
+  static constexpr int kBar = kRing + kRingSlots * kTileBytes;
   static constexpr int kBytes = kBar + 1024;
   static constexpr int kLaunchBytes = kBytes + 1024;  // slack for 1024-byte alignment
 };
 
 struct Bars {
   uint64_t q_full, q_empty;
-  uint64_t k_full[kKStages], k_empty[kKStages], v_full[kVStages], v_empty[kVStages];
+  uint64_t r_full[kRingSlots], r_empty[kRingSlots];
   uint64_t s_full[2], p_full[2], o_done[2], o_free[2];
-  uint64_t drain;
+  uint64_t drain[2];
   uint32_t tmem_base;
   int abort;
   int never;  // stays 0: abort flag for waits that must not give up early
@@ -125,6 +128,11 @@ __device__ __forceinline__ Item load_item(const int4* items, const kev_interval*
   return x;
 }
 
+// Item order of a CTA: in round r it takes item r*G + b (r even) or r*G + G-1-b (r odd) of the
+// longest-first list (G = grid size, b = its index), so a CTA that took one of the longest items
+// of a round takes one of the shortest of the next; all roles walk the same sequence.
+__device__ __forceinline__ int snake_item(int r, int b, int G) { return r * G + ((r & 1) ? G - 1 - b : b); }
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -144,22 +152,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->q_full, 1);
-    mbar_init(&bars->q_empty, 1);
-    for (int s = 0; s < kKStages; ++s) {
-      mbar_init(&bars->k_full[s], 1);
-      mbar_init(&bars->k_empty[s], 1);
-    }
-    for (int s = 0; s < kVStages; ++s) {
-      mbar_init(&bars->v_full[s], 1);
-      mbar_init(&bars->v_empty[s], 1);
+    mbar_init(&bars->q_empty, 2);  // the Q tiles and the ring slots are released by both MMA issuers
+    for (int s = 0; s < kRingSlots; ++s) {
+      mbar_init(&bars->r_full[s], 1);
+      mbar_init(&bars->r_empty[s], 2);
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&bars->s_full[t], 1);
-      mbar_init(&bars->p_full[t], 128);
+      mbar_init(&bars->p_full[t], 4);  // one arrival per softmax warp
       mbar_init(&bars->o_done[t], 1);
-      mbar_init(&bars->o_free[t], 128);
+      mbar_init(&bars->o_free[t], 4);
     }
-    mbar_init(&bars->drain, 1);
+    mbar_init(&bars->drain[0], 1);
+    mbar_init(&bars->drain[1], 1);
     bars->abort = 0;
     bars->never = 0;
     fence_mbar_init();
@@ -185,16 +190,49 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp >= kProducerWarp) {
   regs_dec<kRegsControl>();
   if (warp == kProducerWarp) {
-    // ------------------------------------------------------------------ Q and K producer
+    // ------------------------------------------------------------------ K/V producer
     if (lane == 0) {
-      uint32_t k_iter = 0, n = 0, q_loads = 0;
-      uint32_t k_loads[kKStages] = {0, 0, 0};
+      uint32_t seq = 0;  // ring sequence: 2 ki is K(ki), 2 ki + 1 is V(ki)
+      uint32_t loads[kRingSlots] = {0, 0, 0, 0, 0};
       bool ok = true;
       Item x_next = load_item(items, p.intervals, blockIdx.x);
-      for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, ++n) {
+      for (int rnd = 0, it = blockIdx.x; it < n_items && ok; it = snake_item(++rnd, blockIdx.x, gridDim.x)) {
         const Item x = x_next;  // loaded one item ahead: its latency hides behind this item
-        if (it + (int)gridDim.x < n_items) x_next = load_item(items, p.intervals, it + gridDim.x);
+        const int it_next = snake_item(rnd + 1, blockIdx.x, gridDim.x);
+        if (it_next < n_items) x_next = load_item(items, p.intervals, it_next);
         const int g = x.h0 / p.group;
+        for (int j = 0; j < x.nkv && ok; ++j) {
+          for (int is_v = 0; is_v < 2; ++is_v, ++seq) {
+            const int s = seq % kRingSlots;
+            const uint32_t round = seq / kRingSlots;
+            if (round > 0 && !mbar_wait(&bars->r_empty[s], (round - 1) & 1, abort_flag, budget)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(&bars->r_full[s], L::kTileBytes);
+            for (int c = 0; c < L::kSub; ++c)
+              tma_load_2d(smem + L::kRing + s * L::kTileBytes + c * L::kSubBytes, is_v ? &tm_v : &tm_k,
+                          g * D + c * 64, x.seg_begin + j * kBN, &bars->r_full[s]);
+            ++loads[s];
+          }
+        }
+      }
+      if (!ok) raise_timeout(p, bars);
+      if (*abort_flag) {  // every copy issued by this thread lands before the CTA leaves
+        for (int s = 0; s < kRingSlots; ++s)
+          if (loads[s]) mbar_wait(&bars->r_full[s], (loads[s] - 1) & 1, never, kDrainBudget);
+      }
+    }
+  } else if (warp == kQProducerWarp) {
+    // ------------------------------------------------------------------ Q producer
+    if (lane == 0) {
+      uint32_t n = 0, q_loads = 0;
+      bool ok = true;
+      Item x_next = load_item(items, p.intervals, blockIdx.x);
+      for (int rnd = 0, it = blockIdx.x; it < n_items && ok; it = snake_item(++rnd, blockIdx.x, gridDim.x), ++n) {
+        const Item x = x_next;
+        const int it_next = snake_item(rnd + 1, blockIdx.x, gridDim.x);
+        if (it_next < n_items) x_next = load_item(items, p.intervals, it_next);
         if (n > 0 && !mbar_wait(&bars->q_empty, (n - 1) & 1, abort_flag, budget)) {
           ok = false;
           break;
@@ -205,158 +243,135 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_2d(smem + L::kQ + t * L::kTileBytes + c * L::kSubBytes, &tm_q, (x.h0 + t) * D + c * 64, x.row0,
                         &bars->q_full);
         ++q_loads;
-        // warm L2 (and the address translation) for the next item's query tiles and first
-        // K/V tile while this item runs: its Q load is issued only when this item's last S
-        // MMA has read the Q buffer
-        if (it + (int)gridDim.x < n_items) {
+        // pull the next item's query tiles into L2 while this item runs: their load into
+        // shared memory starts only when this item's last S MMA has read the Q buffer
+        if (it_next < n_items) {
           const Item& nx = x_next;
-          const int ng = nx.h0 / p.group;
           for (int t = 0; t < nx.nh; ++t)
             for (int c = 0; c < L::kSub; ++c) tma_prefetch_l2_2d(&tm_q, (nx.h0 + t) * D + c * 64, nx.row0);
-          for (int c = 0; c < L::kSub; ++c) {
-            tma_prefetch_l2_2d(&tm_k, ng * D + c * 64, nx.seg_begin);
-            tma_prefetch_l2_2d(&tm_v, ng * D + c * 64, nx.seg_begin);
-          }
-        }
-        for (int j = 0; j < x.nkv; ++j, ++k_iter) {
-          const int s = k_iter % kKStages;
-          const uint32_t round = k_iter / kKStages;
-          if (round > 0 && !mbar_wait(&bars->k_empty[s], (round - 1) & 1, abort_flag, budget)) {
-            ok = false;
-            break;
-          }
-          mbar_arrive_expect_tx(&bars->k_full[s], L::kTileBytes);
-          for (int c = 0; c < L::kSub; ++c)
-            tma_load_2d(smem + L::kK + s * L::kTileBytes + c * L::kSubBytes, &tm_k, g * D + c * 64,
-                        x.seg_begin + j * kBN, &bars->k_full[s]);
-          ++k_loads[s];
         }
       }
       if (!ok) raise_timeout(p, bars);
-      if (*abort_flag) {
-        // every copy issued by this thread lands before the CTA leaves
-        if (q_loads) mbar_wait(&bars->q_full, (q_loads - 1) & 1, never, kDrainBudget);
-        for (int s = 0; s < kKStages; ++s)
-          if (k_loads[s]) mbar_wait(&bars->k_full[s], (k_loads[s] - 1) & 1, never, kDrainBudget);
-      }
+      if (*abort_flag && q_loads) mbar_wait(&bars->q_full, (q_loads - 1) & 1, never, kDrainBudget);
     }
-  } else if (warp == kVProducerWarp) {
-    // ------------------------------------------------------------------ V producer
-    if (lane == 0) {
-      uint32_t v_iter = 0;
-      uint32_t v_loads[kVStages] = {0, 0};
-      bool ok = true;
-      Item x_next = load_item(items, p.intervals, blockIdx.x);
-      for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
-        const Item x = x_next;  // loaded one item ahead: its latency hides behind this item
-        if (it + (int)gridDim.x < n_items) x_next = load_item(items, p.intervals, it + gridDim.x);
-        const int g = x.h0 / p.group;
-        for (int j = 0; j < x.nkv; ++j, ++v_iter) {
-          const int s = v_iter % kVStages;
-          const uint32_t round = v_iter / kVStages;
-          if (round > 0 && !mbar_wait(&bars->v_empty[s], (round - 1) & 1, abort_flag, budget)) {
-            ok = false;
-            break;
-          }
-          mbar_arrive_expect_tx(&bars->v_full[s], L::kTileBytes);
-          for (int c = 0; c < L::kSub; ++c)
-            tma_load_2d(smem + L::kV + s * L::kTileBytes + c * L::kSubBytes, &tm_v, g * D + c * 64,
-                        x.seg_begin + j * kBN, &bars->v_full[s]);
-          ++v_loads[s];
-        }
-      }
-      if (!ok) raise_timeout(p, bars);
-      if (*abort_flag) {
-        for (int s = 0; s < kVStages; ++s)
-          if (v_loads[s]) mbar_wait(&bars->v_full[s], (v_loads[s] - 1) & 1, never, kDrainBudget);
-      }
-    }
-  } else if (warp == kMmaWarp) {
-    // ------------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc_s = idesc_bf16(kBM, kBN, false, false);
-      constexpr uint32_t idesc_o = idesc_bf16(kBM, D, false, true);
-      uint32_t kv_iter = 0, n = 0;
-      uint32_t p_cnt[2] = {0, 0}, items_done[2] = {0, 0};
-      bool ok = true;
+  } else if (warp == kMmaWarp || warp == kMmaWarpB) {
+    // ------------------------------------------------------------------ MMA issuers
+    // Warp 9 issues the MMAs of query tile A, warp 11 those of tile B, taking strict turns on
+    // the tensor core: A's group of a key step (PV_A, then S_A of the next key tile), then B's,
+    // then A's next, handed over with named barriers (a few cycles, no shared memory).  Each
+    // issuer does its waits while the other one issues, so their latency stays off the
+    // tensor core, and the groups never interleave, so tile B's softmax runs while tile A's
+    // MMAs execute and the other way round.  Both release the shared Q tiles and ring slots
+    // (their empty barriers count two arrivals); an issuer whose tile is absent from an item
+    // (a single q-head left in the group) takes its turns without issuing.  After a failed
+    // wait an issuer keeps taking its turns (issuing nothing) until both reach the end.
+    const int t = warp == kMmaWarp ? 0 : 1;
+    const bool leader = lane == 0;
+    constexpr uint32_t idesc_s = idesc_bf16(kBM, kBN, false, false);
+    constexpr uint32_t idesc_o = idesc_bf16(kBM, D, false, true);
+    uint32_t kv_iter = 0, n = 0, p_cnt = 0, items_done = 0;
+    bool ok = true;
+    bool first_turn = true;
+    auto wait_ok = [&](uint64_t* bar, uint32_t parity) {
+      if (!ok) return;
+      ok = warp_wait(bar, parity, abort_flag, budget);
+      if (!ok) *abort_flag = 1;
+    };
+    // turn hand-over: barrier 2 = "A's group is issued", barrier 3 = "B's group is issued"
+    auto take_turn = [&]() {
+      if (t == 1) asm volatile("bar.sync 2, 64;" ::: "memory");
+      else if (!first_turn) asm volatile("bar.sync 3, 64;" ::: "memory");
+      first_turn = false;
+    };
+    auto pass_turn = [&]() {
+      __syncwarp();
+      if (t == 0) asm volatile("bar.arrive 2, 64;" ::: "memory");
+      else asm volatile("bar.arrive 3, 64;" ::: "memory");
+    };
 
-      auto issue_s = [&](int t, int stage) {
-        const uint32_t q_addr = smem_u32(smem + L::kQ + t * L::kTileBytes);
-        const uint32_t k_addr = smem_u32(smem + L::kK + stage * L::kTileBytes);  // K ring stage
+    auto issue_s = [&](int stage) {
+      const uint32_t q_addr = smem_u32(smem + L::kQ + t * L::kTileBytes);
+      const uint32_t k_addr = smem_u32(smem + L::kRing + stage * L::kTileBytes);  // K tile's ring slot
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * L::kSubBytes + (kk & 3) * 32;
-          umma_bf16(tmem + t * kBN, sdesc_sw128(q_addr + off, 16, 1024), sdesc_sw128(k_addr + off, 16, 1024), idesc_s,
-                    kk > 0);
-        }
-        umma_commit(&bars->s_full[t]);
-      };
-      auto issue_pv = [&](int t, int stage, bool accumulate) {
-        const uint32_t v_addr = smem_u32(smem + L::kV + stage * L::kTileBytes);
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = (kk >> 2) * L::kSubBytes + (kk & 3) * 32;
+        umma_bf16(tmem + t * kBN, sdesc_sw128(q_addr + off, 16, 1024), sdesc_sw128(k_addr + off, 16, 1024), idesc_s,
+                  kk > 0);
+      }
+      umma_commit(&bars->s_full[t]);
+    };
+    auto issue_pv = [&](int stage, bool accumulate) {
+      const uint32_t v_addr = smem_u32(smem + L::kRing + stage * L::kTileBytes);  // V tile's ring slot
 #pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk) {
-          const uint64_t b = sdesc_sw128(v_addr + kk * 16 * 128, L::kSubBytes, 1024);
-          umma_bf16_ts(tmem + 256 + t * D, tmem + t * kBN + kk * 8, b, idesc_o, (accumulate || kk > 0) ? 1u : 0u);
-        }
-      };
+      for (int kk = 0; kk < kBN / 16; ++kk) {
+        const uint64_t b = sdesc_sw128(v_addr + kk * 16 * 128, L::kSubBytes, 1024);
+        umma_bf16_ts(tmem + 256 + t * D, tmem + t * kBN + kk * 8, b, idesc_o, (accumulate || kk > 0) ? 1u : 0u);
+      }
+    };
+    // ring slot and phase of K(ki) (sequence 2 ki) and V(ki) (sequence 2 ki + 1)
+    auto slot = [](uint32_t q) { return (int)(q % kRingSlots); };
+    auto phase = [](uint32_t q) { return (q / kRingSlots) & 1; };
 
-      Item x_next = load_item(items, p.intervals, blockIdx.x);
-      for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, ++n) {
-        const Item x = x_next;  // loaded one item ahead: its latency hides behind this item
-        if (it + (int)gridDim.x < n_items) x_next = load_item(items, p.intervals, it + gridDim.x);
-        {
-          const int k0 = kv_iter % kKStages;
-          if (!mbar_wait(&bars->q_full, n & 1, abort_flag, budget) ||
-              !mbar_wait(&bars->k_full[k0], (kv_iter / kKStages) & 1, abort_flag, budget)) {
-            ok = false;
-            break;
-          }
+    Item x_next = load_item(items, p.intervals, blockIdx.x);
+    for (int rnd = 0, it = blockIdx.x; it < n_items; it = snake_item(++rnd, blockIdx.x, gridDim.x), ++n) {
+      const Item x = x_next;  // loaded one item ahead: its latency hides behind this item
+      const int it_next = snake_item(rnd + 1, blockIdx.x, gridDim.x);
+      if (it_next < n_items) x_next = load_item(items, p.intervals, it_next);
+      const bool mine = t < x.nh;
+      {
+        const uint32_t qk = 2 * kv_iter;
+        wait_ok(&bars->q_full, n & 1);
+        wait_ok(&bars->r_full[slot(qk)], phase(qk));
+        take_turn();
+        if (ok && leader) {
           tc_fence_after();
-          for (int t = 0; t < x.nh; ++t) issue_s(t, k0);
-          umma_commit(&bars->k_empty[k0]);
+          if (mine) issue_s(slot(qk));
+          umma_commit(&bars->r_empty[slot(qk)]);
           if (x.nkv == 1) umma_commit(&bars->q_empty);
         }
-        for (int j = 0; j < x.nkv && ok; ++j) {
-          const uint32_t ki = kv_iter + j;
-          const int vs = ki % kVStages;
-          const bool has_next = j + 1 < x.nkv;
-          const int kn = (ki + 1) % kKStages;
-          if (!mbar_wait(&bars->v_full[vs], (ki / kVStages) & 1, abort_flag, budget) ||
-              (has_next && !mbar_wait(&bars->k_full[kn], ((ki + 1) / kKStages) & 1, abort_flag, budget))) {
-            ok = false;
-            break;
+        pass_turn();
+      }
+      for (int j = 0; j < x.nkv; ++j) {
+        const uint32_t ki = kv_iter + j;
+        const uint32_t qv = 2 * ki + 1, qk = 2 * ki + 2;  // V(ki), K(ki + 1)
+        const int vs = slot(qv), kn = slot(qk);
+        const bool has_next = j + 1 < x.nkv;
+        wait_ok(&bars->r_full[vs], phase(qv));
+        if (has_next) wait_ok(&bars->r_full[kn], phase(qk));
+        if (mine) {
+          wait_ok(&bars->p_full[t], p_cnt & 1);
+          if (j == 0 && items_done > 0) wait_ok(&bars->o_free[t], (items_done - 1) & 1);
+          ++p_cnt;
+        }
+        take_turn();
+        if (ok && leader) {
+          tc_fence_after();
+          if (mine) {
+            issue_pv(vs, j > 0);
+            umma_commit(&bars->r_empty[vs]);  // this issuer's use of the V tile ends with the PV
+            if (has_next) issue_s(kn);        // overwrites S_t / P_t after the PV above read it (in order)
+            else umma_commit(&bars->o_done[t]);
+          } else {
+            umma_commit(&bars->r_empty[vs]);
           }
-          for (int t = 0; t < x.nh; ++t) {
-            if (!mbar_wait(&bars->p_full[t], p_cnt[t] & 1, abort_flag, budget) ||
-                (j == 0 && items_done[t] > 0 &&
-                 !mbar_wait(&bars->o_free[t], (items_done[t] - 1) & 1, abort_flag, budget))) {
-              ok = false;
-              break;
-            }
-            ++p_cnt[t];
-            tc_fence_after();
-            issue_pv(t, vs, j > 0);
-            if (has_next) {
-              issue_s(t, kn);  // overwrites S_t / P_t after the PV above has read it (in order)
-            } else {
-              umma_commit(&bars->o_done[t]);
-            }
-          }
-          if (!ok) break;
-          umma_commit(&bars->v_empty[vs]);
           if (has_next) {
-            umma_commit(&bars->k_empty[kn]);
+            umma_commit(&bars->r_empty[kn]);
             if (j + 1 == x.nkv - 1) umma_commit(&bars->q_empty);  // last use of the Q tiles issued
           }
         }
-        for (int t = 0; t < x.nh; ++t) ++items_done[t];
-        kv_iter += x.nkv;
+        pass_turn();
       }
-      if (!ok) raise_timeout(p, bars);
-      // every MMA this thread issued is complete before TMEM is freed
-      umma_commit(&bars->drain);
-      mbar_wait(&bars->drain, 0, never, kDrainBudget);
+      if (mine) ++items_done;
+      kv_iter += x.nkv;
     }
+    if (t == 0 && !first_turn) asm volatile("bar.sync 3, 64;" ::: "memory");  // B's last hand-over
+    if (!ok && leader) raise_timeout(p, bars);
+    // every MMA this thread issued is complete before TMEM is freed
+    if (leader) {
+      umma_commit(&bars->drain[t]);
+      mbar_wait(&bars->drain[t], 0, never, kDrainBudget);
+    }
+    __syncwarp();
   }
   } else {
     regs_inc<kRegsSoftmax>();
@@ -375,9 +390,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool out32 = (reinterpret_cast<uintptr_t>(p.out) & 31) == 0;
 
     Item x_next = load_item(items, p.intervals, blockIdx.x);
-    for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+    for (int rnd = 0, it = blockIdx.x; it < n_items && ok; it = snake_item(++rnd, blockIdx.x, gridDim.x)) {
       const Item x = x_next;  // loaded one item ahead: its latency hides behind this item
-      if (it + (int)gridDim.x < n_items) x_next = load_item(items, p.intervals, it + gridDim.x);
+      const int it_next = snake_item(rnd + 1, blockIdx.x, gridDim.x);
+      if (it_next < n_items) x_next = load_item(items, p.intervals, it_next);
       if (t >= x.nh) continue;
       float m_run = -INFINITY, l_run = 0.f;
 
@@ -471,7 +487,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         l_run += lt;
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(&bars->p_full[t]);
+        mbar_arrive_warp(&bars->p_full[t]);
       }
       if (!ok) break;
 
@@ -510,7 +526,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       tc_fence_before();
-      mbar_arrive(&bars->o_free[t]);
+      mbar_arrive_warp(&bars->o_free[t]);
     }
     if (!ok && lane == 0) raise_timeout(p, bars);
   }
