@@ -46,10 +46,10 @@ using namespace sm100;
 
 constexpr int kBM = 128;            // query rows per tile
 constexpr int kBN = 128;            // keys per tile
-// K and V tiles share one ring, in the order K(0) V(0) K(1) V(1) ...: with 5 slots, K(j) reuses
-// the slot of V(j-3) and V(j) that of K(j-2), so each tile's load starts 2-3 key steps before
-// its MMA needs it (a TMA round trip takes ~4700 cycles under load, more than one step).
-constexpr int kRingSlots = 5;
+// K and V tiles share one ring, in the order K(0) V(0) K(1) V(1) ...: with 4 slots, K(j) reuses
+// the slot of K(j-2) and V(j) that of V(j-2), so each tile's load starts about two key steps
+// before its MMA needs it (measured: 4 slots beat 3 and 5, and free 32 KB for the output stage).
+constexpr int kRingSlots = 4;
 constexpr int kThreads = 384;       // 3 warpgroups
 constexpr int kProducerWarp = 8;    // warpgroup 2: K/V producer, MMA issuer A, Q producer, MMA issuer B
 constexpr int kMmaWarp = 9;
@@ -83,7 +83,8 @@ struct Smem {
   static constexpr int kTileBytes = kBM * D * 2;  // one Q/K/V tile
   static constexpr int kQ = 0;                    // two query tiles
   static constexpr int kRing = kQ + 2 * kTileBytes;  // K/V ring
-  static constexpr int kBar = kRing + kRingSlots * kTileBytes;
+  static constexpr int kStage = kRing + kRingSlots * kTileBytes;  // one output tile, TMA-store box layout
+  static constexpr int kBar = kStage + kTileBytes;
   static constexpr int kBytes = kBar + 1024;
   static constexpr int kLaunchBytes = kBytes + 1024;  // slack for 1024-byte alignment
 };
@@ -92,6 +93,7 @@ struct Bars {
   uint64_t q_full, q_empty;
   uint64_t r_full[kRingSlots], r_empty[kRingSlots];
   uint64_t s_full[2], p_full[2], o_done[2], o_free[2];
+  uint64_t stg_free[4];  // slice q (rows 32q..32q+31) of the output stage has been read by its last store
   uint64_t drain[2];
   uint32_t tmem_base;
   int abort;
@@ -136,7 +138,8 @@ __device__ __forceinline__ int snake_item(int r, int b, int G) { return r * G + 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                      const __grid_constant__ CUtensorMap tm_v, const TcParams p) {
+                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_out,
+                      const TcParams p) {
   using L = Smem<D>;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem =
@@ -163,6 +166,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars->o_done[t], 1);
       mbar_init(&bars->o_free[t], 4);
     }
+    for (int q = 0; q < 4; ++q) mbar_init(&bars->stg_free[q], 1);
     mbar_init(&bars->drain[0], 1);
     mbar_init(&bars->drain[1], 1);
     bars->abort = 0;
@@ -173,6 +177,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
+    tma_prefetch_desc(&tm_out);
   }
   if (warp == kMmaWarp) {
     tmem_alloc(&bars->tmem_base, kTmemCols);
@@ -193,7 +198,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------------ K/V producer
     if (lane == 0) {
       uint32_t seq = 0;  // ring sequence: 2 ki is K(ki), 2 ki + 1 is V(ki)
-      uint32_t loads[kRingSlots] = {0, 0, 0, 0, 0};
+      uint32_t loads[kRingSlots] = {};
       bool ok = true;
       Item x_next = load_item(items, p.intervals, blockIdx.x);
       for (int rnd = 0, it = blockIdx.x; it < n_items && ok; it = snake_item(++rnd, blockIdx.x, gridDim.x)) {
@@ -385,6 +390,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float sl2 = p.scale_log2;
     const unsigned long long sl2x2 = f2pack(sl2, sl2);
     uint32_t s_cnt = 0, o_cnt = 0;
+    uint32_t stg_uses = 0;  // output-stage uses before the current item (tile A's, then tile B's)
     bool ok = true;
     __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
     const bool out32 = (reinterpret_cast<uintptr_t>(p.out) & 31) == 0;
@@ -394,6 +400,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const Item x = x_next;  // loaded one item ahead: its latency hides behind this item
       const int it_next = snake_item(rnd + 1, blockIdx.x, gridDim.x);
       if (it_next < n_items) x_next = load_item(items, p.intervals, it_next);
+      const uint32_t my_use = stg_uses + (uint32_t)t;
+      if (x.rows == kBM) stg_uses += (uint32_t)x.nh;
       if (t >= x.nh) continue;
       float m_run = -INFINITY, l_run = 0.f;
 
@@ -499,36 +507,73 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++o_cnt;
       tc_fence_after();
       const float inv = 1.f / l_run;
-      const bool valid = r < x.rows;
-      __nv_bfloat16* orow = out + ((int64_t)(x.row0 + r) * p.h_q + x.h0 + t) * D;
-      {
-        uint32_t o[D / 32][32];
+      uint32_t o[D / 32][32];
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) tmem_ld32(tm_o + c * 32, o[c]);
+      for (int c = 0; c < D / 32; ++c) tmem_ld32(tm_o + c * 32, o[c]);
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) tmem_ld_wait(o[c]);
-        if (valid) {
+      for (int c = 0; c < D / 32; ++c) tmem_ld_wait(o[c]);
+      tc_fence_before();
+      mbar_arrive_warp(&bars->o_free[t]);  // O_t is in registers: the next item's PV may start
+      if (x.rows == kBM) {
+        // A whole tile: each warp writes its 32 rows as bf16 into its slice of the output stage
+        // (the 128-byte swizzled box layout) and one lane stores the slice with two bulk tensor
+        // copies of 32 rows; the warp waits only for the copy engine to have read its 8 KB.
+        // Tile A's use of a slice comes before tile B's (its warps 4-7 wait on warps 0-3).
+        const int q = warp & 3;
+        const bool okw = my_use == 0 || warp_wait(&bars->stg_free[q], (my_use - 1) & 1, abort_flag, budget);
+        if (!okw) {
+          ok = false;
+          break;
+        }
+        unsigned char* stg = smem + L::kStage;
 #pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t w[16];
+        for (int c = 0; c < L::kSub; ++c)
 #pragma unroll
-            for (int e = 0; e < 16; ++e)
-              w[e] = pack_bf16x2(__uint_as_float(o[c][2 * e]) * inv, __uint_as_float(o[c][2 * e + 1]) * inv);
-            if (out32) {  // 32-byte stores when the output allows them (the ABI promises 16)
-              st_global_v8(orow + c * 32, w);
-              st_global_v8(orow + c * 32 + 16, w + 8);
-            } else {
-              uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+          for (int k = 0; k < 8; ++k) {
+            const int col = c * 64 + k * 8;  // 8 columns = one 16-byte chunk
+            const uint32_t w0 = pack_bf16x2(__uint_as_float(o[col / 32][col % 32]) * inv,
+                                            __uint_as_float(o[col / 32][col % 32 + 1]) * inv);
+            const uint32_t w1 = pack_bf16x2(__uint_as_float(o[col / 32][col % 32 + 2]) * inv,
+                                            __uint_as_float(o[col / 32][col % 32 + 3]) * inv);
+            const uint32_t w2 = pack_bf16x2(__uint_as_float(o[col / 32][col % 32 + 4]) * inv,
+                                            __uint_as_float(o[col / 32][col % 32 + 5]) * inv);
+            const uint32_t w3 = pack_bf16x2(__uint_as_float(o[col / 32][col % 32 + 6]) * inv,
+                                            __uint_as_float(o[col / 32][col % 32 + 7]) * inv);
+            st_shared_v4(smem_u32(stg + c * L::kSubBytes + r * 128 + ((k ^ (r & 7)) << 4)), w0, w1, w2, w3);
+          }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          for (int c = 0; c < L::kSub; ++c)
+            tma_store_2d(&tm_out, stg + c * L::kSubBytes + q * 32 * 128, (x.h0 + t) * D + c * 64, x.row0 + q * 32);
+          bulk_commit_group();
+          bulk_wait_read_all();
+          mbar_arrive(&bars->stg_free[q]);
+        }
+        __syncwarp();
+      } else if (r < x.rows) {
+        // the question's last, partial tile: row by row (a whole box would overwrite the
+        // next question's rows)
+        __nv_bfloat16* orow = out + ((int64_t)(x.row0 + r) * p.h_q + x.h0 + t) * D;
 #pragma unroll
-              for (int e = 0; e < 4; ++e) dst[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
-            }
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t w[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            w[e] = pack_bf16x2(__uint_as_float(o[c][2 * e]) * inv, __uint_as_float(o[c][2 * e + 1]) * inv);
+          if (out32) {  // 32-byte stores when the output allows them (the ABI promises 16)
+            st_global_v8(orow + c * 32, w);
+            st_global_v8(orow + c * 32 + 16, w + 8);
+          } else {
+            uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) dst[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
           }
         }
       }
-      tc_fence_before();
-      mbar_arrive_warp(&bars->o_free[t]);
     }
     if (!ok && lane == 0) raise_timeout(p, bars);
+    if (lane == 0) bulk_wait_all();  // this lane's output stores are complete
   }
 
   tc_fence_before();
@@ -559,13 +604,13 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// 2-D bf16 view [rows, cols] (cols contiguous), boxes of 64 columns x 128 rows, 128-byte swizzle.
-bool make_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows) {
+// 2-D bf16 view [rows, cols] (cols contiguous), boxes of 64 columns x box_rows rows, 128-byte swizzle.
+bool make_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint32_t box_rows = 128) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   const cuuint64_t dims[2] = {cols, rows};
   const cuuint64_t strides[1] = {cols * 2};
-  const cuuint32_t box[2] = {64, 128};
+  const cuuint32_t box[2] = {64, box_rows};
   const cuuint32_t estr[2] = {1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -583,8 +628,8 @@ long long wait_budget_cycles() {
 
 template <int D>
 cudaError_t launch_tc(const PrefillArgs& a, int num_sms, cudaStream_t s) {
-  CUtensorMap mq, mk, mv;
-  if (!make_map(&mq, a.q, (uint64_t)a.h_q * D, (uint64_t)a.T) ||
+  CUtensorMap mq, mk, mv, mo;
+  if (!make_map(&mq, a.q, (uint64_t)a.h_q * D, (uint64_t)a.T) || !make_map(&mo, a.out, (uint64_t)a.h_q * D, (uint64_t)a.T, 32) ||
       !make_map(&mk, a.k, (uint64_t)a.h_kv * D, (uint64_t)a.T) ||
       !make_map(&mv, a.v, (uint64_t)a.h_kv * D, (uint64_t)a.T))
     return cudaErrorInvalidValue;
@@ -603,7 +648,7 @@ cudaError_t launch_tc(const PrefillArgs& a, int num_sms, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   const int64_t max_items = a.layout.max_items;
   const int grid = (int)(max_items < num_sms ? max_items : num_sms);
-  prefill_tc_kernel<D><<<grid, kThreads, smem, s>>>(mq, mk, mv, p);
+  prefill_tc_kernel<D><<<grid, kThreads, smem, s>>>(mq, mk, mv, mo, p);
   return cudaGetLastError();
 }
 
