@@ -287,11 +287,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
         bool ok = true;
         const BatchPlan plan = make_plan(total, gridDim.x);
         int k = 0;  // position in the stage ring
-        // two grabs stay in flight ahead of the batch being issued (a grab's round trip is
-        // longer than a single-chunk batch)
-        int bat = grab, bat1 = atomicAdd(&sched[0], 1);
+        // the next grab goes out when a batch starts: its round trip hides behind the batch
+        // (two in flight measured slower: a CTA then holds more work when the list runs out)
+        int bat = grab;
         while (ok && bat < plan.nbat) {
-          const int bat2 = atomicAdd(&sched[0], 1);
+          const int next = atomicAdd(&sched[0], 1);
           const int x0 = plan.start(bat), x1 = plan.end(bat);
           Cursor u = cursor_at(a, item_base, meta, x0);
           for (int x = x0; x < x1; ++x, ++k) {
@@ -318,8 +318,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
             ++issued[s];
             cursor_next(u, a, item_base, meta);
           }
-          bat = bat1;
-          bat1 = bat2;
+          bat = next;
         }
         // no more work for this CTA: the merge grid may be launched (it waits for this grid)
         asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
