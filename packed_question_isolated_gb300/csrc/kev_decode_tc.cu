@@ -40,7 +40,7 @@ using dec::ItemInfo;
 constexpr int kD = 128;
 constexpr int kN = 16;             // MMA N: q-heads of one group, padded to 16
 constexpr int kC = dec::kChunk;    // 128 keys per chunk
-constexpr int kBatch = 4;          // consecutive chunks per dynamic grab (before the tail)
+constexpr int kBatch = 4;          // most consecutive chunks per dynamic grab
 constexpr int kTailPerCta = 0;     // single-chunk grabs at the end, per CTA of the grid (measured: none is best)
 constexpr int kThreads = 352;
 constexpr int kQuad = 128;         // threads of the softmax (warps 2-5) and of the epilogue (warps 7-10)
@@ -165,21 +165,21 @@ __device__ __forceinline__ bool reduce_writer(int lane) {
   return (lane & (32 / NH - 1)) == 0;
 }
 
-// The fixed plan of the dynamic grabs: batches of kBatch chunks over [0, x1), then one batch
-// per chunk over [x1, total) so the last grabs are short and every CTA finishes at about the
-// same time.  Batch boundaries depend on the chunk index only (not on which CTA grabs what),
-// so the pieces, and hence the results, are the same on every run.
+// The fixed plan of the dynamic grabs: batches of B = kBatch consecutive chunks over [0, x1),
+// then one batch per chunk over [x1, total).  Batch boundaries depend on the chunk index only (not on which CTA grabs what), so
+// the pieces, and hence the results, are the same on every run.
 struct BatchPlan {
-  int n1, x1, nbat;
-  __device__ int start(int b) const { return b < n1 ? b * kBatch : x1 + (b - n1); }
-  __device__ int end(int b) const { return b < n1 ? (b + 1) * kBatch : x1 + (b - n1) + 1; }
-  __device__ int of(int x) const { return x < x1 ? x / kBatch : n1 + (x - x1); }
+  int B, n1, x1, nbat;
+  __device__ int start(int b) const { return b < n1 ? b * B : x1 + (b - n1); }
+  __device__ int end(int b) const { return b < n1 ? (b + 1) * B : x1 + (b - n1) + 1; }
+  __device__ int of(int x) const { return x < x1 ? x / B : n1 + (x - x1); }
 };
 __device__ __forceinline__ BatchPlan make_plan(int total, int ctas) {
   const int tail = kTailPerCta * ctas;
   BatchPlan p;
-  p.n1 = total > tail ? (total - tail) / kBatch : 0;
-  p.x1 = p.n1 * kBatch;
+  p.B = kBatch;  // measured: fixed 4-chunk batches beat a per-call size on small and large decodes
+  p.n1 = total > tail ? (total - tail) / p.B : 0;
+  p.x1 = p.n1 * p.B;
   p.nbat = p.n1 + (total - p.x1);
   return p;
 }
@@ -228,6 +228,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   int* sched = reinterpret_cast<int*>(a.ws + a.layout.sched);
 
+  pdl_wait();  // lens, the pool and the counters are as the kernels before this one left them
   // the first batch grab goes out now; its latency hides behind the validation (the merge
   // kernel that follows resets the counter for the next call)
   int grab = 0;
@@ -243,6 +244,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
       const BatchPlan plan = make_plan(total, gridDim.x);
       sched[1] = plan.x1;
       sched[3] = plan.n1;
+      sched[4] = plan.B;
     }
     if (tid == 0) {
       for (int s = 0; s < NS; ++s) {
@@ -321,7 +323,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
           bat = next;
         }
         // no more work for this CTA: the merge grid may be launched (it waits for this grid)
-        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+        pdl_trigger();
         if (ok) {  // end of the stream: a stage whose info says so, completed without copies
           const int s = k % NS;
           const uint32_t round = k / NS;
@@ -653,7 +655,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
 
   // the merge kernel may be scheduled as soon as every CTA got here (it still waits for this
   // grid to complete before it reads anything)
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  pdl_trigger();
 }
 
 // Merge of the pieces of every (question, kv head) that the decode kernel split (one CTA per
@@ -663,13 +665,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
 // resets the decode kernel's batch counter for the next call.
 template <int NH>
 __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeArgs a) {
-  asm volatile("griddepcontrol.wait;" ::: "memory");  // the decode grid is complete and visible
+  pdl_wait();  // the decode grid is complete and visible
   int* sched = reinterpret_cast<int*>(a.ws + a.layout.sched);
   if (blockIdx.x == 0 && threadIdx.x == 0) sched[0] = 0;
   if (sched[2] != ST_OK) return;  // invalid call (or timeout): nothing to merge
   BatchPlan plan;
   plan.x1 = sched[1];
   plan.n1 = sched[3];
+  plan.B = sched[4];
   __shared__ float mg_m[128], mg_l[128];
   const int r = threadIdx.x;
   const float* partials = reinterpret_cast<const float*>(a.ws + a.layout.partials);
@@ -788,22 +791,11 @@ cudaError_t launch_ns(const DecodeArgs& a, int num_sms, cudaStream_t st, const C
   DTcParams p;
   p.a = a;
   p.wait_budget = wait_budget_cycles();
-  decode_tc_kernel<NS, NH><<<num_sms, kThreads, smem, st>>>(mk, mv, mq, p);
-  e = cudaGetLastError();
+  e = launch_pdl(decode_tc_kernel<NS, NH>, dim3(num_sms), dim3(kThreads), (size_t)smem, st, mk, mv, mq, p);
   if (e != cudaSuccess) return e;
   // the merge kernel, programmatically dependent on the decode kernel (its launch overlaps the
   // decode kernel's end; its griddepcontrol.wait orders every read after the decode grid)
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)min(a.n * a.h_kv, 8 * num_sms));
-  cfg.blockDim = dim3(128);
-  cfg.dynamicSmemBytes = 0;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_merge_kernel<NH>, a);
+  return launch_pdl(decode_merge_kernel<NH>, dim3((unsigned)min(a.n * a.h_kv, 8 * num_sms)), dim3(128), 0, st, a);
 }
 
 template <int NH>

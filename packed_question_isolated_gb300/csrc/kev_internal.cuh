@@ -77,7 +77,8 @@ inline PrefillLayout prefill_layout(int32_t n, int32_t T, int32_t h_q) {
 // decode workspace
 // ---------------------------------------------------------------------------------------
 struct DecodeLayout {
-  size_t sched;     // int32[4]  tensor-core decode: [0] batch-grab counter (left at zero), [2] validation code
+  size_t sched;     // int32[8]  tensor-core decode: [0] batch-grab counter (left at zero), [1] [3] [4] grab
+                    // plan, [2] validation code
   size_t xi0;       // int32[N * H_kv]  tensor-core decode: global index of chunk 0 of each (question, kv head)
   size_t counters;  // int32[N * H_kv * n_hblocks]  arrivals per (question, kv head, head block); left at zero
   size_t partials;  // float[N * H_kv * n_hblocks * max_chunks * GT * (d + 2)]
@@ -102,7 +103,7 @@ inline DecodeLayout decode_layout(int32_t n, int32_t cap, int32_t h_q, int32_t h
   const int32_t GT = tc ? 16 : decode_head_block_size(G);
   size_t off = 0;
   L.sched = off;
-  off = align_up(off + 4 * sizeof(int32_t), 256);
+  off = align_up(off + 8 * sizeof(int32_t), 256);
   L.xi0 = off;
   off = align_up(off + (tc ? sizeof(int32_t) * (size_t)n * h_kv : 0), 256);
   L.counters = off;
@@ -217,6 +218,29 @@ __device__ __forceinline__ float warp_sum(float x) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
   return x;
+}
+
+// Programmatic dependent launch: a kernel launched with launch_pdl may be scheduled while the
+// kernel before it in the stream finishes; it calls pdl_wait() before it reads anything (the
+// wait returns once that kernel has completed and its writes are visible), and pdl_trigger()
+// lets the kernel after it be scheduled the same way.  Both are no-ops without the attribute.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                              Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
 // First error wins; later kernels of the call read the word and write nothing.

@@ -17,6 +17,8 @@ namespace kev {
 namespace {
 
 __global__ void __launch_bounds__(256) aux_kernel(AuxArgs a) {
+  pdl_wait();  // the work list and status of the kernels before this one are complete
+  pdl_trigger();
   const PrefillHeader* hdr = reinterpret_cast<const PrefillHeader*>(a.ws);
   if (hdr->status != ST_OK) return;
   const int32_t* cu = reinterpret_cast<const int32_t*>(a.ws + a.layout.cu_seqlens);
@@ -64,8 +66,7 @@ __global__ void __launch_bounds__(256) aux_kernel(AuxArgs a) {
 }  // namespace
 
 cudaError_t launch_aux(const AuxArgs& a, int num_sms, cudaStream_t s) {
-  aux_kernel<<<num_sms * 4, 256, 0, s>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(aux_kernel, dim3(num_sms * 4), dim3(256), 0, s, a);
 }
 
 }  // namespace kev

@@ -147,6 +147,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   Bars* bars = reinterpret_cast<Bars*>(smem + L::kBar);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
+  pdl_wait();  // the segment builder's work list is complete
+  pdl_trigger();
   const PrefillHeader* hdr = reinterpret_cast<const PrefillHeader*>(p.ws);
   if (hdr->status != ST_OK) return;
   const int n_items = hdr->n_items;
@@ -648,8 +650,7 @@ cudaError_t launch_tc(const PrefillArgs& a, int num_sms, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   const int64_t max_items = a.layout.max_items;
   const int grid = (int)(max_items < num_sms ? max_items : num_sms);
-  prefill_tc_kernel<D><<<grid, kThreads, smem, s>>>(mq, mk, mv, mo, p);
-  return cudaGetLastError();
+  return launch_pdl(prefill_tc_kernel<D>, dim3(grid), dim3(kThreads), smem, s, mq, mk, mv, mo, p);
 }
 
 }  // namespace

@@ -76,6 +76,8 @@ __global__ void __launch_bounds__(kThreads) segments_kernel(SegmentsArgs a) {
   int4* items = reinterpret_cast<int4*>(a.ws + a.layout.items);
   int2* gaps = reinterpret_cast<int2*>(a.ws + a.layout.gaps);
 
+  pdl_wait();     // the intervals and slot ids may come from the kernel before this one
+  pdl_trigger();  // the attention kernel after this one may be scheduled on the other SMs
   const int n = a.n;
   const int tid = threadIdx.x;
   if (tid == 0) s_flags = 0;
@@ -251,8 +253,7 @@ __global__ void __launch_bounds__(kThreads) segments_kernel(SegmentsArgs a) {
 }  // namespace
 
 cudaError_t launch_segments(const SegmentsArgs& a, cudaStream_t s) {
-  segments_kernel<<<1, kThreads, 0, s>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(segments_kernel, dim3(1), dim3(kThreads), 0, s, a);
 }
 
 }  // namespace kev
