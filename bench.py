@@ -42,6 +42,23 @@ DECODE_WORKLOAD = ("qwen3_8b_decode: [64, 8, 2458, 128] bf16 pools, lens U{64..2
 FLUSH_BYTES = 512 << 20   # > 2 x L2 (129 MB)
 
 
+def max_over_ranks(x: float, world: int, device="cpu") -> float:
+    """The largest of every rank's value (the slowest rank's elapsed time); x itself on one rank."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_rate(units_per_rank: float, steps: int, world: int, max_ms: float) -> float:
+    """Whole-job throughput under weak scaling: every rank processes units_per_rank per step, the
+    job takes as long as its slowest rank (max_ms for all steps)."""
+    return units_per_rank * steps * world / (max_ms * 1e-3)
+
+
 class L2Flush:
     """Evicts every L2 line before a timed step: a 512 MB buffer is written (none of the step's
     data can survive that), then a second 512 MB buffer is read, so the dirty lines of the
@@ -331,13 +348,9 @@ def main(argv=None):
     torch.cuda.synchronize()
     step_ms = [ev[s][0].elapsed_time(ev[s][3]) for s in range(K)]
     attn_ms = [ev[s][1].elapsed_time(ev[s][2]) for s in range(K)]
-    total_ms = float(sum(step_ms))
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(float(sum(step_ms)), world, dev)
     useful = RL.prefill_useful_flops(w.lengths, w.h_q, w.d)
-    value = useful * K * world / (total_ms * 1e-3) / 1e12
+    value = aggregate_rate(useful, K, world, total_ms) / 1e12
     hbm_peak, tf_peak, tf_sust, peak_src = _peaks()
     attn_avg_ms = statistics.mean(attn_ms)
     achieved = useful / (attn_avg_ms * 1e-3) / 1e12
@@ -373,12 +386,8 @@ def main(argv=None):
         e2e_step()
     e1.record()
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_value = useful * Ke * world / (e2e_ms * 1e-3) / 1e12
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+    e2e_value = aggregate_rate(useful, Ke, world, e2e_ms) / 1e12
 
     # ---- decode workload ----------------------------------------------------------------
     dwl = W.qwen3_8b_decode()
@@ -409,7 +418,8 @@ def main(argv=None):
     torch.cuda.synchronize()
     dec_ms = statistics.mean(a.elapsed_time(b) for a, b in dev_ev)
     dec_bytes = RL.decode_bytes(dwl.lens, dwl.active, dwl.h_q, dwl.h_kv, dwl.d, 2)
-    dec_gbs = dec_bytes / (dec_ms * 1e-3) / 1e9
+    dec_gbs = dec_bytes / (dec_ms * 1e-3) / 1e9  # this GPU's kernel rate (the roofline is per GPU)
+    dec_job_gbs = aggregate_rate(dec_bytes, 1, world, max_over_ranks(dec_ms, world, dev)) / 1e9
     dec_traffic = _traffic("decode")
 
     cpu = None
@@ -433,7 +443,7 @@ def main(argv=None):
                          "frac": achieved / tf_peak, "traffic": traffic,
                          "kernel": "prefill attention (kev_prefill_from_segments)",
                          "peak_source": f"bf16_tflops burst, {peak_src}", "launch_ms": attn_avg_ms},
-            "decode": {"workload": DECODE_WORKLOAD, "value": dec_gbs, "unit": "GB/s", "ms_per_step": dec_ms,
+            "decode": {"workload": DECODE_WORKLOAD, "value": dec_job_gbs, "unit": "GB/s", "ms_per_step": dec_ms,
                        "roofline": {"bound": "hbm", "achieved": dec_gbs, "peak": hbm_peak, "unit": "GB/s",
                                     "frac": dec_gbs / hbm_peak, "traffic": dec_traffic,
                                     "algorithmic_bytes": dec_bytes, "peak_source": f"hbm_gbs, {peak_src}"}},
