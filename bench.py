@@ -39,6 +39,8 @@ WORKLOAD = ("qwen25_7b_prefill: 8 questions, lengths U{256..2048} seed 2 (T=7921
             "slot cap 2458; step = segment build + prefill attention + slot write + 1 decode step per question")
 DECODE_WORKLOAD = ("qwen3_8b_decode: [64, 8, 2458, 128] bf16 pools, lens U{64..2400} seed 4, 32 of 64 questions "
                    "live, 1 new token each")
+PREFILL3_WORKLOAD = ("qwen3_8b_prefill: 32 questions, lengths clip(rint(exp(N(ln 512, 0.8))), 1, 4096) seed 3 "
+                     "(T=24100), H_q 32, H_kv 8, d 128, bf16, prefill attention alone")
 FLUSH_BYTES = 512 << 20   # > 2 x L2 (129 MB)
 
 
@@ -191,6 +193,37 @@ def cpu_baseline(heads=(0, 1, 2, 3)):
     return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
             "sample": f"oracle dense-mask fp64 prefill of q-heads {heads[0]}-{heads[-1]} (of 28, kv-head 0) "
                       f"over the full 8-question packed batch (T=7921); {dt:.2f} s"}
+
+
+def cpu_fair_baseline():
+    """A labelled second CPU number (not the oracle): per-question fp32 attention with BLAS
+    matmuls over each question's own causal block, all q-heads of the packed batch."""
+    import numpy as np
+    if "w" not in _W_CACHE:
+        _W_CACHE["w"] = W.qwen25_7b_prefill()
+    w = _W_CACHE["w"]
+    G = w.h_q // w.h_kv
+    q = W.to_float64(w.q, "bf16").astype(np.float32)
+    k = W.to_float64(w.k, "bf16").astype(np.float32)
+    v = W.to_float64(w.v, "bf16").astype(np.float32)
+    scale = np.float32(1.0 / np.sqrt(w.d))
+    t0 = time.perf_counter()
+    for s0, e0 in w.intervals:
+        L = e0 - s0
+        tri = np.triu(np.ones((L, L), dtype=bool), 1)
+        for h in range(w.h_q):
+            g = h // G
+            sc = (q[s0:e0, h] @ k[s0:e0, g].T) * scale
+            sc[tri] = -np.inf
+            sc -= sc.max(axis=1, keepdims=True)
+            np.exp(sc, out=sc)
+            sc /= sc.sum(axis=1, keepdims=True)
+            _ = sc @ v[s0:e0, g]
+    dt = time.perf_counter() - t0
+    flops = RL.prefill_useful_flops(w.lengths, w.h_q, w.d)
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "fair (not the oracle)",
+            "sample": f"per-question fp32 numpy/BLAS causal attention, all 28 q-heads of the 8-question batch "
+                      f"(T=7921), useful flops only; {dt:.2f} s"}
 
 
 def run_reference(args):
@@ -422,9 +455,37 @@ def main(argv=None):
     dec_job_gbs = aggregate_rate(dec_bytes, 1, world, max_over_ranks(dec_ms, world, dev)) / 1e9
     dec_traffic = _traffic("decode")
 
-    cpu = None
+    # ---- second prefill workload (Qwen3-8B-shaped batch): measured, not the headline ---------
+    w3 = W.qwen3_8b_prefill()
+    shape3 = kev.make_shape(w3.h_q, w3.h_kv, w3.d, "bf16")
+    q3, k3, v3, iv3 = tdev(w3.q), tdev(w3.k), tdev(w3.v), tdev(w3.intervals)
+    out3 = torch.empty((w3.total_tokens, w3.h_q, w3.d), dtype=torch.bfloat16, device=dev)
+    ws3_bytes = kev.kev_prefill_workspace_size(w3.n_questions, w3.total_tokens, shape3)
+    ws3 = torch.empty(ws3_bytes, dtype=torch.uint8, device=dev)
+    st3 = torch.zeros(1, dtype=torch.int32, device=dev)
+    kev.kev_build_segments(iv3, w3.n_questions, w3.total_tokens, None, 0, 0, shape3, ws3, ws3_bytes, st3)
+    p3_ms = []
+    for it in range(args.warmup + max(5, K // 2)):
+        flush()
+        a3 = torch.cuda.Event(enable_timing=True)
+        b3 = torch.cuda.Event(enable_timing=True)
+        a3.record()
+        kev.kev_prefill_from_segments(q3, k3, v3, w3.total_tokens, iv3, w3.n_questions, None, None, None, 0, 0, out3,
+                                      shape3, ws3, ws3_bytes, st3)
+        b3.record()
+        if it >= args.warmup:
+            p3_ms.append((a3, b3))
+    torch.cuda.synchronize()
+    assert kev.kev_read_status(st3) == 0
+    p3_avg = statistics.mean(a.elapsed_time(b) for a, b in p3_ms)
+    useful3 = RL.prefill_useful_flops(w3.lengths, w3.h_q, w3.d)
+    p3_tf = useful3 / (p3_avg * 1e-3) / 1e12
+    del q3, k3, v3, out3, ws3
+
+    cpu = cpu_fair = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline()
+        cpu_fair = cpu_fair_baseline()
 
     if rank == 0:
         clocks = clk.summary()
@@ -447,7 +508,11 @@ def main(argv=None):
                        "roofline": {"bound": "hbm", "achieved": dec_gbs, "peak": hbm_peak, "unit": "GB/s",
                                     "frac": dec_gbs / hbm_peak, "traffic": dec_traffic,
                                     "algorithmic_bytes": dec_bytes, "peak_source": f"hbm_gbs, {peak_src}"}},
+            "prefill_qwen3_8b": {"workload": PREFILL3_WORKLOAD, "value": p3_tf, "unit": "TFLOP/s",
+                                 "ms_per_launch": p3_avg, "useful_gflop": useful3 / 1e9,
+                                 "frac": p3_tf / tf_peak, "peak_source": f"bf16_tflops burst, {peak_src}"},
             "cpu_baseline": cpu,
+            "cpu_fair_baseline": cpu_fair,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
