@@ -258,6 +258,84 @@ def run_reference(args):
 # GPU arm
 # ---------------------------------------------------------------------------------------
 
+def _stress_decode_graph(kev, torch, dev, tdev):
+    """The stress batch: prefill into the slot pools, then its 128-step decode loop with early
+    stop (decode + lens advance per step, each step with its own live set and inputs) captured
+    once as a CUDA graph and replayed.  L2 is not flushed between the steps of a replay."""
+    import numpy as np
+    s = W.stress()
+    w = s.prefill
+    shape = kev.make_shape(w.h_q, w.h_kv, w.d, "bf16")
+    N = w.n_questions
+    q, k, v, iv, sl = tdev(w.q), tdev(w.k), tdev(w.v), tdev(w.intervals), tdev(w.slot_ids)
+    pk = torch.zeros((w.n_slots, w.h_kv, w.cap, w.d), dtype=torch.bfloat16, device=dev)
+    pv = torch.zeros_like(pk)
+    out = torch.empty((w.total_tokens, w.h_q, w.d), dtype=torch.bfloat16, device=dev)
+    pws_bytes = kev.kev_prefill_workspace_size(N, w.total_tokens, shape)
+    pws = torch.empty(pws_bytes, dtype=torch.uint8, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    pre_ms = []
+    for it in range(4):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        kev.kev_prefill_attn(q, k, v, w.total_tokens, iv, N, sl, pk, pv, w.n_slots, w.cap, out, shape, pws, pws_bytes, st)
+        b.record()
+        pre_ms.append((a, b))
+    torch.cuda.synchronize()
+    assert kev.kev_read_status(st) == 0
+    pre_avg = statistics.mean(a.elapsed_time(b) for a, b in pre_ms[1:])
+    steps = s.n_steps
+    act = tdev(np.stack([s.active_at(t) for t in range(steps)]))
+    ins = [s.step_inputs(t) for t in range(steps)]
+    qn = tdev(np.stack([x[0] for x in ins]))
+    kn = tdev(np.stack([x[1] for x in ins]))
+    vn = tdev(np.stack([x[2] for x in ins]))
+    del ins
+    lens0 = tdev(s.lens_at(0))
+    lens = lens0.clone()
+    dout = torch.empty((N, w.h_q, w.d), dtype=torch.bfloat16, device=dev)
+    dws_bytes = kev.kev_decode_workspace_size(N, w.cap, shape)
+    dws = torch.zeros(dws_bytes, dtype=torch.uint8, device=dev)
+    pk0, pv0 = pk.clone(), pv.clone()
+
+    def loop():
+        for t in range(steps):
+            kev.kev_decode_attn(qn[t], kn[t], vn[t], pk, pv, w.n_slots, w.cap, sl, lens, act[t], N, dout, shape, dws,
+                                dws_bytes, st)
+            kev.kev_decode_advance(lens, act[t], N)
+
+    loop()  # eager pass: first-call work happens outside the capture
+    torch.cuda.synchronize()
+    assert kev.kev_read_status(st) == 0
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        loop()
+    reps = []
+    for _ in range(3):
+        pk.copy_(pk0)
+        pv.copy_(pv0)
+        lens.copy_(lens0)
+        torch.cuda.synchronize()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        g.replay()
+        b.record()
+        torch.cuda.synchronize()
+        reps.append(a.elapsed_time(b))
+    assert kev.kev_read_status(st) == 0
+    total_bytes = sum(RL.decode_bytes(s.lens_at(t), s.active_at(t), w.h_q, w.h_kv, w.d, 2) for t in range(steps))
+    ms = statistics.mean(reps)
+    useful = RL.prefill_useful_flops(w.lengths, w.h_q, w.d)
+    return {"workload": "stress: 256 questions (T=19483), H_q 32, H_kv 8, d 128, bf16, cap 4224; prefill with slot "
+                        "write, then 128 decode steps with early stop (116 with live questions)",
+            "prefill_tflops": useful / (pre_avg * 1e-3) / 1e12, "prefill_ms": pre_avg,
+            "decode_graph_ms": ms, "decode_steps": steps, "decode_bytes": total_bytes,
+            "decode_gbs": total_bytes / (ms * 1e-3) / 1e9, "launches_per_step": kev.kev_launch_count(4) + 1,
+            "l2": "not flushed between the steps of a graph replay (L2 may hold part of the working set)"}
+
+
 def _decode_only(args, kev, torch, dev, tdev, flush):
     """Warm-up and timed loop of the decode workload alone (profiling aid)."""
     dwl = W.qwen3_8b_decode()
@@ -482,6 +560,8 @@ def main(argv=None):
     p3_tf = useful3 / (p3_avg * 1e-3) / 1e12
     del q3, k3, v3, out3, ws3
 
+    stress = _stress_decode_graph(kev, torch, dev, tdev)
+
     cpu = cpu_fair = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline()
@@ -511,6 +591,7 @@ def main(argv=None):
             "prefill_qwen3_8b": {"workload": PREFILL3_WORKLOAD, "value": p3_tf, "unit": "TFLOP/s",
                                  "ms_per_launch": p3_avg, "useful_gflop": useful3 / 1e9,
                                  "frac": p3_tf / tf_peak, "peak_source": f"bf16_tflops burst, {peak_src}"},
+            "stress": stress,
             "cpu_baseline": cpu,
             "cpu_fair_baseline": cpu_fair,
         }
