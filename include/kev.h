@@ -107,10 +107,13 @@ kev_status kev_build_segments(const kev_interval* intervals, int32_t n_questions
                               int32_t* dev_status, kev_stream_t stream);
 
 /* Host copy of the work list built by kev_build_segments (synchronises `stream`).
- * Each item is {question, q_row_begin, q_rows, first_head | (n_heads << 16)}: n_heads
- * consecutive q-heads of one kv group (2 for bf16, whose kernel runs two query tiles that
- * share every K/V tile; 1 for fp32).  Returns the item count, or -1 on error.  Writes at
- * most `max_items` items to `items_out` (host int32[4*max_items]). */
+ * Each item is {question, q_row_begin, q_rows, first_head | (n_heads << 16) | (two_tiles << 30)}:
+ * without two_tiles, n_heads consecutive q-heads of one kv group over one query tile (2 for
+ * bf16, whose kernel runs two query tiles that share every K/V tile; 1 for fp32); with
+ * two_tiles (bf16, when a group of an odd size leaves one q-head over), that q-head's query
+ * tiles starting at q_row_begin and q_row_begin + 128, q_rows being the second tile's rows.
+ * Items come longest first.  Returns the item count, or -1 on error.  Writes at most
+ * `max_items` items to `items_out` (host int32[4*max_items]). */
 int32_t kev_read_work_list(const void* workspace, size_t workspace_bytes, int32_t* items_out,
                            int32_t max_items, kev_stream_t stream);
 

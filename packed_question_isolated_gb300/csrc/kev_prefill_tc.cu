@@ -115,18 +115,43 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const 
 }
 
 struct Item {
-  int q, row0, rows, h0, nh, seg_begin, nkv;
+  int q, seg_begin;
+  int h0;    // q-head of tile A (the kv group is h0 / group)
+  int nh;    // query tiles in the item (1 or 2)
+  int nkv;   // key tiles the item loads (the larger of its tiles' counts)
+  bool two;  // tiles A and B are consecutive query tiles of one q-head (else: one tile, heads h0, h0+1)
+  int row0a, rowsa, nkva;  // tile A: first row, rows, key tiles
+  int row0b, rowsb, nkvb;  // tile B
+  __device__ int row0_of(int t) const { return t ? row0b : row0a; }
+  __device__ int rows_of(int t) const { return t ? rowsb : rowsa; }
+  __device__ int head_of(int t) const { return two ? h0 : h0 + t; }
+  __device__ int nkv_of(int t) const { return t ? nkvb : nkva; }
 };
+// Work item {question, row_begin, rows, first_head | n_heads << 16 | two_tiles << 30}; with
+// two_tiles, the item is query tiles (row_begin, row_begin + 128) of one q-head, and `rows` is the
+// second tile's row count.
 __device__ __forceinline__ Item load_item(const int4* items, const kev_interval* iv, int it) {
   const int4 w = items[it];
   Item x;
   x.q = w.x;
-  x.row0 = w.y;
-  x.rows = w.z;
-  x.h0 = w.w & 0xffff;
-  x.nh = w.w >> 16;
   x.seg_begin = iv[w.x].begin;
-  x.nkv = (w.y - x.seg_begin) / kBM + 1;
+  x.h0 = w.w & 0xffff;
+  x.two = (w.w >> 30) & 1;
+  x.row0a = w.y;
+  x.nkva = (w.y - x.seg_begin) / kBM + 1;
+  if (x.two) {
+    x.nh = 2;
+    x.rowsa = kBM;
+    x.row0b = w.y + kBM;
+    x.rowsb = w.z;
+    x.nkvb = x.nkva + 1;
+  } else {
+    x.nh = (w.w >> 16) & 0x3fff;
+    x.rowsa = x.rowsb = w.z;
+    x.row0b = w.y;
+    x.nkvb = x.nkva;
+  }
+  x.nkv = x.nkvb;
   return x;
 }
 
@@ -247,15 +272,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive_expect_tx(&bars->q_full, x.nh * L::kTileBytes);
         for (int t = 0; t < x.nh; ++t)
           for (int c = 0; c < L::kSub; ++c)
-            tma_load_2d(smem + L::kQ + t * L::kTileBytes + c * L::kSubBytes, &tm_q, (x.h0 + t) * D + c * 64, x.row0,
-                        &bars->q_full);
+            tma_load_2d(smem + L::kQ + t * L::kTileBytes + c * L::kSubBytes, &tm_q, x.head_of(t) * D + c * 64,
+                        x.row0_of(t), &bars->q_full);
         ++q_loads;
         // pull the next item's query tiles into L2 while this item runs: their load into
         // shared memory starts only when this item's last S MMA has read the Q buffer
         if (it_next < n_items) {
           const Item& nx = x_next;
           for (int t = 0; t < nx.nh; ++t)
-            for (int c = 0; c < L::kSub; ++c) tma_prefetch_l2_2d(&tm_q, (nx.h0 + t) * D + c * 64, nx.row0);
+            for (int c = 0; c < L::kSub; ++c) tma_prefetch_l2_2d(&tm_q, nx.head_of(t) * D + c * 64, nx.row0_of(t));
         }
       }
       if (!ok) raise_timeout(p, bars);
@@ -325,6 +350,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int it_next = snake_item(rnd + 1, blockIdx.x, gridDim.x);
       if (it_next < n_items) x_next = load_item(items, p.intervals, it_next);
       const bool mine = t < x.nh;
+      // this tile's key tiles (an absent tile runs the item's steps, releasing stages only)
+      const int nkv_t = mine ? x.nkv_of(t) : x.nkv;
       {
         const uint32_t qk = 2 * kv_iter;
         wait_ok(&bars->q_full, n & 1);
@@ -334,7 +361,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           if (mine) issue_s(slot(qk));
           umma_commit(&bars->r_empty[slot(qk)]);
-          if (x.nkv == 1) umma_commit(&bars->q_empty);
+          if (nkv_t == 1) umma_commit(&bars->q_empty);
         }
         pass_turn();
       }
@@ -342,10 +369,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t ki = kv_iter + j;
         const uint32_t qv = 2 * ki + 1, qk = 2 * ki + 2;  // V(ki), K(ki + 1)
         const int vs = slot(qv), kn = slot(qk);
-        const bool has_next = j + 1 < x.nkv;
+        const bool has_next = j + 1 < x.nkv;     // the item loads K(ki + 1)
+        const bool act = mine && j < nkv_t;      // this tile uses key tile j
+        const bool next_s = act && j + 1 < nkv_t;
         wait_ok(&bars->r_full[vs], phase(qv));
         if (has_next) wait_ok(&bars->r_full[kn], phase(qk));
-        if (mine) {
+        if (act) {
           wait_ok(&bars->p_full[t], p_cnt & 1);
           if (j == 0 && items_done > 0) wait_ok(&bars->o_free[t], (items_done - 1) & 1);
           ++p_cnt;
@@ -353,18 +382,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         take_turn();
         if (ok && leader) {
           tc_fence_after();
-          if (mine) {
+          if (act) {
             issue_pv(vs, j > 0);
             umma_commit(&bars->r_empty[vs]);  // this issuer's use of the V tile ends with the PV
-            if (has_next) issue_s(kn);        // overwrites S_t / P_t after the PV above read it (in order)
+            if (next_s) issue_s(kn);          // overwrites S_t / P_t after the PV above read it (in order)
             else umma_commit(&bars->o_done[t]);
           } else {
             umma_commit(&bars->r_empty[vs]);
           }
-          if (has_next) {
-            umma_commit(&bars->r_empty[kn]);
-            if (j + 1 == x.nkv - 1) umma_commit(&bars->q_empty);  // last use of the Q tiles issued
-          }
+          if (has_next) umma_commit(&bars->r_empty[kn]);
+          if (j + 1 == nkv_t - 1) umma_commit(&bars->q_empty);  // this tile's last S is issued
         }
         pass_turn();
       }
@@ -402,12 +429,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       const Item x = x_next;  // loaded one item ahead: its latency hides behind this item
       const int it_next = snake_item(rnd + 1, blockIdx.x, gridDim.x);
       if (it_next < n_items) x_next = load_item(items, p.intervals, it_next);
-      const uint32_t my_use = stg_uses + (uint32_t)t;
-      if (x.rows == kBM) stg_uses += (uint32_t)x.nh;
+      const bool full_a = x.rows_of(0) == kBM, full_b = x.nh == 2 && x.rows_of(1) == kBM;
+      const uint32_t my_use = stg_uses + ((t == 1 && full_a) ? 1u : 0u);  // tile A's use comes first
+      stg_uses += (full_a ? 1u : 0u) + (full_b ? 1u : 0u);
       if (t >= x.nh) continue;
+      const int nkv = x.nkv_of(t), rows_t = x.rows_of(t), row0_t = x.row0_of(t), head_t = x.head_of(t);
       float m_run = -INFINITY, l_run = 0.f;
 
-      for (int j = 0; j < x.nkv; ++j) {
+      for (int j = 0; j < nkv; ++j) {
         if (!warp_wait(&bars->s_full[t], s_cnt & 1, abort_flag, budget)) {
           ok = false;
           break;
@@ -420,7 +449,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < 4; ++c) tmem_ld32(tm_s + c * 32, sr[c]);
 #pragma unroll
         for (int c = 0; c < 4; ++c) tmem_ld_wait(sr[c]);
-        if (j == x.nkv - 1) {  // diagonal tile: key k is visible to row r iff k <= r
+        if (j == nkv - 1) {  // diagonal tile: key k is visible to row r iff k <= r
 #pragma unroll
           for (int c = 0; c < 4; ++c)
 #pragma unroll
@@ -516,7 +545,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int c = 0; c < D / 32; ++c) tmem_ld_wait(o[c]);
       tc_fence_before();
       mbar_arrive_warp(&bars->o_free[t]);  // O_t is in registers: the next item's PV may start
-      if (x.rows == kBM) {
+      if (rows_t == kBM) {
         // A whole tile: each warp writes its 32 rows as bf16 into its slice of the output stage
         // (the 128-byte swizzled box layout) and one lane stores the slice with two bulk tensor
         // copies of 32 rows; the warp waits only for the copy engine to have read its 8 KB.
@@ -547,16 +576,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) {
           for (int c = 0; c < L::kSub; ++c)
-            tma_store_2d(&tm_out, stg + c * L::kSubBytes + q * 32 * 128, (x.h0 + t) * D + c * 64, x.row0 + q * 32);
+            tma_store_2d(&tm_out, stg + c * L::kSubBytes + q * 32 * 128, head_t * D + c * 64, row0_t + q * 32);
           bulk_commit_group();
           bulk_wait_read_all();
           mbar_arrive(&bars->stg_free[q]);
         }
         __syncwarp();
-      } else if (r < x.rows) {
+      } else if (r < rows_t) {
         // the question's last, partial tile: row by row (a whole box would overwrite the
         // next question's rows)
-        __nv_bfloat16* orow = out + ((int64_t)(x.row0 + r) * p.h_q + x.h0 + t) * D;
+        __nv_bfloat16* orow = out + ((int64_t)(row0_t + r) * p.h_q + head_t) * D;
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t w[16];

@@ -207,7 +207,6 @@ __global__ void __launch_bounds__(kThreads) segments_kernel(SegmentsArgs a) {
       acc += bin_count[b];
     }
     hdr->n_tiles = acc;
-    hdr->n_items = acc * (a.h_q / a.group) * ((a.group + a.heads_per_item - 1) / a.heads_per_item);
   }
   __syncthreads();
   for (int i = tid; i < n; i += blockDim.x) {
@@ -222,23 +221,51 @@ __global__ void __launch_bounds__(kThreads) segments_kernel(SegmentsArgs a) {
 
   // 7. expand tiles into (tile, head block) items: a block is heads_per_item consecutive
   //    q-heads of one kv group (they share every K/V tile); the blocks of one tile stay
-  //    adjacent so the q-heads that share a kv-head run close together (L2 reuse).
+  //    adjacent so the q-heads that share a kv-head run close together (L2 reuse).  When the
+  //    group leaves a single q-head over (odd group, two heads per item), that head's query
+  //    tiles m-1 and m of a question form one item instead (m odd; bit 30 of the last word,
+  //    `rows` = rows of tile m): the two tiles share the K/V tiles of tile m-1.  A question's
+  //    last tile of an odd count keeps a single-head item.
   const int n_tiles = hdr->n_tiles;
   const int per_group = (a.group + a.heads_per_item - 1) / a.heads_per_item;
-  const int per_tile = (a.h_q / a.group) * per_group;
-  const long long n_items = (long long)n_tiles * per_tile;
-  for (long long k = tid; k < n_items; k += blockDim.x) {
-    const int t = (int)(k / per_tile);
-    const int r = (int)(k % per_tile);
-    const int g = r / per_group, b = r % per_group;
-    const int h0 = g * a.group + b * a.heads_per_item;
-    const int nh = min(a.heads_per_item, a.group - b * a.heads_per_item);
-    const int2 tl = tiles[t];
+  const int h_kv = a.h_q / a.group;
+  const bool odd_single = a.heads_per_item == 2 && (a.group & 1);
+  // items of the tile at longest-first position `pos`
+  auto tile_items = [&](int pos, int2& tl, int& nt) {
+    tl = tiles[pos];
     const kev_interval iv = a.intervals[tl.x];
-    const int r0 = iv.begin + tl.y * kTileM;
-    const int rows = min(kTileM, iv.end - r0);
-    items[k] = make_int4(tl.x, r0, rows, h0 | (nh << 16));
+    nt = (iv.end - iv.begin + kTileM - 1) / kTileM;
+    int cnt = h_kv * per_group;
+    if (odd_single && (tl.y & 1) == 0 && tl.y + 1 < nt) cnt -= h_kv;  // covered by the pair at m+1
+    return cnt;
+  };
+  long long running = 0;
+  for (int base = 0; base < n_tiles; base += blockDim.x) {
+    const int pos = base + tid;
+    int2 tl = make_int2(0, 0);
+    int nt = 0;
+    const int cnt = pos < n_tiles ? tile_items(pos, tl, nt) : 0;
+    int blk_total;
+    const int off = block_exclusive_scan(cnt, scan_tmp, &blk_total);
+    if (pos < n_tiles) {
+      const kev_interval iv = a.intervals[tl.x];
+      const int r0 = iv.begin + tl.y * kTileM;
+      const int rows = min(kTileM, iv.end - r0);
+      long long k = running + off;
+      for (int g = 0; g < h_kv; ++g)
+        for (int b = 0; b < per_group; ++b) {
+          const int h0 = g * a.group + b * a.heads_per_item;
+          const int nh = min(a.heads_per_item, a.group - b * a.heads_per_item);
+          if (odd_single && nh == 1 && tl.y + 1 < nt && (tl.y & 1) == 0) continue;
+          if (odd_single && nh == 1 && (tl.y & 1) == 1)
+            items[k++] = make_int4(tl.x, r0 - kTileM, rows, h0 | (1 << 16) | (1 << 30));  // tiles m-1, m
+          else
+            items[k++] = make_int4(tl.x, r0, rows, h0 | (nh << 16));
+        }
+    }
+    running += blk_total;
   }
+  if (tid == 0) hdr->n_items = (int)running;
   if (tid == 0) {
     hdr->status = ST_OK;
     hdr->n_gaps = s_ngaps;

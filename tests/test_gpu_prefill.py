@@ -124,9 +124,11 @@ def test_deterministic_and_isolated_bitwise():
         assert np.array_equal(host(b.out)[5:5 + e - s], first[s:e]), f"question {i} not bitwise isolated"
 
 
-def test_work_list_covers_exactly_the_allowed_tiles():
+@pytest.mark.parametrize("h_q,h_kv", [(4, 2), (7, 1), (14, 2)])
+def test_work_list_covers_exactly_the_allowed_tiles(h_q, h_kv):
     import packed_question_isolated_gb300 as kev
-    w = W.random_case(99, [300, 1, 0, 129, 128, 257], 4, 2, 64, "bf16", gaps=[0, 2, 1, 0, 3, 1], tail=5)
+    w = W.random_case(99, [300, 1, 0, 129, 128, 257, 640], h_q, h_kv, 64, "bf16", gaps=[0, 2, 1, 0, 3, 1, 0],
+                      tail=5)
     run = PrefillRun(w)
     run.run()
     items, n = kev.kev_read_work_list(run.ws, run.ws_bytes, 100000)
@@ -136,21 +138,35 @@ def test_work_list_covers_exactly_the_allowed_tiles():
     covered = np.zeros((w.h_q, T, T), dtype=np.int32)
     costs = []
     G = w.h_q // w.h_kv
+    n_two = 0
     for (qi, r0, rows, hw) in items:
-        h0, nh = hw & 0xffff, hw >> 16
-        assert 1 <= nh <= 2 and h0 // G == (h0 + nh - 1) // G, "an item's heads share one kv head"
+        h0, nh, two = hw & 0xffff, (hw >> 16) & 0x3fff, (hw >> 30) & 1
         s, e = w.intervals[qi]
-        assert s <= r0 and r0 + rows <= e and 0 < rows <= 128 and (r0 - s) % 128 == 0
-        # key range of the item: [s, r0 + rows)
-        blk = allowed[r0:r0 + rows, s:r0 + rows]
-        assert blk.any(), "an item with no allowed entry was scheduled"
-        for h in range(h0, h0 + nh):
-            covered[h, r0:r0 + rows, s:r0 + rows] += 1
-        costs.append((r0 - s) // 128 + 1)
+        if two:
+            # one q-head, query tiles starting at r0 (whole) and r0 + 128 (`rows` rows)
+            n_two += 1
+            assert nh == 1 and G % 2 == 1 and h0 % G == G - 1, "only the odd head left over in a group"
+            assert (r0 - s) % 256 == 0 and r0 + 128 + rows <= e and 0 < rows <= 128
+            tiles = [(r0, 128), (r0 + 128, rows)]
+            heads = [h0]
+        else:
+            assert 1 <= nh <= 2 and h0 // G == (h0 + nh - 1) // G, "an item's heads share one kv head"
+            assert s <= r0 and r0 + rows <= e and 0 < rows <= 128 and (r0 - s) % 128 == 0
+            tiles = [(r0, rows)]
+            heads = list(range(h0, h0 + nh))
+        for (t0, tr) in tiles:
+            # key range of the tile: [s, t0 + tr)
+            assert allowed[t0:t0 + tr, s:t0 + tr].any(), "an item with no allowed entry was scheduled"
+            for h in heads:
+                covered[h, t0:t0 + tr, s:t0 + tr] += 1
+        last = tiles[-1][0]
+        costs.append((last - s) // 128 + 1)
     for h in range(w.h_q):
         assert (covered[h][allowed] == 1).all(), "allowed entry not covered exactly once"
         assert (covered[h] <= 1).all()
     assert costs == sorted(costs, reverse=True), "items are not ordered longest first"
+    if G % 2 == 1 and G > 1:
+        assert n_two > 0
 
 
 def test_scores_growing_past_the_reference_max():
