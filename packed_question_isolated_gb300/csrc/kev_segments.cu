@@ -6,13 +6,16 @@
 // lower triangle of its own diagonal block).  This is the varlen "cu_seqlens" form the
 // article moves to for long inputs (§5.2, §6.4), extended to a tile work list.
 //
-// One CTA of 1024 threads; at most kMaxQuestions questions.
+// One CTA of 512 threads; at most kMaxQuestions questions.
 #include "kev_internal.cuh"
 
 namespace kev {
 namespace {
 
-constexpr int kThreads = 1024;
+constexpr int kThreads = 512;
+// Up to this many questions the checks run as one pass of all pairs per thread out of shared
+// memory (no sort, no barrier per sorting stage); larger batches use bitonic sorts.
+constexpr int kSmall = 1024;
 
 // In-place ascending bitonic sort of `n2` (power of two) keys in shared memory.
 __device__ void bitonic_sort(unsigned long long* key, int n2) {
@@ -69,6 +72,9 @@ __global__ void __launch_bounds__(kThreads) segments_kernel(SegmentsArgs a) {
   __shared__ int bin_count[kCostBins];
   __shared__ int bin_cursor[kCostBins];
   __shared__ int s_ngaps;
+  __shared__ int s_ntiles;
+  __shared__ int2 s_iv[kSmall];  // small batches: intervals and slot ids in shared memory
+  __shared__ int s_slot[kSmall];
 
   PrefillHeader* hdr = reinterpret_cast<PrefillHeader*>(a.ws);
   int32_t* cu = reinterpret_cast<int32_t*>(a.ws + a.layout.cu_seqlens);
@@ -84,70 +90,116 @@ __global__ void __launch_bounds__(kThreads) segments_kernel(SegmentsArgs a) {
   if (tid < kCostBins) bin_count[tid] = 0;
   __syncthreads();
 
-  // 1. per-question range checks
+  int n2 = 1;
+  while (n2 < n) n2 <<= 1;
+  const bool small = n <= kSmall;
+
+  // 1. per-question range checks (and, for a small batch, a shared-memory copy of the inputs)
   for (int i = tid; i < n; i += blockDim.x) {
     const kev_interval iv = a.intervals[i];
     if (!(iv.begin >= 0 && iv.begin <= iv.end && iv.end <= a.T)) atomicOr(&s_flags, 1);
+    int s = -1;
     if (a.slot_ids) {
-      const int s = a.slot_ids[i];
+      s = a.slot_ids[i];
       if (s < 0 || s >= a.n_slots) atomicOr(&s_flags, 2);
       if (iv.end - iv.begin > a.cap) atomicOr(&s_flags, 4);
     }
+    if (small) {
+      s_iv[i] = make_int2(iv.begin, iv.end);
+      s_slot[i] = s;
+    }
   }
   __syncthreads();
 
-  int n2 = 1;
-  while (n2 < n) n2 <<= 1;
-
-  // 2. overlap: sort non-empty intervals by begin, neighbours must not intersect
-  if ((s_flags & 1) == 0 && n > 1) {
-    for (int i = tid; i < n2; i += blockDim.x) {
-      unsigned long long kk = ~0ull;
-      if (i < n) {
-        const kev_interval iv = a.intervals[i];
-        if (iv.end > iv.begin) kk = ((unsigned long long)(unsigned)iv.begin << 32) | (unsigned)iv.end;
+  if (small) {
+    // 2-4 for a small batch: every non-empty interval against every other one (overlap, and a
+    // slot shared by two non-empty questions), and its rank by (begin, index) places it in
+    // `keys`, begin-sorted; empty intervals sort last
+    const bool ranges_ok = (s_flags & 1) == 0;
+    for (int i = tid; i < n; i += blockDim.x) {
+      const int2 me = s_iv[i];
+      if (me.y <= me.x) continue;
+      int rank = 0;
+      bool overlap = false, dup = false;
+      for (int j = 0; j < n; ++j) {
+        const int2 o = s_iv[j];
+        if (j == i || o.y <= o.x) continue;
+        overlap |= (me.x < o.y) && (o.x < me.y);
+        dup |= a.slot_ids != nullptr && s_slot[j] == s_slot[i];
+        rank += (o.x < me.x) || (o.x == me.x && j < i);
       }
-      keys[i] = kk;
+      if (overlap) atomicOr(&s_flags, 1);
+      if (dup) atomicOr(&s_flags, 8);
+      if (ranges_ok) keys[rank] = ((unsigned long long)(unsigned)me.x << 32) | (unsigned)me.y;
     }
     __syncthreads();
-    bitonic_sort(keys, n2);
-    for (int i = tid + 1; i < n; i += blockDim.x) {
-      const unsigned long long cur = keys[i], prev = keys[i - 1];
-      if (cur != ~0ull && prev != ~0ull) {
-        if ((unsigned)(cur >> 32) < (unsigned)(prev & 0xffffffffu)) atomicOr(&s_flags, 1);
-      }
+    // the ranks of the non-empty intervals fill keys[0, n_ne); the rest marks the end
+    if (ranges_ok) {
+      int ne = 0;
+      for (int i = tid; i < n; i += blockDim.x) ne += s_iv[i].y > s_iv[i].x;
+      int n_ne;
+      block_exclusive_scan(ne, scan_tmp, &n_ne);
+      for (int i = n_ne + tid; i < n2; i += blockDim.x) keys[i] = ~0ull;
+      __syncthreads();
     }
-    __syncthreads();
   } else {
-    for (int i = tid; i < n2; i += blockDim.x) {
-      unsigned long long kk = ~0ull;
-      if (i < n) {
-        const kev_interval iv = a.intervals[i];
-        if (iv.end > iv.begin) kk = ((unsigned long long)(unsigned)iv.begin << 32) | (unsigned)iv.end;
+    // 2. overlap: sort non-empty intervals by begin, neighbours must not intersect
+    if ((s_flags & 1) == 0 && n > 1) {
+      for (int i = tid; i < n2; i += blockDim.x) {
+        unsigned long long kk = ~0ull;
+        if (i < n) {
+          const kev_interval iv = a.intervals[i];
+          if (iv.end > iv.begin) kk = ((unsigned long long)(unsigned)iv.begin << 32) | (unsigned)iv.end;
+        }
+        keys[i] = kk;
       }
-      keys[i] = kk;
+      __syncthreads();
+      bitonic_sort(keys, n2);
+      for (int i = tid + 1; i < n; i += blockDim.x) {
+        const unsigned long long cur = keys[i], prev = keys[i - 1];
+        if (cur != ~0ull && prev != ~0ull) {
+          if ((unsigned)(cur >> 32) < (unsigned)(prev & 0xffffffffu)) atomicOr(&s_flags, 1);
+        }
+      }
+      __syncthreads();
+    } else {
+      for (int i = tid; i < n2; i += blockDim.x) {
+        unsigned long long kk = ~0ull;
+        if (i < n) {
+          const kev_interval iv = a.intervals[i];
+          if (iv.end > iv.begin) kk = ((unsigned long long)(unsigned)iv.begin << 32) | (unsigned)iv.end;
+        }
+        keys[i] = kk;
+      }
+      __syncthreads();
     }
-    __syncthreads();
   }
 
-  // 3. gaps: tokens in no interval, from the begin-sorted intervals
-  if ((s_flags & 1) == 0 && tid == 0) {
-    int ng = 0;
-    int pos = 0;
-    for (int i = 0; i < n; ++i) {
-      const unsigned long long kk = keys[i];
-      if (kk == ~0ull) break;
-      const int b = (int)(kk >> 32), e = (int)(kk & 0xffffffffu);
-      if (b > pos) gaps[ng++] = make_int2(pos, b);
-      pos = e;
+  // 3. gaps: tokens in no interval, from the begin-sorted intervals; gap k lies before the
+  //    k-th non-empty interval (k = n_ne: after the last one), placed with a scan
+  if ((s_flags & 1) == 0) {
+    int ng_total = 0;
+    for (int base = 0; base <= n; base += blockDim.x) {
+      const int k = base + tid;
+      int g0 = 0, g1 = 0;
+      bool has = false;
+      if (k <= n && (k == 0 || keys[k - 1] != ~0ull)) {  // k ranges over [0, n_ne]
+        const bool at_end = k == n || keys[k] == ~0ull;
+        g0 = k == 0 ? 0 : (int)(keys[k - 1] & 0xffffffffu);
+        g1 = at_end ? a.T : (int)(keys[k] >> 32);
+        has = g1 > g0;
+      }
+      int blk_total;
+      const int off = block_exclusive_scan(has ? 1 : 0, scan_tmp, &blk_total);
+      if (has) gaps[ng_total + off] = make_int2(g0, g1);
+      ng_total += blk_total;
     }
-    if (pos < a.T) gaps[ng++] = make_int2(pos, a.T);
-    s_ngaps = ng;
+    if (tid == 0) s_ngaps = ng_total;
   }
   __syncthreads();
 
-  // 4. duplicate slots among non-empty questions
-  if (a.slot_ids && s_flags == 0 && n > 1) {
+  // 4. duplicate slots among non-empty questions (small batches did it in the pair pass)
+  if (!small && a.slot_ids && s_flags == 0 && n > 1) {
     for (int i = tid; i < n2; i += blockDim.x) {
       unsigned long long kk = ~0ull;
       if (i < n) {
@@ -200,21 +252,34 @@ __global__ void __launch_bounds__(kThreads) segments_kernel(SegmentsArgs a) {
     for (int m = 0; m < nt; ++m) atomicAdd(&bin_count[m < kCostBins ? m : kCostBins - 1], 1);
   }
   __syncthreads();
-  if (tid == 0) {
-    int acc = 0;
-    for (int b = kCostBins - 1; b >= 0; --b) {
-      bin_cursor[b] = acc;
-      acc += bin_count[b];
+  static_assert(kCostBins == 64, "one warp places the 64 bins, two per lane");
+  if (tid < 32) {  // bins in descending order: bin b starts after every bin above it
+    const int hi = kCostBins - 1 - 2 * tid, lo = hi - 1;
+    const int c_hi = bin_count[hi], c_lo = bin_count[lo];
+    int x = c_hi + c_lo;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, o);
+      if (tid >= o) x += y;
     }
-    hdr->n_tiles = acc;
+    const int base = x - (c_hi + c_lo);
+    bin_cursor[hi] = base;
+    bin_cursor[lo] = base + c_hi;
+    if (tid == 31) {
+      hdr->n_tiles = x;
+      s_ntiles = x;
+    }
   }
   __syncthreads();
+  // the tile list stays in shared memory (the sort keys are dead) when it fits
+  const int n_tiles = s_ntiles;
+  int2* tl_list = n_tiles <= kMaxQuestions ? reinterpret_cast<int2*>(keys) : tiles;
   for (int i = tid; i < n; i += blockDim.x) {
     const int L = a.intervals[i].end - a.intervals[i].begin;
     const int nt = (L + kTileM - 1) / kTileM;
     for (int m = nt - 1; m >= 0; --m) {
       const int pos = atomicAdd(&bin_cursor[m < kCostBins ? m : kCostBins - 1], 1);
-      tiles[pos] = make_int2(i, m);
+      tl_list[pos] = make_int2(i, m);
     }
   }
   __syncthreads();
@@ -226,13 +291,12 @@ __global__ void __launch_bounds__(kThreads) segments_kernel(SegmentsArgs a) {
   //    tiles m-1 and m of a question form one item instead (m odd; bit 30 of the last word,
   //    `rows` = rows of tile m): the two tiles share the K/V tiles of tile m-1.  A question's
   //    last tile of an odd count keeps a single-head item.
-  const int n_tiles = hdr->n_tiles;
   const int per_group = (a.group + a.heads_per_item - 1) / a.heads_per_item;
   const int h_kv = a.h_q / a.group;
   const bool odd_single = a.heads_per_item == 2 && (a.group & 1);
   // items of the tile at longest-first position `pos`
   auto tile_items = [&](int pos, int2& tl, int& nt) {
-    tl = tiles[pos];
+    tl = tl_list[pos];
     const kev_interval iv = a.intervals[tl.x];
     nt = (iv.end - iv.begin + kTileM - 1) / kTileM;
     int cnt = h_kv * per_group;
