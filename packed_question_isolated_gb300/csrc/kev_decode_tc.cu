@@ -228,6 +228,36 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   int* sched = reinterpret_cast<int*>(a.ws + a.layout.sched);
 
+  // barriers, tensor maps and the TMEM columns depend on nothing the kernels before this one
+  // write: set them up while those finish
+  if (tid == 0) {
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&bars->full[s], 1);
+      mbar_init(&bars->empty[s], 1);
+    }
+    mbar_init(&bars->fixed, kQuad);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&bars->s_full[b], 1);
+      mbar_init(&bars->s_free[b], kQuad);
+      mbar_init(&bars->p_full[b], kQuad);
+      mbar_init(&bars->o_done[b], 1);
+      mbar_init(&bars->o_full[b], 1);
+      mbar_init(&bars->o_free[b], kQuad);
+      mbar_init(&bars->pc_full[b], kQuad);
+    }
+    mbar_init(&bars->drain_s, 1);
+    mbar_init(&bars->drain_p, 1);
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+    tma_prefetch_desc(&tm_q);
+  }
+  if (warp == 1) {
+    tmem_alloc(&bars->tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
   pdl_wait();  // lens, the pool and the counters are as the kernels before this one left them
   // the first batch grab goes out now; its latency hides behind the validation (the merge
   // kernel that follows resets the counter for the next call)
@@ -245,34 +275,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
       sched[1] = plan.x1;
       sched[3] = plan.n1;
       sched[4] = plan.B;
-    }
-    if (tid == 0) {
-      for (int s = 0; s < NS; ++s) {
-        mbar_init(&bars->full[s], 1);
-        mbar_init(&bars->empty[s], 1);
-      }
-      mbar_init(&bars->fixed, kQuad);
-      for (int b = 0; b < 2; ++b) {
-        mbar_init(&bars->s_full[b], 1);
-        mbar_init(&bars->s_free[b], kQuad);
-        mbar_init(&bars->p_full[b], kQuad);
-        mbar_init(&bars->o_done[b], 1);
-        mbar_init(&bars->o_full[b], 1);
-        mbar_init(&bars->o_free[b], kQuad);
-        mbar_init(&bars->pc_full[b], kQuad);
-      }
-      mbar_init(&bars->drain_s, 1);
-      mbar_init(&bars->drain_p, 1);
-      fence_mbar_init();
-    }
-    if (warp == 0 && lane == 0) {
-      tma_prefetch_desc(&tm_k);
-      tma_prefetch_desc(&tm_v);
-      tma_prefetch_desc(&tm_q);
-    }
-    if (warp == 1) {
-      tmem_alloc(&bars->tmem_base, kTmemCols);
-      tmem_relinquish();
     }
     tc_fence_before();
     __syncthreads();  // the hash is dead from here on: the stages may be written
@@ -651,6 +653,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
       tc_fence_after();
       tmem_dealloc(tmem, kTmemCols);
     }
+  } else if (warp == 1) {  // invalid call: nothing ran on the tensor cores
+    tc_fence_after();
+    tmem_dealloc(bars->tmem_base, kTmemCols);
   }
 
   // the merge kernel may be scheduled as soon as every CTA got here (it still waits for this
