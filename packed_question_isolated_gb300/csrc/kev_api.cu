@@ -176,9 +176,11 @@ kev_status kev_prefill_from_segments(const void* q, const void* k, const void* v
   x.h_q = shape->h_q;
   x.h_kv = shape->h_kv;
   x.cap = slot_cap;
+  x.n_slots = n_slots;
   x.row_bytes = shape->d_h * elem_size(shape);
   x.ws = static_cast<const char*>(workspace);
   x.layout = layout;
+  x.after_attention = total_tokens > 0;  // the attention kernel was launched just before
   return from_cuda(launch_aux(x, sms, s));
 }
 
@@ -230,9 +232,11 @@ kev_status kev_kv_write(const void* k, const void* v, int32_t total_tokens, cons
   x.h_q = shape->h_q;
   x.h_kv = shape->h_kv;
   x.cap = slot_cap;
+  x.n_slots = n_slots;
   x.row_bytes = shape->d_h * elem_size(shape);
   x.ws = static_cast<const char*>(workspace);
   x.layout = prefill_layout(n_questions, total_tokens, shape->h_q);
+  x.after_attention = false;
   return from_cuda(launch_aux(x, sms, (cudaStream_t)stream));
 }
 

@@ -162,9 +162,13 @@ struct AuxArgs {  // slot write + zero rows of tokens in no question
   int32_t h_q;
   int32_t h_kv;
   int32_t cap;
+  int32_t n_slots;
   int32_t row_bytes;  // d * element size
   const char* ws;
   PrefillLayout layout;
+  // launched right after an attention kernel that waited for the segment builder before letting
+  // this grid start: run alongside its tail, wait for it at the end
+  bool after_attention;
 };
 
 struct DecodeArgs {

@@ -8,52 +8,96 @@
 // Tokens outside every interval (boundary / padding tokens between questions) are keys for
 // nobody (the article's §4.1 PAD-leak fix) and their own output rows are written as 0.
 //
-// Grid-stride over 16-byte vectors; the item space is (question, kv head, row) for the
-// slot write and (gap, row) for the zero fill, enumerated from the segment builder's
-// cu_seqlens and gap list.
+// Work unit of the slot write: one (row, kv head) of K and of V, row_bytes each, in
+// cu_seqlens order (consecutive units are consecutive in the packed K/V).  A warp copies
+// 32 / (row_bytes / 16) units per pass with one 16-byte vector per lane, kUnroll passes with
+// all their loads in flight before the stores.  Each block keeps cu_seqlens, the interval
+// starts and the slot ids in shared memory, so a unit's question is a binary search there.
+//
+// After the attention kernel, this kernel overlaps the attention's tail: it reads nothing the
+// attention writes and writes nothing the attention reads (the pools; output rows of gap
+// tokens, which no query tile covers), so it waits for the attention grid only at its end,
+// which keeps the completion order of the stream (this grid completes after the attention).
+// The segment builder's results it reads are complete by then: the attention kernel lets it
+// launch only after every attention CTA has waited for the builder.
 #include "kev_internal.cuh"
 
 namespace kev {
 namespace {
 
-__global__ void __launch_bounds__(256) aux_kernel(AuxArgs a) {
-  pdl_wait();  // the work list and status of the kernels before this one are complete
+constexpr int kAuxThreads = 256;
+constexpr int kUnroll = 4;
+
+__device__ __forceinline__ int question_of(const int32_t* cu, int n, int r) {
+  int lo = 0, hi = n;  // cu[lo] <= r < cu[hi]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (cu[mid] <= r) lo = mid; else hi = mid;
+  }
+  return lo;
+}
+
+__global__ void __launch_bounds__(kAuxThreads) aux_kernel(AuxArgs a) {
+  extern __shared__ int32_t s_cu[];             // [n + 1]
+  int2* s_bs = reinterpret_cast<int2*>(s_cu + ((a.n + 2) & ~1));  // [n] {begin, slot}
+  __shared__ int s_ok;
+  if (!a.after_attention) pdl_wait();  // the segment builder's results are complete
   pdl_trigger();
   const PrefillHeader* hdr = reinterpret_cast<const PrefillHeader*>(a.ws);
-  if (hdr->status != ST_OK) return;
   const int32_t* cu = reinterpret_cast<const int32_t*>(a.ws + a.layout.cu_seqlens);
-  const int vec_per_row = a.row_bytes / 16;
-  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  const int64_t tid0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-
+  if (threadIdx.x == 0) s_ok = hdr->status == ST_OK;
   if (a.slot_ids) {
-    // rows of all questions, in cu_seqlens order: r in [0, cu[n]) -> (question, j)
-    const int total = cu[a.n];
-    const int64_t work = (int64_t)total * a.h_kv * vec_per_row;
-    for (int64_t w = tid0; w < work; w += stride) {
-      const int vec = (int)(w % vec_per_row);
-      const int64_t rest = w / vec_per_row;
-      const int g = (int)(rest % a.h_kv);
-      const int r = (int)(rest / a.h_kv);
-      // question owning packed-length position r (binary search in cu_seqlens)
-      int lo = 0, hi = a.n;  // cu[lo] <= r < cu[hi]
-      while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (cu[mid] <= r) lo = mid; else hi = mid;
+    for (int i = threadIdx.x; i <= a.n; i += blockDim.x) s_cu[i] = cu[i];
+    for (int i = threadIdx.x; i < a.n; i += blockDim.x) s_bs[i] = make_int2(a.intervals[i].begin, a.slot_ids[i]);
+  }
+  __syncthreads();
+
+  if (s_ok && a.slot_ids) {
+    const int vpr = a.row_bytes / 16;  // 16-byte vectors per row of one head (8, 16 or 32)
+    const int upp = 32 / vpr;          // units per warp pass
+    const int lane = threadIdx.x & 31, sub = lane / vpr, v = lane % vpr;
+    const int64_t units = (int64_t)s_cu[a.n] * a.h_kv;
+    const int64_t per_chunk = (int64_t)upp * kUnroll;
+    const int64_t n_chunks = (units + per_chunk - 1) / per_chunk;
+    const int warps = gridDim.x * (kAuxThreads / 32);
+    const int4* k = reinterpret_cast<const int4*>(a.k);
+    const int4* vv = reinterpret_cast<const int4*>(a.v);
+    int4* pk = reinterpret_cast<int4*>(a.pool_k);
+    int4* pv = reinterpret_cast<int4*>(a.pool_v);
+    for (int64_t c = blockIdx.x * (kAuxThreads / 32) + (threadIdx.x >> 5); c < n_chunks; c += warps) {
+      int4 bk[kUnroll], bv[kUnroll];
+      int64_t dst[kUnroll];
+#pragma unroll
+      for (int t = 0; t < kUnroll; ++t) {
+        const int64_t u = c * per_chunk + t * upp + sub;
+        dst[t] = -1;
+        if (u < units) {
+          const int r = (int)(u / a.h_kv), g = (int)(u % a.h_kv);
+          const int i = question_of(s_cu, a.n, r);
+          const int j = r - s_cu[i];
+          const int2 bs = s_bs[i];
+          if (bs.y < 0 || bs.y >= a.n_slots || j >= a.cap) continue;  // a work list built for other slots
+          const int64_t src = ((int64_t)(bs.x + j) * a.h_kv + g) * vpr + v;
+          dst[t] = (((int64_t)bs.y * a.h_kv + g) * a.cap + j) * vpr + v;
+          bk[t] = __ldg(k + src);
+          bv[t] = __ldg(vv + src);
+        }
       }
-      const int j = r - cu[lo];
-      const int tok = a.intervals[lo].begin + j;
-      const int slot = a.slot_ids[lo];
-      const int64_t src = ((int64_t)tok * a.h_kv + g) * vec_per_row + vec;
-      const int64_t dst = (((int64_t)slot * a.h_kv + g) * a.cap + j) * vec_per_row + vec;
-      reinterpret_cast<int4*>(a.pool_k)[dst] = __ldg(reinterpret_cast<const int4*>(a.k) + src);
-      reinterpret_cast<int4*>(a.pool_v)[dst] = __ldg(reinterpret_cast<const int4*>(a.v) + src);
+#pragma unroll
+      for (int t = 0; t < kUnroll; ++t) {
+        if (dst[t] >= 0) {
+          pk[dst[t]] = bk[t];
+          pv[dst[t]] = bv[t];
+        }
+      }
     }
   }
-  if (a.out) {
+  if (s_ok && a.out) {
     const int2* gaps = reinterpret_cast<const int2*>(a.ws + a.layout.gaps);
     const int ng = hdr->n_gaps;
-    const int64_t out_vec_row = (int64_t)a.h_q * vec_per_row;  // output row: H_q * d elements
+    const int64_t out_vec_row = (int64_t)a.h_q * (a.row_bytes / 16);  // output row: H_q * d elements
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    const int64_t tid0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     for (int gi = 0; gi < ng; ++gi) {
       const int2 gp = gaps[gi];
       const int64_t base = (int64_t)gp.x * out_vec_row;
@@ -61,12 +105,18 @@ __global__ void __launch_bounds__(256) aux_kernel(AuxArgs a) {
       for (int64_t w = tid0; w < cnt; w += stride) reinterpret_cast<int4*>(a.out)[base + w] = make_int4(0, 0, 0, 0);
     }
   }
+  if (a.after_attention) pdl_wait();  // this grid completes after the attention grid
 }
 
 }  // namespace
 
 cudaError_t launch_aux(const AuxArgs& a, int num_sms, cudaStream_t s) {
-  return launch_pdl(aux_kernel, dim3(num_sms * 4), dim3(256), 0, s, a);
+  const size_t smem = a.slot_ids ? sizeof(int32_t) * (size_t)((a.n + 2) & ~1) + sizeof(int2) * (size_t)a.n : 0;
+  if (smem > 48 * 1024) {
+    const cudaError_t e = cudaFuncSetAttribute(aux_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  return launch_pdl(aux_kernel, dim3(num_sms * 4), dim3(kAuxThreads), smem, s, a);
 }
 
 }  // namespace kev
