@@ -60,3 +60,29 @@ def decode_one(q_row, k_rows, v_rows, scale):
     total = sum(weights)
     d = len(v_rows[0])
     return [sum(w * vr[c] for w, vr in zip(weights, v_rows)) / total for c in range(d)]
+
+
+def rope_rows(x, positions, theta):
+    """Rotary position encoding, one scalar at a time: x [P][H][d] nested lists,
+    positions [P] ints (negative: row unchanged).  Element j < d/2 pairs with
+    element j + d/2; the pair turns by the angle p * theta**(-2j/d) (KV-cache
+    isolation article, hnwysp.cn, §7.2: the rotation multiplies Q and K)."""
+    out = []
+    for row, p in zip(x, positions):
+        if p < 0:
+            out.append([list(hv) for hv in row])
+            continue
+        new_row = []
+        for hv in row:
+            d = len(hv)
+            half = d // 2
+            nv = [0.0] * d
+            for j in range(half):
+                ang = p * theta ** (-(2.0 * j) / d)
+                c, s = math.cos(ang), math.sin(ang)
+                a, b = hv[j], hv[j + half]
+                nv[j] = a * c - b * s
+                nv[j + half] = b * c + a * s
+            new_row.append(nv)
+        out.append(new_row)
+    return out

@@ -27,12 +27,21 @@ dense T x T mask, in float64:
   full recompute).
 * Early stop (Kev pipeline article, §1.2 and §2.3: a question that has
   finished takes no further part in attention).
+* Rotary position encoding with per-question positions (KV-cache isolation
+  article, hnwysp.cn, §7.2: the rotation multiplies Q and K, a cached K
+  keeps the rotation of its own position, and the new token's position is
+  the cache length counted from 0).  Packed with isolation, every question
+  counts its positions from 0 as if it ran alone.
 
 Readings taken where the pages are silent or garbled (each listed in the
 design notes): intervals are half-open [s, e); scale = 1/sqrt(d_h) unless
 given; a q-head h uses kv-head h // (H_q / H_kv); tokens in no interval are
 keys for nobody and their own output row is 0; an empty interval is allowed;
-a decode step attends over lens + 1 positions, the new K/V written first.
+a decode step attends over lens + 1 positions, the new K/V written first;
+RoPE is the rotate-half form (pair (x_i, x_{i+d/2}) turned by p * w_i with
+w_i = theta^(-2i/d), theta given by the caller), the position of token t of
+question i is t - s_i, that of a decode token is lens_i, tokens in no
+question are not rotated.
 
 Pinned by ``tests/test_oracle.py`` against the pages' worked example, closed
 forms, invariants (a)-(d), a library routine and a pure-Python brute force.
@@ -324,3 +333,65 @@ def decode(q_new, k_new, v_new, pool_k, pool_v, slot_ids, lens, active, dtype: s
             p = softmax_rows(((K @ qv) * sc)[None, :])[0]
             o[i, h] = p @ V
     return o, pk, pv
+
+
+# ---------------------------------------------------------------------------
+# rotary position encoding, positions counted per question
+# ---------------------------------------------------------------------------
+
+def rope_freqs(d: int, theta: float) -> np.ndarray:
+    """w_i = theta^(-2i/d) for i = 0 .. d/2 - 1 (float64)."""
+    return np.power(float(theta), -np.arange(0, d, 2, dtype=np.float64) / d)
+
+
+def rope_rotate(x, positions, theta: float) -> np.ndarray:
+    """Rotate-half RoPE of x [P, H, d] (float64 values) at positions[P].
+
+    The pair (x_i, x_{i+d/2}) of every head turns by the angle p * w_i:
+    (a, b) -> (a cos - b sin, b cos + a sin).  Rows whose position is
+    negative (tokens in no question) are returned unchanged.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    half = x.shape[-1] // 2
+    pos = np.asarray(positions, dtype=np.float64).reshape(-1)
+    ang = pos[:, None] * rope_freqs(x.shape[-1], theta)[None, :]
+    c = np.cos(ang)[:, None, :]
+    s = np.sin(ang)[:, None, :]
+    a, b = x[..., :half], x[..., half:]
+    out = np.concatenate([a * c - b * s, b * c + a * s], axis=-1)
+    keep = pos < 0
+    out[keep] = x[keep]
+    return out
+
+
+def prefill_positions(intervals, total_tokens: int) -> np.ndarray:
+    """Position of token t inside its own question, t - s_i (-1 for a token in
+    no question): each question counts from 0, as it would alone."""
+    pos = np.full(int(total_tokens), -1, dtype=np.int64)
+    for s, e in np.asarray(intervals, dtype=np.int64).reshape(-1, 2):
+        pos[s:e] = np.arange(e - s)
+    return pos
+
+
+def prefill_rope(q, k, v, intervals, theta: float, scale=None):
+    """Packed prefill with RoPE: q and k rotated at their per-question
+    positions, then the isolated causal attention of ``prefill``.  Returns
+    (out, q_rot, k_rot), float64."""
+    pos = prefill_positions(intervals, np.asarray(q).shape[0])
+    q_rot = rope_rotate(q, pos, theta)
+    k_rot = rope_rotate(k, pos, theta)
+    return prefill(q_rot, k_rot, v, intervals, scale=scale), q_rot, k_rot
+
+
+def round_to_stored(x64: np.ndarray, dtype: str) -> np.ndarray:
+    """float64 values -> the stored array of ``dtype``: bfloat16 bits rounded
+    once, to nearest with ties to even, from the float64 value (8 significant
+    bits: x = m 2^e with 1/2 <= |m| < 1 becomes rint(256 m) 2^(e-8), which
+    float32 then holds exactly), or float32."""
+    from workloads import f32_to_bf16_bits
+    x64 = np.asarray(x64, dtype=np.float64)
+    if dtype == "bf16":
+        m, e = np.frexp(x64)
+        r = np.ldexp(np.rint(m * 256.0), e - 8)
+        return f32_to_bf16_bits(r.astype(np.float32))  # exact: r has at most 8 significant bits
+    return x64.astype(np.float32)

@@ -401,3 +401,140 @@ def test_planted_mistakes_are_caught(monkeypatch):
         return plain_softmax(scores.T).T
     monkeypatch.setattr(O, "softmax_rows", transposed_pv)
     assert not _pins_pass(lambda q, k, v, iv, sc: O.prefill(q, k, v, iv, scale=sc))
+
+
+# ---------------------------------------------------------------------------
+# rotary position encoding with per-question positions (KV-cache isolation
+# article, hnwysp.cn, §7.2)
+# ---------------------------------------------------------------------------
+
+def _rope_case(seed, P=5, H=3, d=8):
+    rng = np.random.default_rng(seed)
+    return rng.standard_normal((P, H, d)), rng.integers(0, 3000, P)
+
+
+def test_rope_is_the_complex_rotation():
+    """Pair (x_j, x_{j+d/2}) as the complex number x_j + i x_{j+d/2}: RoPE multiplies it by
+    exp(i p w_j).  Complex arithmetic, not the oracle's real-valued formula."""
+    x, pos = _rope_case(1)
+    d = x.shape[-1]
+    theta = 10000.0
+    z = x[..., :d // 2] + 1j * x[..., d // 2:]
+    w = np.exp(-np.log(theta) * np.arange(d // 2) * 2.0 / d)
+    zr = z * np.exp(1j * pos[:, None, None] * w[None, None, :])
+    want = np.concatenate([zr.real, zr.imag], axis=-1)
+    np.testing.assert_allclose(O.rope_rotate(x, pos, theta), want, rtol=0, atol=1e-12)
+
+
+def test_rope_brute_force_scalar_loops():
+    x, pos = _rope_case(2, P=4, H=2, d=16)
+    pos[1] = -1  # a token in no question: unchanged
+    want = np.array(brute.rope_rows(x.tolist(), pos.tolist(), 1e6))
+    np.testing.assert_allclose(O.rope_rotate(x, pos, 1e6), want, rtol=0, atol=1e-12)
+
+
+def test_rope_closed_forms():
+    d, theta = 128, 1e6
+    w = O.rope_freqs(d, theta)
+    assert w[0] == 1.0 and len(w) == d // 2
+    assert math.isclose(w[-1], theta ** (-(d - 2) / d), rel_tol=1e-14)
+    np.testing.assert_allclose(w[1:] / w[:-1], theta ** (-2.0 / d), rtol=1e-13)
+    x, _ = _rope_case(3)
+    np.testing.assert_array_equal(O.rope_rotate(x, np.zeros(len(x), int), theta), x)  # position 0: identity
+    np.testing.assert_array_equal(O.rope_rotate(x, -np.ones(len(x), int), theta), x)  # no question: unchanged
+    y = O.rope_rotate(x, np.arange(len(x)) * 977, theta)
+    np.testing.assert_allclose(np.linalg.norm(y, axis=-1), np.linalg.norm(x, axis=-1), rtol=1e-13)
+
+
+def test_rope_scores_depend_on_the_position_difference_only():
+    rng = np.random.default_rng(4)
+    q, k = rng.standard_normal((1, 2, 64)), rng.standard_normal((1, 2, 64))
+    for p1, p2, shift in [(5, 3, 100), (0, 0, 2457), (1000, 17, 3)]:
+        a = (O.rope_rotate(q, [p1], 1e6) * O.rope_rotate(k, [p2], 1e6)).sum(-1)
+        b = (O.rope_rotate(q, [p1 + shift], 1e6) * O.rope_rotate(k, [p2 + shift], 1e6)).sum(-1)
+        np.testing.assert_allclose(a, b, rtol=0, atol=1e-11)
+
+
+def test_rope_positions_restart_in_every_question():
+    iv = np.array([[5, 8], [0, 3], [10, 10], [11, 13]])  # unsorted, an empty one, gaps at 3, 4, 8, 9, 10
+    pos = O.prefill_positions(iv, 14)
+    assert pos.tolist() == [0, 1, 2, -1, -1, 0, 1, 2, -1, -1, -1, 0, 1, -1]
+
+
+def test_rope_packed_equals_alone_and_the_cache_needs_per_question_positions():
+    """Invariant (b) with RoPE: with positions counted per question, each question's output rows
+    and rotated K rows in the packed batch equal those of the question run alone.  Positions
+    counted over the packed sequence shift a question's positions by a constant: its attention
+    output stays the same (scores see position differences only), but the K it would cache is
+    rotated differently from the K it caches alone, so a later decode at position lens (the cache
+    length) would no longer match -- the reason positions restart in every question."""
+    rng = np.random.default_rng(5)
+    lengths, h_q, h_kv, d, theta = [6, 9, 4], 4, 2, 16, 1e4
+    iv = W.pack_intervals(lengths, gaps=[1, 0, 2])
+    T = int(iv[-1, 1])
+    q, k, v = (rng.standard_normal((T, h, d)) for h in (h_q, h_kv, h_kv))
+    out, _, k_rot = O.prefill_rope(q, k, v, iv, theta)
+    k_glob = O.rope_rotate(k, np.arange(T), theta)
+    out_glob = O.prefill(O.rope_rotate(q, np.arange(T), theta), k_glob, v, iv)
+    for s, e in iv:
+        alone, _, k_alone = O.prefill_rope(q[s:e], k[s:e], v[s:e], np.array([[0, e - s]]), theta)
+        np.testing.assert_allclose(out[s:e], alone, rtol=0, atol=1e-12)
+        np.testing.assert_allclose(k_rot[s:e], k_alone, rtol=0, atol=1e-12)
+        np.testing.assert_allclose(out_glob[s:e], alone, rtol=0, atol=1e-9)
+        if s > 0:
+            assert np.abs(k_glob[s:e] - k_alone).max() > 1e-3
+    seg = O.segment_ids(iv, T)
+    assert (out[seg < 0] == 0).all()
+    np.testing.assert_array_equal(k_rot[seg < 0], k[seg < 0])
+
+
+def test_rope_decode_with_rotated_cache_equals_last_row_of_recompute():
+    """Invariant (c) with RoPE: the cache holds K rotated at its own positions 0..n-1, the new
+    token is rotated at position n = lens (the cache length), and the decode output equals the
+    last row of the full recompute with RoPE."""
+    rng = np.random.default_rng(6)
+    n, h_q, h_kv, d, cap, theta = 11, 4, 2, 16, 16, 1e6
+    q, k, v = (rng.standard_normal((n + 1, h, d)) for h in (h_q, h_kv, h_kv))
+    full, _, k_rot = O.prefill_rope(q, k, v, np.array([[0, n + 1]]), theta)
+    pool_k = np.zeros((1, h_kv, cap, d))
+    pool_v = np.zeros((1, h_kv, cap, d))
+    pool_k[0, :, :n] = np.swapaxes(k_rot[:n], 0, 1)
+    pool_v[0, :, :n] = np.swapaxes(v[:n], 0, 1)
+    q_new = O.rope_rotate(q[n:], [n], theta)
+    k_new = O.rope_rotate(k[n:], [n], theta)
+    o, pk, _ = O.decode(q_new, k_new, v[n:], pool_k, pool_v, [0], [n], [1], "fp64")
+    np.testing.assert_allclose(o[0], full[n], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(pk[0, :, n], k_rot[n], rtol=0, atol=1e-12)
+
+
+def test_round_to_stored_is_one_rounding_to_nearest_even():
+    one = 1.0
+    ulp = 2.0 ** -7  # bf16 spacing in [1, 2)
+    xs = np.array([one + ulp / 2, one + 1.5 * ulp, one + ulp / 2 + 2.0 ** -40, -(one + 1.5 * ulp), 0.0])
+    got = W.bf16_bits_to_f32(O.round_to_stored(xs, "bf16")).astype(np.float64)
+    assert got.tolist() == [1.0, 1.0 + 2 * ulp, 1.0 + ulp, -(1.0 + 2 * ulp), 0.0]
+    # values a float32 holds exactly are rounded once either way
+    x32 = np.random.default_rng(7).standard_normal(1000).astype(np.float32)
+    np.testing.assert_array_equal(O.round_to_stored(x32.astype(np.float64), "bf16"), W.f32_to_bf16_bits(x32))
+
+
+def test_rope_planted_mistakes_are_caught(monkeypatch):
+    """Each plausible RoPE mistake -- the frequency exponent -j/d instead of -2j/d, the rotation
+    turned the other way, adjacent (interleaved) pairs instead of (j, j + d/2) -- disagrees with
+    the scalar-loop brute force the oracle is pinned to."""
+    x, pos = _rope_case(8, P=3, H=2, d=8)
+    theta = 1e4
+    ref = np.array(brute.rope_rows(x.tolist(), pos.tolist(), theta))
+
+    def agrees(y):
+        return np.allclose(y, ref, rtol=0, atol=1e-12)
+
+    assert agrees(O.rope_rotate(x, pos, theta))
+    good = O.rope_freqs
+    monkeypatch.setattr(O, "rope_freqs", lambda d, th: good(2 * d, th)[: d // 2])
+    assert not agrees(O.rope_rotate(x, pos, theta))
+    monkeypatch.undo()
+    assert not agrees(O.rope_rotate(x, -pos, theta))  # turned the other way
+    perm = np.arange(8).reshape(4, 2).T.reshape(-1)    # (0, 1), (2, 3), ... as the pairs
+    inter = O.rope_rotate(x[..., perm], pos, theta)[..., np.argsort(perm)]
+    assert not agrees(inter)

@@ -60,11 +60,13 @@ def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
 
 
 def to_float64(arr: np.ndarray, dtype: str) -> np.ndarray:
-    """Exact float64 value of a stored tensor (``dtype`` is 'bf16' or 'fp32')."""
+    """Exact float64 value of a stored tensor (``dtype`` is 'bf16', 'fp32' or 'fp64')."""
     if dtype == "bf16":
         return bf16_bits_to_f32(arr).astype(np.float64)
     if dtype == "fp32":
         return np.asarray(arr, dtype=np.float32).astype(np.float64)
+    if dtype == "fp64":
+        return np.asarray(arr, dtype=np.float64)
     raise ValueError(dtype)
 
 
