@@ -58,7 +58,8 @@ typedef enum {
   KEV_ERR_SLOT = 4,          /* (device) slot id outside [0,n_slots) or shared by two live questions */
   KEV_ERR_SLOT_OVERFLOW = 5, /* (device) a question longer than slot_cap, or no room for a decode row */
   KEV_ERR_TIMEOUT = 6,       /* (device) a bounded wait inside a kernel gave up; outputs are invalid */
-  KEV_ERR_CUDA = 7           /* a CUDA runtime call failed (launch error, no device, ...) */
+  KEV_ERR_CUDA = 7,          /* a CUDA runtime call failed (launch error, no device, ...) */
+  KEV_ERR_POSITION = 8       /* (device) a position at or past the RoPE table's max_pos */
 } kev_status;
 
 typedef enum { KEV_BF16 = 0, KEV_FP32 = 1 } kev_dtype;
@@ -202,6 +203,66 @@ kev_status kev_decode_attn_static(const void* q_new, const void* k_new, const vo
 kev_status kev_decode_advance(int32_t* lens, const uint8_t* active, int32_t n, kev_stream_t stream);
 
 /* ---------------------------------------------------------------------------------------
+ * Rotary position encoding with positions counted per question
+ *
+ * KV-cache isolation article (hnwysp.cn, news 130224), §7.2: the rotation multiplies Q and
+ * K, the cache holds K after its rotation, and a new token's position is the cache length
+ * counted from 0.  Packed with isolation, every question counts from 0 as it would alone:
+ * token t of question i has position t - begin_i, the decode token of question i position
+ * lens_i.  Form: rotate-half -- element j < d_h/2 of a head pairs with element j + d_h/2 and
+ * the pair (a, b) turns by p * w_j, w_j = theta^(-2j/d_h): (a cos - b sin, b cos + a sin).
+ * Arithmetic in fp32 with the table's cos/sin, results rounded to the storage type (bf16:
+ * to nearest even).  Tokens in no question are not rotated.
+ * ------------------------------------------------------------------------------------- */
+
+/* Bytes of the cos/sin table for positions [0, max_pos) and head size d_h: max_pos * d_h/2
+ * pairs of floats.  0 for max_pos <= 0 or an odd d_h. */
+size_t kev_rope_table_size(int32_t max_pos, int32_t d_h);
+
+/* table[p * d_h/2 + j] = {cos(p w_j), sin(p w_j)} for p < max_pos, j < d_h/2: angles and
+ * cos/sin in double precision, then rounded to float (one kernel).  `table`: device,
+ * 16-byte aligned, kev_rope_table_size bytes, caller-owned.  Build once per (theta, d_h,
+ * max_pos) and reuse.  theta > 1. */
+kev_status kev_rope_table(void* table, int32_t max_pos, int32_t d_h, double theta, kev_stream_t stream);
+
+/* Prefill-side RoPE over the work list kev_build_segments built in `workspace` for the same
+ * intervals and slots: q [T,H_q,d] and k [T,H_kv,d] are rotated IN PLACE at their
+ * per-question positions.  With slot_ids != NULL the rotated K rows and the V rows also go
+ * into the slots (the slot write, fused: call kev_prefill_from_segments afterwards with
+ * slot_ids = NULL).  A question longer than max_pos sets KEV_ERR_POSITION and the call,
+ * like the calls after it on the same workspace, writes nothing.  One kernel. */
+kev_status kev_rope_prefill(void* q, void* k, const void* v, int32_t total_tokens, const kev_interval* intervals,
+                            int32_t n_questions, const int32_t* slot_ids, void* pool_k, void* pool_v,
+                            int32_t n_slots, int32_t slot_cap, const kev_attn_shape* shape, const void* rope_table,
+                            int32_t max_pos, void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                            kev_stream_t stream);
+
+/* Full prefill with RoPE: kev_build_segments, kev_rope_prefill (with the slot write), then
+ * kev_prefill_from_segments without a slot write.  q and k are rotated in place. */
+kev_status kev_prefill_attn_rope(void* q, void* k, const void* v, int32_t total_tokens,
+                                 const kev_interval* intervals, int32_t n_questions, const int32_t* slot_ids,
+                                 void* pool_k, void* pool_v, int32_t n_slots, int32_t slot_cap, void* out,
+                                 const kev_attn_shape* shape, const void* rope_table, int32_t max_pos,
+                                 void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                                 kev_stream_t stream);
+
+/* Decode-side RoPE: q_new [N,H_q,d] and k_new [N,H_kv,d] of every live question rotated IN
+ * PLACE at position lens_i (the cache length before the step); rows of dropped questions
+ * are untouched.  A live lens_i >= max_pos sets KEV_ERR_POSITION and nothing is written.
+ * One kernel. */
+kev_status kev_rope_decode(void* q_new, void* k_new, const int32_t* lens, const uint8_t* active,
+                           int32_t n_questions, const kev_attn_shape* shape, const void* rope_table,
+                           int32_t max_pos, int32_t* dev_status, kev_stream_t stream);
+
+/* kev_rope_decode followed by kev_decode_attn: the pool receives the rotated new K row. */
+kev_status kev_decode_attn_rope(void* q_new, void* k_new, const void* v_new, void* pool_k, void* pool_v,
+                                int32_t n_slots, int32_t slot_cap, const int32_t* slot_ids, const int32_t* lens,
+                                const uint8_t* active, int32_t n_questions, void* out,
+                                const kev_attn_shape* shape, const void* rope_table, int32_t max_pos,
+                                void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                                kev_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------
  * Status
  * ------------------------------------------------------------------------------------- */
 
@@ -215,8 +276,8 @@ const char* kev_status_string(kev_status status);
 /* Number of kernel launches the most recent successful call of each entry point enqueues
  * (for launch accounting): 0 = prefill_attn, 1 = prefill_from_segments, 2 = build_segments,
  * 3 = kv_write, 4 = decode_attn (2 when the last call ran on the tensor cores: bf16 with
- * d_h = 128, decode and merge kernels; 1 otherwise and before any call), 5 = decode_advance.
- * -1 for an unknown id. */
+ * d_h = 128, decode and merge kernels; 1 otherwise and before any call), 5 = decode_advance,
+ * 6 = rope_table, 7 = rope_prefill, 8 = rope_decode (1 each).  -1 for an unknown id. */
 int32_t kev_launch_count(int32_t entry_point);
 
 #ifdef __cplusplus

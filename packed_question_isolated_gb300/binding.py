@@ -30,12 +30,14 @@ KEV_ERR_SLOT = 4
 KEV_ERR_SLOT_OVERFLOW = 5
 KEV_ERR_TIMEOUT = 6
 KEV_ERR_CUDA = 7
+KEV_ERR_POSITION = 8
 KEV_BF16 = 0
 KEV_FP32 = 1
 
 STATUS_NAMES = {
     0: "KEV_OK", 1: "KEV_ERR_INVALID_ARG", 2: "KEV_ERR_UNSUPPORTED", 3: "KEV_ERR_INTERVALS",
     4: "KEV_ERR_SLOT", 5: "KEV_ERR_SLOT_OVERFLOW", 6: "KEV_ERR_TIMEOUT", 7: "KEV_ERR_CUDA",
+    8: "KEV_ERR_POSITION",
 }
 
 # every symbol include/kev.h declares
@@ -44,6 +46,8 @@ EXPORTED = [
     "kev_prefill_from_segments", "kev_prefill_attn", "kev_kv_write",
     "kev_decode_workspace_size", "kev_decode_attn", "kev_decode_advance",
     "kev_read_status", "kev_status_string", "kev_launch_count", "kev_decode_attn_static",
+    "kev_rope_table_size", "kev_rope_table", "kev_rope_prefill", "kev_prefill_attn_rope", "kev_rope_decode",
+    "kev_decode_attn_rope",
 ]
 
 
@@ -90,6 +94,15 @@ _c = {
     "kev_read_status": _sig("kev_read_status", _I, _P, _P),
     "kev_status_string": _sig("kev_status_string", ctypes.c_char_p, _I),
     "kev_launch_count": _sig("kev_launch_count", _I, _I),
+    "kev_rope_table_size": _sig("kev_rope_table_size", _Z, _I, _I),
+    "kev_rope_table": _sig("kev_rope_table", _I, _P, _I, _I, ctypes.c_double, _P),
+    "kev_rope_prefill": _sig("kev_rope_prefill", _I, _P, _P, _P, _I, _P, _I, _P, _P, _P, _I, _I, _S, _P, _I,
+                             _P, _Z, _P, _P),
+    "kev_prefill_attn_rope": _sig("kev_prefill_attn_rope", _I, _P, _P, _P, _I, _P, _I, _P, _P, _P, _I, _I, _P,
+                                  _S, _P, _I, _P, _Z, _P, _P),
+    "kev_rope_decode": _sig("kev_rope_decode", _I, _P, _P, _P, _P, _I, _S, _P, _I, _P, _P),
+    "kev_decode_attn_rope": _sig("kev_decode_attn_rope", _I, _P, _P, _P, _P, _P, _I, _I, _P, _P, _P, _I, _P,
+                                 _S, _P, _I, _P, _Z, _P, _P),
 }
 
 
@@ -236,3 +249,53 @@ def kev_decode_advance(lens, active, n, stream=None, check=True) -> int:
 
 def kev_read_status(dev_status, stream=None) -> int:
     return int(_c["kev_read_status"](_ptr(dev_status), _stream(stream)))
+
+
+def kev_rope_table_size(max_pos: int, d_h: int) -> int:
+    return int(_c["kev_rope_table_size"](int(max_pos), int(d_h)))
+
+
+def kev_rope_table(table, max_pos, d_h, theta, stream=None, check=True) -> int:
+    st = _c["kev_rope_table"](_ptr(table), int(max_pos), int(d_h), float(theta), _stream(stream))
+    return _check(st, "kev_rope_table", check)
+
+
+def kev_rope_prefill(q, k, v, total_tokens, intervals, n_questions, slot_ids, pool_k, pool_v, n_slots, slot_cap,
+                     shape, rope_table, max_pos, workspace, workspace_bytes, dev_status=None, stream=None,
+                     check=True) -> int:
+    s = _shape(shape)
+    st = _c["kev_rope_prefill"](_ptr(q), _ptr(k), _ptr(v), int(total_tokens), _ptr(intervals), int(n_questions),
+                                _ptr(slot_ids), _ptr(pool_k), _ptr(pool_v), int(n_slots), int(slot_cap),
+                                ctypes.byref(s), _ptr(rope_table), int(max_pos), _ptr(workspace),
+                                int(workspace_bytes), _ptr(dev_status), _stream(stream))
+    return _check(st, "kev_rope_prefill", check)
+
+
+def kev_prefill_attn_rope(q, k, v, total_tokens, intervals, n_questions, slot_ids, pool_k, pool_v, n_slots,
+                          slot_cap, out, shape, rope_table, max_pos, workspace, workspace_bytes, dev_status=None,
+                          stream=None, check=True) -> int:
+    s = _shape(shape)
+    st = _c["kev_prefill_attn_rope"](_ptr(q), _ptr(k), _ptr(v), int(total_tokens), _ptr(intervals),
+                                     int(n_questions), _ptr(slot_ids), _ptr(pool_k), _ptr(pool_v), int(n_slots),
+                                     int(slot_cap), _ptr(out), ctypes.byref(s), _ptr(rope_table), int(max_pos),
+                                     _ptr(workspace), int(workspace_bytes), _ptr(dev_status), _stream(stream))
+    return _check(st, "kev_prefill_attn_rope", check)
+
+
+def kev_rope_decode(q_new, k_new, lens, active, n_questions, shape, rope_table, max_pos, dev_status=None,
+                    stream=None, check=True) -> int:
+    s = _shape(shape)
+    st = _c["kev_rope_decode"](_ptr(q_new), _ptr(k_new), _ptr(lens), _ptr(active), int(n_questions),
+                               ctypes.byref(s), _ptr(rope_table), int(max_pos), _ptr(dev_status), _stream(stream))
+    return _check(st, "kev_rope_decode", check)
+
+
+def kev_decode_attn_rope(q_new, k_new, v_new, pool_k, pool_v, n_slots, slot_cap, slot_ids, lens, active,
+                         n_questions, out, shape, rope_table, max_pos, workspace, workspace_bytes, dev_status=None,
+                         stream=None, check=True) -> int:
+    s = _shape(shape)
+    st = _c["kev_decode_attn_rope"](_ptr(q_new), _ptr(k_new), _ptr(v_new), _ptr(pool_k), _ptr(pool_v),
+                                    int(n_slots), int(slot_cap), _ptr(slot_ids), _ptr(lens), _ptr(active),
+                                    int(n_questions), _ptr(out), ctypes.byref(s), _ptr(rope_table), int(max_pos),
+                                    _ptr(workspace), int(workspace_bytes), _ptr(dev_status), _stream(stream))
+    return _check(st, "kev_decode_attn_rope", check)

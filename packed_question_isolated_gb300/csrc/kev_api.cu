@@ -240,6 +240,132 @@ kev_status kev_kv_write(const void* k, const void* v, int32_t total_tokens, cons
   return from_cuda(launch_aux(x, sms, (cudaStream_t)stream));
 }
 
+size_t kev_rope_table_size(int32_t max_pos, int32_t d_h) {
+  if (max_pos <= 0 || d_h <= 0 || (d_h & 1)) return 0;
+  return sizeof(float2) * (size_t)max_pos * (size_t)(d_h / 2);
+}
+
+kev_status kev_rope_table(void* table, int32_t max_pos, int32_t d_h, double theta, kev_stream_t stream) {
+  if (!table || !aligned16(table) || max_pos <= 0 || max_pos > (1 << 24)) return KEV_ERR_INVALID_ARG;
+  if (d_h != 64 && d_h != 128) return KEV_ERR_UNSUPPORTED;
+  if (!(theta > 1.0) || isinf(theta)) return KEV_ERR_INVALID_ARG;
+  return from_cuda(launch_rope_table(static_cast<float2*>(table), max_pos, d_h, theta, (cudaStream_t)stream));
+}
+
+kev_status kev_rope_prefill(void* q, void* k, const void* v, int32_t total_tokens, const kev_interval* intervals,
+                            int32_t n_questions, const int32_t* slot_ids, void* pool_k, void* pool_v,
+                            int32_t n_slots, int32_t slot_cap, const kev_attn_shape* shape, const void* rope_table,
+                            int32_t max_pos, void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                            kev_stream_t stream) {
+  kev_status st = check_prefill_common(total_tokens, intervals, n_questions, shape, workspace, workspace_bytes);
+  if (st != KEV_OK) return st;
+  if (total_tokens > 0 && (!q || !k || !v || !aligned16(q) || !aligned16(k) || !aligned16(v)))
+    return KEV_ERR_INVALID_ARG;
+  st = check_slots(slot_ids, pool_k, pool_v, n_slots, slot_cap, n_questions);
+  if (st != KEV_OK) return st;
+  if (!rope_table || !aligned16(rope_table) || max_pos <= 0) return KEV_ERR_INVALID_ARG;
+  if (dev_status && ((uintptr_t)dev_status & 3u)) return KEV_ERR_INVALID_ARG;
+  const int sms = num_sms_of_current_device();
+  if (sms <= 0) return KEV_ERR_CUDA;
+  RopePrefillArgs a;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.intervals = intervals;
+  a.slot_ids = slot_ids;
+  a.pool_k = pool_k;
+  a.pool_v = pool_v;
+  a.n = n_questions;
+  a.T = total_tokens;
+  a.h_q = shape->h_q;
+  a.h_kv = shape->h_kv;
+  a.d = shape->d_h;
+  a.n_slots = slot_ids ? n_slots : 0;
+  a.cap = slot_ids ? slot_cap : 0;
+  a.max_pos = max_pos;
+  a.elem = elem_size(shape);
+  a.table = static_cast<const float2*>(rope_table);
+  a.ws = static_cast<const char*>(workspace);
+  a.layout = prefill_layout(n_questions, total_tokens, shape->h_q);
+  a.dev_status = dev_status;
+  return from_cuda(launch_rope_prefill(a, sms, (cudaStream_t)stream));
+}
+
+kev_status kev_prefill_attn_rope(void* q, void* k, const void* v, int32_t total_tokens,
+                                 const kev_interval* intervals, int32_t n_questions, const int32_t* slot_ids,
+                                 void* pool_k, void* pool_v, int32_t n_slots, int32_t slot_cap, void* out,
+                                 const kev_attn_shape* shape, const void* rope_table, int32_t max_pos,
+                                 void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                                 kev_stream_t stream) {
+  // full argument check before the first launch, so an invalid call enqueues nothing
+  kev_status st = check_prefill_common(total_tokens, intervals, n_questions, shape, workspace, workspace_bytes);
+  if (st != KEV_OK) return st;
+  if (total_tokens > 0 && (!q || !k || !v || !out || !aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)))
+    return KEV_ERR_INVALID_ARG;
+  st = check_slots(slot_ids, pool_k, pool_v, n_slots, slot_cap, n_questions);
+  if (st != KEV_OK) return st;
+  if (!rope_table || !aligned16(rope_table) || max_pos <= 0) return KEV_ERR_INVALID_ARG;
+  if (dev_status && ((uintptr_t)dev_status & 3u)) return KEV_ERR_INVALID_ARG;
+  st = kev_build_segments(intervals, n_questions, total_tokens, slot_ids, n_slots, slot_cap, shape, workspace,
+                          workspace_bytes, dev_status, stream);
+  if (st != KEV_OK) return st;
+  st = kev_rope_prefill(q, k, v, total_tokens, intervals, n_questions, slot_ids, pool_k, pool_v, n_slots, slot_cap,
+                        shape, rope_table, max_pos, workspace, workspace_bytes, dev_status, stream);
+  if (st != KEV_OK) return st;
+  return kev_prefill_from_segments(q, k, v, total_tokens, intervals, n_questions, nullptr, nullptr, nullptr, 0, 0,
+                                   out, shape, workspace, workspace_bytes, dev_status, stream);
+}
+
+kev_status kev_rope_decode(void* q_new, void* k_new, const int32_t* lens, const uint8_t* active,
+                           int32_t n_questions, const kev_attn_shape* shape, const void* rope_table,
+                           int32_t max_pos, int32_t* dev_status, kev_stream_t stream) {
+  kev_status st = check_shape(shape);
+  if (st != KEV_OK) return st;
+  if (n_questions < 0) return KEV_ERR_INVALID_ARG;
+  if (n_questions > kMaxQuestions) return KEV_ERR_UNSUPPORTED;
+  if (dev_status && ((uintptr_t)dev_status & 3u)) return KEV_ERR_INVALID_ARG;
+  if (n_questions == 0) return KEV_OK;
+  if (!q_new || !k_new || !lens || !active || !aligned16(q_new) || !aligned16(k_new) || ((uintptr_t)lens & 3u))
+    return KEV_ERR_INVALID_ARG;
+  if (!rope_table || !aligned16(rope_table) || max_pos <= 0) return KEV_ERR_INVALID_ARG;
+  RopeDecodeArgs a;
+  a.q_new = q_new;
+  a.k_new = k_new;
+  a.lens = lens;
+  a.active = active;
+  a.n = n_questions;
+  a.h_q = shape->h_q;
+  a.h_kv = shape->h_kv;
+  a.d = shape->d_h;
+  a.max_pos = max_pos;
+  a.elem = elem_size(shape);
+  a.table = static_cast<const float2*>(rope_table);
+  a.dev_status = dev_status;
+  return from_cuda(launch_rope_decode(a, (cudaStream_t)stream));
+}
+
+kev_status kev_decode_attn_rope(void* q_new, void* k_new, const void* v_new, void* pool_k, void* pool_v,
+                                int32_t n_slots, int32_t slot_cap, const int32_t* slot_ids, const int32_t* lens,
+                                const uint8_t* active, int32_t n_questions, void* out,
+                                const kev_attn_shape* shape, const void* rope_table, int32_t max_pos,
+                                void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                                kev_stream_t stream) {
+  // a table that covers the slot: a lens past the table is also past the slot, which the
+  // decode rejects on its own, so neither call writes anything for such a step
+  if (max_pos < slot_cap) return KEV_ERR_INVALID_ARG;
+  kev_status st = check_shape(shape);
+  if (st != KEV_OK) return st;
+  if (n_questions < 0 || n_slots <= 0 || slot_cap <= 0) return KEV_ERR_INVALID_ARG;
+  if (n_questions > 0 && (!v_new || !pool_k || !pool_v || !out || !slot_ids)) return KEV_ERR_INVALID_ARG;
+  const DecodeLayout layout =
+      decode_layout(n_questions, slot_cap, shape->h_q, shape->h_kv, shape->d_h, decode_on_tensor_cores(shape));
+  if (!workspace || ((uintptr_t)workspace & 255u) || workspace_bytes < layout.total) return KEV_ERR_INVALID_ARG;
+  st = kev_rope_decode(q_new, k_new, lens, active, n_questions, shape, rope_table, max_pos, dev_status, stream);
+  if (st != KEV_OK) return st;
+  return kev_decode_attn(q_new, k_new, v_new, pool_k, pool_v, n_slots, slot_cap, slot_ids, lens, active, n_questions,
+                         out, shape, workspace, workspace_bytes, dev_status, stream);
+}
+
 size_t kev_decode_workspace_size(int32_t n_questions, int32_t slot_cap, const kev_attn_shape* shape) {
   if (check_shape(shape) != KEV_OK || n_questions < 0 || slot_cap <= 0 || n_questions > kMaxQuestions) return 0;
   return decode_layout(n_questions, slot_cap, shape->h_q, shape->h_kv, shape->d_h, decode_on_tensor_cores(shape)).total;
@@ -310,7 +436,7 @@ kev_status kev_read_status(const int32_t* dev_status, kev_stream_t stream) {
   if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return KEV_ERR_CUDA;
   int32_t h = 0;
   if (cudaMemcpy(&h, dev_status, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) return KEV_ERR_CUDA;
-  if (h < KEV_OK || h > KEV_ERR_CUDA) return KEV_ERR_CUDA;
+  if (h < KEV_OK || h > KEV_ERR_POSITION) return KEV_ERR_CUDA;
   return (kev_status)h;
 }
 
@@ -324,6 +450,7 @@ const char* kev_status_string(kev_status s) {
     case KEV_ERR_SLOT_OVERFLOW: return "question longer than slot capacity or no room for the decode row";
     case KEV_ERR_TIMEOUT: return "a bounded device wait gave up";
     case KEV_ERR_CUDA: return "CUDA runtime error";
+    case KEV_ERR_POSITION: return "a position at or past the RoPE table's max_pos";
   }
   return "unknown status";
 }
@@ -336,6 +463,9 @@ int32_t kev_launch_count(int32_t entry_point) {
     case 3: return 2;  // segments, slot write
     case 4: return g_decode_launches.load();
     case 5: return 1;
+    case 6: return 1;
+    case 7: return 1;
+    case 8: return 1;
   }
   return -1;
 }

@@ -28,6 +28,7 @@ enum : int32_t {
   ST_SLOT = KEV_ERR_SLOT,
   ST_OVERFLOW = KEV_ERR_SLOT_OVERFLOW,
   ST_TIMEOUT = KEV_ERR_TIMEOUT,
+  ST_POSITION = KEV_ERR_POSITION,
 };
 
 // ---------------------------------------------------------------------------------------
@@ -198,6 +199,38 @@ cudaError_t launch_segments(const SegmentsArgs& a, cudaStream_t s);
 cudaError_t launch_prefill_simt(const PrefillArgs& a, int d, int num_sms, cudaStream_t s);  // fp32
 cudaError_t launch_prefill_tc(const PrefillArgs& a, int d, int num_sms, cudaStream_t s);    // bf16
 cudaError_t launch_aux(const AuxArgs& a, int num_sms, cudaStream_t s);
+
+// ---------------------------------------------------------------------------------------
+// rotary position encoding (kev_rope.cu)
+// ---------------------------------------------------------------------------------------
+struct RopePrefillArgs {
+  void* q;  // [T, H_q, d], rotated in place
+  void* k;  // [T, H_kv, d], rotated in place
+  const void* v;
+  const kev_interval* intervals;
+  const int32_t* slot_ids;  // null: no slot write
+  void* pool_k;
+  void* pool_v;
+  int32_t n, T, h_q, h_kv, d, n_slots, cap, max_pos;
+  int32_t elem;  // bytes per element: 2 (bf16) or 4 (fp32)
+  const float2* table;
+  const char* ws;
+  PrefillLayout layout;
+  int32_t* dev_status;
+};
+struct RopeDecodeArgs {
+  void* q_new;  // [N, H_q, d]
+  void* k_new;  // [N, H_kv, d]
+  const int32_t* lens;
+  const uint8_t* active;
+  int32_t n, h_q, h_kv, d, max_pos;
+  int32_t elem;
+  const float2* table;
+  int32_t* dev_status;
+};
+cudaError_t launch_rope_table(float2* table, int32_t max_pos, int32_t d, double theta, cudaStream_t s);
+cudaError_t launch_rope_prefill(const RopePrefillArgs& a, int num_sms, cudaStream_t s);
+cudaError_t launch_rope_decode(const RopeDecodeArgs& a, cudaStream_t s);
 cudaError_t launch_decode(const DecodeArgs& a, int d, kev_dtype dt, int num_sms, cudaStream_t s);     // CUDA cores
 cudaError_t launch_decode_tc(const DecodeArgs& a, int num_sms, cudaStream_t s);                       // bf16, d = 128
 cudaError_t launch_advance(int32_t* lens, const uint8_t* active, int32_t n, cudaStream_t s);

@@ -33,10 +33,11 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_status_strings_and_launch_counts(lib):
-    for code in range(8):
-        assert lib.kev_status_string(code)
+    for code in range(9):
+        assert lib.kev_status_string(code) != "unknown status"
     assert lib.kev_status_string(99) == "unknown status"
     assert lib.kev_launch_count(0) == 3 and lib.kev_launch_count(4) == 1 and lib.kev_launch_count(9) == -1
+    assert [lib.kev_launch_count(i) for i in (6, 7, 8)] == [1, 1, 1]
 
 
 def test_workspace_sizes(lib):
@@ -68,3 +69,25 @@ def test_host_argument_errors_without_gpu(lib):
     assert lib.kev_decode_advance(None, None, -1, stream=0, check=False) == b.KEV_ERR_INVALID_ARG
     with pytest.raises(b.KevError):
         lib.kev_decode_advance(None, None, -1, stream=0)
+
+
+def test_rope_table_size_and_host_errors_without_gpu(lib):
+    b = lib.binding
+    assert lib.kev_rope_table_size(4224, 128) == 4224 * 64 * 8
+    assert lib.kev_rope_table_size(0, 128) == 0 and lib.kev_rope_table_size(16, 63) == 0
+    s = lib.make_shape(4, 2, 64, "bf16")
+    assert lib.kev_rope_table(None, 16, 64, 1e4, stream=0, check=False) == b.KEV_ERR_INVALID_ARG
+    assert lib.kev_rope_table(0x1000, 16, 96, 1e4, stream=0, check=False) == b.KEV_ERR_UNSUPPORTED
+    assert lib.kev_rope_table(0x1000, 16, 64, 1.0, stream=0, check=False) == b.KEV_ERR_INVALID_ARG
+    assert lib.kev_rope_table(0x1008, 16, 64, 1e4, stream=0, check=False) == b.KEV_ERR_INVALID_ARG
+    # no table / misaligned table / bad max_pos are refused before any CUDA call
+    assert lib.kev_rope_prefill(0x1000, 0x1000, 0x1000, 10, 0x1000, 1, None, None, None, 0, 0, s, None, 16,
+                                0x1000, 1 << 20, None, stream=0, check=False) == b.KEV_ERR_INVALID_ARG
+    assert lib.kev_rope_decode(0x1000, 0x1000, 0x1000, 0x1000, 1, s, 0x1008, 16, None, stream=0,
+                               check=False) == b.KEV_ERR_INVALID_ARG
+    assert lib.kev_rope_decode(0x1000, 0x1000, 0x1000, 0x1000, 1, s, 0x1000, 0, None, stream=0,
+                               check=False) == b.KEV_ERR_INVALID_ARG
+    # the decode-side table must cover the slot
+    assert lib.kev_decode_attn_rope(0x1000, 0x1000, 0x1000, 0x1000, 0x1000, 1, 64, 0x1000, 0x1000, 0x1000, 1,
+                                    0x1000, s, 0x1000, 32, 0x1000, 1 << 20, None, stream=0, check=False) == \
+        b.KEV_ERR_INVALID_ARG
