@@ -321,6 +321,57 @@ def _stress_decode_graph(kev, torch, dev, tdev):
             "l2": "not flushed between the steps of a graph replay (L2 may hold part of the working set)"}
 
 
+ROPE_THETA = 1e6  # Qwen2.5 / Qwen3 rotary base
+
+
+def _rope_step(kev, torch, w, shape, copies, step_buffers, ws_bytes, dws_bytes, K, warmup, useful, hbm_peak):
+    """The headline step with RoPE: segment build, prefill-side RoPE with the slot write, attention
+    (no second slot write), then decode-side RoPE and the decode of one new token per question;
+    back to back over the same buffer sets (q, k, q_new, k_new are rotated in place every step)."""
+    N, T = w.n_questions, w.total_tokens
+    table = torch.empty(kev.kev_rope_table_size(w.cap, w.d) // 4, dtype=torch.float32, device=copies[0]["q"].device)
+    kev.kev_rope_table(table, w.cap, w.d, ROPE_THETA)
+
+    def rstep(c, ev_a=None, ev_b=None):
+        kev.kev_build_segments(c["iv"], N, T, c["sl"], w.n_slots, w.cap, shape, c["ws"], ws_bytes, c["st"])
+        if ev_a is not None:
+            ev_a.record()
+        kev.kev_rope_prefill(c["q"], c["k"], c["v"], T, c["iv"], N, c["sl"], c["pk"], c["pv"], w.n_slots, w.cap,
+                             shape, table, w.cap, c["ws"], ws_bytes, c["st"])
+        if ev_b is not None:
+            ev_b.record()
+        kev.kev_prefill_from_segments(c["q"], c["k"], c["v"], T, c["iv"], N, None, None, None, 0, 0, c["out"],
+                                      shape, c["ws"], ws_bytes, c["st"])
+        kev.kev_decode_attn_rope(c["qn"], c["kn"], c["vn"], c["pk"], c["pv"], w.n_slots, w.cap, c["sl"], c["ln"],
+                                 c["act"], N, c["on"], shape, table, w.cap, c["dws"], dws_bytes, c["dst"])
+
+    for _ in range(warmup):
+        for c in copies:
+            rstep(c)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for s in range(K):
+        rstep(copies[s % len(copies)])
+    b.record()
+    torch.cuda.synchronize()
+    step_ms = a.elapsed_time(b) / K
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    for s in range(K):
+        rstep(copies[s % len(copies)], ev[s][0], ev[s][1])
+    torch.cuda.synchronize()
+    ok = all(kev.kev_read_status(c["st"]) == 0 and kev.kev_read_status(c["dst"]) == 0 for c in copies)
+    rope_ms = statistics.mean(x.elapsed_time(y) for x, y in ev)
+    rbytes = RL.rope_prefill_bytes(w.lengths, w.h_q, w.h_kv, w.d, 2, slots=True)
+    return {"workload": "the step above with RoPE (theta 1e6, positions restart in every question): segment build, "
+                        "prefill-side RoPE with the slot write, attention, decode-side RoPE and decode",
+            "value": useful / (step_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": step_ms, "status_ok": ok,
+            "roofline": {"kernel": "rope_prefill_kernel (rotation in place + slot write)", "bound": "hbm",
+                         "achieved": rbytes / (rope_ms * 1e-3) / 1e9, "peak": hbm_peak, "unit": "GB/s",
+                         "frac": rbytes / (rope_ms * 1e-3) / 1e9 / hbm_peak, "algorithmic_bytes": rbytes,
+                         "launch_ms": rope_ms, "traffic": None}}
+
+
 def _decode_setup(kev, torch, dev, tdev):
     """The decode workload's buffer sets (DECODE_COPIES of them) and its call."""
     dwl = W.qwen3_8b_decode()
@@ -359,7 +410,7 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="kev", choices=["kev", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", choices=["step", "decode"], default=None,
+    ap.add_argument("--only", choices=["step", "decode", "rope"], default=None,
                     help="run only one workload's warm-up and timed loop (for profiling); prints no JSON line")
     args = ap.parse_args(argv)
     if args.warmup < 3:
@@ -441,6 +492,10 @@ def main(argv=None):
             step(copies[s % STEP_COPIES])
         torch.cuda.synchronize()
         return None
+    if args.only == "rope":
+        _rope_step(kev, torch, w, shape, copies, step_buffers, ws_bytes, dws_bytes, args.steps, args.warmup,
+                   RL.prefill_useful_flops(w.lengths, w.h_q, w.d), 1.0)
+        return None
 
     K = args.steps
     e_a, e_b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -504,6 +559,10 @@ def main(argv=None):
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
     e2e_value = aggregate_rate(useful, Ke, world, e2e_ms) / 1e12
+
+    # ---- the same step with rotary position encoding (positions counted per question) ---------
+    rope = _rope_step(kev, torch, w, shape, copies, step_buffers, ws_bytes, dws_bytes, K, args.warmup, useful,
+                      hbm_peak)
 
     # ---- decode workload: calls back to back over DECODE_COPIES pools (2 x 178 MB read per cycle) --
     dwl, dcopies, dstep = _decode_setup(kev, torch, dev, tdev)
@@ -600,6 +659,7 @@ def main(argv=None):
             "prefill_qwen3_8b": {"workload": PREFILL3_WORKLOAD, "value": p3_tf, "unit": "TFLOP/s",
                                  "ms_per_launch": p3_avg, "useful_gflop": useful3 / 1e9,
                                  "frac": p3_tf / tf_peak, "peak_source": f"bf16_tflops burst, {peak_src}"},
+            "rope": rope,
             "stress": stress,
             "cpu_baseline": cpu,
             "cpu_fair_baseline": cpu_fair,

@@ -9,10 +9,10 @@
 //
 // rope_table_kernel     cos/sin of every (position, j) in double precision, stored as floats
 //                       (computed once, then read from L2 by the two kernels below).
-// rope_prefill_kernel   one warp per token row of a question (cu_seqlens order, the question
-//                       found by binary search in shared memory): every lane rotates 16-byte
-//                       chunks (chunk c of the first half with chunk c of the second half) of
-//                       the token's q-heads and kv-heads in place; with a slot pool the rotated
+// rope_prefill_kernel   one thread per 16-byte chunk pair (chunk c of the first half of a head
+//                       row with chunk c of the second half) of the q-heads and kv-heads of a
+//                       question token, in cu_seqlens order (the question found by binary
+//                       search in shared memory), rotated in place; with a slot pool the rotated
 //                       K chunks and the V row also go into the question's slot (the slot write,
 //                       fused into the same pass).  HBM-bound: q, k and v are read once, q and k
 //                       written once, the slot rows written once.
@@ -52,20 +52,15 @@ __device__ __forceinline__ uint4 pack(const float* f, float*) {
   return make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]), __float_as_uint(f[3]));
 }
 
-// Rotates chunk c of one head row in place: elements [c*EV, c*EV + EV) of the first half with
-// the same elements of the second half; cs = the table's cos/sin of those j at this position.
-// With `pool_row`, the rotated chunk pair is written there too.
+// The rotation of one chunk pair held in registers (va: first-half chunk, vb: second-half chunk);
+// cs = the table's cos/sin of those j at this position.
 template <typename E>
-__device__ __forceinline__ void rotate_chunk(E* __restrict__ row, int c, int half, const float2* __restrict__ cs,
-                                             E* __restrict__ pool_row) {
+__device__ __forceinline__ void rotate_regs(uint4& va, uint4& vb, const float2* __restrict__ cs) {
   constexpr int EV = 16 / sizeof(E);
-  uint4* pa = reinterpret_cast<uint4*>(row + c * EV);
-  uint4* pb = reinterpret_cast<uint4*>(row + half + c * EV);
-  const uint4 va = *pa, vb = *pb;
   float a[EV], b[EV], ra[EV], rb[EV];
   unpack(va, a, static_cast<E*>(nullptr));
   unpack(vb, b, static_cast<E*>(nullptr));
-  const float4* cs4 = reinterpret_cast<const float4*>(cs + c * EV);
+  const float4* cs4 = reinterpret_cast<const float4*>(cs);
 #pragma unroll
   for (int e = 0; e < EV; e += 2) {
     const float4 t = __ldg(cs4 + e / 2);  // {cos_j, sin_j, cos_j+1, sin_j+1}
@@ -74,13 +69,21 @@ __device__ __forceinline__ void rotate_chunk(E* __restrict__ row, int c, int hal
     ra[e + 1] = a[e + 1] * t.z - b[e + 1] * t.w;
     rb[e + 1] = b[e + 1] * t.z + a[e + 1] * t.w;
   }
-  const uint4 oa = pack(ra, static_cast<E*>(nullptr)), ob = pack(rb, static_cast<E*>(nullptr));
-  *pa = oa;
-  *pb = ob;
-  if (pool_row) {
-    *reinterpret_cast<uint4*>(pool_row + c * EV) = oa;
-    *reinterpret_cast<uint4*>(pool_row + half + c * EV) = ob;
-  }
+  va = pack(ra, static_cast<E*>(nullptr));
+  vb = pack(rb, static_cast<E*>(nullptr));
+}
+
+// Rotates chunk c of one head row in place: elements [c*EV, c*EV + EV) of the first half with
+// the same elements of the second half.
+template <typename E>
+__device__ __forceinline__ void rotate_chunk(E* __restrict__ row, int c, int half, const float2* __restrict__ cs) {
+  constexpr int EV = 16 / sizeof(E);
+  uint4* pa = reinterpret_cast<uint4*>(row + c * EV);
+  uint4* pb = reinterpret_cast<uint4*>(row + half + c * EV);
+  uint4 va = *pa, vb = *pb;
+  rotate_regs<E>(va, vb, cs + c * EV);
+  *pa = va;
+  *pb = vb;
 }
 
 __device__ __forceinline__ int question_of(const int32_t* cu, int n, int r) {
@@ -127,40 +130,48 @@ __global__ void __launch_bounds__(kRopeThreads) rope_prefill_kernel(RopePrefillA
     return;
   }
 
+  // one task per thread: a chunk pair of one head row of a token (rotation in place; the
+  // rotated K chunk also to the slot), or, with a slot pool, one 16-byte vector of the token's
+  // V row to the slot.  Consecutive threads take consecutive chunks of one token.
   constexpr int EV = 16 / sizeof(E);
   const int half = a.d / 2;
-  const int vh = half / EV;  // chunks per half row
+  const int vh = half / EV;   // chunk pairs per head row
   const int vrow = a.d / EV;  // 16-byte vectors per head row
-  const int tasks = (a.h_q + a.h_kv) * vh;
-  const int lane = threadIdx.x & 31;
-  const int warps = gridDim.x * (kRopeThreads / 32);
-  const int total = s_cu[a.n];
-  for (int r = blockIdx.x * (kRopeThreads / 32) + (threadIdx.x >> 5); r < total; r += warps) {
+  const int rot = (a.h_q + a.h_kv) * vh;
+  const int per_row = rot + (a.slot_ids ? a.h_kv * vrow : 0);
+  const int64_t tasks = (int64_t)s_cu[a.n] * per_row;
+  for (int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; u < tasks; u += (int64_t)gridDim.x * blockDim.x) {
+    const int r = (int)(u / per_row), w = (int)(u % per_row);
     const int i = question_of(s_cu, a.n, r);
     const int j = r - s_cu[i];  // position inside the question
     const int2 bs = s_bs[i];
     const int64_t t = bs.x + j;  // packed token
-    const float2* cs = a.table + (int64_t)j * half;
-    E* qrow = static_cast<E*>(a.q) + t * a.h_q * a.d;
-    E* krow = static_cast<E*>(a.k) + t * a.h_kv * a.d;
     const bool to_slot = bs.y >= 0 && bs.y < a.n_slots && j < a.cap;  // (the segment builder checked them)
-    for (int u = lane; u < tasks; u += 32) {
-      const int h = u / vh, c = u % vh;
+    if (w < rot) {
+      const int h = w / vh, c = w % vh;
+      E* row;
+      E* prow = nullptr;
       if (h < a.h_q) {
-        rotate_chunk<E>(qrow + h * a.d, c, half, cs, nullptr);
+        row = static_cast<E*>(a.q) + (t * a.h_q + h) * a.d;
       } else {
         const int g = h - a.h_q;
-        E* prow = to_slot ? static_cast<E*>(a.pool_k) + (((int64_t)bs.y * a.h_kv + g) * a.cap + j) * a.d : nullptr;
-        rotate_chunk<E>(krow + g * a.d, c, half, cs, prow);
+        row = static_cast<E*>(a.k) + (t * a.h_kv + g) * a.d;
+        if (to_slot) prow = static_cast<E*>(a.pool_k) + (((int64_t)bs.y * a.h_kv + g) * a.cap + j) * a.d;
       }
-    }
-    if (to_slot) {
-      const uint4* vsrc = static_cast<const uint4*>(a.v) + t * a.h_kv * vrow;
-      for (int u = lane; u < a.h_kv * vrow; u += 32) {
-        const int g = u / vrow, c = u % vrow;
-        uint4* dst = static_cast<uint4*>(a.pool_v) + (((int64_t)bs.y * a.h_kv + g) * a.cap + j) * vrow + c;
-        *dst = __ldg(vsrc + u);
+      uint4* pa = reinterpret_cast<uint4*>(row + c * EV);
+      uint4* pb = reinterpret_cast<uint4*>(row + half + c * EV);
+      uint4 va = *pa, vb = *pb;
+      rotate_regs<E>(va, vb, a.table + (int64_t)j * half + c * EV);
+      *pa = va;
+      *pb = vb;
+      if (prow) {
+        *reinterpret_cast<uint4*>(prow + c * EV) = va;
+        *reinterpret_cast<uint4*>(prow + half + c * EV) = vb;
       }
+    } else if (to_slot) {
+      const int x = w - rot, g = x / vrow, c = x % vrow;
+      static_cast<uint4*>(a.pool_v)[(((int64_t)bs.y * a.h_kv + g) * a.cap + j) * vrow + c] =
+          __ldg(static_cast<const uint4*>(a.v) + (t * a.h_kv + g) * vrow + c);
     }
   }
 }
@@ -187,7 +198,7 @@ __global__ void __launch_bounds__(kRopeThreads) rope_decode_kernel(RopeDecodeArg
     const float2* cs = a.table + (int64_t)a.lens[i] * half;
     E* row = h < a.h_q ? static_cast<E*>(a.q_new) + ((int64_t)i * a.h_q + h) * a.d
                        : static_cast<E*>(a.k_new) + ((int64_t)i * a.h_kv + (h - a.h_q)) * a.d;
-    rotate_chunk<E>(row, c, half, cs, nullptr);
+    rotate_chunk<E>(row, c, half, cs);
   }
 }
 
@@ -208,7 +219,10 @@ cudaError_t launch_rope_prefill(const RopePrefillArgs& a, int num_sms, cudaStrea
     const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
   }
-  return launch_pdl(kern, dim3(num_sms * 8), dim3(kRopeThreads), smem, s, a);
+  int per_sm = 0;  // one resident wave: every block loops over the tasks
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kRopeThreads, smem) != cudaSuccess || per_sm < 1)
+    per_sm = 1;
+  return launch_pdl(kern, dim3(num_sms * per_sm), dim3(kRopeThreads), smem, s, a);
 }
 
 cudaError_t launch_rope_decode(const RopeDecodeArgs& a, cudaStream_t s) {

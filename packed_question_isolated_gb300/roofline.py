@@ -15,6 +15,9 @@ Algorithmic work counted for this path:
 * decode bytes = sum over live questions of 2 H_kv lens_i d elem (cached K, V)
   + 2 H_kv d elem (new K/V row) + 2 H_q d elem (query in, output out);
   dropped questions count zero.
+* prefill-side RoPE bytes = sum_i L_i (2 H_q + 5 H_kv) d elem: q and k rows
+  of question tokens read and written back rotated, and (with a slot pool)
+  the v row read plus the rotated k row and the v row written to the slot.
 """
 from __future__ import annotations
 
@@ -50,3 +53,9 @@ def decode_bytes(lens, active, h_q: int, h_kv: int, d: int, elem: int) -> float:
     live = np.asarray(active).astype(bool)
     per = 2.0 * h_kv * lens * d * elem + 2.0 * h_kv * d * elem + 2.0 * h_q * d * elem
     return float(np.sum(per[live]))
+
+
+def rope_prefill_bytes(lengths, h_q: int, h_kv: int, d: int, elem: int, slots: bool = True) -> float:
+    tokens = float(np.sum(np.asarray(lengths, dtype=np.float64)))
+    per_token = 2 * (h_q + h_kv) + (3 * h_kv if slots else 0)
+    return tokens * per_token * d * elem
