@@ -369,7 +369,7 @@ def _rope_step(kev, torch, w, shape, copies, step_buffers, ws_bytes, dws_bytes, 
             "roofline": {"kernel": "rope_prefill_kernel (rotation in place + slot write)", "bound": "hbm",
                          "achieved": rbytes / (rope_ms * 1e-3) / 1e9, "peak": hbm_peak, "unit": "GB/s",
                          "frac": rbytes / (rope_ms * 1e-3) / 1e9 / hbm_peak, "algorithmic_bytes": rbytes,
-                         "launch_ms": rope_ms, "traffic": None}}
+                         "launch_ms": rope_ms, "traffic": _traffic("rope")}}
 
 
 def _decode_setup(kev, torch, dev, tdev):
