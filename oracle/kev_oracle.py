@@ -27,6 +27,10 @@ dense T x T mask, in float64:
   full recompute).
 * Early stop (Kev pipeline article, §1.2 and §2.3: a question that has
   finished takes no further part in attention).
+* Paged slot pool (inference-engine notes, §2.5: K/V kept in fixed-size
+  blocks allocated on demand, a block table records where each block is and
+  attention reads K/V through it; Kev pipeline article, §4.3: blocks of one
+  batch placed at neighbouring addresses first).
 * Rotary position encoding with per-question positions (KV-cache isolation
   article, hnwysp.cn, §7.2: the rotation multiplies Q and K, a cached K
   keeps the rotation of its own position, and the new token's position is
@@ -395,3 +399,118 @@ def round_to_stored(x64: np.ndarray, dtype: str) -> np.ndarray:
         r = np.ldexp(np.rint(m * 256.0), e - 8)
         return f32_to_bf16_bits(r.astype(np.float32))  # exact: r has at most 8 significant bits
     return x64.astype(np.float32)
+
+
+# ---------------------------------------------------------------------------
+# paged slot pool
+# ---------------------------------------------------------------------------
+
+PAGE = 128  # positions per block
+
+
+def paged_gather(pool, table_row, n: int, page: int = PAGE) -> np.ndarray:
+    """Positions 0..n-1 of one question through its block table row: [H_kv, n, d]
+    (position p lives in block table_row[p // page], row p % page)."""
+    pool = np.asarray(pool)
+    if n == 0:
+        return pool[:0, :, :0].reshape(pool.shape[1], 0, pool.shape[3])
+    assert all(int(table_row[p // page]) >= 0 for p in range(n)), "a position without a block"
+    rows = [pool[int(table_row[p // page]), :, p % page, :] for p in range(n)]
+    return np.stack(rows, axis=1)
+
+
+def paged_slot_write(pool_k, pool_v, k, v, intervals, block_table, page: int = PAGE):
+    """pool[table_i[j // page], g, j % page, :] = k/v[s_i + j, g, :] for j < L_i (a bit
+    copy); every other row keeps its contents.  Returns new arrays."""
+    pk = np.array(pool_k, copy=True)
+    pv = np.array(pool_v, copy=True)
+    for (s, e), row in zip(np.asarray(intervals).reshape(-1, 2), np.asarray(block_table)):
+        for j in range(int(e - s)):
+            blk, r = int(row[j // page]), j % page
+            assert blk >= 0, "a position without a block"
+            pk[blk, :, r, :] = np.asarray(k)[s + j]
+            pv[blk, :, r, :] = np.asarray(v)[s + j]
+    return pk, pv
+
+
+def validate_paged(lengths, block_table, n_blocks: int, live=None, page: int = PAGE):
+    """Return None if the tables are valid for questions of the given lengths (positions
+    0..length-1 are used), else the error kind: a question needing more blocks than its
+    table row holds -> SLOT_OVERFLOW; a used entry outside [0, n_blocks) -> SLOT; one
+    block used by two questions, or twice by one -> SLOT.  ``live`` masks the questions
+    that are checked (all when None)."""
+    tb = np.asarray(block_table, dtype=np.int64)
+    ln = np.asarray(lengths, dtype=np.int64)
+    live = np.ones(len(ln), bool) if live is None else np.asarray(live).astype(bool)
+    need = (ln + page - 1) // page
+    if np.any(live & (need > tb.shape[1])):
+        return SLOT_OVERFLOW
+    used = [int(tb[i, b]) for i in range(len(ln)) if live[i] for b in range(int(need[i]))]
+    if any(b < 0 or b >= n_blocks for b in used):
+        return SLOT
+    if len(set(used)) != len(used):
+        return SLOT
+    return None
+
+
+def decode_paged(q_new, k_new, v_new, pool_k, pool_v, block_table, lens, active, dtype: str,
+                 scale=None, page: int = PAGE):
+    """One decode step over the paged pool: for every live question the new K/V
+    row goes to position n = lens_i (block table_i[n // page], row n % page), then
+    the question's positions 0..n, gathered through its table, are attended as in
+    ``decode``.  Returns (o_new, pool_k', pool_v')."""
+    pk = np.array(pool_k, copy=True)
+    pv = np.array(pool_v, copy=True)
+    N, h_q, d = np.asarray(q_new).shape
+    h_kv = np.asarray(k_new).shape[1]
+    G = _group(h_q, h_kv)
+    sc = _scale(scale, d)
+    o = np.full((N, h_q, d), np.nan, dtype=np.float64)
+    for i in range(N):
+        if not active[i]:
+            continue
+        n = int(lens[i])
+        row = np.asarray(block_table)[i]
+        assert int(row[n // page]) >= 0, "no block for the new row"
+        pk[int(row[n // page]), :, n % page, :] = np.asarray(k_new)[i]
+        pv[int(row[n // page]), :, n % page, :] = np.asarray(v_new)[i]
+        K = to_float64(paged_gather(pk, row, n + 1, page), dtype)
+        V = to_float64(paged_gather(pv, row, n + 1, page), dtype)
+        for h in range(h_q):
+            qv = to_float64(np.asarray(q_new)[i, h], dtype)
+            p = softmax_rows(((K[h // G] @ qv) * sc)[None, :])[0]
+            o[i, h] = p @ V[h // G]
+    return o, pk, pv
+
+
+def assign_blocks(need, free, max_blocks: int, contiguous_first: bool = True):
+    """Block tables for questions needing need[i] blocks, taken from the free map
+    ``free`` (bool per block, True = free), in question order.  Contiguous first (Kev
+    pipeline article, §4.3): a question takes the lowest run of need[i] consecutive
+    free blocks; without such a run, or with contiguous_first False, its lowest free
+    blocks one by one.  Returns (table [N, max_blocks] with -1 past each row's blocks,
+    free') or None when the free blocks do not suffice or a row would not fit."""
+    fr = np.array(free, dtype=bool, copy=True)
+    table = np.full((len(need), max_blocks), -1, dtype=np.int32)
+    for i, m in enumerate(need):
+        m = int(m)
+        if m > max_blocks:
+            return None
+        if m == 0:
+            continue
+        pick = None
+        if contiguous_first:
+            run = 0
+            for b in range(len(fr)):
+                run = run + 1 if fr[b] else 0
+                if run == m:
+                    pick = list(range(b - m + 1, b + 1))
+                    break
+        if pick is None:
+            idx = np.nonzero(fr)[0]
+            if len(idx) < m:
+                return None
+            pick = [int(x) for x in idx[:m]]
+        table[i, :m] = pick
+        fr[pick] = False
+    return table, fr

@@ -538,3 +538,121 @@ def test_rope_planted_mistakes_are_caught(monkeypatch):
     perm = np.arange(8).reshape(4, 2).T.reshape(-1)    # (0, 1), (2, 3), ... as the pairs
     inter = O.rope_rotate(x[..., perm], pos, theta)[..., np.argsort(perm)]
     assert not agrees(inter)
+
+
+# ---------------------------------------------------------------------------
+# paged slot pool (inference-engine notes, sakurs2.com, §2.5; Kev pipeline
+# article, gsyq.cn, §4.3)
+# ---------------------------------------------------------------------------
+
+def _paged_case(seed, lengths, h_kv=2, d=8, page=O.PAGE, extra=0):
+    """Random block tables: every question gets blocks for its length + ``extra`` positions."""
+    rng = np.random.default_rng(seed)
+    iv = W.pack_intervals(lengths, gaps=[1] * len(lengths))
+    T = int(iv[-1, 1])
+    k = rng.standard_normal((T, h_kv, d))
+    v = rng.standard_normal((T, h_kv, d))
+    need = [(L + extra + page - 1) // page for L in lengths]
+    mb = max(need + [1]) + 1
+    n_blocks = sum(need) + 5
+    perm = rng.permutation(n_blocks)
+    table = np.full((len(lengths), mb), -1, np.int64)
+    at = 0
+    for i, m in enumerate(need):
+        table[i, :m] = perm[at:at + m]
+        at += m
+    return iv, k, v, table, n_blocks, mb
+
+
+def test_paged_write_then_gather_equals_the_contiguous_slot():
+    lengths = [300, 129, 1, 0, 256]
+    iv, k, v, table, n_blocks, mb = _paged_case(1, lengths)
+    pool = np.full((n_blocks, 2, O.PAGE, 8), -7.0)
+    pk, pv = O.paged_slot_write(pool, pool, k, v, iv, table)
+    ck, cv = O.slot_write(np.zeros((len(lengths), 2, 512, 8)), np.zeros((len(lengths), 2, 512, 8)), k, v, iv,
+                          np.arange(len(lengths)))
+    for i, L in enumerate(lengths):
+        np.testing.assert_array_equal(O.paged_gather(pk, table[i], L), ck[i, :, :L])
+        np.testing.assert_array_equal(O.paged_gather(pv, table[i], L), cv[i, :, :L])
+    used = {int(b) for i, L in enumerate(lengths) for b in table[i, :(L + 127) // 128]}
+    for b in set(range(n_blocks)) - used:  # blocks no question uses keep their contents
+        assert (pk[b] == -7.0).all() and (pv[b] == -7.0).all()
+
+
+def test_paged_identity_table_is_the_contiguous_layout_reshaped():
+    """With block i * mb + b for block b of question i, the paged pool [n * mb, H, page, d] holds
+    exactly the contiguous pool [n, H, mb * page, d] split along positions."""
+    lengths = [200, 77, 300]
+    iv, k, v, _, _, mb = _paged_case(2, lengths)
+    n = len(lengths)
+    table = np.arange(n * mb).reshape(n, mb)
+    pk, _ = O.paged_slot_write(np.zeros((n * mb, 2, O.PAGE, 8)), np.zeros((n * mb, 2, O.PAGE, 8)), k, v, iv, table)
+    ck, _ = O.slot_write(np.zeros((n, 2, mb * O.PAGE, 8)), np.zeros((n, 2, mb * O.PAGE, 8)), k, v, iv, np.arange(n))
+    as_contig = pk.reshape(n, mb, 2, O.PAGE, 8).transpose(0, 2, 1, 3, 4).reshape(n, 2, mb * O.PAGE, 8)
+    np.testing.assert_array_equal(as_contig, ck)
+
+
+def test_paged_decode_equals_contiguous_decode():
+    rng = np.random.default_rng(3)
+    lengths = [300, 129, 7, 0, 255]
+    h_q, h_kv, d = 4, 2, 8
+    iv, k, v, table, n_blocks, mb = _paged_case(3, lengths, h_kv, d, extra=1)  # room for the new row
+    N = len(lengths)
+    pk, pv = O.paged_slot_write(np.zeros((n_blocks, h_kv, O.PAGE, d)), np.zeros((n_blocks, h_kv, O.PAGE, d)), k, v,
+                                iv, table)
+    cap = mb * O.PAGE
+    ck, cv = O.slot_write(np.zeros((N, h_kv, cap, d)), np.zeros((N, h_kv, cap, d)), k, v, iv, np.arange(N))
+    q_new, k_new, v_new = (rng.standard_normal((N, h, d)) for h in (h_q, h_kv, h_kv))
+    lens = np.array(lengths)
+    active = np.array([1, 0, 1, 1, 1])
+    assert O.validate_paged(lens + 1, table, n_blocks, live=active) is None
+    o_p, pk2, _ = O.decode_paged(q_new, k_new, v_new, pk, pv, table, lens, active, "fp64")
+    o_c, ck2, _ = O.decode(q_new, k_new, v_new, ck, cv, np.arange(N), lens, active, "fp64")
+    np.testing.assert_array_equal(np.isnan(o_p), np.isnan(o_c))
+    live = active.astype(bool)
+    np.testing.assert_allclose(o_p[live], o_c[live], rtol=0, atol=1e-12)
+    for i in np.nonzero(live)[0]:
+        np.testing.assert_array_equal(O.paged_gather(pk2, table[i], lens[i] + 1), ck2[i, :, :lens[i] + 1])
+
+
+def test_validate_paged_cases():
+    table = np.array([[3, 4, -1], [5, -1, -1], [0, 1, 2]])
+    assert O.validate_paged([200, 100, 300], table, 6) is None
+    assert O.validate_paged([257, 100, 300], table, 6) == O.SLOT  # a third block: -1
+    assert O.validate_paged([200, 100, 385], table, 6) == O.SLOT_OVERFLOW  # 4 blocks, rows hold 3
+    assert O.validate_paged([200, 100, 300], table, 5) == O.SLOT  # block 5 out of range
+    dup = np.array([[3, 4, -1], [4, -1, -1], [0, 1, 2]])
+    assert O.validate_paged([200, 100, 300], dup, 6) == O.SLOT  # block 4 shared
+    assert O.validate_paged([200, 100, 300], dup, 6, live=[1, 0, 1]) is None  # the sharer is dropped
+    same = np.array([[3, 3, -1]])
+    assert O.validate_paged([200], same, 6) == O.SLOT  # twice in one question
+    assert O.validate_paged([0, 0], np.full((2, 1), -1), 1) is None  # empty questions use no block
+
+
+def test_assign_blocks_contiguous_first_example_and_invariants():
+    free = np.array([1, 1, 0, 1, 1, 1, 0, 1], bool)
+    table, fr = O.assign_blocks([2, 2, 2], free, 3)
+    assert table.tolist() == [[0, 1, -1], [3, 4, -1], [5, 7, -1]]  # the last one has no run of 2 left
+    assert fr.tolist() == [False] * 8
+    table, _ = O.assign_blocks([2, 2, 2], free, 3, contiguous_first=False)
+    assert table.tolist() == [[0, 1, -1], [3, 4, -1], [5, 7, -1]]
+    table, _ = O.assign_blocks([1, 3], free, 3)
+    assert table.tolist() == [[0, -1, -1], [3, 4, 5]]  # lowest run of 3, not blocks 1, 3, 4
+    table, _ = O.assign_blocks([1, 3], free, 3, contiguous_first=False)
+    assert table.tolist() == [[0, -1, -1], [1, 3, 4]]
+    assert O.assign_blocks([3, 4], free, 4) is None  # 6 free blocks for 7
+    assert O.assign_blocks([4], free, 3) is None     # a row holds 3
+    rng = np.random.default_rng(4)
+    for _ in range(20):
+        free = rng.random(64) < 0.7
+        need = rng.integers(0, 5, 6)
+        res = O.assign_blocks(need, free, 5)
+        if res is None:
+            assert need.sum() > free.sum()
+            continue
+        table, fr = res
+        used = [int(b) for i, m in enumerate(need) for b in table[i, :m]]
+        assert len(set(used)) == len(used) and all(free[b] for b in used)
+        assert (table[np.arange(5)[None, :] >= need[:, None]] == -1).all()
+        assert sorted(np.nonzero(free & ~fr)[0].tolist()) == sorted(used)
+        assert O.validate_paged(need * O.PAGE, table, 64) is None
