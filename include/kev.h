@@ -203,6 +203,61 @@ kev_status kev_decode_attn_static(const void* q_new, const void* k_new, const vo
 kev_status kev_decode_advance(int32_t* lens, const uint8_t* active, int32_t n, kev_stream_t stream);
 
 /* ---------------------------------------------------------------------------------------
+ * Paged slot pool
+ *
+ * Inference-engine notes (sakurs2.com), §2.5: K/V are kept in fixed-size blocks taken on
+ * demand, a block table records where each block lies, and attention reads K/V through the
+ * table.  pool_{k,v}: [n_blocks, H_kv, KEV_PAGE, d_h]; block_table: device int32
+ * [n_questions, max_blocks]; position p of question i lives in block
+ * block_table[i * max_blocks + p / KEV_PAGE], row p % KEV_PAGE.  Entries past a question's
+ * pages are never read.  n_questions * max_blocks <= KEV_MAX_PAGED_ENTRIES, else
+ * KEV_ERR_UNSUPPORTED.  A block used by two questions (or twice by one) is KEV_ERR_SLOT --
+ * the shared-state bug of the KV-cache isolation article (hnwysp.cn), §2.3 -- and a table
+ * row with fewer blocks than the question's pages KEV_ERR_SLOT_OVERFLOW; both are found
+ * before anything is written.
+ * ------------------------------------------------------------------------------------- */
+#define KEV_PAGE 128
+#define KEV_MAX_PAGED_ENTRIES 16384
+
+/* Prefill with a paged pool: kev_build_segments (no slot checks), a check of the block tables
+ * of the questions' lengths (ceil(L_i / KEV_PAGE) blocks each), the attention, then the bit
+ * copy of every question's K/V rows into its blocks.  Other pool rows are not touched. */
+kev_status kev_prefill_attn_paged(const void* q, const void* k, const void* v, int32_t total_tokens,
+                                  const kev_interval* intervals, int32_t n_questions, const int32_t* block_table,
+                                  int32_t max_blocks, void* pool_k, void* pool_v, int32_t n_blocks, void* out,
+                                  const kev_attn_shape* shape, void* workspace, size_t workspace_bytes,
+                                  int32_t* dev_status, kev_stream_t stream);
+
+/* The paged write alone: kev_build_segments, the table check, the copy of K/V rows into the
+ * blocks (prefill workspace). */
+kev_status kev_kv_write_paged(const void* k, const void* v, int32_t total_tokens, const kev_interval* intervals,
+                              int32_t n_questions, const int32_t* block_table, int32_t max_blocks, void* pool_k,
+                              void* pool_v, int32_t n_blocks, const kev_attn_shape* shape, void* workspace,
+                              size_t workspace_bytes, int32_t* dev_status, kev_stream_t stream);
+
+/* One decode step over a paged pool (bf16, d_h = 128; else KEV_ERR_UNSUPPORTED): as
+ * kev_decode_attn, the new row going to position lens_i, i.e. block
+ * block_table[i][lens_i / KEV_PAGE], row lens_i % KEV_PAGE.  A live question needs blocks for
+ * pages 0 .. lens_i / KEV_PAGE (else KEV_ERR_SLOT_OVERFLOW), in [0, n_blocks) and distinct
+ * among live questions (else KEV_ERR_SLOT).  Workspace: kev_decode_workspace_size(n,
+ * max_blocks * KEV_PAGE, shape), zero-filled once as for kev_decode_attn. */
+kev_status kev_decode_attn_paged(const void* q_new, const void* k_new, const void* v_new, void* pool_k,
+                                 void* pool_v, int32_t n_blocks, const int32_t* block_table, int32_t max_blocks,
+                                 const int32_t* lens, const uint8_t* active, int32_t n_questions, void* out,
+                                 const kev_attn_shape* shape, void* workspace, size_t workspace_bytes,
+                                 int32_t* dev_status, kev_stream_t stream);
+
+/* Host helper (no CUDA call): block tables for questions needing need[i] blocks, taken from
+ * free_map (host uint8[n_blocks], 1 = free) in question order.  Contiguous first (Kev pipeline
+ * article, gsyq.cn, §4.3: a batch's questions on neighbouring addresses): a question takes the
+ * lowest run of need[i] consecutive free blocks, or, without one (or with contiguous_first =
+ * 0), its lowest free blocks one by one.  Writes table (host int32[n * max_blocks], -1 past
+ * each row's blocks) and clears the taken blocks in free_map.  Returns 0, or -1 with nothing
+ * changed when the free blocks do not suffice or a need[i] exceeds max_blocks. */
+int32_t kev_assign_blocks(const int32_t* need, int32_t n, uint8_t* free_map, int32_t n_blocks, int32_t* table,
+                          int32_t max_blocks, int32_t contiguous_first);
+
+/* ---------------------------------------------------------------------------------------
  * Rotary position encoding with positions counted per question
  *
  * KV-cache isolation article (hnwysp.cn, news 130224), §7.2: the rotation multiplies Q and
@@ -277,7 +332,9 @@ const char* kev_status_string(kev_status status);
  * (for launch accounting): 0 = prefill_attn, 1 = prefill_from_segments, 2 = build_segments,
  * 3 = kv_write, 4 = decode_attn (2 when the last call ran on the tensor cores: bf16 with
  * d_h = 128, decode and merge kernels; 1 otherwise and before any call), 5 = decode_advance,
- * 6 = rope_table, 7 = rope_prefill, 8 = rope_decode (1 each).  -1 for an unknown id. */
+ * 6 = rope_table, 7 = rope_prefill, 8 = rope_decode (1 each), 9 = prefill_attn_paged (4:
+ * segments, table check, attention, paged write), 10 = kv_write_paged (3), 11 =
+ * decode_attn_paged (2).  -1 for an unknown id. */
 int32_t kev_launch_count(int32_t entry_point);
 
 #ifdef __cplusplus

@@ -33,6 +33,8 @@ KEV_ERR_CUDA = 7
 KEV_ERR_POSITION = 8
 KEV_BF16 = 0
 KEV_FP32 = 1
+KEV_PAGE = 128
+KEV_MAX_PAGED_ENTRIES = 16384
 
 STATUS_NAMES = {
     0: "KEV_OK", 1: "KEV_ERR_INVALID_ARG", 2: "KEV_ERR_UNSUPPORTED", 3: "KEV_ERR_INTERVALS",
@@ -47,7 +49,8 @@ EXPORTED = [
     "kev_decode_workspace_size", "kev_decode_attn", "kev_decode_advance",
     "kev_read_status", "kev_status_string", "kev_launch_count", "kev_decode_attn_static",
     "kev_rope_table_size", "kev_rope_table", "kev_rope_prefill", "kev_prefill_attn_rope", "kev_rope_decode",
-    "kev_decode_attn_rope",
+    "kev_decode_attn_rope", "kev_prefill_attn_paged", "kev_kv_write_paged", "kev_decode_attn_paged",
+    "kev_assign_blocks",
 ]
 
 
@@ -103,6 +106,12 @@ _c = {
     "kev_rope_decode": _sig("kev_rope_decode", _I, _P, _P, _P, _P, _I, _S, _P, _I, _P, _P),
     "kev_decode_attn_rope": _sig("kev_decode_attn_rope", _I, _P, _P, _P, _P, _P, _I, _I, _P, _P, _P, _I, _P,
                                  _S, _P, _I, _P, _Z, _P, _P),
+    "kev_prefill_attn_paged": _sig("kev_prefill_attn_paged", _I, _P, _P, _P, _I, _P, _I, _P, _I, _P, _P, _I, _P,
+                                   _S, _P, _Z, _P, _P),
+    "kev_kv_write_paged": _sig("kev_kv_write_paged", _I, _P, _P, _I, _P, _I, _P, _I, _P, _P, _I, _S, _P, _Z, _P, _P),
+    "kev_decode_attn_paged": _sig("kev_decode_attn_paged", _I, _P, _P, _P, _P, _P, _I, _P, _I, _P, _P, _I, _P, _S,
+                                  _P, _Z, _P, _P),
+    "kev_assign_blocks": _sig("kev_assign_blocks", _I, _P, _I, _P, _I, _P, _I, _I),
 }
 
 
@@ -299,3 +308,51 @@ def kev_decode_attn_rope(q_new, k_new, v_new, pool_k, pool_v, n_slots, slot_cap,
                                     int(n_questions), _ptr(out), ctypes.byref(s), _ptr(rope_table), int(max_pos),
                                     _ptr(workspace), int(workspace_bytes), _ptr(dev_status), _stream(stream))
     return _check(st, "kev_decode_attn_rope", check)
+
+
+def kev_prefill_attn_paged(q, k, v, total_tokens, intervals, n_questions, block_table, max_blocks, pool_k, pool_v,
+                           n_blocks, out, shape, workspace, workspace_bytes, dev_status=None, stream=None,
+                           check=True) -> int:
+    s = _shape(shape)
+    st = _c["kev_prefill_attn_paged"](_ptr(q), _ptr(k), _ptr(v), int(total_tokens), _ptr(intervals),
+                                      int(n_questions), _ptr(block_table), int(max_blocks), _ptr(pool_k),
+                                      _ptr(pool_v), int(n_blocks), _ptr(out), ctypes.byref(s), _ptr(workspace),
+                                      int(workspace_bytes), _ptr(dev_status), _stream(stream))
+    return _check(st, "kev_prefill_attn_paged", check)
+
+
+def kev_kv_write_paged(k, v, total_tokens, intervals, n_questions, block_table, max_blocks, pool_k, pool_v, n_blocks,
+                       shape, workspace, workspace_bytes, dev_status=None, stream=None, check=True) -> int:
+    s = _shape(shape)
+    st = _c["kev_kv_write_paged"](_ptr(k), _ptr(v), int(total_tokens), _ptr(intervals), int(n_questions),
+                                  _ptr(block_table), int(max_blocks), _ptr(pool_k), _ptr(pool_v), int(n_blocks),
+                                  ctypes.byref(s), _ptr(workspace), int(workspace_bytes), _ptr(dev_status),
+                                  _stream(stream))
+    return _check(st, "kev_kv_write_paged", check)
+
+
+def kev_decode_attn_paged(q_new, k_new, v_new, pool_k, pool_v, n_blocks, block_table, max_blocks, lens, active,
+                          n_questions, out, shape, workspace, workspace_bytes, dev_status=None, stream=None,
+                          check=True) -> int:
+    s = _shape(shape)
+    st = _c["kev_decode_attn_paged"](_ptr(q_new), _ptr(k_new), _ptr(v_new), _ptr(pool_k), _ptr(pool_v),
+                                     int(n_blocks), _ptr(block_table), int(max_blocks), _ptr(lens), _ptr(active),
+                                     int(n_questions), _ptr(out), ctypes.byref(s), _ptr(workspace),
+                                     int(workspace_bytes), _ptr(dev_status), _stream(stream))
+    return _check(st, "kev_decode_attn_paged", check)
+
+
+def kev_assign_blocks(need, free_map, max_blocks: int, contiguous_first: bool = True):
+    """Host block assignment (no CUDA call).  ``need``: ints per question; ``free_map``: numpy
+    uint8/bool array (1 = free), updated in place on success.  Returns the table as a numpy
+    int32 [n, max_blocks] array, or None when the free blocks do not suffice."""
+    import numpy as np
+    nd = np.ascontiguousarray(need, dtype=np.int32)
+    fm = np.ascontiguousarray(free_map, dtype=np.uint8)
+    table = np.empty((len(nd), int(max_blocks)), dtype=np.int32)
+    r = _c["kev_assign_blocks"](nd.ctypes.data, len(nd), fm.ctypes.data, len(fm), table.ctypes.data,
+                                int(max_blocks), int(bool(contiguous_first)))
+    if r != 0:
+        return None
+    free_map[...] = fm.astype(np.asarray(free_map).dtype)
+    return table

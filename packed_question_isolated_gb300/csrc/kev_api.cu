@@ -240,6 +240,211 @@ kev_status kev_kv_write(const void* k, const void* v, int32_t total_tokens, cons
   return from_cuda(launch_aux(x, sms, (cudaStream_t)stream));
 }
 
+namespace {
+
+kev_status check_paged(const int32_t* block_table, int32_t max_blocks, void* pool_k, void* pool_v, int32_t n_blocks,
+                       int32_t n) {
+  if (!block_table || ((uintptr_t)block_table & 3u) || max_blocks <= 0 || n_blocks <= 0) return KEV_ERR_INVALID_ARG;
+  if (!pool_k || !pool_v || !aligned16(pool_k) || !aligned16(pool_v)) return KEV_ERR_INVALID_ARG;
+  if ((int64_t)n * max_blocks > kMaxPagedEntries || (int64_t)max_blocks * kPage > (1 << 30)) return KEV_ERR_UNSUPPORTED;
+  return KEV_OK;
+}
+
+// table check and paged write of a prefill whose work list kev_build_segments just built
+kev_status paged_prefill_tail(const void* q, const void* k, const void* v, int32_t T, const kev_interval* intervals,
+                              int32_t n, const int32_t* block_table, int32_t max_blocks, void* pool_k, void* pool_v,
+                              int32_t n_blocks, void* out, const kev_attn_shape* shape, void* ws, int32_t* dev_status,
+                              cudaStream_t s) {
+  const int sms = num_sms_of_current_device();
+  if (sms <= 0) return KEV_ERR_CUDA;
+  const PrefillLayout layout = prefill_layout(n, T, shape->h_q);
+  PagedCheckArgs c;
+  c.intervals = intervals;
+  c.block_table = block_table;
+  c.n = n;
+  c.max_blocks = max_blocks;
+  c.n_blocks = n_blocks;
+  c.ws = static_cast<char*>(ws);
+  c.dev_status = dev_status;
+  if (launch_paged_check(c, s) != cudaSuccess) return KEV_ERR_CUDA;
+  bool attention = false;
+  if (out) {
+    PrefillArgs p;
+    p.q = q;
+    p.k = k;
+    p.v = v;
+    p.out = out;
+    p.intervals = intervals;
+    p.T = T;
+    p.n = n;
+    p.h_q = shape->h_q;
+    p.h_kv = shape->h_kv;
+    p.group = shape->h_q / shape->h_kv;
+    p.scale = effective_scale(shape);
+    p.ws = static_cast<const char*>(ws);
+    p.layout = layout;
+    p.dev_status = dev_status;
+    const cudaError_t e = shape->dtype == KEV_BF16 ? launch_prefill_tc(p, shape->d_h, sms, s)
+                                                   : launch_prefill_simt(p, shape->d_h, sms, s);
+    if (e != cudaSuccess) return KEV_ERR_CUDA;
+    attention = T > 0;
+  }
+  AuxArgs x;
+  x.k = k;
+  x.v = v;
+  x.out = out;
+  x.intervals = intervals;
+  x.slot_ids = nullptr;
+  x.pool_k = pool_k;
+  x.pool_v = pool_v;
+  x.n = n;
+  x.T = T;
+  x.h_q = shape->h_q;
+  x.h_kv = shape->h_kv;
+  x.cap = max_blocks * kPage;
+  x.n_slots = n_blocks;
+  x.block_table = block_table;
+  x.max_blocks = max_blocks;
+  x.row_bytes = shape->d_h * elem_size(shape);
+  x.ws = static_cast<const char*>(ws);
+  x.layout = layout;
+  x.after_attention = attention;
+  return from_cuda(launch_aux(x, sms, s));
+}
+
+}  // namespace
+
+kev_status kev_prefill_attn_paged(const void* q, const void* k, const void* v, int32_t total_tokens,
+                                  const kev_interval* intervals, int32_t n_questions, const int32_t* block_table,
+                                  int32_t max_blocks, void* pool_k, void* pool_v, int32_t n_blocks, void* out,
+                                  const kev_attn_shape* shape, void* workspace, size_t workspace_bytes,
+                                  int32_t* dev_status, kev_stream_t stream) {
+  kev_status st = check_prefill_common(total_tokens, intervals, n_questions, shape, workspace, workspace_bytes);
+  if (st != KEV_OK) return st;
+  if (total_tokens > 0 && (!q || !k || !v || !out || !aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)))
+    return KEV_ERR_INVALID_ARG;
+  st = check_paged(block_table, max_blocks, pool_k, pool_v, n_blocks, n_questions);
+  if (st != KEV_OK) return st;
+  if (dev_status && ((uintptr_t)dev_status & 3u)) return KEV_ERR_INVALID_ARG;
+  st = kev_build_segments(intervals, n_questions, total_tokens, nullptr, 0, 0, shape, workspace, workspace_bytes,
+                          dev_status, stream);
+  if (st != KEV_OK) return st;
+  return paged_prefill_tail(q, k, v, total_tokens, intervals, n_questions, block_table, max_blocks, pool_k, pool_v,
+                            n_blocks, out, shape, workspace, dev_status, (cudaStream_t)stream);
+}
+
+kev_status kev_kv_write_paged(const void* k, const void* v, int32_t total_tokens, const kev_interval* intervals,
+                              int32_t n_questions, const int32_t* block_table, int32_t max_blocks, void* pool_k,
+                              void* pool_v, int32_t n_blocks, const kev_attn_shape* shape, void* workspace,
+                              size_t workspace_bytes, int32_t* dev_status, kev_stream_t stream) {
+  kev_status st = check_prefill_common(total_tokens, intervals, n_questions, shape, workspace, workspace_bytes);
+  if (st != KEV_OK) return st;
+  if (total_tokens > 0 && (!k || !v || !aligned16(k) || !aligned16(v))) return KEV_ERR_INVALID_ARG;
+  st = check_paged(block_table, max_blocks, pool_k, pool_v, n_blocks, n_questions);
+  if (st != KEV_OK) return st;
+  if (dev_status && ((uintptr_t)dev_status & 3u)) return KEV_ERR_INVALID_ARG;
+  st = kev_build_segments(intervals, n_questions, total_tokens, nullptr, 0, 0, shape, workspace, workspace_bytes,
+                          dev_status, stream);
+  if (st != KEV_OK) return st;
+  return paged_prefill_tail(nullptr, k, v, total_tokens, intervals, n_questions, block_table, max_blocks, pool_k,
+                            pool_v, n_blocks, nullptr, shape, workspace, dev_status, (cudaStream_t)stream);
+}
+
+kev_status kev_decode_attn_paged(const void* q_new, const void* k_new, const void* v_new, void* pool_k,
+                                 void* pool_v, int32_t n_blocks, const int32_t* block_table, int32_t max_blocks,
+                                 const int32_t* lens, const uint8_t* active, int32_t n_questions, void* out,
+                                 const kev_attn_shape* shape, void* workspace, size_t workspace_bytes,
+                                 int32_t* dev_status, kev_stream_t stream) {
+  kev_status st = check_shape(shape);
+  if (st != KEV_OK) return st;
+  if (!decode_on_tensor_cores(shape)) return KEV_ERR_UNSUPPORTED;
+  if (n_questions < 0) return KEV_ERR_INVALID_ARG;
+  if (n_questions > kMaxQuestions) return KEV_ERR_UNSUPPORTED;
+  st = check_paged(block_table, max_blocks, pool_k, pool_v, n_blocks, n_questions);
+  if (st != KEV_OK) return st;
+  if (dev_status && ((uintptr_t)dev_status & 3u)) return KEV_ERR_INVALID_ARG;
+  if (n_questions == 0) {
+    if (dev_status) return from_cuda(cudaMemsetAsync(dev_status, 0, sizeof(int32_t), (cudaStream_t)stream));
+    return KEV_OK;
+  }
+  if (!q_new || !k_new || !v_new || !out || !lens || !active) return KEV_ERR_INVALID_ARG;
+  if (!aligned16(q_new) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(out) || ((uintptr_t)lens & 3u))
+    return KEV_ERR_INVALID_ARG;
+  const int32_t cap = max_blocks * kPage;
+  const DecodeLayout layout = decode_layout(n_questions, cap, shape->h_q, shape->h_kv, shape->d_h, true);
+  if (!workspace || ((uintptr_t)workspace & 255u) || workspace_bytes < layout.total) return KEV_ERR_INVALID_ARG;
+  const int sms = num_sms_of_current_device();
+  if (sms <= 0) return KEV_ERR_CUDA;
+  DecodeArgs a;
+  a.q_new = q_new;
+  a.k_new = k_new;
+  a.v_new = v_new;
+  a.pool_k = pool_k;
+  a.pool_v = pool_v;
+  a.slot_ids = nullptr;
+  a.lens = lens;
+  a.active = active;
+  a.out = out;
+  a.n = n_questions;
+  a.n_slots = 0;
+  a.cap = cap;
+  a.h_q = shape->h_q;
+  a.h_kv = shape->h_kv;
+  a.group = shape->h_q / shape->h_kv;
+  a.scale = effective_scale(shape);
+  a.ws = static_cast<char*>(workspace);
+  a.layout = layout;
+  a.dev_status = dev_status;
+  a.block_table = block_table;
+  a.max_blocks = max_blocks;
+  a.n_blocks = n_blocks;
+  return from_cuda(launch_decode_tc(a, sms, (cudaStream_t)stream));
+}
+
+int32_t kev_assign_blocks(const int32_t* need, int32_t n, uint8_t* free_map, int32_t n_blocks, int32_t* table,
+                          int32_t max_blocks, int32_t contiguous_first) {
+  if (n < 0 || n_blocks < 0 || max_blocks <= 0 || (n > 0 && (!need || !table)) || (n_blocks > 0 && !free_map))
+    return -1;
+  int64_t total = 0, avail = 0;
+  for (int32_t i = 0; i < n; ++i) {
+    if (need[i] < 0 || need[i] > max_blocks) return -1;
+    total += need[i];
+  }
+  for (int32_t b = 0; b < n_blocks; ++b) avail += free_map[b] != 0;
+  if (total > avail) return -1;  // every question can take its blocks one by one: no partial change
+  for (int32_t i = 0; i < n; ++i) {
+    int32_t* row = table + (int64_t)i * max_blocks;
+    for (int32_t c = 0; c < max_blocks; ++c) row[c] = -1;
+    const int32_t m = need[i];
+    if (m == 0) continue;
+    int32_t start = -1;
+    if (contiguous_first) {
+      int32_t run = 0;
+      for (int32_t b = 0; b < n_blocks; ++b) {
+        run = free_map[b] ? run + 1 : 0;
+        if (run == m) {
+          start = b - m + 1;
+          break;
+        }
+      }
+    }
+    if (start >= 0) {
+      for (int32_t c = 0; c < m; ++c) {
+        row[c] = start + c;
+        free_map[start + c] = 0;
+      }
+    } else {
+      int32_t c = 0;
+      for (int32_t b = 0; b < n_blocks && c < m; ++b)
+        if (free_map[b]) {
+          row[c++] = b;
+          free_map[b] = 0;
+        }
+    }
+  }
+  return 0;
+}
+
 size_t kev_rope_table_size(int32_t max_pos, int32_t d_h) {
   if (max_pos <= 0 || d_h <= 0 || (d_h & 1)) return 0;
   return sizeof(float2) * (size_t)max_pos * (size_t)(d_h / 2);
@@ -466,6 +671,9 @@ int32_t kev_launch_count(int32_t entry_point) {
     case 6: return 1;
     case 7: return 1;
     case 8: return 1;
+    case 9: return 4;
+    case 10: return 3;
+    case 11: return 2;
   }
   return -1;
 }

@@ -85,12 +85,46 @@ __device__ int prologue(const DecodeArgs& a, int n_hblocks, int* item_base, int2
                         int* scan_tmp, int* code_out = nullptr) {
   const int tid = threadIdx.x;
   const int n = a.n;
+  const bool paged = a.block_table != nullptr;
   int hs = 1;
-  while (hs < 2 * n) hs <<= 1;
+  // contiguous pool: a hash of the live slots; paged pool: of the blocks live questions use
+  // (n * max_blocks <= kMaxPagedEntries, checked on the host, so the caller's area holds it)
+  while (hs < 2 * (paged ? n * a.max_blocks : n)) hs <<= 1;
   if (tid == 0) *flags = 0;
   for (int j = tid; j < hs; j += NT) hash[j] = -1;
   __syncthreads();
-  for (int i = tid; i < n; i += NT) {
+  if (paged) {
+    // every live question needs a block for each page of positions 0..len (the new row
+    // included): a row too short is SLOT_OVERFLOW, an entry out of range or used twice SLOT
+    for (int i = tid; i < n; i += NT) {
+      const int len = a.lens[i];
+      meta[i] = make_int2(len, i);
+      if (a.active[i] && (len < 0 || len / kChunk >= a.max_blocks)) atomicOr(flags, 2);
+    }
+    const int64_t entries = (int64_t)n * a.max_blocks;
+    for (int64_t e = tid; e < entries; e += NT) {
+      const int i = (int)(e / a.max_blocks), b = (int)(e % a.max_blocks);
+      if (!a.active[i]) continue;
+      const int len = a.lens[i];
+      if (len < 0 || b > len / kChunk) continue;
+      const int blk = a.block_table[e];
+      if (blk < 0 || blk >= a.n_blocks) {
+        atomicOr(flags, 1);
+        continue;
+      }
+      unsigned h = ((unsigned)blk * 2654435761u) & (unsigned)(hs - 1);
+      for (int probe = 0; probe < hs; ++probe) {
+        const int prev = atomicCAS(&hash[h], -1, blk);
+        if (prev == -1) break;
+        if (prev == blk) {
+          atomicOr(flags, 4);
+          break;
+        }
+        h = (h + 1) & (unsigned)(hs - 1);
+      }
+    }
+  }
+  for (int i = tid; i < n && !paged; i += NT) {
     const int live = a.active[i];
     const int slot = a.slot_ids[i];
     const int len = a.lens[i];
@@ -114,7 +148,8 @@ __device__ int prologue(const DecodeArgs& a, int n_hblocks, int* item_base, int2
   }
   __syncthreads();
   const int f = *flags;
-  const int code = (f & 1) ? ST_SLOT : (f & 2) ? ST_OVERFLOW : (f & 4) ? ST_SLOT : ST_OK;
+  const int code = paged ? ((f & 2) ? ST_OVERFLOW : (f & 5) ? ST_SLOT : ST_OK)
+                         : ((f & 1) ? ST_SLOT : (f & 2) ? ST_OVERFLOW : (f & 4) ? ST_SLOT : ST_OK);
   if (blockIdx.x == 0 && tid == 0) {
     if (a.dev_status) *a.dev_status = code;
     if (code_out) *code_out = code;

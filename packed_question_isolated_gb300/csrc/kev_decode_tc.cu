@@ -57,7 +57,8 @@ struct DTcParams {
 
 // What the producer knows about the chunk in a stage; the consumers read it from here.
 struct StageInfo {
-  int i, g, c, nch, len, slot;
+  int i, g, c, nch, len;
+  int row0;   // pool row (of the [rows, d] view) of the chunk's first position for kv head g
   int xi0;    // global index of chunk 0 of this (question, kv head)
   int flags;  // kFirst / kLast of a piece, kFix: holds position n, kEnd: no more chunks
 };
@@ -309,9 +310,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
             if (x == x0 || u.c == 0) flags |= kFirst;
             if (x == x1 - 1 || u.c == u.nch - 1) flags |= kLast;
             if (u.c == u.nch - 1) flags |= kFix;
-            info[s] = StageInfo{u.i, u.g, u.c, u.nch, u.len, u.slot, x - u.c, flags};
+            // contiguous pool: slot row block; paged pool: the chunk is one block (its table entry)
+            const int row0 = a.block_table ? (a.block_table[(int64_t)u.i * a.max_blocks + u.c] * a.h_kv + u.g) * kC
+                                           : (u.slot * a.h_kv + u.g) * a.cap + u.c * kC;
+            info[s] = StageInfo{u.i, u.g, u.c, u.nch, u.len, row0, x - u.c, flags};
             unsigned char* st = smem + L::kStage + s * L::kStageBytes;
-            const int row0 = (u.slot * a.h_kv + u.g) * a.cap + u.c * kC;
             const int qrow = u.i * a.h_q + u.g * a.group;
             mbar_arrive_expect_tx(&bars->full[s], L::kStageBytes);  // release: info[s] is visible with the phase
             for (int c = 0; c < 2; ++c) {
@@ -470,7 +473,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
           // but stale pool contents could hold NaN bit patterns)
           const int rn = inf.len - p0;
           const int64_t src = ((int64_t)inf.i * a.h_kv + inf.g) * kD * 2;
-          const int64_t dst = (((int64_t)inf.slot * a.h_kv + inf.g) * a.cap + inf.len) * kD * 2;
+          const int64_t dst = ((int64_t)inf.row0 + rn) * kD * 2;  // the new row's pool row
           if (sid < 32) {
             const int ch = sid & 15;  // 16-byte chunk of the 256-byte row
             const bool isv = sid >= 16;
@@ -817,7 +820,7 @@ cudaError_t launch_decode_tc(const DecodeArgs& a, int num_sms, cudaStream_t st) 
   static_assert(kDecodeTcMaxGroup == kN, "one MMA covers the q-heads of a group");
   if (a.group < 1 || a.group > kDecodeTcMaxGroup) return cudaErrorInvalidValue;
   CUtensorMap mk, mv, mq;
-  const uint64_t pool_rows = (uint64_t)a.n_slots * a.h_kv * a.cap;
+  const uint64_t pool_rows = a.block_table ? (uint64_t)a.n_blocks * a.h_kv * kC : (uint64_t)a.n_slots * a.h_kv * a.cap;
   if (!make_map(&mk, a.pool_k, pool_rows, kC) || !make_map(&mv, a.pool_v, pool_rows, kC) ||
       !make_map(&mq, a.q_new, (uint64_t)a.n * a.h_q, kN))
     return cudaErrorInvalidValue;

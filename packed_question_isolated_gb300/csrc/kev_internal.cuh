@@ -164,12 +164,14 @@ struct AuxArgs {  // slot write + zero rows of tokens in no question
   int32_t h_kv;
   int32_t cap;
   int32_t n_slots;
+  const int32_t* block_table = nullptr;  // paged pool (null: contiguous slots): see DecodeArgs
+  int32_t max_blocks = 0;
   int32_t row_bytes;  // d * element size
   const char* ws;
   PrefillLayout layout;
   // launched right after an attention kernel that waited for the segment builder before letting
   // this grid start: run alongside its tail, wait for it at the end
-  bool after_attention;
+  bool after_attention = false;
 };
 
 struct DecodeArgs {
@@ -192,6 +194,11 @@ struct DecodeArgs {
   char* ws;
   DecodeLayout layout;
   int32_t* dev_status;
+  // paged pool (null: the contiguous [n_slots, H_kv, cap, d] pool): pool [n_blocks, H_kv, kPage, d],
+  // position p of question i in block block_table[i * max_blocks + p / kPage]; cap = max_blocks * kPage
+  const int32_t* block_table = nullptr;
+  int32_t max_blocks = 0;
+  int32_t n_blocks = 0;
 };
 
 // Host-side launchers (each returns the launch's cudaError_t).
@@ -199,6 +206,21 @@ cudaError_t launch_segments(const SegmentsArgs& a, cudaStream_t s);
 cudaError_t launch_prefill_simt(const PrefillArgs& a, int d, int num_sms, cudaStream_t s);  // fp32
 cudaError_t launch_prefill_tc(const PrefillArgs& a, int d, int num_sms, cudaStream_t s);    // bf16
 cudaError_t launch_aux(const AuxArgs& a, int num_sms, cudaStream_t s);
+
+// ---------------------------------------------------------------------------------------
+// paged slot pool (kev_paged.cu)
+// ---------------------------------------------------------------------------------------
+constexpr int kPage = 128;                  // positions per block (= a decode chunk, a prefill tile)
+constexpr int kMaxPagedEntries = 16384;     // n_questions * max_blocks: the validation's hash capacity
+static_assert(kPage == KEV_PAGE && kMaxPagedEntries == KEV_MAX_PAGED_ENTRIES, "kev.h and the kernels agree");
+struct PagedCheckArgs {                     // prefill side: the block tables of the questions' lengths
+  const kev_interval* intervals;
+  const int32_t* block_table;
+  int32_t n, max_blocks, n_blocks;
+  char* ws;  // prefill workspace: the header's status word is set on an error
+  int32_t* dev_status;
+};
+cudaError_t launch_paged_check(const PagedCheckArgs& a, cudaStream_t s);
 
 // ---------------------------------------------------------------------------------------
 // rotary position encoding (kev_rope.cu)

@@ -3,7 +3,9 @@
 // Slot pool of the Kev pipeline article (gsyq.cn news 368355, §2.2): a preallocated pool
 // cut into fixed-size slots, one per question.  Question i's rows are copied bit for bit:
 //   pool_{k,v}[slot_i, g, j, :] = {k,v}[begin_i + j, g, :]    for j < L_i.
-// Positions >= L_i and slots no question uses are not touched.
+// Positions >= L_i and slots no question uses are not touched.  With a paged pool (block
+// table, inference-engine notes §2.5) position j of question i goes to block
+// block_table[i][j / 128], row j % 128 (n_slots then counts blocks).
 //
 // Tokens outside every interval (boundary / padding tokens between questions) are keys for
 // nobody (the article's §4.1 PAD-leak fix) and their own output rows are written as 0.
@@ -46,13 +48,16 @@ __global__ void __launch_bounds__(kAuxThreads) aux_kernel(AuxArgs a) {
   const PrefillHeader* hdr = reinterpret_cast<const PrefillHeader*>(a.ws);
   const int32_t* cu = reinterpret_cast<const int32_t*>(a.ws + a.layout.cu_seqlens);
   if (threadIdx.x == 0) s_ok = hdr->status == ST_OK;
-  if (a.slot_ids) {
+  const bool paged = a.block_table != nullptr;
+  const bool to_pool = a.slot_ids != nullptr || paged;
+  if (to_pool) {
     for (int i = threadIdx.x; i <= a.n; i += blockDim.x) s_cu[i] = cu[i];
-    for (int i = threadIdx.x; i < a.n; i += blockDim.x) s_bs[i] = make_int2(a.intervals[i].begin, a.slot_ids[i]);
+    for (int i = threadIdx.x; i < a.n; i += blockDim.x)
+      s_bs[i] = make_int2(a.intervals[i].begin, paged ? i : a.slot_ids[i]);
   }
   __syncthreads();
 
-  if (s_ok && a.slot_ids) {
+  if (s_ok && to_pool) {
     const int vpr = a.row_bytes / 16;  // 16-byte vectors per row of one head (8, 16 or 32)
     const int upp = 32 / vpr;          // units per warp pass
     const int lane = threadIdx.x & 31, sub = lane / vpr, v = lane % vpr;
@@ -76,9 +81,16 @@ __global__ void __launch_bounds__(kAuxThreads) aux_kernel(AuxArgs a) {
           const int i = question_of(s_cu, a.n, r);
           const int j = r - s_cu[i];
           const int2 bs = s_bs[i];
-          if (bs.y < 0 || bs.y >= a.n_slots || j >= a.cap) continue;  // a work list built for other slots
           const int64_t src = ((int64_t)(bs.x + j) * a.h_kv + g) * vpr + v;
-          dst[t] = (((int64_t)bs.y * a.h_kv + g) * a.cap + j) * vpr + v;
+          if (paged) {  // block of position j (the tables were checked before the attention)
+            if (j / kPage >= a.max_blocks) continue;
+            const int blk = a.block_table[(int64_t)bs.y * a.max_blocks + j / kPage];
+            if (blk < 0 || blk >= a.n_slots) continue;
+            dst[t] = (((int64_t)blk * a.h_kv + g) * kPage + j % kPage) * vpr + v;
+          } else {
+            if (bs.y < 0 || bs.y >= a.n_slots || j >= a.cap) continue;  // a work list built for other slots
+            dst[t] = (((int64_t)bs.y * a.h_kv + g) * a.cap + j) * vpr + v;
+          }
           bk[t] = __ldg(k + src);
           bv[t] = __ldg(vv + src);
         }
@@ -111,7 +123,9 @@ __global__ void __launch_bounds__(kAuxThreads) aux_kernel(AuxArgs a) {
 }  // namespace
 
 cudaError_t launch_aux(const AuxArgs& a, int num_sms, cudaStream_t s) {
-  const size_t smem = a.slot_ids ? sizeof(int32_t) * (size_t)((a.n + 2) & ~1) + sizeof(int2) * (size_t)a.n : 0;
+  const size_t smem = a.slot_ids || a.block_table
+                          ? sizeof(int32_t) * (size_t)((a.n + 2) & ~1) + sizeof(int2) * (size_t)a.n
+                          : 0;
   if (smem > 48 * 1024) {
     const cudaError_t e = cudaFuncSetAttribute(aux_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;

@@ -4,6 +4,7 @@ import ctypes
 import os
 import re
 
+import numpy as np
 import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
@@ -36,8 +37,8 @@ def test_status_strings_and_launch_counts(lib):
     for code in range(9):
         assert lib.kev_status_string(code) != "unknown status"
     assert lib.kev_status_string(99) == "unknown status"
-    assert lib.kev_launch_count(0) == 3 and lib.kev_launch_count(4) == 1 and lib.kev_launch_count(9) == -1
-    assert [lib.kev_launch_count(i) for i in (6, 7, 8)] == [1, 1, 1]
+    assert lib.kev_launch_count(0) == 3 and lib.kev_launch_count(4) == 1 and lib.kev_launch_count(99) == -1
+    assert [lib.kev_launch_count(i) for i in (6, 7, 8, 9, 10, 11)] == [1, 1, 1, 4, 3, 2]
 
 
 def test_workspace_sizes(lib):
@@ -91,3 +92,39 @@ def test_rope_table_size_and_host_errors_without_gpu(lib):
     assert lib.kev_decode_attn_rope(0x1000, 0x1000, 0x1000, 0x1000, 0x1000, 1, 64, 0x1000, 0x1000, 0x1000, 1,
                                     0x1000, s, 0x1000, 32, 0x1000, 1 << 20, None, stream=0, check=False) == \
         b.KEV_ERR_INVALID_ARG
+
+
+def test_assign_blocks_matches_the_oracle(lib):
+    """Host logic, no GPU: the library's contiguous-first block assignment against the oracle's."""
+    from oracle import kev_oracle as O
+    free = np.array([1, 1, 0, 1, 1, 1, 0, 1], np.uint8)
+    assert lib.kev_assign_blocks([2, 2, 2], free, 3).tolist() == [[0, 1, -1], [3, 4, -1], [5, 7, -1]]
+    assert not free.any()
+    rng = np.random.default_rng(1)
+    for it in range(300):
+        fr = rng.random(64) < 0.6
+        need = rng.integers(0, 6, 8)
+        cf = bool(it % 2)
+        ref = O.assign_blocks(need, fr, 5, contiguous_first=cf)
+        fm = fr.astype(np.uint8)
+        got = lib.kev_assign_blocks(need, fm, 5, contiguous_first=cf)
+        if ref is None:
+            assert got is None and (fm.astype(bool) == fr).all()  # nothing taken on failure
+        else:
+            np.testing.assert_array_equal(got, ref[0])
+            np.testing.assert_array_equal(fm.astype(bool), ref[1])
+
+
+def test_paged_host_errors_without_gpu(lib):
+    b = lib.binding
+    s = lib.make_shape(4, 2, 128, "bf16")
+    # no table, a misaligned table, too many entries, a decode shape off the tensor cores
+    assert lib.kev_prefill_attn_paged(0x1000, 0x1000, 0x1000, 10, 0x1000, 1, None, 4, 0x1000, 0x1000, 8, 0x1000, s,
+                                      0x1000, 1 << 20, None, stream=0, check=False) == b.KEV_ERR_INVALID_ARG
+    assert lib.kev_kv_write_paged(0x1000, 0x1000, 10, 0x1000, 1, 0x1002, 4, 0x1000, 0x1000, 8, s, 0x1000, 1 << 20,
+                                  None, stream=0, check=False) == b.KEV_ERR_INVALID_ARG
+    assert lib.kev_decode_attn_paged(0x1000, 0x1000, 0x1000, 0x1000, 0x1000, 8, 0x1000, 20000, 0x1000, 0x1000, 1,
+                                     0x1000, s, 0x1000, 1 << 20, None, stream=0, check=False) == b.KEV_ERR_UNSUPPORTED
+    assert lib.kev_decode_attn_paged(0x1000, 0x1000, 0x1000, 0x1000, 0x1000, 8, 0x1000, 4, 0x1000, 0x1000, 1,
+                                     0x1000, lib.make_shape(4, 2, 64, "bf16"), 0x1000, 1 << 20, None, stream=0,
+                                     check=False) == b.KEV_ERR_UNSUPPORTED
