@@ -372,6 +372,66 @@ def _rope_step(kev, torch, w, shape, copies, step_buffers, ws_bytes, dws_bytes, 
                          "launch_ms": rope_ms, "traffic": _traffic("rope")}}
 
 
+def _paged_decode(kev, torch, tdev, dev, K, warmup):
+    """The decode workload over a paged pool (128-position blocks, block tables from the library's
+    host assignment): contiguous-first tables on an empty pool, and scattered tables (a pool with
+    every other block taken); calls back to back over two pool sets."""
+    dw = W.qwen3_8b_decode()
+    N, h_q, h_kv, d, page = dw.n_questions, dw.h_q, dw.h_kv, dw.d, kev.binding.KEV_PAGE
+    shape = kev.make_shape(h_q, h_kv, d, "bf16")
+    lens = np.asarray(dw.lens)
+    live = np.asarray(dw.active).astype(bool)
+    need = np.array([(int(n) + 1 + page - 1) // page if a else 0 for n, a in zip(lens, live)], np.int32)
+    max_blocks = (dw.cap + page - 1) // page
+    dec_bytes = RL.decode_bytes(dw.lens, dw.active, h_q, h_kv, d, 2)
+    out = {"workload": DECODE_WORKLOAD + ", copied into 128-position blocks", "unit": "GB/s"}
+    for policy in ("contiguous_first", "scattered"):
+        if policy == "contiguous_first":
+            n_blocks = int(need.sum())
+            free = np.ones(n_blocks, np.uint8)
+        else:
+            n_blocks = 2 * int(need.sum())
+            free = (np.arange(n_blocks) % 2).astype(np.uint8)  # every other block already taken
+        table = kev.kev_assign_blocks(need, free, max_blocks, contiguous_first=(policy == "contiguous_first"))
+        pk = np.zeros((n_blocks, h_kv, page, d), np.uint16)
+        pv = np.zeros((n_blocks, h_kv, page, d), np.uint16)
+        for i in np.nonzero(live)[0]:
+            for b in range(int(need[i])):
+                rows = slice(b * page, min((b + 1) * page, dw.cap))
+                pk[table[i, b], :, :rows.stop - rows.start] = dw.pool_k[int(dw.slot_ids[i]), :, rows]
+                pv[table[i, b], :, :rows.stop - rows.start] = dw.pool_v[int(dw.slot_ids[i]), :, rows]
+        nb = kev.kev_decode_workspace_size(N, max_blocks * page, shape)
+        copies = []
+        for _ in range(DECODE_COPIES):
+            copies.append({"pk": tdev(pk), "pv": tdev(pv), "tb": tdev(table), "ln": tdev(lens.astype(np.int32)),
+                           "act": tdev(np.asarray(dw.active, np.uint8)), "q": tdev(dw.q_new), "k": tdev(dw.k_new),
+                           "v": tdev(dw.v_new),
+                           "out": torch.empty((N, h_q, d), dtype=torch.bfloat16, device=dev),
+                           "ws": torch.zeros(nb, dtype=torch.uint8, device=dev),
+                           "st": torch.zeros(1, dtype=torch.int32, device=dev)})
+        del pk, pv
+
+        def call(c):
+            kev.kev_decode_attn_paged(c["q"], c["k"], c["v"], c["pk"], c["pv"], n_blocks, c["tb"], max_blocks,
+                                      c["ln"], c["act"], N, c["out"], shape, c["ws"], nb, c["st"])
+
+        for _ in range(warmup):
+            for c in copies:
+                call(c)
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for s in range(K):
+            call(copies[s % DECODE_COPIES])
+        b.record()
+        torch.cuda.synchronize()
+        assert all(kev.kev_read_status(c["st"]) == 0 for c in copies)
+        ms = a.elapsed_time(b) / K
+        out[policy] = {"ms_per_step": ms, "value": dec_bytes / (ms * 1e-3) / 1e9, "n_blocks": n_blocks}
+        del copies
+    return out
+
+
 def _decode_setup(kev, torch, dev, tdev):
     """The decode workload's buffer sets (DECODE_COPIES of them) and its call."""
     dwl = W.qwen3_8b_decode()
@@ -587,6 +647,8 @@ def main(argv=None):
     dec_traffic = _traffic("decode")
     del dcopies
 
+    paged = _paged_decode(kev, torch, tdev, dev, Kd, args.warmup)
+
     # ---- second prefill workload (Qwen3-8B-shaped batch): measured, not the headline ---------
     # two buffer sets (each ~490 MB of q, k, v and output) used in turn, launches back to back
     w3 = W.qwen3_8b_prefill()
@@ -660,6 +722,7 @@ def main(argv=None):
                                  "ms_per_launch": p3_avg, "useful_gflop": useful3 / 1e9,
                                  "frac": p3_tf / tf_peak, "peak_source": f"bf16_tflops burst, {peak_src}"},
             "rope": rope,
+            "paged_decode": paged,
             "stress": stress,
             "cpu_baseline": cpu,
             "cpu_fair_baseline": cpu_fair,
