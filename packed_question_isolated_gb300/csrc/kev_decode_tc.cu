@@ -674,6 +674,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
 template <int NH>
 __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeArgs a) {
   pdl_wait();  // the decode grid is complete and visible
+  // the next kernel may be scheduled now: it waits for this grid before it touches memory
+  // (the next step's segment builder launches during the merge instead of after it)
+  pdl_trigger();
   int* sched = reinterpret_cast<int*>(a.ws + a.layout.sched);
   if (blockIdx.x == 0 && threadIdx.x == 0) sched[0] = 0;
   if (sched[2] != ST_OK) return;  // invalid call (or timeout): nothing to merge
