@@ -31,6 +31,9 @@ dense T x T mask, in float64:
   blocks allocated on demand, a block table records where each block is and
   attention reads K/V through it; Kev pipeline article, §4.3: blocks of one
   batch placed at neighbouring addresses first).
+* Chunked prefill into slots (inference-engine notes, §2.6: a long input is
+  prefilled in pieces that share rounds with decode steps, each later piece
+  using the K/V of the pieces before it).
 * Rotary position encoding with per-question positions (KV-cache isolation
   article, hnwysp.cn, §7.2: the rotation multiplies Q and K, a cached K
   keeps the rotation of its own position, and the new token's position is
@@ -60,6 +63,7 @@ from workloads import to_float64
 INTERVALS = "intervals"
 SLOT = "slot"
 SLOT_OVERFLOW = "slot_overflow"
+PREFIX = "prefix"
 
 
 # ---------------------------------------------------------------------------
@@ -514,3 +518,67 @@ def assign_blocks(need, free, max_blocks: int, contiguous_first: bool = True):
         table[i, :m] = pick
         fr[pick] = False
     return table, fr
+
+
+# ---------------------------------------------------------------------------
+# chunked prefill into slots
+# ---------------------------------------------------------------------------
+
+def validate_chunk(intervals, total_tokens, prefix_lens, slot_ids, n_slots, cap, align: int = PAGE):
+    """Return None if a chunked prefill is valid, else the error kind, in this order:
+    intervals (as ``validate_prefill``); a slot id outside [0, n_slots) -> SLOT; a cached
+    prefix length that is negative or not a multiple of ``align`` (the library's
+    restriction: chunks start on a tile boundary) -> PREFIX; prefix + chunk longer than the
+    slot -> SLOT_OVERFLOW; a slot shared by two non-empty chunks -> SLOT."""
+    err = validate_prefill(intervals, total_tokens)
+    if err is not None:
+        return err
+    iv = np.asarray(intervals, dtype=np.int64).reshape(-1, 2)
+    sl = np.asarray(slot_ids, dtype=np.int64)
+    pre = np.asarray(prefix_lens, dtype=np.int64)
+    L = iv[:, 1] - iv[:, 0]
+    if np.any((sl < 0) | (sl >= n_slots)):
+        return SLOT
+    if np.any((pre < 0) | (pre % align != 0)):
+        return PREFIX
+    if np.any(pre + L > cap):
+        return SLOT_OVERFLOW
+    used = sl[L > 0]
+    if len(np.unique(used)) != len(used):
+        return SLOT
+    return None
+
+
+def prefill_chunk(q, k, v, intervals, prefix_lens, slot_ids, pool_k, pool_v, dtype: str, scale=None):
+    """Chunked prefill into slots.  Question i's chunk is packed tokens [s_i, e_i): its
+    positions P_i .. P_i + L_i - 1, after the P_i = prefix_lens[i] positions already in slot
+    slot_ids[i].  The chunk's K/V rows go into the slot first (positions P_i + j, bit copies),
+    then token s_i + j attends to positions 0 .. P_i + j of its slot: the cached prefix and its
+    own chunk causally, nothing of another question.  Rows of tokens in no chunk are 0.
+
+    ``q``/``k``/``v`` and the pools are stored arrays of ``dtype``.  Returns (out [T, H_q, d]
+    float64, pool_k', pool_v')."""
+    pk = np.array(pool_k, copy=True)
+    pv = np.array(pool_v, copy=True)
+    q = np.asarray(q)
+    T, h_q, d = q.shape
+    h_kv = np.asarray(k).shape[1]
+    G = _group(h_q, h_kv)
+    sc = _scale(scale, d)
+    out = np.zeros((T, h_q, d), dtype=np.float64)
+    for (s, e), P, slot in zip(np.asarray(intervals).reshape(-1, 2), np.asarray(prefix_lens), np.asarray(slot_ids)):
+        s, e, P, slot = int(s), int(e), int(P), int(slot)
+        L = e - s
+        if L <= 0:
+            continue
+        pk[slot, :, P:P + L, :] = np.swapaxes(np.asarray(k)[s:e], 0, 1)
+        pv[slot, :, P:P + L, :] = np.swapaxes(np.asarray(v)[s:e], 0, 1)
+        allowed = np.arange(P + L)[None, :] <= (P + np.arange(L))[:, None]  # key u for chunk row j: u <= P + j
+        for h in range(h_q):
+            g = h // G
+            K = to_float64(pk[slot, g, :P + L, :], dtype)
+            V = to_float64(pv[slot, g, :P + L, :], dtype)
+            Q = to_float64(q[s:e, h], dtype)
+            scores = np.where(allowed, (Q @ K.T) * sc, -np.inf)
+            out[s:e, h] = softmax_rows(scores) @ V
+    return out, pk, pv

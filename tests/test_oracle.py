@@ -656,3 +656,81 @@ def test_assign_blocks_contiguous_first_example_and_invariants():
         assert (table[np.arange(5)[None, :] >= need[:, None]] == -1).all()
         assert sorted(np.nonzero(free & ~fr)[0].tolist()) == sorted(used)
         assert O.validate_paged(need * O.PAGE, table, 64) is None
+
+
+# ---------------------------------------------------------------------------
+# chunked prefill into slots (inference-engine notes, sakurs2.com, §2.6)
+# ---------------------------------------------------------------------------
+
+def _chunk_case(seed, lengths, h_q=4, h_kv=2, d=8):
+    rng = np.random.default_rng(seed)
+    iv = W.pack_intervals(lengths, gaps=[1] * len(lengths))
+    T = int(iv[-1, 1])
+    q, k, v = (rng.standard_normal((T, h, d)) for h in (h_q, h_kv, h_kv))
+    return iv, q, k, v
+
+
+def test_chunk_with_empty_prefixes_is_the_plain_prefill():
+    lengths = [30, 17, 0, 45]
+    iv, q, k, v = _chunk_case(1, lengths)
+    n, cap = len(lengths), 64
+    pool = np.full((n + 1, 2, cap, 8), -3.0)
+    slots = np.array([2, 0, 4, 1])
+    out, pk, pv = O.prefill_chunk(q, k, v, iv, np.zeros(n, int), slots, pool, pool, "fp64")
+    np.testing.assert_allclose(out, O.prefill(q, k, v, iv), rtol=0, atol=1e-12)
+    ek, ev = O.slot_write(pool, pool, k, v, iv, slots)
+    np.testing.assert_array_equal(pk, ek)
+    np.testing.assert_array_equal(pv, ev)
+
+
+@pytest.mark.parametrize("split", [1, 7, 20, 29])
+def test_chunks_in_sequence_equal_one_prefill(split):
+    """A question prefilled as chunk [0, split) then chunk [split, L) with prefix = split gives the
+    one-shot prefill's rows and the same slot contents."""
+    L = 30
+    iv, q, k, v = _chunk_case(2, [L])
+    s = int(iv[0, 0])
+    full = O.prefill(q, k, v, iv)
+    pool = np.zeros((1, 2, 40, 8))
+    a_iv = np.array([[s, s + split]])
+    out1, pk, pv = O.prefill_chunk(q, k, v, a_iv, [0], [0], pool, pool, "fp64")
+    b_iv = np.array([[s + split, s + L]])
+    out2, pk, pv = O.prefill_chunk(q, k, v, b_iv, [split], [0], pk, pv, "fp64")
+    np.testing.assert_allclose(out1[s:s + split], full[s:s + split], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(out2[s + split:s + L], full[s + split:s + L], rtol=0, atol=1e-12)
+    ek, ev = O.slot_write(pool, pool, k, v, iv, [0])
+    np.testing.assert_array_equal(pk, ek)
+    np.testing.assert_array_equal(pv, ev)
+
+
+def test_one_token_chunk_is_a_decode_step():
+    rng = np.random.default_rng(3)
+    n, h_q, h_kv, d, cap = 3, 4, 2, 8, 32
+    pool_k = rng.standard_normal((n, h_kv, cap, d))
+    pool_v = rng.standard_normal((n, h_kv, cap, d))
+    prefix = np.array([5, 0, 17])
+    q, k, v = (rng.standard_normal((n, h, d)) for h in (h_q, h_kv, h_kv))
+    iv = np.array([[0, 1], [1, 2], [2, 3]])
+    slots = np.array([1, 2, 0])
+    out, pk, pv = O.prefill_chunk(q, k, v, iv, prefix, slots, pool_k, pool_v, "fp64")
+    o, dk, dv = O.decode(q, k, v, pool_k, pool_v, slots, prefix, np.ones(n), "fp64")
+    np.testing.assert_allclose(out, o, rtol=0, atol=1e-12)
+    np.testing.assert_array_equal(pk, dk)
+    np.testing.assert_array_equal(pv, dv)
+
+
+def test_validate_chunk_cases():
+    iv = np.array([[0, 100], [100, 100], [105, 300]])
+    ok = dict(total_tokens=300, slot_ids=[0, 1, 2], n_slots=3, cap=512)
+    assert O.validate_chunk(iv, prefix_lens=[0, 0, 256], **ok) is None
+    assert O.validate_chunk(iv, prefix_lens=[0, 0, 100], **ok) == O.PREFIX       # not on a tile boundary
+    assert O.validate_chunk(iv, prefix_lens=[-128, 0, 0], **ok) == O.PREFIX
+    assert O.validate_chunk(iv, prefix_lens=[0, 0, 384], **ok) == O.SLOT_OVERFLOW  # 384 + 195 > 512
+    assert O.validate_chunk(iv, prefix_lens=[0, 0, 0], total_tokens=300, slot_ids=[0, 0, 2], n_slots=3,
+                            cap=512) is None  # the empty chunk's slot is not used
+    assert O.validate_chunk(iv, prefix_lens=[0, 0, 0], total_tokens=300, slot_ids=[2, 1, 2], n_slots=3,
+                            cap=512) == O.SLOT
+    assert O.validate_chunk(iv, prefix_lens=[0, 0, 0], total_tokens=300, slot_ids=[0, 1, 3], n_slots=3,
+                            cap=512) == O.SLOT
+    assert O.validate_chunk(np.array([[0, 100], [50, 120]]), 300, prefix_lens=[0, 0], slot_ids=[0, 1], n_slots=3,
+                            cap=512) == O.INTERVALS
