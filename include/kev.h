@@ -59,7 +59,8 @@ typedef enum {
   KEV_ERR_SLOT_OVERFLOW = 5, /* (device) a question longer than slot_cap, or no room for a decode row */
   KEV_ERR_TIMEOUT = 6,       /* (device) a bounded wait inside a kernel gave up; outputs are invalid */
   KEV_ERR_CUDA = 7,          /* a CUDA runtime call failed (launch error, no device, ...) */
-  KEV_ERR_POSITION = 8       /* (device) a position at or past the RoPE table's max_pos */
+  KEV_ERR_POSITION = 8,      /* (device) a position at or past the RoPE table's max_pos */
+  KEV_ERR_PREFIX = 9         /* (device) a cached prefix length negative or not a multiple of 128 */
 } kev_status;
 
 typedef enum { KEV_BF16 = 0, KEV_FP32 = 1 } kev_dtype;
@@ -203,6 +204,32 @@ kev_status kev_decode_attn_static(const void* q_new, const void* k_new, const vo
 kev_status kev_decode_advance(int32_t* lens, const uint8_t* active, int32_t n, kev_stream_t stream);
 
 /* ---------------------------------------------------------------------------------------
+ * Chunked prefill into slots
+ *
+ * Inference-engine notes (sakurs2.com), §2.6: a long input is prefilled in pieces that share
+ * rounds with decode steps, each later piece using the K/V of the pieces before it.  Question
+ * i's chunk is packed tokens [begin_i, end_i): its positions P_i .. P_i + L_i - 1 after the
+ * P_i = prefix_lens[i] positions already in slot slot_ids[i].  The chunk's K/V rows go into the
+ * slot first, then token begin_i + j attends to positions 0 .. P_i + j of its slot (the cached
+ * prefix, and its own chunk causally):
+ *   out[begin_i + j, h] = softmax_u(scale q . pool_k[slot_i, g, u]) pool_v[slot_i, g, u],  u <= P_i + j
+ * ------------------------------------------------------------------------------------- */
+
+/* Chunked prefill: segment build, slot write, attention.  bf16 only, slot_cap a multiple of 128
+ * (else KEV_ERR_UNSUPPORTED); prefix_lens: device int32[n_questions], each a multiple of 128
+ * (chunks start on a 128-row tile; else KEV_ERR_PREFIX) with P_i + L_i <= slot_cap (else
+ * KEV_ERR_SLOT_OVERFLOW); slots as for kev_prefill_attn (required here).  Besides positions
+ * P_i .. P_i + L_i - 1, the slot rows from P_i + L_i up to the next multiple of 128 are set to
+ * zero (they hold no position yet; the attention's last key tile reads them).  Rows of tokens in
+ * no interval are written as zeros.  A decode step is the one-token chunk at P_i = lens_i
+ * without the alignment; use kev_decode_attn for it. */
+kev_status kev_prefill_chunk(const void* q, const void* k, const void* v, int32_t total_tokens,
+                             const kev_interval* intervals, int32_t n_questions, const int32_t* prefix_lens,
+                             const int32_t* slot_ids, void* pool_k, void* pool_v, int32_t n_slots, int32_t slot_cap,
+                             void* out, const kev_attn_shape* shape, void* workspace, size_t workspace_bytes,
+                             int32_t* dev_status, kev_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------
  * Paged slot pool
  *
  * Inference-engine notes (sakurs2.com), §2.5: K/V are kept in fixed-size blocks taken on
@@ -334,7 +361,8 @@ const char* kev_status_string(kev_status status);
  * d_h = 128, decode and merge kernels; 1 otherwise and before any call), 5 = decode_advance,
  * 6 = rope_table, 7 = rope_prefill, 8 = rope_decode (1 each), 9 = prefill_attn_paged (4:
  * segments, table check, attention, paged write), 10 = kv_write_paged (3), 11 =
- * decode_attn_paged (2).  -1 for an unknown id. */
+ * decode_attn_paged (2), 12 = prefill_chunk (3: segments, slot write, attention).  -1 for an
+ * unknown id. */
 int32_t kev_launch_count(int32_t entry_point);
 
 #ifdef __cplusplus

@@ -31,6 +31,7 @@ KEV_ERR_SLOT_OVERFLOW = 5
 KEV_ERR_TIMEOUT = 6
 KEV_ERR_CUDA = 7
 KEV_ERR_POSITION = 8
+KEV_ERR_PREFIX = 9
 KEV_BF16 = 0
 KEV_FP32 = 1
 KEV_PAGE = 128
@@ -39,7 +40,7 @@ KEV_MAX_PAGED_ENTRIES = 16384
 STATUS_NAMES = {
     0: "KEV_OK", 1: "KEV_ERR_INVALID_ARG", 2: "KEV_ERR_UNSUPPORTED", 3: "KEV_ERR_INTERVALS",
     4: "KEV_ERR_SLOT", 5: "KEV_ERR_SLOT_OVERFLOW", 6: "KEV_ERR_TIMEOUT", 7: "KEV_ERR_CUDA",
-    8: "KEV_ERR_POSITION",
+    8: "KEV_ERR_POSITION", 9: "KEV_ERR_PREFIX",
 }
 
 # every symbol include/kev.h declares
@@ -50,7 +51,7 @@ EXPORTED = [
     "kev_read_status", "kev_status_string", "kev_launch_count", "kev_decode_attn_static",
     "kev_rope_table_size", "kev_rope_table", "kev_rope_prefill", "kev_prefill_attn_rope", "kev_rope_decode",
     "kev_decode_attn_rope", "kev_prefill_attn_paged", "kev_kv_write_paged", "kev_decode_attn_paged",
-    "kev_assign_blocks",
+    "kev_assign_blocks", "kev_prefill_chunk",
 ]
 
 
@@ -112,6 +113,8 @@ _c = {
     "kev_decode_attn_paged": _sig("kev_decode_attn_paged", _I, _P, _P, _P, _P, _P, _I, _P, _I, _P, _P, _I, _P, _S,
                                   _P, _Z, _P, _P),
     "kev_assign_blocks": _sig("kev_assign_blocks", _I, _P, _I, _P, _I, _P, _I, _I),
+    "kev_prefill_chunk": _sig("kev_prefill_chunk", _I, _P, _P, _P, _I, _P, _I, _P, _P, _P, _P, _I, _I, _P, _S, _P,
+                              _Z, _P, _P),
 }
 
 
@@ -356,3 +359,14 @@ def kev_assign_blocks(need, free_map, max_blocks: int, contiguous_first: bool = 
         return None
     free_map[...] = fm.astype(np.asarray(free_map).dtype)
     return table
+
+
+def kev_prefill_chunk(q, k, v, total_tokens, intervals, n_questions, prefix_lens, slot_ids, pool_k, pool_v, n_slots,
+                      slot_cap, out, shape, workspace, workspace_bytes, dev_status=None, stream=None,
+                      check=True) -> int:
+    s = _shape(shape)
+    st = _c["kev_prefill_chunk"](_ptr(q), _ptr(k), _ptr(v), int(total_tokens), _ptr(intervals), int(n_questions),
+                                 _ptr(prefix_lens), _ptr(slot_ids), _ptr(pool_k), _ptr(pool_v), int(n_slots),
+                                 int(slot_cap), _ptr(out), ctypes.byref(s), _ptr(workspace), int(workspace_bytes),
+                                 _ptr(dev_status), _stream(stream))
+    return _check(st, "kev_prefill_chunk", check)

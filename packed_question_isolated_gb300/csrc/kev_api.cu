@@ -314,6 +314,75 @@ kev_status paged_prefill_tail(const void* q, const void* k, const void* v, int32
 
 }  // namespace
 
+kev_status kev_prefill_chunk(const void* q, const void* k, const void* v, int32_t total_tokens,
+                             const kev_interval* intervals, int32_t n_questions, const int32_t* prefix_lens,
+                             const int32_t* slot_ids, void* pool_k, void* pool_v, int32_t n_slots, int32_t slot_cap,
+                             void* out, const kev_attn_shape* shape, void* workspace, size_t workspace_bytes,
+                             int32_t* dev_status, kev_stream_t stream) {
+  kev_status st = check_prefill_common(total_tokens, intervals, n_questions, shape, workspace, workspace_bytes);
+  if (st != KEV_OK) return st;
+  if (shape->dtype != KEV_BF16 || slot_cap % kTileM != 0) return KEV_ERR_UNSUPPORTED;
+  if (total_tokens > 0 && (!q || !k || !v || !out || !aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)))
+    return KEV_ERR_INVALID_ARG;
+  if (!slot_ids || (n_questions > 0 && (!prefix_lens || ((uintptr_t)prefix_lens & 3u)))) return KEV_ERR_INVALID_ARG;
+  st = check_slots(slot_ids, pool_k, pool_v, n_slots, slot_cap, n_questions);
+  if (st != KEV_OK) return st;
+  if (dev_status && ((uintptr_t)dev_status & 3u)) return KEV_ERR_INVALID_ARG;
+  const int sms = num_sms_of_current_device();
+  if (sms <= 0) return KEV_ERR_CUDA;
+  const cudaStream_t s = (cudaStream_t)stream;
+  // 1. segments, with the prefixes (validation, costs)
+  SegmentsArgs sa = segments_args(intervals, n_questions, total_tokens, slot_ids, n_slots, slot_cap, shape, workspace,
+                                  dev_status);
+  sa.prefix_lens = prefix_lens;
+  if (launch_segments(sa, s) != cudaSuccess) return KEV_ERR_CUDA;
+  const PrefillLayout layout = prefill_layout(n_questions, total_tokens, shape->h_q);
+  // 2. the chunk's K/V rows into the slots (the attention reads them there), gap rows of out
+  AuxArgs x;
+  x.k = k;
+  x.v = v;
+  x.out = out;
+  x.intervals = intervals;
+  x.slot_ids = slot_ids;
+  x.pool_k = pool_k;
+  x.pool_v = pool_v;
+  x.n = n_questions;
+  x.T = total_tokens;
+  x.h_q = shape->h_q;
+  x.h_kv = shape->h_kv;
+  x.cap = slot_cap;
+  x.n_slots = n_slots;
+  x.prefix_lens = prefix_lens;
+  x.row_bytes = shape->d_h * elem_size(shape);
+  x.ws = static_cast<const char*>(workspace);
+  x.layout = layout;
+  x.after_attention = false;
+  if (launch_aux(x, sms, s) != cudaSuccess) return KEV_ERR_CUDA;
+  // 3. attention over each slot's prefix and the chunk
+  PrefillArgs p;
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.out = out;
+  p.intervals = intervals;
+  p.T = total_tokens;
+  p.n = n_questions;
+  p.h_q = shape->h_q;
+  p.h_kv = shape->h_kv;
+  p.group = shape->h_q / shape->h_kv;
+  p.scale = effective_scale(shape);
+  p.ws = static_cast<const char*>(workspace);
+  p.layout = layout;
+  p.dev_status = dev_status;
+  p.prefix_lens = prefix_lens;
+  p.slot_ids = slot_ids;
+  p.pool_k = pool_k;
+  p.pool_v = pool_v;
+  p.n_slots = n_slots;
+  p.cap = slot_cap;
+  return from_cuda(launch_prefill_tc(p, shape->d_h, sms, s));
+}
+
 kev_status kev_prefill_attn_paged(const void* q, const void* k, const void* v, int32_t total_tokens,
                                   const kev_interval* intervals, int32_t n_questions, const int32_t* block_table,
                                   int32_t max_blocks, void* pool_k, void* pool_v, int32_t n_blocks, void* out,
@@ -641,7 +710,7 @@ kev_status kev_read_status(const int32_t* dev_status, kev_stream_t stream) {
   if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return KEV_ERR_CUDA;
   int32_t h = 0;
   if (cudaMemcpy(&h, dev_status, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) return KEV_ERR_CUDA;
-  if (h < KEV_OK || h > KEV_ERR_POSITION) return KEV_ERR_CUDA;
+  if (h < KEV_OK || h > KEV_ERR_PREFIX) return KEV_ERR_CUDA;
   return (kev_status)h;
 }
 
@@ -656,6 +725,7 @@ const char* kev_status_string(kev_status s) {
     case KEV_ERR_TIMEOUT: return "a bounded device wait gave up";
     case KEV_ERR_CUDA: return "CUDA runtime error";
     case KEV_ERR_POSITION: return "a position at or past the RoPE table's max_pos";
+    case KEV_ERR_PREFIX: return "a cached prefix length negative or not a multiple of 128";
   }
   return "unknown status";
 }
@@ -674,6 +744,7 @@ int32_t kev_launch_count(int32_t entry_point) {
     case 9: return 4;
     case 10: return 3;
     case 11: return 2;
+    case 12: return 3;
   }
   return -1;
 }

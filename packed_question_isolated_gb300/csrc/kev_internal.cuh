@@ -29,6 +29,7 @@ enum : int32_t {
   ST_OVERFLOW = KEV_ERR_SLOT_OVERFLOW,
   ST_TIMEOUT = KEV_ERR_TIMEOUT,
   ST_POSITION = KEV_ERR_POSITION,
+  ST_PREFIX = KEV_ERR_PREFIX,
 };
 
 // ---------------------------------------------------------------------------------------
@@ -131,6 +132,7 @@ struct SegmentsArgs {
   char* ws;
   PrefillLayout layout;
   int32_t* dev_status;  // may be null
+  const int32_t* prefix_lens = nullptr;  // chunked prefill: cached positions before each chunk
 };
 
 struct PrefillArgs {
@@ -148,6 +150,14 @@ struct PrefillArgs {
   const char* ws;
   PrefillLayout layout;
   int32_t* dev_status;
+  // chunked prefill: keys and values come from the slots [n_slots, H_kv, cap, d], where the
+  // chunk's rows were written first; question i's queries sit at positions prefix_lens[i] + j
+  const int32_t* prefix_lens = nullptr;
+  const int32_t* slot_ids = nullptr;
+  const void* pool_k = nullptr;
+  const void* pool_v = nullptr;
+  int32_t n_slots = 0;
+  int32_t cap = 0;
 };
 
 struct AuxArgs {  // slot write + zero rows of tokens in no question
@@ -166,6 +176,8 @@ struct AuxArgs {  // slot write + zero rows of tokens in no question
   int32_t n_slots;
   const int32_t* block_table = nullptr;  // paged pool (null: contiguous slots): see DecodeArgs
   int32_t max_blocks = 0;
+  const int32_t* prefix_lens = nullptr;  // chunked prefill: chunk row j goes to slot position P_i + j,
+                                         // and the slot rows up to the next multiple of 128 are zeroed
   int32_t row_bytes;  // d * element size
   const char* ws;
   PrefillLayout layout;

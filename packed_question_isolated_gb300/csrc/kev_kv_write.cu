@@ -88,8 +88,9 @@ __global__ void __launch_bounds__(kAuxThreads) aux_kernel(AuxArgs a) {
             if (blk < 0 || blk >= a.n_slots) continue;
             dst[t] = (((int64_t)blk * a.h_kv + g) * kPage + j % kPage) * vpr + v;
           } else {
-            if (bs.y < 0 || bs.y >= a.n_slots || j >= a.cap) continue;  // a work list built for other slots
-            dst[t] = (((int64_t)bs.y * a.h_kv + g) * a.cap + j) * vpr + v;
+            const int pos = j + (a.prefix_lens ? a.prefix_lens[i] : 0);  // chunked prefill: after the prefix
+            if (bs.y < 0 || bs.y >= a.n_slots || pos >= a.cap) continue;  // a work list built for other slots
+            dst[t] = (((int64_t)bs.y * a.h_kv + g) * a.cap + pos) * vpr + v;
           }
           bk[t] = __ldg(k + src);
           bv[t] = __ldg(vv + src);
@@ -101,6 +102,25 @@ __global__ void __launch_bounds__(kAuxThreads) aux_kernel(AuxArgs a) {
           pk[dst[t]] = bk[t];
           pv[dst[t]] = bv[t];
         }
+      }
+    }
+  }
+  if (s_ok && a.prefix_lens && a.slot_ids) {
+    // chunked prefill: slot rows from the chunk's end up to the next multiple of 128 become zero
+    // (no position lives there yet, but the attention's last key tile of the chunk reads them)
+    const int vpr = a.row_bytes / 16;
+    for (int i = blockIdx.x; i < a.n; i += gridDim.x) {
+      const int L = s_cu[i + 1] - s_cu[i];
+      const int slot = s_bs[i].y;
+      if (L == 0 || slot < 0 || slot >= a.n_slots) continue;
+      const int p0 = a.prefix_lens[i] + L;
+      const int p1 = min(a.cap, (p0 + 127) / 128 * 128);
+      const int per_head = (p1 - p0) * vpr;
+      for (int w = threadIdx.x; w < per_head * a.h_kv; w += blockDim.x) {
+        const int g = w / per_head, r = w % per_head;
+        const int64_t dst = (((int64_t)slot * a.h_kv + g) * a.cap + p0) * vpr + r;
+        reinterpret_cast<int4*>(a.pool_k)[dst] = make_int4(0, 0, 0, 0);
+        reinterpret_cast<int4*>(a.pool_v)[dst] = make_int4(0, 0, 0, 0);
       }
     }
   }

@@ -74,6 +74,11 @@ struct TcParams {
   float scale_log2;  // scale * log2(e)
   int32_t* dev_status;
   long long wait_budget;  // cycles per bounded wait
+  // chunked prefill: K/V from the slots (the maps tm_k / tm_v are the pools' [rows, D] views)
+  const int32_t* prefix_lens;
+  const int32_t* slot_ids;
+  int32_t h_kv;
+  int32_t cap;
 };
 
 template <int D>
@@ -122,6 +127,7 @@ struct Item {
   bool two;  // tiles A and B are consecutive query tiles of one q-head (else: one tile, heads h0, h0+1)
   int row0a, rowsa, nkva;  // tile A: first row, rows, key tiles
   int row0b, rowsb, nkvb;  // tile B
+  int kv_row0;             // chunked prefill: pool row of position 0 of the question's slot, kv head
   __device__ int row0_of(int t) const { return t ? row0b : row0a; }
   __device__ int rows_of(int t) const { return t ? rowsb : rowsa; }
   __device__ int head_of(int t) const { return two ? h0 : h0 + t; }
@@ -155,12 +161,28 @@ __device__ __forceinline__ Item load_item(const int4* items, const kev_interval*
   return x;
 }
 
+// Work item of the kernel instance: a chunk's query tiles sit after the prefix_lens[q] cached
+// positions of its slot (a multiple of the tile), so every tile has that many more key tiles, the
+// last one still the diagonal one; its keys and values are rows of the slot.
+template <bool kChunk>
+__device__ __forceinline__ Item load_work(const int4* items, const TcParams& p, int it) {
+  Item x = load_item(items, p.intervals, it);
+  if (kChunk) {
+    const int pt = p.prefix_lens[x.q] / kBM;
+    x.nkva += pt;
+    x.nkvb += pt;
+    x.nkv += pt;
+    x.kv_row0 = (p.slot_ids[x.q] * p.h_kv + x.h0 / p.group) * p.cap;
+  }
+  return x;
+}
+
 // Item order of a CTA: in round r it takes item r*G + b (r even) or r*G + G-1-b (r odd) of the
 // longest-first list (G = grid size, b = its index), so a CTA that took one of the longest items
 // of a round takes one of the shortest of the next; all roles walk the same sequence.
 __device__ __forceinline__ int snake_item(int r, int b, int G) { return r * G + ((r & 1) ? G - 1 - b : b); }
 
-template <int D>
+template <int D, bool kChunk>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_out,
@@ -227,11 +249,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t seq = 0;  // ring sequence: 2 ki is K(ki), 2 ki + 1 is V(ki)
       uint32_t loads[kRingSlots] = {};
       bool ok = true;
-      Item x_next = load_item(items, p.intervals, blockIdx.x);
+      Item x_next = load_work<kChunk>(items, p, blockIdx.x);
       for (int rnd = 0, it = blockIdx.x; it < n_items && ok; it = snake_item(++rnd, blockIdx.x, gridDim.x)) {
         const Item x = x_next;  // loaded one item ahead: its latency hides behind this item
         const int it_next = snake_item(rnd + 1, blockIdx.x, gridDim.x);
-        if (it_next < n_items) x_next = load_item(items, p.intervals, it_next);
+        if (it_next < n_items) x_next = load_work<kChunk>(items, p, it_next);
         const int g = x.h0 / p.group;
         for (int j = 0; j < x.nkv && ok; ++j) {
           for (int is_v = 0; is_v < 2; ++is_v, ++seq) {
@@ -244,7 +266,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive_expect_tx(&bars->r_full[s], L::kTileBytes);
             for (int c = 0; c < L::kSub; ++c)
               tma_load_2d(smem + L::kRing + s * L::kTileBytes + c * L::kSubBytes, is_v ? &tm_v : &tm_k,
-                          g * D + c * 64, x.seg_begin + j * kBN, &bars->r_full[s]);
+                          kChunk ? c * 64 : g * D + c * 64, kChunk ? x.kv_row0 + j * kBN : x.seg_begin + j * kBN,
+                          &bars->r_full[s]);
             ++loads[s];
           }
         }
@@ -260,11 +283,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       uint32_t n = 0, q_loads = 0;
       bool ok = true;
-      Item x_next = load_item(items, p.intervals, blockIdx.x);
+      Item x_next = load_work<kChunk>(items, p, blockIdx.x);
       for (int rnd = 0, it = blockIdx.x; it < n_items && ok; it = snake_item(++rnd, blockIdx.x, gridDim.x), ++n) {
         const Item x = x_next;
         const int it_next = snake_item(rnd + 1, blockIdx.x, gridDim.x);
-        if (it_next < n_items) x_next = load_item(items, p.intervals, it_next);
+        if (it_next < n_items) x_next = load_work<kChunk>(items, p, it_next);
         if (n > 0 && !mbar_wait(&bars->q_empty, (n - 1) & 1, abort_flag, budget)) {
           ok = false;
           break;
@@ -344,11 +367,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto slot = [](uint32_t q) { return (int)(q % kRingSlots); };
     auto phase = [](uint32_t q) { return (q / kRingSlots) & 1; };
 
-    Item x_next = load_item(items, p.intervals, blockIdx.x);
+    Item x_next = load_work<kChunk>(items, p, blockIdx.x);
     for (int rnd = 0, it = blockIdx.x; it < n_items; it = snake_item(++rnd, blockIdx.x, gridDim.x), ++n) {
       const Item x = x_next;  // loaded one item ahead: its latency hides behind this item
       const int it_next = snake_item(rnd + 1, blockIdx.x, gridDim.x);
-      if (it_next < n_items) x_next = load_item(items, p.intervals, it_next);
+      if (it_next < n_items) x_next = load_work<kChunk>(items, p, it_next);
       const bool mine = t < x.nh;
       // this tile's key tiles (an absent tile runs the item's steps, releasing stages only)
       const int nkv_t = mine ? x.nkv_of(t) : x.nkv;
@@ -424,11 +447,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
     const bool out32 = (reinterpret_cast<uintptr_t>(p.out) & 31) == 0;
 
-    Item x_next = load_item(items, p.intervals, blockIdx.x);
+    Item x_next = load_work<kChunk>(items, p, blockIdx.x);
     for (int rnd = 0, it = blockIdx.x; it < n_items && ok; it = snake_item(++rnd, blockIdx.x, gridDim.x)) {
       const Item x = x_next;  // loaded one item ahead: its latency hides behind this item
       const int it_next = snake_item(rnd + 1, blockIdx.x, gridDim.x);
-      if (it_next < n_items) x_next = load_item(items, p.intervals, it_next);
+      if (it_next < n_items) x_next = load_work<kChunk>(items, p, it_next);
       const bool full_a = x.rows_of(0) == kBM, full_b = x.nh == 2 && x.rows_of(1) == kBM;
       const uint32_t my_use = stg_uses + ((t == 1 && full_a) ? 1u : 0u);  // tile A's use comes first
       stg_uses += (full_a ? 1u : 0u) + (full_b ? 1u : 0u);
@@ -659,11 +682,17 @@ long long wait_budget_cycles() {
 
 template <int D>
 cudaError_t launch_tc(const PrefillArgs& a, int num_sms, cudaStream_t s) {
+  const bool chunk = a.prefix_lens != nullptr;
   CUtensorMap mq, mk, mv, mo;
-  if (!make_map(&mq, a.q, (uint64_t)a.h_q * D, (uint64_t)a.T) || !make_map(&mo, a.out, (uint64_t)a.h_q * D, (uint64_t)a.T, 32) ||
-      !make_map(&mk, a.k, (uint64_t)a.h_kv * D, (uint64_t)a.T) ||
-      !make_map(&mv, a.v, (uint64_t)a.h_kv * D, (uint64_t)a.T))
+  if (!make_map(&mq, a.q, (uint64_t)a.h_q * D, (uint64_t)a.T) || !make_map(&mo, a.out, (uint64_t)a.h_q * D, (uint64_t)a.T, 32))
     return cudaErrorInvalidValue;
+  if (chunk) {  // keys and values: the slots as [n_slots * H_kv * cap, D] rows
+    const uint64_t rows = (uint64_t)a.n_slots * a.h_kv * a.cap;
+    if (!make_map(&mk, a.pool_k, D, rows) || !make_map(&mv, a.pool_v, D, rows)) return cudaErrorInvalidValue;
+  } else if (!make_map(&mk, a.k, (uint64_t)a.h_kv * D, (uint64_t)a.T) ||
+             !make_map(&mv, a.v, (uint64_t)a.h_kv * D, (uint64_t)a.T)) {
+    return cudaErrorInvalidValue;
+  }
   TcParams p;
   p.ws = const_cast<char*>(a.ws);
   p.layout = a.layout;
@@ -674,12 +703,17 @@ cudaError_t launch_tc(const PrefillArgs& a, int num_sms, cudaStream_t s) {
   p.scale_log2 = a.scale * 1.4426950408889634f;
   p.dev_status = a.dev_status;
   p.wait_budget = wait_budget_cycles();
+  p.prefix_lens = a.prefix_lens;
+  p.slot_ids = a.slot_ids;
+  p.h_kv = a.h_kv;
+  p.cap = a.cap;
   const int smem = Smem<D>::kLaunchBytes;
-  cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  auto kern = chunk ? prefill_tc_kernel<D, true> : prefill_tc_kernel<D, false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const int64_t max_items = a.layout.max_items;
   const int grid = (int)(max_items < num_sms ? max_items : num_sms);
-  return launch_pdl(prefill_tc_kernel<D>, dim3(grid), dim3(kThreads), smem, s, mq, mk, mv, mo, p);
+  return launch_pdl(kern, dim3(grid), dim3(kThreads), smem, s, mq, mk, mv, mo, p);
 }
 
 }  // namespace

@@ -67,7 +67,7 @@ __device__ int block_exclusive_scan(int v, int* tmp /* [kThreads/32 + 1] */, int
 
 __global__ void __launch_bounds__(kThreads) segments_kernel(SegmentsArgs a) {
   __shared__ unsigned long long keys[kMaxQuestions];
-  __shared__ int s_flags;  // bit 0 intervals, bit 1 slot range, bit 2 overflow, bit 3 duplicate slot
+  __shared__ int s_flags;  // bit 0 intervals, bit 1 slot range, bit 2 overflow, bit 3 duplicate slot, bit 4 prefix
   __shared__ int scan_tmp[kThreads / 32 + 1];
   __shared__ int bin_count[kCostBins];
   __shared__ int bin_cursor[kCostBins];
@@ -99,10 +99,13 @@ __global__ void __launch_bounds__(kThreads) segments_kernel(SegmentsArgs a) {
     const kev_interval iv = a.intervals[i];
     if (!(iv.begin >= 0 && iv.begin <= iv.end && iv.end <= a.T)) atomicOr(&s_flags, 1);
     int s = -1;
+    // chunked prefill: the chunk sits after prefix_lens[i] cached positions (a tile boundary)
+    const int pre = a.prefix_lens ? a.prefix_lens[i] : 0;
+    if (pre < 0 || pre % kTileM != 0) atomicOr(&s_flags, 16);
     if (a.slot_ids) {
       s = a.slot_ids[i];
       if (s < 0 || s >= a.n_slots) atomicOr(&s_flags, 2);
-      if (iv.end - iv.begin > a.cap) atomicOr(&s_flags, 4);
+      if ((int64_t)iv.end - iv.begin + pre > a.cap) atomicOr(&s_flags, 4);
     }
     if (small) {
       s_iv[i] = make_int2(iv.begin, iv.end);
@@ -217,7 +220,12 @@ __global__ void __launch_bounds__(kThreads) segments_kernel(SegmentsArgs a) {
   }
 
   const int f = s_flags;
-  const int code = (f & 1) ? ST_INTERVALS : (f & 2) ? ST_SLOT : (f & 4) ? ST_OVERFLOW : (f & 8) ? ST_SLOT : ST_OK;
+  const int code = (f & 1)    ? ST_INTERVALS
+                   : (f & 2)  ? ST_SLOT
+                   : (f & 16) ? ST_PREFIX
+                   : (f & 4)  ? ST_OVERFLOW
+                   : (f & 8)  ? ST_SLOT
+                              : ST_OK;
   if (code != ST_OK) {
     if (tid == 0) {
       hdr->status = code;
@@ -246,10 +254,12 @@ __global__ void __launch_bounds__(kThreads) segments_kernel(SegmentsArgs a) {
   if (tid == 0) cu[n] = total_len;
 
   // 6. tile histogram over cost bins, then longest-first placement
+  // a tile's cost is its number of key tiles: m + 1, plus the cached prefix's tiles
   for (int i = tid; i < n; i += blockDim.x) {
     const int L = a.intervals[i].end - a.intervals[i].begin;
     const int nt = (L + kTileM - 1) / kTileM;
-    for (int m = 0; m < nt; ++m) atomicAdd(&bin_count[m < kCostBins ? m : kCostBins - 1], 1);
+    const int pt = a.prefix_lens ? a.prefix_lens[i] / kTileM : 0;
+    for (int m = 0; m < nt; ++m) atomicAdd(&bin_count[min(m + pt, kCostBins - 1)], 1);
   }
   __syncthreads();
   static_assert(kCostBins == 64, "one warp places the 64 bins, two per lane");
@@ -277,8 +287,9 @@ __global__ void __launch_bounds__(kThreads) segments_kernel(SegmentsArgs a) {
   for (int i = tid; i < n; i += blockDim.x) {
     const int L = a.intervals[i].end - a.intervals[i].begin;
     const int nt = (L + kTileM - 1) / kTileM;
+    const int pt = a.prefix_lens ? a.prefix_lens[i] / kTileM : 0;
     for (int m = nt - 1; m >= 0; --m) {
-      const int pos = atomicAdd(&bin_cursor[m < kCostBins ? m : kCostBins - 1], 1);
+      const int pos = atomicAdd(&bin_cursor[min(m + pt, kCostBins - 1)], 1);
       tl_list[pos] = make_int2(i, m);
     }
   }

@@ -34,11 +34,11 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_status_strings_and_launch_counts(lib):
-    for code in range(9):
+    for code in range(10):
         assert lib.kev_status_string(code) != "unknown status"
     assert lib.kev_status_string(99) == "unknown status"
     assert lib.kev_launch_count(0) == 3 and lib.kev_launch_count(4) == 1 and lib.kev_launch_count(99) == -1
-    assert [lib.kev_launch_count(i) for i in (6, 7, 8, 9, 10, 11)] == [1, 1, 1, 4, 3, 2]
+    assert [lib.kev_launch_count(i) for i in (6, 7, 8, 9, 10, 11, 12)] == [1, 1, 1, 4, 3, 2, 3]
 
 
 def test_workspace_sizes(lib):
@@ -128,3 +128,18 @@ def test_paged_host_errors_without_gpu(lib):
     assert lib.kev_decode_attn_paged(0x1000, 0x1000, 0x1000, 0x1000, 0x1000, 8, 0x1000, 4, 0x1000, 0x1000, 1,
                                      0x1000, lib.make_shape(4, 2, 64, "bf16"), 0x1000, 1 << 20, None, stream=0,
                                      check=False) == b.KEV_ERR_UNSUPPORTED
+
+
+def test_chunk_host_errors_without_gpu(lib):
+    b = lib.binding
+    s = lib.make_shape(4, 2, 128, "bf16")
+    args = (0x1000, 0x1000, 0x1000, 10, 0x1000, 1, 0x1000, 0x1000, 0x1000, 0x1000, 4)
+    # slot capacity not a multiple of 128, fp32, no prefix array, no slots
+    assert lib.kev_prefill_chunk(*args, 2458, 0x1000, s, 0x1000, 1 << 20, None, stream=0, check=False) == \
+        b.KEV_ERR_UNSUPPORTED
+    assert lib.kev_prefill_chunk(*args, 2560, 0x1000, lib.make_shape(4, 2, 128, "fp32"), 0x1000, 1 << 20, None,
+                                 stream=0, check=False) == b.KEV_ERR_UNSUPPORTED
+    assert lib.kev_prefill_chunk(0x1000, 0x1000, 0x1000, 10, 0x1000, 1, None, 0x1000, 0x1000, 0x1000, 4, 2560,
+                                 0x1000, s, 0x1000, 1 << 20, None, stream=0, check=False) == b.KEV_ERR_INVALID_ARG
+    assert lib.kev_prefill_chunk(0x1000, 0x1000, 0x1000, 10, 0x1000, 1, 0x1000, None, 0x1000, 0x1000, 4, 2560,
+                                 0x1000, s, 0x1000, 1 << 20, None, stream=0, check=False) == b.KEV_ERR_INVALID_ARG
