@@ -34,6 +34,9 @@ dense T x T mask, in float64:
 * Chunked prefill into slots (inference-engine notes, §2.6: a long input is
   prefilled in pieces that share rounds with decode steps, each later piece
   using the K/V of the pieces before it).
+* Per-question temperature sampling (Kev architecture article, §4.1: each
+  question brings its own temperature, applied to the softmax of its logits
+  at every decode step; nothing else in the model changes).
 * Rotary position encoding with per-question positions (KV-cache isolation
   article, hnwysp.cn, §7.2: the rotation multiplies Q and K, a cached K
   keeps the rotation of its own position, and the new token's position is
@@ -45,6 +48,10 @@ design notes): intervals are half-open [s, e); scale = 1/sqrt(d_h) unless
 given; a q-head h uses kv-head h // (H_q / H_kv); tokens in no interval are
 keys for nobody and their own output row is 0; an empty interval is allowed;
 a decode step attends over lens + 1 positions, the new K/V written first;
+sampling takes token k, the smallest index whose cumulative probability under
+softmax(logits / T_i) exceeds the question's uniform u_i in [0, 1) (inverse
+CDF; the uniforms are inputs), and T_i = 0 means the greedy argmax, ties to
+the lowest index;
 RoPE is the rotate-half form (pair (x_i, x_{i+d/2}) turned by p * w_i with
 w_i = theta^(-2i/d), theta given by the caller), the position of token t of
 question i is t - s_i, that of a decode token is lens_i, tokens in no
@@ -582,3 +589,50 @@ def prefill_chunk(q, k, v, intervals, prefix_lens, slot_ids, pool_k, pool_v, dty
             scores = np.where(allowed, (Q @ K.T) * sc, -np.inf)
             out[s:e, h] = softmax_rows(scores) @ V
     return out, pk, pv
+
+
+# ---------------------------------------------------------------------------
+# per-question temperature sampling
+# ---------------------------------------------------------------------------
+
+SAMPLING = "sampling"
+
+
+def sample_probs(logits_row, temperature: float) -> np.ndarray:
+    """softmax(logits / T) in float64 (T > 0), the stable form of ``softmax_rows``."""
+    z = np.asarray(logits_row, dtype=np.float64) / float(temperature)
+    return softmax_rows(z[None, :])[0]
+
+
+def sample_tokens(logits, temperature, uniforms, active=None):
+    """Token per question: argmax of its logits (lowest index among equal maxima) when its
+    temperature is 0, else the smallest k with sum_{j <= k} p_j > u, p = softmax(logits / T)
+    (the last k with p_k > 0 if rounding leaves no such k).  ``logits`` [N, V] float64
+    values.  Dropped questions get -1.  Returns int64 [N]."""
+    lg = np.asarray(logits, dtype=np.float64)
+    N = lg.shape[0]
+    live = np.ones(N, bool) if active is None else np.asarray(active).astype(bool)
+    out = np.full(N, -1, dtype=np.int64)
+    for i in range(N):
+        if not live[i]:
+            continue
+        if float(temperature[i]) == 0.0:
+            out[i] = int(np.argmax(lg[i]))  # numpy: the first maximum
+            continue
+        p = sample_probs(lg[i], temperature[i])
+        cdf = np.cumsum(p)
+        k = int(np.searchsorted(cdf, float(uniforms[i]), side="right"))
+        if k >= len(p):
+            k = int(np.nonzero(p > 0)[0][-1])
+        out[i] = k
+    return out
+
+
+def validate_sampling(temperature, uniforms, active=None):
+    """None, or SAMPLING when a live question's temperature is negative or not finite or its
+    uniform lies outside [0, 1)."""
+    t = np.asarray(temperature, dtype=np.float64)
+    u = np.asarray(uniforms, dtype=np.float64)
+    live = np.ones(len(t), bool) if active is None else np.asarray(active).astype(bool)
+    bad = ~np.isfinite(t) | (t < 0) | ~(u >= 0) | ~(u < 1)
+    return SAMPLING if np.any(live & bad) else None

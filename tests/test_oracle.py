@@ -734,3 +734,48 @@ def test_validate_chunk_cases():
                             cap=512) == O.SLOT
     assert O.validate_chunk(np.array([[0, 100], [50, 120]]), 300, prefix_lens=[0, 0], slot_ids=[0, 1], n_slots=3,
                             cap=512) == O.INTERVALS
+
+
+# ---------------------------------------------------------------------------
+# per-question temperature sampling (Kev architecture article, icman.com.cn, §4.1)
+# ---------------------------------------------------------------------------
+
+def test_sampling_closed_form_two_tokens():
+    # logits (0, ln 3) at T = 1: p = (1/4, 3/4); at T = 2: p = (1, sqrt 3) / (1 + sqrt 3)
+    lg = np.array([[0.0, np.log(3.0)]] * 4)
+    got = O.sample_tokens(lg, [1.0, 1.0, 2.0, 2.0], [0.2499, 0.2501, 0.366, 0.367])
+    assert got.tolist() == [0, 1, 0, 1]  # 1 / (1 + sqrt 3) = 0.36603
+
+
+def test_sampling_frequencies_over_a_uniform_grid_are_the_probabilities():
+    """Inverse CDF: the share of a fine grid of u in [0, 1) that picks token k is p_k (up to the grid step)."""
+    rng = np.random.default_rng(1)
+    lg = rng.standard_normal(7) * 2
+    for T in (0.5, 1.0, 3.0):
+        grid = (np.arange(20000) + 0.5) / 20000
+        toks = O.sample_tokens(np.tile(lg, (len(grid), 1)), np.full(len(grid), T), grid)
+        freq = np.bincount(toks, minlength=7) / len(grid)
+        p = np.exp(lg / T) / np.exp(lg / T).sum()  # the plain softmax, not the oracle's stable form
+        np.testing.assert_allclose(freq, p, atol=1.0 / 20000 + 1e-12)
+
+
+def test_sampling_greedy_ties_and_temperature_identity():
+    lg = np.array([[1.0, 5.0, 5.0, 2.0], [0.0, 0.0, 0.0, 0.0]])
+    assert O.sample_tokens(lg, [0.0, 0.0], [0.9, 0.9]).tolist() == [1, 0]  # lowest index among maxima
+    rng = np.random.default_rng(2)
+    x = rng.standard_normal((6, 50))
+    T = np.array([0.3, 0.7, 1.0, 1.5, 2.0, 4.0])
+    u = rng.random(6)
+    # sampling x at temperature T is sampling x / T at temperature 1
+    assert O.sample_tokens(x, T, u).tolist() == O.sample_tokens(x / T[:, None], np.ones(6), u).tolist()
+    # dropped questions: -1
+    assert O.sample_tokens(x, T, u, active=[1, 0, 1, 0, 1, 0]).tolist()[1::2] == [-1, -1, -1]
+
+
+def test_validate_sampling_cases():
+    assert O.validate_sampling([0.0, 1.0], [0.0, 0.999]) is None
+    assert O.validate_sampling([-1.0, 1.0], [0.5, 0.5]) == O.SAMPLING
+    assert O.validate_sampling([np.inf, 1.0], [0.5, 0.5]) == O.SAMPLING
+    assert O.validate_sampling([1.0, 1.0], [1.0, 0.5]) == O.SAMPLING
+    assert O.validate_sampling([1.0, 1.0], [np.nan, 0.5]) == O.SAMPLING
+    assert O.validate_sampling([1.0, -1.0], [0.5, 0.5], active=[1, 0]) is None
