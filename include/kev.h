@@ -60,7 +60,8 @@ typedef enum {
   KEV_ERR_TIMEOUT = 6,       /* (device) a bounded wait inside a kernel gave up; outputs are invalid */
   KEV_ERR_CUDA = 7,          /* a CUDA runtime call failed (launch error, no device, ...) */
   KEV_ERR_POSITION = 8,      /* (device) a position at or past the RoPE table's max_pos */
-  KEV_ERR_PREFIX = 9         /* (device) a cached prefix length negative or not a multiple of 128 */
+  KEV_ERR_PREFIX = 9,        /* (device) a cached prefix length negative or not a multiple of 128 */
+  KEV_ERR_SAMPLING = 10      /* (device) a live temperature negative / not finite, or a uniform outside [0,1) */
 } kev_status;
 
 typedef enum { KEV_BF16 = 0, KEV_FP32 = 1 } kev_dtype;
@@ -202,6 +203,25 @@ kev_status kev_decode_attn_static(const void* q_new, const void* k_new, const vo
 /* lens[i] += (active[i] != 0) for i < n, on the device (no host synchronisation), so a
  * decode loop can be captured in a CUDA graph. */
 kev_status kev_decode_advance(int32_t* lens, const uint8_t* active, int32_t n, kev_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------
+ * Per-question temperature sampling
+ *
+ * Kev architecture article (icman.com.cn), §4.1: each question brings its own temperature,
+ * applied to the softmax of its logits at every decode step.  For a live question i with
+ * T_i > 0 the token is the smallest k whose cumulative probability under softmax(logits_i /
+ * T_i) exceeds u_i (inverse CDF; the uniforms u_i in [0, 1) are inputs, so a step can be
+ * replayed); T_i = 0 takes the argmax, ties to the lowest index.  fp32 arithmetic: near a
+ * boundary of the cumulative distribution (within its rounding) either neighbour can result.
+ * ------------------------------------------------------------------------------------- */
+
+/* logits: device [n_questions, vocab] of `dtype` (kev_dtype; vocab a multiple of 8 for bf16,
+ * 4 for fp32, so rows stay 16-byte aligned); temperature, uniforms: device float[n]; active:
+ * device uint8[n]; tokens: device int32[n], written for live questions only.  An invalid
+ * live temperature or uniform sets KEV_ERR_SAMPLING and no token is written.  One kernel. */
+kev_status kev_sample(const void* logits, int32_t n_questions, int32_t vocab, int32_t dtype, const float* temperature,
+                      const float* uniforms, const uint8_t* active, int32_t* tokens, int32_t* dev_status,
+                      kev_stream_t stream);
 
 /* ---------------------------------------------------------------------------------------
  * Chunked prefill into slots
@@ -361,8 +381,8 @@ const char* kev_status_string(kev_status status);
  * d_h = 128, decode and merge kernels; 1 otherwise and before any call), 5 = decode_advance,
  * 6 = rope_table, 7 = rope_prefill, 8 = rope_decode (1 each), 9 = prefill_attn_paged (4:
  * segments, table check, attention, paged write), 10 = kv_write_paged (3), 11 =
- * decode_attn_paged (2), 12 = prefill_chunk (3: segments, slot write, attention).  -1 for an
- * unknown id. */
+ * decode_attn_paged (2), 12 = prefill_chunk (3: segments, slot write, attention), 13 =
+ * sample (1).  -1 for an unknown id. */
 int32_t kev_launch_count(int32_t entry_point);
 
 #ifdef __cplusplus

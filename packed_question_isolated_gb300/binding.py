@@ -32,6 +32,7 @@ KEV_ERR_TIMEOUT = 6
 KEV_ERR_CUDA = 7
 KEV_ERR_POSITION = 8
 KEV_ERR_PREFIX = 9
+KEV_ERR_SAMPLING = 10
 KEV_BF16 = 0
 KEV_FP32 = 1
 KEV_PAGE = 128
@@ -40,7 +41,7 @@ KEV_MAX_PAGED_ENTRIES = 16384
 STATUS_NAMES = {
     0: "KEV_OK", 1: "KEV_ERR_INVALID_ARG", 2: "KEV_ERR_UNSUPPORTED", 3: "KEV_ERR_INTERVALS",
     4: "KEV_ERR_SLOT", 5: "KEV_ERR_SLOT_OVERFLOW", 6: "KEV_ERR_TIMEOUT", 7: "KEV_ERR_CUDA",
-    8: "KEV_ERR_POSITION", 9: "KEV_ERR_PREFIX",
+    8: "KEV_ERR_POSITION", 9: "KEV_ERR_PREFIX", 10: "KEV_ERR_SAMPLING",
 }
 
 # every symbol include/kev.h declares
@@ -51,7 +52,7 @@ EXPORTED = [
     "kev_read_status", "kev_status_string", "kev_launch_count", "kev_decode_attn_static",
     "kev_rope_table_size", "kev_rope_table", "kev_rope_prefill", "kev_prefill_attn_rope", "kev_rope_decode",
     "kev_decode_attn_rope", "kev_prefill_attn_paged", "kev_kv_write_paged", "kev_decode_attn_paged",
-    "kev_assign_blocks", "kev_prefill_chunk",
+    "kev_assign_blocks", "kev_prefill_chunk", "kev_sample",
 ]
 
 
@@ -113,6 +114,7 @@ _c = {
     "kev_decode_attn_paged": _sig("kev_decode_attn_paged", _I, _P, _P, _P, _P, _P, _I, _P, _I, _P, _P, _I, _P, _S,
                                   _P, _Z, _P, _P),
     "kev_assign_blocks": _sig("kev_assign_blocks", _I, _P, _I, _P, _I, _P, _I, _I),
+    "kev_sample": _sig("kev_sample", _I, _P, _I, _I, _I, _P, _P, _P, _P, _P, _P),
     "kev_prefill_chunk": _sig("kev_prefill_chunk", _I, _P, _P, _P, _I, _P, _I, _P, _P, _P, _P, _I, _I, _P, _S, _P,
                               _Z, _P, _P),
 }
@@ -370,3 +372,12 @@ def kev_prefill_chunk(q, k, v, total_tokens, intervals, n_questions, prefix_lens
                                  int(slot_cap), _ptr(out), ctypes.byref(s), _ptr(workspace), int(workspace_bytes),
                                  _ptr(dev_status), _stream(stream))
     return _check(st, "kev_prefill_chunk", check)
+
+
+def kev_sample(logits, n_questions, vocab, dtype, temperature, uniforms, active, tokens, dev_status=None, stream=None,
+               check=True) -> int:
+    if isinstance(dtype, str):
+        dtype = {"bf16": KEV_BF16, "fp32": KEV_FP32}[dtype]
+    st = _c["kev_sample"](_ptr(logits), int(n_questions), int(vocab), int(dtype), _ptr(temperature), _ptr(uniforms),
+                          _ptr(active), _ptr(tokens), _ptr(dev_status), _stream(stream))
+    return _check(st, "kev_sample", check)

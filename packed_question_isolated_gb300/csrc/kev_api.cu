@@ -314,6 +314,31 @@ kev_status paged_prefill_tail(const void* q, const void* k, const void* v, int32
 
 }  // namespace
 
+kev_status kev_sample(const void* logits, int32_t n_questions, int32_t vocab, int32_t dtype, const float* temperature,
+                      const float* uniforms, const uint8_t* active, int32_t* tokens, int32_t* dev_status,
+                      kev_stream_t stream) {
+  if (n_questions < 0 || vocab <= 0) return KEV_ERR_INVALID_ARG;
+  if (dtype != KEV_BF16 && dtype != KEV_FP32) return KEV_ERR_UNSUPPORTED;
+  if (n_questions > (1 << 20)) return KEV_ERR_UNSUPPORTED;
+  if (vocab % (dtype == KEV_BF16 ? 8 : 4)) return KEV_ERR_UNSUPPORTED;
+  if (dev_status && ((uintptr_t)dev_status & 3u)) return KEV_ERR_INVALID_ARG;
+  if (n_questions == 0) return KEV_OK;
+  if (!logits || !aligned16(logits) || !temperature || !uniforms || !active || !tokens || ((uintptr_t)temperature & 3u) ||
+      ((uintptr_t)uniforms & 3u) || ((uintptr_t)tokens & 3u))
+    return KEV_ERR_INVALID_ARG;
+  SampleArgs a;
+  a.logits = logits;
+  a.n = n_questions;
+  a.vocab = vocab;
+  a.elem = dtype == KEV_BF16 ? 2 : 4;
+  a.temperature = temperature;
+  a.uniforms = uniforms;
+  a.active = active;
+  a.tokens = tokens;
+  a.dev_status = dev_status;
+  return from_cuda(launch_sample(a, (cudaStream_t)stream));
+}
+
 kev_status kev_prefill_chunk(const void* q, const void* k, const void* v, int32_t total_tokens,
                              const kev_interval* intervals, int32_t n_questions, const int32_t* prefix_lens,
                              const int32_t* slot_ids, void* pool_k, void* pool_v, int32_t n_slots, int32_t slot_cap,
@@ -710,7 +735,7 @@ kev_status kev_read_status(const int32_t* dev_status, kev_stream_t stream) {
   if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return KEV_ERR_CUDA;
   int32_t h = 0;
   if (cudaMemcpy(&h, dev_status, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) return KEV_ERR_CUDA;
-  if (h < KEV_OK || h > KEV_ERR_PREFIX) return KEV_ERR_CUDA;
+  if (h < KEV_OK || h > KEV_ERR_SAMPLING) return KEV_ERR_CUDA;
   return (kev_status)h;
 }
 
@@ -726,6 +751,7 @@ const char* kev_status_string(kev_status s) {
     case KEV_ERR_CUDA: return "CUDA runtime error";
     case KEV_ERR_POSITION: return "a position at or past the RoPE table's max_pos";
     case KEV_ERR_PREFIX: return "a cached prefix length negative or not a multiple of 128";
+    case KEV_ERR_SAMPLING: return "a live temperature negative or not finite, or a uniform outside [0, 1)";
   }
   return "unknown status";
 }
@@ -745,6 +771,7 @@ int32_t kev_launch_count(int32_t entry_point) {
     case 10: return 3;
     case 11: return 2;
     case 12: return 3;
+    case 13: return 1;
   }
   return -1;
 }

@@ -30,6 +30,7 @@ enum : int32_t {
   ST_TIMEOUT = KEV_ERR_TIMEOUT,
   ST_POSITION = KEV_ERR_POSITION,
   ST_PREFIX = KEV_ERR_PREFIX,
+  ST_SAMPLING = KEV_ERR_SAMPLING,
 };
 
 // ---------------------------------------------------------------------------------------
@@ -233,6 +234,21 @@ struct PagedCheckArgs {                     // prefill side: the block tables of
   int32_t* dev_status;
 };
 cudaError_t launch_paged_check(const PagedCheckArgs& a, cudaStream_t s);
+
+// ---------------------------------------------------------------------------------------
+// per-question temperature sampling (kev_sample.cu)
+// ---------------------------------------------------------------------------------------
+struct SampleArgs {
+  const void* logits;  // [n, vocab]
+  int32_t n, vocab;
+  int32_t elem;  // 2: bf16, 4: fp32
+  const float* temperature;
+  const float* uniforms;
+  const uint8_t* active;
+  int32_t* tokens;
+  int32_t* dev_status;
+};
+cudaError_t launch_sample(const SampleArgs& a, cudaStream_t s);
 
 // ---------------------------------------------------------------------------------------
 // rotary position encoding (kev_rope.cu)
