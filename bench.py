@@ -431,6 +431,40 @@ def _chunked_prefill(kev, torch, tdev, dev, K, warmup):
                              "useful_gflop": second / 1e9}}
 
 
+def _sampling(kev, torch, tdev, dev, K, warmup):
+    """Per-question temperature sampling of the decode batch: 32 live questions, a 151,936-token
+    bf16 vocabulary (Qwen3), temperatures 0.3 .. 1.5, uniforms from a seeded generator; calls back
+    to back over two logit buffers (19 MB)."""
+    rng = np.random.default_rng(50)
+    n, vocab = 32, 151936
+    sets = []
+    for _ in range(2):
+        lg = W.f32_to_bf16_bits(rng.standard_normal((n, vocab), dtype=np.float32) * 2)
+        sets.append({"lg": tdev(lg), "t": tdev(rng.choice([0.3, 0.7, 1.0, 1.5], n).astype(np.float32)),
+                     "u": tdev(rng.random(n).astype(np.float32)), "a": tdev(np.ones(n, np.uint8)),
+                     "tok": torch.empty(n, dtype=torch.int32, device=dev),
+                     "st": torch.zeros(1, dtype=torch.int32, device=dev)})
+
+    def call(c):
+        kev.kev_sample(c["lg"], n, vocab, "bf16", c["t"], c["u"], c["a"], c["tok"], c["st"])
+
+    for _ in range(warmup):
+        for c in sets:
+            call(c)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for s in range(K):
+        call(sets[s % 2])
+    b.record()
+    torch.cuda.synchronize()
+    assert all(kev.kev_read_status(c["st"]) == 0 for c in sets)
+    ms = a.elapsed_time(b) / K
+    logit_bytes = n * vocab * 2
+    return {"workload": "32 questions x 151,936 bf16 logits, per-question temperatures, inverse CDF",
+            "ms_per_step": ms, "value": logit_bytes / (ms * 1e-3) / 1e9, "unit": "GB/s (logits read once)"}
+
+
 def _paged_decode(kev, torch, tdev, dev, K, warmup):
     """The decode workload over a paged pool (128-position blocks, block tables from the library's
     host assignment): contiguous-first tables on an empty pool, and scattered tables (a pool with
@@ -708,6 +742,7 @@ def main(argv=None):
 
     paged = _paged_decode(kev, torch, tdev, dev, Kd, args.warmup)
     chunked = _chunked_prefill(kev, torch, tdev, dev, max(10, K // 2), args.warmup)
+    sampling = _sampling(kev, torch, tdev, dev, Kd, args.warmup)
 
     # ---- second prefill workload (Qwen3-8B-shaped batch): measured, not the headline ---------
     # two buffer sets (each ~490 MB of q, k, v and output) used in turn, launches back to back
@@ -784,6 +819,7 @@ def main(argv=None):
             "rope": rope,
             "paged_decode": paged,
             "chunked_prefill": chunked,
+            "sampling": sampling,
             "stress": stress,
             "cpu_baseline": cpu,
             "cpu_fair_baseline": cpu_fair,
