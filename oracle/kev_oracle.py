@@ -37,6 +37,10 @@ dense T x T mask, in float64:
 * Per-question temperature sampling (Kev architecture article, §4.1: each
   question brings its own temperature, applied to the softmax of its logits
   at every decode step; nothing else in the model changes).
+* Token-grouped LoRA (Kev architecture article, §3.2: the base layer stays
+  fixed and each token takes the low-rank delta of its own question's
+  adapter, computed per adapter group rather than for every adapter over the
+  whole sequence; §3.3: the scale is the adapter's alpha / rank).
 * Rotary position encoding with per-question positions (KV-cache isolation
   article, hnwysp.cn, §7.2: the rotation multiplies Q and K, a cached K
   keeps the rotation of its own position, and the new token's position is
@@ -636,3 +640,47 @@ def validate_sampling(temperature, uniforms, active=None):
     live = np.ones(len(t), bool) if active is None else np.asarray(active).astype(bool)
     bad = ~np.isfinite(t) | (t < 0) | ~(u >= 0) | ~(u < 1)
     return SAMPLING if np.any(live & bad) else None
+
+
+# ---------------------------------------------------------------------------
+# token-grouped LoRA
+# ---------------------------------------------------------------------------
+
+ADAPTER = "adapter"
+
+
+def lora_apply(y, x, intervals, adapter_ids, lora_a, lora_b, scales):
+    """Token t of question i with adapter a = adapter_ids[i] >= 0 gets
+    y[t] + scales[a] * B_a (A_a x[t]), A_a = lora_a[a] [r, d_in], B_a = lora_b[a] [d_out, r];
+    rows of questions without an adapter (-1) and of tokens in no question are unchanged.
+    float64 in and out."""
+    out = np.array(y, dtype=np.float64, copy=True)
+    x = np.asarray(x, dtype=np.float64)
+    for (s, e), a in zip(np.asarray(intervals).reshape(-1, 2), np.asarray(adapter_ids)):
+        if a < 0 or e <= s:
+            continue
+        A = np.asarray(lora_a[a], dtype=np.float64)
+        B = np.asarray(lora_b[a], dtype=np.float64)
+        out[s:e] += float(scales[a]) * (x[s:e] @ A.T) @ B.T
+    return out
+
+
+def lora_router(y, x, intervals, adapter_ids, lora_a, lora_b, scales):
+    """The same result in the routing form the article describes: every adapter's delta over
+    the whole sequence, kept where a token's adapter id matches (a mask per adapter)."""
+    out = np.array(y, dtype=np.float64, copy=True)
+    x = np.asarray(x, dtype=np.float64)
+    T = x.shape[0]
+    token_adapter = np.full(T, -1)
+    for (s, e), a in zip(np.asarray(intervals).reshape(-1, 2), np.asarray(adapter_ids)):
+        token_adapter[s:e] = a
+    for a in range(len(lora_a)):
+        delta = float(scales[a]) * (x @ np.asarray(lora_a[a], np.float64).T) @ np.asarray(lora_b[a], np.float64).T
+        out += (token_adapter == a)[:, None] * delta
+    return out
+
+
+def validate_lora(adapter_ids, n_adapters: int):
+    """None, or ADAPTER when an adapter id lies outside [-1, n_adapters)."""
+    a = np.asarray(adapter_ids, dtype=np.int64)
+    return ADAPTER if np.any((a < -1) | (a >= n_adapters)) else None

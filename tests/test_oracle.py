@@ -779,3 +779,46 @@ def test_validate_sampling_cases():
     assert O.validate_sampling([1.0, 1.0], [1.0, 0.5]) == O.SAMPLING
     assert O.validate_sampling([1.0, 1.0], [np.nan, 0.5]) == O.SAMPLING
     assert O.validate_sampling([1.0, -1.0], [0.5, 0.5], active=[1, 0]) is None
+
+
+# ---------------------------------------------------------------------------
+# token-grouped LoRA (Kev architecture article, icman.com.cn, §3.2, §3.3)
+# ---------------------------------------------------------------------------
+
+def _lora_case(seed, lengths, d_in=24, d_out=20, r=4, n_ad=3):
+    rng = np.random.default_rng(seed)
+    iv = W.pack_intervals(lengths, gaps=[1] * len(lengths))
+    T = int(iv[-1, 1]) + 2
+    x = rng.standard_normal((T, d_in))
+    y = rng.standard_normal((T, d_out))
+    A = rng.standard_normal((n_ad, r, d_in))
+    B = rng.standard_normal((n_ad, d_out, r))
+    scales = rng.random(n_ad) + 0.5
+    return iv, x, y, A, B, scales
+
+
+def test_lora_grouped_equals_the_routed_form():
+    iv, x, y, A, B, sc = _lora_case(1, [5, 9, 0, 7, 3])
+    ids = np.array([2, -1, 0, 0, 1])  # two questions share adapter 0, one has none
+    np.testing.assert_allclose(O.lora_apply(y, x, iv, ids, A, B, sc), O.lora_router(y, x, iv, ids, A, B, sc),
+                               rtol=0, atol=1e-12)
+
+
+def test_lora_is_the_merged_weight_and_leaves_other_rows():
+    """For a question with adapter a, base output x W^T plus the delta is x (W + s B A)^T (the
+    article's merged alternative); rows without an adapter, and gap rows, keep the base output."""
+    iv, x, _, A, B, sc = _lora_case(2, [6, 4])
+    Wb = np.random.default_rng(3).standard_normal((20, 24))
+    y0 = x @ Wb.T
+    got = O.lora_apply(y0, x, iv, [1, -1], A, B, sc)
+    s0, e0 = iv[0]
+    np.testing.assert_allclose(got[s0:e0], x[s0:e0] @ (Wb + sc[1] * B[1] @ A[1]).T, rtol=0, atol=1e-11)
+    mask = np.ones(len(x), bool)
+    mask[s0:e0] = False
+    np.testing.assert_array_equal(got[mask], y0[mask])
+
+
+def test_validate_lora_cases():
+    assert O.validate_lora([-1, 0, 2], 3) is None
+    assert O.validate_lora([-2, 0], 3) == O.ADAPTER
+    assert O.validate_lora([0, 3], 3) == O.ADAPTER
