@@ -61,7 +61,8 @@ typedef enum {
   KEV_ERR_CUDA = 7,          /* a CUDA runtime call failed (launch error, no device, ...) */
   KEV_ERR_POSITION = 8,      /* (device) a position at or past the RoPE table's max_pos */
   KEV_ERR_PREFIX = 9,        /* (device) a cached prefix length negative or not a multiple of 128 */
-  KEV_ERR_SAMPLING = 10      /* (device) a live temperature negative / not finite, or a uniform outside [0,1) */
+  KEV_ERR_SAMPLING = 10,     /* (device) a live temperature negative / not finite, or a uniform outside [0,1) */
+  KEV_ERR_ADAPTER = 11       /* (device) a LoRA adapter id outside [-1, n_adapters) */
 } kev_status;
 
 typedef enum { KEV_BF16 = 0, KEV_FP32 = 1 } kev_dtype;
@@ -224,6 +225,29 @@ kev_status kev_sample(const void* logits, int32_t n_questions, int32_t vocab, in
                       kev_stream_t stream);
 
 /* ---------------------------------------------------------------------------------------
+ * Token-grouped LoRA
+ *
+ * Kev architecture article (icman.com.cn), §3.2: the base layer stays fixed and every token
+ * takes the low-rank delta of its own question's adapter, computed per adapter group rather
+ * than for every adapter over the whole sequence; §3.3: the scale is the adapter's alpha / rank.
+ *   y[t] += scales[a] * lora_b[a] (lora_a[a] x[t])   for t in question i, a = adapter_ids[i] >= 0
+ * ------------------------------------------------------------------------------------- */
+
+/* Over the work list kev_build_segments built in `workspace` for the same intervals: x [T,
+ * d_in] and y [T, d_out] bf16 (y updated in place; rows of questions without an adapter, id -1,
+ * and of tokens in no question are not touched); lora_a [n_adapters, rank, d_in], lora_b
+ * [n_adapters, d_out, rank] bf16; scales float[n_adapters]; adapter_ids int32[n_questions]; all
+ * device.  rank 16, 32 or 64, d_in a multiple of 16, d_out a multiple of 8 (else
+ * KEV_ERR_UNSUPPORTED).  An adapter id outside [-1, n_adapters) sets KEV_ERR_ADAPTER and nothing
+ * is written.  bf16 products on the tensor cores, fp32 accumulation, y rounded to nearest even.
+ * One kernel. */
+kev_status kev_lora_apply(const void* x, void* y, int32_t total_tokens, int32_t d_in, int32_t d_out,
+                          const kev_interval* intervals, int32_t n_questions, const int32_t* adapter_ids,
+                          const void* lora_a, const void* lora_b, const float* scales, int32_t n_adapters,
+                          int32_t rank, void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                          kev_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------
  * Chunked prefill into slots
  *
  * Inference-engine notes (sakurs2.com), §2.6: a long input is prefilled in pieces that share
@@ -382,7 +406,7 @@ const char* kev_status_string(kev_status status);
  * 6 = rope_table, 7 = rope_prefill, 8 = rope_decode (1 each), 9 = prefill_attn_paged (4:
  * segments, table check, attention, paged write), 10 = kv_write_paged (3), 11 =
  * decode_attn_paged (2), 12 = prefill_chunk (3: segments, slot write, attention), 13 =
- * sample (1).  -1 for an unknown id. */
+ * sample (1), 14 = lora_apply (1).  -1 for an unknown id. */
 int32_t kev_launch_count(int32_t entry_point);
 
 #ifdef __cplusplus

@@ -33,6 +33,7 @@ KEV_ERR_CUDA = 7
 KEV_ERR_POSITION = 8
 KEV_ERR_PREFIX = 9
 KEV_ERR_SAMPLING = 10
+KEV_ERR_ADAPTER = 11
 KEV_BF16 = 0
 KEV_FP32 = 1
 KEV_PAGE = 128
@@ -41,7 +42,7 @@ KEV_MAX_PAGED_ENTRIES = 16384
 STATUS_NAMES = {
     0: "KEV_OK", 1: "KEV_ERR_INVALID_ARG", 2: "KEV_ERR_UNSUPPORTED", 3: "KEV_ERR_INTERVALS",
     4: "KEV_ERR_SLOT", 5: "KEV_ERR_SLOT_OVERFLOW", 6: "KEV_ERR_TIMEOUT", 7: "KEV_ERR_CUDA",
-    8: "KEV_ERR_POSITION", 9: "KEV_ERR_PREFIX", 10: "KEV_ERR_SAMPLING",
+    8: "KEV_ERR_POSITION", 9: "KEV_ERR_PREFIX", 10: "KEV_ERR_SAMPLING", 11: "KEV_ERR_ADAPTER",
 }
 
 # every symbol include/kev.h declares
@@ -52,7 +53,7 @@ EXPORTED = [
     "kev_read_status", "kev_status_string", "kev_launch_count", "kev_decode_attn_static",
     "kev_rope_table_size", "kev_rope_table", "kev_rope_prefill", "kev_prefill_attn_rope", "kev_rope_decode",
     "kev_decode_attn_rope", "kev_prefill_attn_paged", "kev_kv_write_paged", "kev_decode_attn_paged",
-    "kev_assign_blocks", "kev_prefill_chunk", "kev_sample",
+    "kev_assign_blocks", "kev_prefill_chunk", "kev_sample", "kev_lora_apply",
 ]
 
 
@@ -114,6 +115,8 @@ _c = {
     "kev_decode_attn_paged": _sig("kev_decode_attn_paged", _I, _P, _P, _P, _P, _P, _I, _P, _I, _P, _P, _I, _P, _S,
                                   _P, _Z, _P, _P),
     "kev_assign_blocks": _sig("kev_assign_blocks", _I, _P, _I, _P, _I, _P, _I, _I),
+    "kev_lora_apply": _sig("kev_lora_apply", _I, _P, _P, _I, _I, _I, _P, _I, _P, _P, _P, _P, _I, _I, _P, _Z, _P,
+                           _P),
     "kev_sample": _sig("kev_sample", _I, _P, _I, _I, _I, _P, _P, _P, _P, _P, _P),
     "kev_prefill_chunk": _sig("kev_prefill_chunk", _I, _P, _P, _P, _I, _P, _I, _P, _P, _P, _P, _I, _I, _P, _S, _P,
                               _Z, _P, _P),
@@ -381,3 +384,12 @@ def kev_sample(logits, n_questions, vocab, dtype, temperature, uniforms, active,
     st = _c["kev_sample"](_ptr(logits), int(n_questions), int(vocab), int(dtype), _ptr(temperature), _ptr(uniforms),
                           _ptr(active), _ptr(tokens), _ptr(dev_status), _stream(stream))
     return _check(st, "kev_sample", check)
+
+
+def kev_lora_apply(x, y, total_tokens, d_in, d_out, intervals, n_questions, adapter_ids, lora_a, lora_b, scales,
+                   n_adapters, rank, workspace, workspace_bytes, dev_status=None, stream=None, check=True) -> int:
+    st = _c["kev_lora_apply"](_ptr(x), _ptr(y), int(total_tokens), int(d_in), int(d_out), _ptr(intervals),
+                              int(n_questions), _ptr(adapter_ids), _ptr(lora_a), _ptr(lora_b), _ptr(scales),
+                              int(n_adapters), int(rank), _ptr(workspace), int(workspace_bytes), _ptr(dev_status),
+                              _stream(stream))
+    return _check(st, "kev_lora_apply", check)

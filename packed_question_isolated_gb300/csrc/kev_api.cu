@@ -314,6 +314,48 @@ kev_status paged_prefill_tail(const void* q, const void* k, const void* v, int32
 
 }  // namespace
 
+kev_status kev_lora_apply(const void* x, void* y, int32_t total_tokens, int32_t d_in, int32_t d_out,
+                          const kev_interval* intervals, int32_t n_questions, const int32_t* adapter_ids,
+                          const void* lora_a, const void* lora_b, const float* scales, int32_t n_adapters,
+                          int32_t rank, void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                          kev_stream_t stream) {
+  if (total_tokens < 0 || n_questions < 0 || n_adapters < 0 || d_in <= 0 || d_out <= 0) return KEV_ERR_INVALID_ARG;
+  if (n_questions > kMaxQuestions || d_in % 16 || d_out % 8 || (rank != 16 && rank != 32 && rank != 64))
+    return KEV_ERR_UNSUPPORTED;
+  if (!workspace || ((uintptr_t)workspace & 255u)) return KEV_ERR_INVALID_ARG;
+  // the work list is that of any shape with one q-head: only cu_seqlens and the status are read
+  if (workspace_bytes < prefill_layout(n_questions, total_tokens, 1).cu_seqlens + sizeof(int32_t) * (n_questions + 1))
+    return KEV_ERR_INVALID_ARG;
+  if (dev_status && ((uintptr_t)dev_status & 3u)) return KEV_ERR_INVALID_ARG;
+  if (total_tokens == 0 || n_questions == 0) return KEV_OK;
+  if (!x || !y || !aligned16(x) || !aligned16(y) || !intervals || ((uintptr_t)intervals & 7u) || !adapter_ids ||
+      ((uintptr_t)adapter_ids & 3u))
+    return KEV_ERR_INVALID_ARG;
+  if (n_adapters > 0 && (!lora_a || !lora_b || !scales || !aligned16(lora_a) || !aligned16(lora_b) ||
+                         ((uintptr_t)scales & 3u)))
+    return KEV_ERR_INVALID_ARG;
+  const int sms = num_sms_of_current_device();
+  if (sms <= 0) return KEV_ERR_CUDA;
+  LoraArgs a;
+  a.x = x;
+  a.y = y;
+  a.T = total_tokens;
+  a.d_in = d_in;
+  a.d_out = d_out;
+  a.n = n_questions;
+  a.n_adapters = n_adapters;
+  a.rank = rank;
+  a.intervals = intervals;
+  a.adapter_ids = adapter_ids;
+  a.lora_a = lora_a;
+  a.lora_b = lora_b;
+  a.scales = scales;
+  a.ws = static_cast<const char*>(workspace);
+  a.layout = prefill_layout(n_questions, total_tokens, 1);
+  a.dev_status = dev_status;
+  return from_cuda(launch_lora(a, sms, (cudaStream_t)stream));
+}
+
 kev_status kev_sample(const void* logits, int32_t n_questions, int32_t vocab, int32_t dtype, const float* temperature,
                       const float* uniforms, const uint8_t* active, int32_t* tokens, int32_t* dev_status,
                       kev_stream_t stream) {
@@ -735,7 +777,7 @@ kev_status kev_read_status(const int32_t* dev_status, kev_stream_t stream) {
   if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return KEV_ERR_CUDA;
   int32_t h = 0;
   if (cudaMemcpy(&h, dev_status, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) return KEV_ERR_CUDA;
-  if (h < KEV_OK || h > KEV_ERR_SAMPLING) return KEV_ERR_CUDA;
+  if (h < KEV_OK || h > KEV_ERR_ADAPTER) return KEV_ERR_CUDA;
   return (kev_status)h;
 }
 
@@ -752,6 +794,7 @@ const char* kev_status_string(kev_status s) {
     case KEV_ERR_POSITION: return "a position at or past the RoPE table's max_pos";
     case KEV_ERR_PREFIX: return "a cached prefix length negative or not a multiple of 128";
     case KEV_ERR_SAMPLING: return "a live temperature negative or not finite, or a uniform outside [0, 1)";
+    case KEV_ERR_ADAPTER: return "a LoRA adapter id outside [-1, n_adapters)";
   }
   return "unknown status";
 }
@@ -772,6 +815,7 @@ int32_t kev_launch_count(int32_t entry_point) {
     case 11: return 2;
     case 12: return 3;
     case 13: return 1;
+    case 14: return 1;
   }
   return -1;
 }

@@ -31,6 +31,7 @@ enum : int32_t {
   ST_POSITION = KEV_ERR_POSITION,
   ST_PREFIX = KEV_ERR_PREFIX,
   ST_SAMPLING = KEV_ERR_SAMPLING,
+  ST_ADAPTER = KEV_ERR_ADAPTER,
 };
 
 // ---------------------------------------------------------------------------------------
@@ -249,6 +250,24 @@ struct SampleArgs {
   int32_t* dev_status;
 };
 cudaError_t launch_sample(const SampleArgs& a, cudaStream_t s);
+
+// ---------------------------------------------------------------------------------------
+// token-grouped LoRA (kev_lora.cu)
+// ---------------------------------------------------------------------------------------
+struct LoraArgs {
+  const void* x;  // [T, d_in] bf16
+  void* y;        // [T, d_out] bf16, updated in place
+  int32_t T, d_in, d_out, n, n_adapters, rank;
+  const kev_interval* intervals;
+  const int32_t* adapter_ids;  // [n], -1: no adapter
+  const void* lora_a;          // [n_adapters, rank, d_in]
+  const void* lora_b;          // [n_adapters, d_out, rank]
+  const float* scales;         // [n_adapters]
+  const char* ws;              // prefill workspace of kev_build_segments for the same intervals
+  PrefillLayout layout;
+  int32_t* dev_status;
+};
+cudaError_t launch_lora(const LoraArgs& a, int num_sms, cudaStream_t s);
 
 // ---------------------------------------------------------------------------------------
 // rotary position encoding (kev_rope.cu)

@@ -34,11 +34,11 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_status_strings_and_launch_counts(lib):
-    for code in range(11):
+    for code in range(12):
         assert lib.kev_status_string(code) != "unknown status"
     assert lib.kev_status_string(99) == "unknown status"
     assert lib.kev_launch_count(0) == 3 and lib.kev_launch_count(4) == 1 and lib.kev_launch_count(99) == -1
-    assert [lib.kev_launch_count(i) for i in (6, 7, 8, 9, 10, 11, 12, 13)] == [1, 1, 1, 4, 3, 2, 3, 1]
+    assert [lib.kev_launch_count(i) for i in (6, 7, 8, 9, 10, 11, 12, 13, 14)] == [1, 1, 1, 4, 3, 2, 3, 1, 1]
 
 
 def test_workspace_sizes(lib):
@@ -153,3 +153,17 @@ def test_sample_host_errors_without_gpu(lib):
     assert lib.kev_sample(0x1000, 2, 128, 7, *args, None, stream=0, check=False) == b.KEV_ERR_UNSUPPORTED
     assert lib.kev_sample(0x1008, 2, 128, "bf16", *args, None, stream=0, check=False) == b.KEV_ERR_INVALID_ARG
     assert lib.kev_sample(None, 0, 128, "bf16", None, None, None, None, None, stream=0, check=False) == b.KEV_OK
+
+
+def test_lora_host_errors_without_gpu(lib):
+    b = lib.binding
+    args = (0x1000, 0x1000, 0x1000, 0x1000, 3)  # adapter ids, lora_a, lora_b, scales, n_adapters
+    # rank, d_in, d_out outside what the kernel takes; a misaligned workspace
+    assert lib.kev_lora_apply(0x1000, 0x1000, 10, 256, 256, 0x1000, 1, *args, 8, 0x1000, 1 << 20, None, stream=0,
+                              check=False) == b.KEV_ERR_UNSUPPORTED
+    assert lib.kev_lora_apply(0x1000, 0x1000, 10, 250, 256, 0x1000, 1, *args, 16, 0x1000, 1 << 20, None, stream=0,
+                              check=False) == b.KEV_ERR_UNSUPPORTED
+    assert lib.kev_lora_apply(0x1000, 0x1000, 10, 256, 254, 0x1000, 1, *args, 16, 0x1000, 1 << 20, None, stream=0,
+                              check=False) == b.KEV_ERR_UNSUPPORTED
+    assert lib.kev_lora_apply(0x1000, 0x1000, 10, 256, 256, 0x1000, 1, *args, 16, 0x1010, 1 << 20, None, stream=0,
+                              check=False) == b.KEV_ERR_INVALID_ARG
