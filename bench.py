@@ -465,6 +465,52 @@ def _sampling(kev, torch, tdev, dev, K, warmup):
             "ms_per_step": ms, "value": logit_bytes / (ms * 1e-3) / 1e9, "unit": "GB/s (logits read once)"}
 
 
+def _lora(kev, torch, tdev, dev, K, warmup):
+    """The Qwen2.5-7B-shaped batch (T = 7921) through a 3584 -> 3584 projection's rank-16 LoRA
+    adapters (4 adapters over 8 questions, one question without), back to back over two buffer
+    sets of x and y (2 x 113 MB)."""
+    w = W.qwen25_7b_prefill()
+    d, rank, n_ad = 3584, 16, 4
+    T, N = w.total_tokens, w.n_questions
+    rng = np.random.default_rng(60)
+    bf = lambda a: W.f32_to_bf16_bits(a.astype(np.float32))
+    shape = kev.make_shape(w.h_q, w.h_kv, w.d, "bf16")
+    nb = kev.kev_prefill_workspace_size(N, T, shape)
+    A = tdev(bf(rng.standard_normal((n_ad, rank, d)) / np.sqrt(d)))
+    B = tdev(bf(rng.standard_normal((n_ad, d, rank)) / np.sqrt(rank)))
+    sc = tdev(np.full(n_ad, 2.0, np.float32))
+    ids = tdev(np.array([0, 1, 2, 3, -1, 0, 1, 2], np.int32))
+    sets = []
+    for _ in range(2):
+        c = {"x": tdev(bf(rng.standard_normal((T, d)))), "y": tdev(bf(rng.standard_normal((T, d)))),
+             "iv": tdev(w.intervals), "ws": torch.empty(nb, dtype=torch.uint8, device=dev),
+             "st": torch.zeros(1, dtype=torch.int32, device=dev)}
+        kev.kev_build_segments(c["iv"], N, T, None, 0, 0, shape, c["ws"], nb, c["st"])
+        sets.append(c)
+
+    def call(c):
+        kev.kev_lora_apply(c["x"], c["y"], T, d, d, c["iv"], N, ids, A, B, sc, n_ad, rank, c["ws"], nb, c["st"])
+
+    for _ in range(warmup):
+        for c in sets:
+            call(c)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for s in range(K):
+        call(sets[s % 2])
+    b.record()
+    torch.cuda.synchronize()
+    assert all(kev.kev_read_status(c["st"]) == 0 for c in sets)
+    ms = a.elapsed_time(b) / K
+    rows = int(sum(L for L, i in zip(w.lengths, [0, 1, 2, 3, -1, 0, 1, 2]) if i >= 0))
+    moved = rows * (d + 2 * d) * 2  # x read, y read and written (adapter rows only)
+    flops = 2.0 * rows * (d * rank + rank * d)
+    return {"workload": "qwen25_7b_prefill batch (T=7921), 3584 x 3584 projection, rank-16 adapters, 7 of 8 "
+                        "questions with an adapter", "ms_per_step": ms, "value": moved / (ms * 1e-3) / 1e9,
+            "unit": "GB/s", "tflops": flops / (ms * 1e-3) / 1e12}
+
+
 def _paged_decode(kev, torch, tdev, dev, K, warmup):
     """The decode workload over a paged pool (128-position blocks, block tables from the library's
     host assignment): contiguous-first tables on an empty pool, and scattered tables (a pool with
@@ -743,6 +789,7 @@ def main(argv=None):
     paged = _paged_decode(kev, torch, tdev, dev, Kd, args.warmup)
     chunked = _chunked_prefill(kev, torch, tdev, dev, max(10, K // 2), args.warmup)
     sampling = _sampling(kev, torch, tdev, dev, Kd, args.warmup)
+    lora = _lora(kev, torch, tdev, dev, Kd, args.warmup)
 
     # ---- second prefill workload (Qwen3-8B-shaped batch): measured, not the headline ---------
     # two buffer sets (each ~490 MB of q, k, v and output) used in turn, launches back to back
@@ -820,6 +867,7 @@ def main(argv=None):
             "paged_decode": paged,
             "chunked_prefill": chunked,
             "sampling": sampling,
+            "lora": lora,
             "stress": stress,
             "cpu_baseline": cpu,
             "cpu_fair_baseline": cpu_fair,

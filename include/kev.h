@@ -237,7 +237,7 @@ kev_status kev_sample(const void* logits, int32_t n_questions, int32_t vocab, in
  * d_in] and y [T, d_out] bf16 (y updated in place; rows of questions without an adapter, id -1,
  * and of tokens in no question are not touched); lora_a [n_adapters, rank, d_in], lora_b
  * [n_adapters, d_out, rank] bf16; scales float[n_adapters]; adapter_ids int32[n_questions]; all
- * device.  rank 16, 32 or 64, d_in a multiple of 16, d_out a multiple of 8 (else
+ * device.  rank 16, 32 or 64, d_in a multiple of 64, d_out a multiple of 32 (else
  * KEV_ERR_UNSUPPORTED).  An adapter id outside [-1, n_adapters) sets KEV_ERR_ADAPTER and nothing
  * is written.  bf16 products on the tensor cores, fp32 accumulation, y rounded to nearest even.
  * One kernel. */

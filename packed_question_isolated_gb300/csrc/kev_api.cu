@@ -320,7 +320,7 @@ kev_status kev_lora_apply(const void* x, void* y, int32_t total_tokens, int32_t 
                           int32_t rank, void* workspace, size_t workspace_bytes, int32_t* dev_status,
                           kev_stream_t stream) {
   if (total_tokens < 0 || n_questions < 0 || n_adapters < 0 || d_in <= 0 || d_out <= 0) return KEV_ERR_INVALID_ARG;
-  if (n_questions > kMaxQuestions || d_in % 16 || d_out % 8 || (rank != 16 && rank != 32 && rank != 64))
+  if (n_questions > kMaxQuestions || d_in % 64 || d_out % 32 || (rank != 16 && rank != 32 && rank != 64))
     return KEV_ERR_UNSUPPORTED;
   if (!workspace || ((uintptr_t)workspace & 255u)) return KEV_ERR_INVALID_ARG;
   // the work list is that of any shape with one q-head: only cu_seqlens and the status are read

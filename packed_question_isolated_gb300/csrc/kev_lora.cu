@@ -8,8 +8,10 @@
 // A question's tokens are contiguous in the packed batch, so a tile of its rows is one adapter
 // group with no gather or scatter.
 //
-// lora_kernel: a CTA takes 64 consecutive rows of one question (4 warps x 16 rows), tiles in
-// cu_seqlens order from the segment builder's work list.  With rank 16 the op reads x and reads
+// lora_kernel: a CTA takes 16 consecutive rows of one question, tiles in cu_seqlens order from the
+// segment builder's work list; its 4 warps split d_in for h (partial sums added through shared
+// memory) and d_out for y, loading the y and B_a fragments of 8 n-tiles before the MMAs (y is
+// read and written in place, so later loads could not move above earlier stores).  With rank 16 the op reads x and reads
 // and writes y for ~10 FLOPs per byte, so it is HBM-bound; the two products run on the warp-level
 // tensor-core MMA (m16n8k16, bf16 in, fp32 accumulate), fragments straight from global memory:
 //   h [16 x r] = x [16 x d_in] . A_a^T      (A_a's rows are the MMA's column-major B operand)
@@ -21,7 +23,8 @@ namespace kev {
 namespace {
 
 constexpr int kLoraWarps = 4;
-constexpr int kLoraRows = 16 * kLoraWarps;  // rows per CTA tile
+constexpr int kLoraRows = 16;  // rows per CTA tile: the 4 warps split d_in, then d_out
+constexpr int kNBatch = 8;     // n-tiles of y a warp loads before it multiplies and stores
 
 __device__ __forceinline__ void mma_bf16_16816(float* d, const uint32_t* a, const uint32_t* b) {
   asm volatile(
@@ -92,28 +95,30 @@ __global__ void __launch_bounds__(32 * kLoraWarps) lora_kernel(LoraArgs a) {
   __syncthreads();
   const int n_tiles = s_tiles[a.n];
 
+  __shared__ float s_h[kLoraWarps][16][R + 1];  // partial h of each warp (padded rows)
   const __nv_bfloat16* X = static_cast<const __nv_bfloat16*>(a.x);
   __nv_bfloat16* Y = static_cast<__nv_bfloat16*>(a.y);
   const int g = lane >> 2, c2 = (lane & 3) * 2;  // fragment row / column pair of this lane
+  const int k_span = a.d_in / kLoraWarps, n_span = a.d_out / kLoraWarps;  // host: multiples of 16 / 8
   for (int t = blockIdx.x; t < n_tiles; t += gridDim.x) {
     const int i = question_of(s_tiles, a.n, t);  // s_tiles is a prefix like cu_seqlens
     const int ad = a.adapter_ids[i];
     const kev_interval iv = a.intervals[i];
-    const int r0 = iv.begin + (t - s_tiles[i]) * kLoraRows + warp * 16;  // this warp's first row
-    const int rows = min(16, iv.end - r0);  // may be <= 0: the warp has nothing in a partial tile
-    if (rows <= 0) continue;
+    const int r0 = iv.begin + (t - s_tiles[i]) * kLoraRows;
+    const int rows = min(kLoraRows, iv.end - r0);
     const bool ok0 = g < rows, ok1 = g + 8 < rows;
     const __nv_bfloat16* x0 = X + (int64_t)(r0 + g) * a.d_in;
     const __nv_bfloat16* x1 = X + (int64_t)(r0 + g + 8) * a.d_in;
     const __nv_bfloat16* A = static_cast<const __nv_bfloat16*>(a.lora_a) + (int64_t)ad * R * a.d_in;
     const __nv_bfloat16* B = static_cast<const __nv_bfloat16*>(a.lora_b) + (int64_t)ad * a.d_out * R;
 
-    // h = x . A^T: R / 8 accumulator tiles of 16 x 8
+    // partial h = x . A^T over this warp's share of d_in: R / 8 accumulator tiles of 16 x 8
     float h[R / 8][4];
 #pragma unroll
     for (int n = 0; n < R / 8; ++n) h[n][0] = h[n][1] = h[n][2] = h[n][3] = 0.f;
+    const int k_beg = warp * k_span, k_end = k_beg + k_span;
 #pragma unroll 4
-    for (int k0 = 0; k0 < a.d_in; k0 += 16) {
+    for (int k0 = k_beg; k0 < k_end; k0 += 16) {
       uint32_t af[4];
       af[0] = ok0 ? __ldg(reinterpret_cast<const uint32_t*>(x0 + k0 + c2)) : 0u;
       af[1] = ok1 ? __ldg(reinterpret_cast<const uint32_t*>(x1 + k0 + c2)) : 0u;
@@ -128,6 +133,30 @@ __global__ void __launch_bounds__(32 * kLoraWarps) lora_kernel(LoraArgs a) {
         mma_bf16_16816(h[n], af, bf);
       }
     }
+#pragma unroll
+    for (int n = 0; n < R / 8; ++n) {
+      s_h[warp][g][n * 8 + c2] = h[n][0];
+      s_h[warp][g][n * 8 + c2 + 1] = h[n][1];
+      s_h[warp][g + 8][n * 8 + c2] = h[n][2];
+      s_h[warp][g + 8][n * 8 + c2 + 1] = h[n][3];
+    }
+    __syncthreads();
+#pragma unroll
+    for (int n = 0; n < R / 8; ++n) {  // every warp: the whole h, summed in a fixed order
+      float v[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int w = 0; w < kLoraWarps; ++w) {
+        v[0] += s_h[w][g][n * 8 + c2];
+        v[1] += s_h[w][g][n * 8 + c2 + 1];
+        v[2] += s_h[w][g + 8][n * 8 + c2];
+        v[3] += s_h[w][g + 8][n * 8 + c2 + 1];
+      }
+      h[n][0] = v[0];
+      h[n][1] = v[1];
+      h[n][2] = v[2];
+      h[n][3] = v[3];
+    }
+    __syncthreads();  // s_h is rewritten by the next tile
     // h (scaled) as the bf16 A operand of y += h . B^T: k-step j takes accumulator tiles 2j, 2j+1
     const float sc = a.scales[ad];
     uint32_t hf[R / 16][4];
@@ -140,24 +169,34 @@ __global__ void __launch_bounds__(32 * kLoraWarps) lora_kernel(LoraArgs a) {
     }
     __nv_bfloat16* y0 = Y + (int64_t)(r0 + g) * a.d_out;
     __nv_bfloat16* y1 = Y + (int64_t)(r0 + g + 8) * a.d_out;
-    for (int n0 = 0; n0 < a.d_out; n0 += 8) {
-      float acc[4];
-      const float2 u0 = ok0 ? f2_of(*reinterpret_cast<const uint32_t*>(y0 + n0 + c2)) : make_float2(0.f, 0.f);
-      const float2 u1 = ok1 ? f2_of(*reinterpret_cast<const uint32_t*>(y1 + n0 + c2)) : make_float2(0.f, 0.f);
-      acc[0] = u0.x;
-      acc[1] = u0.y;
-      acc[2] = u1.x;
-      acc[3] = u1.y;
-      const __nv_bfloat16* brow = B + (int64_t)(n0 + g) * R;  // output column n0+g
+    const int n_beg = warp * n_span, n_end = n_beg + n_span;
+    for (int nb = n_beg; nb < n_end; nb += 8 * kNBatch) {
+      uint32_t yv[kNBatch][2], bv[kNBatch][R / 16][2];
 #pragma unroll
-      for (int j = 0; j < R / 16; ++j) {
-        uint32_t bf[2];
-        bf[0] = __ldg(reinterpret_cast<const uint32_t*>(brow + 16 * j + c2));
-        bf[1] = __ldg(reinterpret_cast<const uint32_t*>(brow + 16 * j + 8 + c2));
-        mma_bf16_16816(acc, hf[j], bf);
+      for (int q = 0; q < kNBatch; ++q) {  // every load of the batch first
+        const int n0 = nb + 8 * q;
+        if (n0 < n_end) {
+          yv[q][0] = ok0 ? *reinterpret_cast<const uint32_t*>(y0 + n0 + c2) : 0u;
+          yv[q][1] = ok1 ? *reinterpret_cast<const uint32_t*>(y1 + n0 + c2) : 0u;
+          const __nv_bfloat16* brow = B + (int64_t)(n0 + g) * R;  // output column n0+g
+#pragma unroll
+          for (int j = 0; j < R / 16; ++j) {
+            bv[q][j][0] = __ldg(reinterpret_cast<const uint32_t*>(brow + 16 * j + c2));
+            bv[q][j][1] = __ldg(reinterpret_cast<const uint32_t*>(brow + 16 * j + 8 + c2));
+          }
+        }
       }
-      if (ok0) *reinterpret_cast<uint32_t*>(y0 + n0 + c2) = bf16x2_of(acc[0], acc[1]);
-      if (ok1) *reinterpret_cast<uint32_t*>(y1 + n0 + c2) = bf16x2_of(acc[2], acc[3]);
+#pragma unroll
+      for (int q = 0; q < kNBatch; ++q) {
+        const int n0 = nb + 8 * q;
+        if (n0 >= n_end) break;
+        const float2 u0 = f2_of(yv[q][0]), u1 = f2_of(yv[q][1]);
+        float acc[4] = {u0.x, u0.y, u1.x, u1.y};
+#pragma unroll
+        for (int j = 0; j < R / 16; ++j) mma_bf16_16816(acc, hf[j], bv[q][j]);
+        if (ok0) *reinterpret_cast<uint32_t*>(y0 + n0 + c2) = bf16x2_of(acc[0], acc[1]);
+        if (ok1) *reinterpret_cast<uint32_t*>(y1 + n0 + c2) = bf16x2_of(acc[2], acc[3]);
+      }
     }
   }
 }

@@ -161,9 +161,9 @@ def test_lora_host_errors_without_gpu(lib):
     # rank, d_in, d_out outside what the kernel takes; a misaligned workspace
     assert lib.kev_lora_apply(0x1000, 0x1000, 10, 256, 256, 0x1000, 1, *args, 8, 0x1000, 1 << 20, None, stream=0,
                               check=False) == b.KEV_ERR_UNSUPPORTED
-    assert lib.kev_lora_apply(0x1000, 0x1000, 10, 250, 256, 0x1000, 1, *args, 16, 0x1000, 1 << 20, None, stream=0,
+    assert lib.kev_lora_apply(0x1000, 0x1000, 10, 240, 256, 0x1000, 1, *args, 16, 0x1000, 1 << 20, None, stream=0,
                               check=False) == b.KEV_ERR_UNSUPPORTED
-    assert lib.kev_lora_apply(0x1000, 0x1000, 10, 256, 254, 0x1000, 1, *args, 16, 0x1000, 1 << 20, None, stream=0,
+    assert lib.kev_lora_apply(0x1000, 0x1000, 10, 256, 248, 0x1000, 1, *args, 16, 0x1000, 1 << 20, None, stream=0,
                               check=False) == b.KEV_ERR_UNSUPPORTED
     assert lib.kev_lora_apply(0x1000, 0x1000, 10, 256, 256, 0x1000, 1, *args, 16, 0x1010, 1 << 20, None, stream=0,
                               check=False) == b.KEV_ERR_INVALID_ARG
