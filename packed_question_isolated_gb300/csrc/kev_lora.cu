@@ -9,22 +9,79 @@
 // group with no gather or scatter.
 //
 // lora_kernel: a CTA takes 16 consecutive rows of one question, tiles in cu_seqlens order from the
-// segment builder's work list; its 4 warps split d_in for h (partial sums added through shared
-// memory) and d_out for y, loading the y and B_a fragments of 8 n-tiles before the MMAs (y is
-// read and written in place, so later loads could not move above earlier stores).  With rank 16 the op reads x and reads
-// and writes y for ~10 FLOPs per byte, so it is HBM-bound; the two products run on the warp-level
-// tensor-core MMA (m16n8k16, bf16 in, fp32 accumulate), fragments straight from global memory:
-//   h [16 x r] = x [16 x d_in] . A_a^T      (A_a's rows are the MMA's column-major B operand)
+// segment builder's work list.  With rank 16 the op reads x and reads and writes y for ~10 FLOPs
+// per byte, so it is HBM-bound, and what sets its speed is the bytes in flight.  So the tile's
+// operands go through shared memory as a pipeline of asynchronous 16-byte copies
+// (cp.async, 3 to 6 stages by rank, waits in hardware only): first chunks of x's columns with the same
+// columns of A_a, then chunks of y's columns with the rows of B_a for them.  The 4 warps split
+// each chunk's 32-wide k-steps (n-blocks); the two products run on the warp-level tensor-core
+// MMA (m16n8k16, bf16 in, fp32 accumulate) with fragments read from shared memory:
+//   h [16 x r] = x [16 x d_in] . A_a^T      (A_a's rows are the MMA's column-major B operand;
+//                                             per-warp partials summed in a fixed order)
 //   y [16 x d_out] += scale h . B_a^T        (h's fp32 accumulator fragments are, pair by pair,
 //                                             the bf16 A operand of the second MMA; C = y)
+// The new y goes back into the stage and leaves it in 16-byte stores.  For h, lane (g, c) reads
+// x and A_a at k0 + 8c .. k0 + 8c + 7 in one 16-byte load: words 0, 1 are the A / B fragment pairs
+// of one MMA, words 2, 3 those of another, i.e. the MMA's k slots map to other columns than its
+// fragment layout names, the same mapping for both operands of a sum over k.
 #include "kev_internal.cuh"
 
 namespace kev {
 namespace {
 
 constexpr int kLoraWarps = 4;
-constexpr int kLoraRows = 16;  // rows per CTA tile: the 4 warps split d_in, then d_out
-constexpr int kNBatch = 8;     // n-tiles of y a warp loads before it multiplies and stores
+
+// A CTA tile is kRows rows, kMT m16 MMA tiles (measured on the Qwen2.5-7B batch through a 3584 x
+// 3584 rank-16 projection: 16-row tiles 55 us, 32-row tiles 65 us; half as many CTAs, each with
+// twice the work per chunk, lose more than the larger share of x and y in a stage gains).
+// Shared-memory stage of one chunk of 128 columns: x (or y) rows, then A_a rows (or B_a rows,
+// one per output column of the chunk).  Rows of x, A_a and y are padded by 64 bytes, so the two rows
+// a quarter warp reads in a 16-byte fragment load fall on different banks; B_a rows by 16 bytes,
+// and placed so that the 8 a fragment load reads are consecutive (b_pos), on 8 bank groups.
+template <int R>
+struct LoraCfg {
+  static constexpr int kRows = 16;
+  static constexpr int kMT = kRows / 16;
+  static constexpr int kC = 128;  // columns of x / y per chunk
+  static constexpr int kStages = R == 16 ? 6 : R == 32 ? 4 : 3;
+  static constexpr int kRowB = kC * 2 + 64;
+  static constexpr int kBRowB = R * 2 + 16;
+  static constexpr int kP1 = (kRows + R) * kRowB;
+  static constexpr int kP2 = kRows * kRowB + kC * kBRowB;
+  static constexpr int kStage = ((kP1 > kP2 ? kP1 : kP2) + 127) / 128 * 128;
+};
+// staged row of output column j of a chunk: bits 3-4 of j move to bits 1-2 and bits 1-2 to 3-4
+__device__ __forceinline__ int b_pos(int j) {
+  return (j & ~31) | (j & 1) | (((j >> 3) & 3) << 1) | (((j >> 1) & 3) << 3);
+}
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
+  // 16 bytes, or 16 zero bytes when !valid (src is not read then)
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(valid ? 16 : 0)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ void sts128(uint32_t addr, const uint32_t (&v)[4]) {
+  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3])
+               : "memory");
+}
 
 __device__ __forceinline__ void mma_bf16_16816(float* d, const uint32_t* a, const uint32_t* b) {
   asm volatile(
@@ -53,9 +110,15 @@ __device__ __forceinline__ int question_of(const int32_t* cu, int n, int r) {
 
 template <int R>  // rank: a multiple of 16
 __global__ void __launch_bounds__(32 * kLoraWarps) lora_kernel(LoraArgs a) {
-  extern __shared__ int32_t s_tiles[];  // [n + 1] exclusive prefix of each question's tile count
+  using Cfg = LoraCfg<R>;
+  constexpr int KC = Cfg::kC, NS = Cfg::kStages, ROWS = Cfg::kRows, MT = Cfg::kMT;
+  extern __shared__ __align__(128) unsigned char lora_smem[];
+  int32_t* s_tiles = reinterpret_cast<int32_t*>(lora_smem);  // [n + 1] first tile of each question
+  const uint32_t stages = static_cast<uint32_t>(__cvta_generic_to_shared(lora_smem)) +
+                          (uint32_t)(((a.n + 1) * 4 + 127) / 128 * 128);
   __shared__ int s_scan[33];
   __shared__ int s_ok;
+  __shared__ float s_h[kLoraWarps][ROWS][R + 1];  // partial h of each warp (padded rows)
   pdl_wait();  // the segment builder's work list, x and y are complete
   pdl_trigger();
   const PrefillHeader* hdr = reinterpret_cast<const PrefillHeader*>(a.ws);
@@ -74,7 +137,7 @@ __global__ void __launch_bounds__(32 * kLoraWarps) lora_kernel(LoraArgs a) {
   int running = 0;
   for (int base = 0; base < a.n; base += blockDim.x) {
     const int i = base + tid;
-    const int cnt = i < a.n && a.adapter_ids[i] >= 0 ? (cu[i + 1] - cu[i] + kLoraRows - 1) / kLoraRows : 0;
+    const int cnt = i < a.n && a.adapter_ids[i] >= 0 ? (cu[i + 1] - cu[i] + ROWS - 1) / ROWS : 0;
     int x = cnt;  // block scan (4 warps)
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -95,122 +158,205 @@ __global__ void __launch_bounds__(32 * kLoraWarps) lora_kernel(LoraArgs a) {
   __syncthreads();
   const int n_tiles = s_tiles[a.n];
 
-  __shared__ float s_h[kLoraWarps][16][R + 1];  // partial h of each warp (padded rows)
   const __nv_bfloat16* X = static_cast<const __nv_bfloat16*>(a.x);
   __nv_bfloat16* Y = static_cast<__nv_bfloat16*>(a.y);
-  const int g = lane >> 2, c2 = (lane & 3) * 2;  // fragment row / column pair of this lane
-  const int k_span = a.d_in / kLoraWarps, n_span = a.d_out / kLoraWarps;  // host: multiples of 16 / 8
+  const int g = lane >> 2, c = lane & 3, c2 = c * 2;  // fragment row, column quad of this lane
+  const int p1 = (a.d_in + KC - 1) / KC, n_chunks = p1 + (a.d_out + KC - 1) / KC;
   for (int t = blockIdx.x; t < n_tiles; t += gridDim.x) {
     const int i = question_of(s_tiles, a.n, t);  // s_tiles is a prefix like cu_seqlens
     const int ad = a.adapter_ids[i];
     const kev_interval iv = a.intervals[i];
-    const int r0 = iv.begin + (t - s_tiles[i]) * kLoraRows;
-    const int rows = min(kLoraRows, iv.end - r0);
-    const bool ok0 = g < rows, ok1 = g + 8 < rows;
-    const __nv_bfloat16* x0 = X + (int64_t)(r0 + g) * a.d_in;
-    const __nv_bfloat16* x1 = X + (int64_t)(r0 + g + 8) * a.d_in;
+    const int r0 = iv.begin + (t - s_tiles[i]) * ROWS;
+    const int rows = min(ROWS, iv.end - r0);
     const __nv_bfloat16* A = static_cast<const __nv_bfloat16*>(a.lora_a) + (int64_t)ad * R * a.d_in;
     const __nv_bfloat16* B = static_cast<const __nv_bfloat16*>(a.lora_b) + (int64_t)ad * a.d_out * R;
 
-    // partial h = x . A^T over this warp's share of d_in: R / 8 accumulator tiles of 16 x 8
-    float h[R / 8][4];
-#pragma unroll
-    for (int n = 0; n < R / 8; ++n) h[n][0] = h[n][1] = h[n][2] = h[n][3] = 0.f;
-    const int k_beg = warp * k_span, k_end = k_beg + k_span;
-#pragma unroll 4
-    for (int k0 = k_beg; k0 < k_end; k0 += 16) {
-      uint32_t af[4];
-      af[0] = ok0 ? __ldg(reinterpret_cast<const uint32_t*>(x0 + k0 + c2)) : 0u;
-      af[1] = ok1 ? __ldg(reinterpret_cast<const uint32_t*>(x1 + k0 + c2)) : 0u;
-      af[2] = ok0 ? __ldg(reinterpret_cast<const uint32_t*>(x0 + k0 + 8 + c2)) : 0u;
-      af[3] = ok1 ? __ldg(reinterpret_cast<const uint32_t*>(x1 + k0 + 8 + c2)) : 0u;
-#pragma unroll
-      for (int n = 0; n < R / 8; ++n) {
-        const __nv_bfloat16* arow = A + (int64_t)(n * 8 + g) * a.d_in + k0;  // rank n*8+g
-        uint32_t bf[2];
-        bf[0] = __ldg(reinterpret_cast<const uint32_t*>(arow + c2));
-        bf[1] = __ldg(reinterpret_cast<const uint32_t*>(arow + 8 + c2));
-        mma_bf16_16816(h[n], af, bf);
-      }
-    }
-#pragma unroll
-    for (int n = 0; n < R / 8; ++n) {
-      s_h[warp][g][n * 8 + c2] = h[n][0];
-      s_h[warp][g][n * 8 + c2 + 1] = h[n][1];
-      s_h[warp][g + 8][n * 8 + c2] = h[n][2];
-      s_h[warp][g + 8][n * 8 + c2 + 1] = h[n][3];
-    }
-    __syncthreads();
-#pragma unroll
-    for (int n = 0; n < R / 8; ++n) {  // every warp: the whole h, summed in a fixed order
-      float v[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int w = 0; w < kLoraWarps; ++w) {
-        v[0] += s_h[w][g][n * 8 + c2];
-        v[1] += s_h[w][g][n * 8 + c2 + 1];
-        v[2] += s_h[w][g + 8][n * 8 + c2];
-        v[3] += s_h[w][g + 8][n * 8 + c2 + 1];
-      }
-      h[n][0] = v[0];
-      h[n][1] = v[1];
-      h[n][2] = v[2];
-      h[n][3] = v[3];
-    }
-    __syncthreads();  // s_h is rewritten by the next tile
-    // h (scaled) as the bf16 A operand of y += h . B^T: k-step j takes accumulator tiles 2j, 2j+1
-    const float sc = a.scales[ad];
-    uint32_t hf[R / 16][4];
-#pragma unroll
-    for (int j = 0; j < R / 16; ++j) {
-      hf[j][0] = bf16x2_of(sc * h[2 * j][0], sc * h[2 * j][1]);
-      hf[j][1] = bf16x2_of(sc * h[2 * j][2], sc * h[2 * j][3]);
-      hf[j][2] = bf16x2_of(sc * h[2 * j + 1][0], sc * h[2 * j + 1][1]);
-      hf[j][3] = bf16x2_of(sc * h[2 * j + 1][2], sc * h[2 * j + 1][3]);
-    }
-    __nv_bfloat16* y0 = Y + (int64_t)(r0 + g) * a.d_out;
-    __nv_bfloat16* y1 = Y + (int64_t)(r0 + g + 8) * a.d_out;
-    const int n_beg = warp * n_span, n_end = n_beg + n_span;
-    for (int nb = n_beg; nb < n_end; nb += 8 * kNBatch) {
-      uint32_t yv[kNBatch][2], bv[kNBatch][R / 16][2];
-#pragma unroll
-      for (int q = 0; q < kNBatch; ++q) {  // every load of the batch first
-        const int n0 = nb + 8 * q;
-        if (n0 < n_end) {
-          yv[q][0] = ok0 ? *reinterpret_cast<const uint32_t*>(y0 + n0 + c2) : 0u;
-          yv[q][1] = ok1 ? *reinterpret_cast<const uint32_t*>(y1 + n0 + c2) : 0u;
-          const __nv_bfloat16* brow = B + (int64_t)(n0 + g) * R;  // output column n0+g
-#pragma unroll
-          for (int j = 0; j < R / 16; ++j) {
-            bv[q][j][0] = __ldg(reinterpret_cast<const uint32_t*>(brow + 16 * j + c2));
-            bv[q][j][1] = __ldg(reinterpret_cast<const uint32_t*>(brow + 16 * j + 8 + c2));
+    // copies of chunk ci into stage ci % NS (every thread a share of its 16-byte pieces), then
+    // one commit group per chunk, empty past the last one so the group count stays uniform;
+    // rows past the tile's end are filled with zeros, not read
+    auto issue = [&](int ci) {
+      if (ci < n_chunks) {
+        const uint32_t st = stages + (uint32_t)(ci % NS) * Cfg::kStage;
+        if (ci < p1) {
+          const int c0 = ci * KC, pr = min(KC, a.d_in - c0) / 8;  // pieces per row
+          for (int e = tid; e < (ROWS + R) * pr; e += blockDim.x) {
+            const int row = e / pr, col = (e - row * pr) * 8;
+            const uint32_t dst = st + row * Cfg::kRowB + col * 2;
+            if (row < ROWS) {
+              const bool v = row < rows;
+              cp_async16(dst, X + (int64_t)(r0 + (v ? row : 0)) * a.d_in + c0 + col, v);
+            } else {
+              cp_async16(dst, A + (int64_t)(row - ROWS) * a.d_in + c0 + col, true);
+            }
+          }
+        } else {
+          const int n0 = (ci - p1) * KC, nc = min(KC, a.d_out - n0), pr = nc / 8;
+          for (int e = tid; e < ROWS * pr; e += blockDim.x) {
+            const int row = e / pr, col = (e - row * pr) * 8;
+            const bool v = row < rows;
+            cp_async16(st + row * Cfg::kRowB + col * 2, Y + (int64_t)(r0 + (v ? row : 0)) * a.d_out + n0 + col, v);
+          }
+          for (int e = tid; e < nc * (R / 8); e += blockDim.x) {
+            const int j = e / (R / 8), part = e - j * (R / 8);
+            cp_async16(st + ROWS * Cfg::kRowB + b_pos(j) * Cfg::kBRowB + part * 16,
+                       B + (int64_t)(n0 + j) * R + part * 8, true);
           }
         }
       }
+      cp_async_commit();
+    };
+
+    for (int ci = 0; ci < NS - 1; ++ci) issue(ci);
+    float h[MT][R / 8][4];
 #pragma unroll
-      for (int q = 0; q < kNBatch; ++q) {
-        const int n0 = nb + 8 * q;
-        if (n0 >= n_end) break;
-        const float2 u0 = f2_of(yv[q][0]), u1 = f2_of(yv[q][1]);
-        float acc[4] = {u0.x, u0.y, u1.x, u1.y};
+    for (int m = 0; m < MT; ++m)
 #pragma unroll
-        for (int j = 0; j < R / 16; ++j) mma_bf16_16816(acc, hf[j], bv[q][j]);
-        if (ok0) *reinterpret_cast<uint32_t*>(y0 + n0 + c2) = bf16x2_of(acc[0], acc[1]);
-        if (ok1) *reinterpret_cast<uint32_t*>(y1 + n0 + c2) = bf16x2_of(acc[2], acc[3]);
+      for (int n = 0; n < R / 8; ++n) h[m][n][0] = h[m][n][1] = h[m][n][2] = h[m][n][3] = 0.f;
+    uint32_t hf[MT][R / 16][4];
+    for (int ci = 0; ci < n_chunks; ++ci) {
+      cp_async_wait<NS - 2>();  // this thread's copies of chunk ci have landed
+      __syncthreads();          // everyone's have, and chunk ci - 1's stage is no longer read
+      issue(ci + NS - 1);
+      const uint32_t st = stages + (uint32_t)(ci % NS) * Cfg::kStage;
+      if (ci < p1) {
+        // partial h over this warp's k-steps of the chunk
+        const int ksteps = min(KC, a.d_in - ci * KC) / 32;
+        for (int s = warp; s < ksteps; s += kLoraWarps) {
+          const uint32_t colb = (uint32_t)(32 * s + 8 * c) * 2;
+          uint4 aw[R / 8];
+#pragma unroll
+          for (int n = 0; n < R / 8; ++n) aw[n] = lds128(st + (ROWS + n * 8 + g) * Cfg::kRowB + colb);  // rank n*8+g
+#pragma unroll
+          for (int m = 0; m < MT; ++m) {
+            const uint4 xa = lds128(st + (16 * m + g) * Cfg::kRowB + colb);
+            const uint4 xb = lds128(st + (16 * m + g + 8) * Cfg::kRowB + colb);
+            const uint32_t af0[4] = {xa.x, xb.x, xa.y, xb.y};
+            const uint32_t af1[4] = {xa.z, xb.z, xa.w, xb.w};
+#pragma unroll
+            for (int n = 0; n < R / 8; ++n) {
+              const uint32_t bf0[2] = {aw[n].x, aw[n].y};
+              const uint32_t bf1[2] = {aw[n].z, aw[n].w};
+              mma_bf16_16816(h[m][n], af0, bf0);
+              mma_bf16_16816(h[m][n], af1, bf1);
+            }
+          }
+        }
+        continue;
+      }
+      if (ci == p1) {  // the whole h, the warps' partials summed in a fixed order
+#pragma unroll
+        for (int m = 0; m < MT; ++m)
+#pragma unroll
+          for (int n = 0; n < R / 8; ++n) {
+            s_h[warp][16 * m + g][n * 8 + c2] = h[m][n][0];
+            s_h[warp][16 * m + g][n * 8 + c2 + 1] = h[m][n][1];
+            s_h[warp][16 * m + g + 8][n * 8 + c2] = h[m][n][2];
+            s_h[warp][16 * m + g + 8][n * 8 + c2 + 1] = h[m][n][3];
+          }
+        __syncthreads();
+#pragma unroll
+        for (int m = 0; m < MT; ++m)
+#pragma unroll
+          for (int n = 0; n < R / 8; ++n) {
+            float v[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int w = 0; w < kLoraWarps; ++w) {
+              v[0] += s_h[w][16 * m + g][n * 8 + c2];
+              v[1] += s_h[w][16 * m + g][n * 8 + c2 + 1];
+              v[2] += s_h[w][16 * m + g + 8][n * 8 + c2];
+              v[3] += s_h[w][16 * m + g + 8][n * 8 + c2 + 1];
+            }
+            h[m][n][0] = v[0];
+            h[m][n][1] = v[1];
+            h[m][n][2] = v[2];
+            h[m][n][3] = v[3];
+          }
+        __syncthreads();  // s_h is rewritten by the next tile
+        // h (scaled) as the bf16 A operand of y += h . B^T: k-step j takes accumulator tiles 2j, 2j+1
+        const float sc = a.scales[ad];
+#pragma unroll
+        for (int m = 0; m < MT; ++m)
+#pragma unroll
+          for (int j = 0; j < R / 16; ++j) {
+            hf[m][j][0] = bf16x2_of(sc * h[m][2 * j][0], sc * h[m][2 * j][1]);
+            hf[m][j][1] = bf16x2_of(sc * h[m][2 * j][2], sc * h[m][2 * j][3]);
+            hf[m][j][2] = bf16x2_of(sc * h[m][2 * j + 1][0], sc * h[m][2 * j + 1][1]);
+            hf[m][j][3] = bf16x2_of(sc * h[m][2 * j + 1][2], sc * h[m][2 * j + 1][3]);
+          }
+      }
+      // y += h . B^T on this warp's n-blocks of the chunk, in place in the stage.  In the block at
+      // n0, lane (g, c) holds y columns n0 + 8c .. n0 + 8c + 7 of rows g and g + 8 of each m-tile
+      // (one 16-byte load each); MMA q (0..3) takes the pair n0 + 8c + 2q, +1 as its C slots 2c,
+      // 2c + 1, so its n-slot j is column n0 + 8 (j / 2) + 2q + j % 2, staged at b_pos = n0 + j + 8q
+      const int n0 = (ci - p1) * KC, nc = min(KC, a.d_out - n0);
+      const uint32_t bst = st + ROWS * Cfg::kRowB;
+      for (int nb = warp; nb < nc / 32; nb += kLoraWarps) {
+        uint32_t wa[MT][4], wb[MT][4];
+#pragma unroll
+        for (int m = 0; m < MT; ++m) {
+          const uint32_t y0 = st + (16 * m + g) * Cfg::kRowB + (uint32_t)(32 * nb + 8 * c) * 2;
+          const uint4 ya = lds128(y0), yb = lds128(y0 + 8 * Cfg::kRowB);
+          wa[m][0] = ya.x; wa[m][1] = ya.y; wa[m][2] = ya.z; wa[m][3] = ya.w;
+          wb[m][0] = yb.x; wb[m][1] = yb.y; wb[m][2] = yb.z; wb[m][3] = yb.w;
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const uint32_t brow = bst + (uint32_t)(32 * nb + 8 * q + g) * Cfg::kBRowB;
+          uint32_t bf[R / 16][2];
+#pragma unroll
+          for (int j = 0; j < R / 16; ++j) {
+            bf[j][0] = lds32(brow + (16 * j + c2) * 2);
+            bf[j][1] = lds32(brow + (16 * j + 8 + c2) * 2);
+          }
+#pragma unroll
+          for (int m = 0; m < MT; ++m) {
+            const float2 u0 = f2_of(wa[m][q]), u1 = f2_of(wb[m][q]);
+            float acc[4] = {u0.x, u0.y, u1.x, u1.y};
+#pragma unroll
+            for (int j = 0; j < R / 16; ++j) mma_bf16_16816(acc, hf[m][j], bf[j]);
+            wa[m][q] = bf16x2_of(acc[0], acc[1]);
+            wb[m][q] = bf16x2_of(acc[2], acc[3]);
+          }
+        }
+#pragma unroll
+        for (int m = 0; m < MT; ++m) {
+          const uint32_t y0 = st + (16 * m + g) * Cfg::kRowB + (uint32_t)(32 * nb + 8 * c) * 2;
+          sts128(y0, wa[m]);
+          sts128(y0 + 8 * Cfg::kRowB, wb[m]);
+        }
+      }
+      __syncthreads();
+      // the chunk's new rows back to y, 16 bytes a thread
+      const int pr = nc / 8;
+      for (int e = tid; e < rows * pr; e += blockDim.x) {
+        const int row = e / pr, col = (e - row * pr) * 8;
+        *reinterpret_cast<uint4*>(Y + (int64_t)(r0 + row) * a.d_out + n0 + col) =
+            lds128(st + row * Cfg::kRowB + col * 2);
       }
     }
+    cp_async_wait<0>();  // only empty groups are left
+    __syncthreads();     // the next tile's copies may overwrite every stage
   }
+}
+
+template <int R>
+cudaError_t launch_rank(const LoraArgs& a, int num_sms, cudaStream_t s) {
+  const size_t smem = (size_t)(((a.n + 1) * 4 + 127) / 128 * 128) + (size_t)LoraCfg<R>::kStages * LoraCfg<R>::kStage;
+  cudaError_t e = cudaFuncSetAttribute(lora_kernel<R>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  int per_sm = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, lora_kernel<R>, 32 * kLoraWarps, smem);
+  if (e != cudaSuccess) return e;
+  if (per_sm < 1) return cudaErrorInvalidConfiguration;
+  return launch_pdl(lora_kernel<R>, dim3(num_sms * per_sm), dim3(32 * kLoraWarps), smem, s, a);
 }
 
 }  // namespace
 
 cudaError_t launch_lora(const LoraArgs& a, int num_sms, cudaStream_t s) {
-  const size_t smem = sizeof(int32_t) * (size_t)(a.n + 1);
-  auto kern = a.rank == 16 ? lora_kernel<16> : a.rank == 32 ? lora_kernel<32> : lora_kernel<64>;
-  if (smem > 48 * 1024) {
-    const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-  }
-  return launch_pdl(kern, dim3(num_sms * 8), dim3(32 * kLoraWarps), smem, s, a);
+  if (a.rank == 16) return launch_rank<16>(a, num_sms, s);
+  if (a.rank == 32) return launch_rank<32>(a, num_sms, s);
+  return launch_rank<64>(a, num_sms, s);
 }
 
 }  // namespace kev

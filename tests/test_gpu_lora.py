@@ -4,10 +4,11 @@ that must write nothing.
 
 Tolerance, from the kernel's arithmetic (bf16 operands, fp32 accumulation): h = scale x A^T is
 accumulated in fp32 over d_in products (at most d_in 2^-24 sum_k |x_k A_rk| off, the worst-case
-bound of a sum of that length) and rounded to bf16 for the second product (at most 2^-9 |h_r|
-more); the new y is rounded once to bf16 (half a unit in the last place of the larger of the
-computed and exact values).  So per element
-  |got - ref| <= ulp(max(|ref|, |got|)) / 2 + sum_r |B[col, r]| (2^-9 |h_r| + d_in 2^-24 h1_r) + 1e-5,
+bound of a sum of that length) and rounded to bf16 for the second product (bf16 keeps 8
+significant bits, so round-to-nearest moves it by at most the unit roundoff 2^-8 |h_r|); the new
+y is rounded once to bf16 (half a unit in the last place of the larger of the computed and exact
+values).  So per element
+  |got - ref| <= ulp(max(|ref|, |got|)) / 2 + sum_r |B[col, r]| (2^-8 |h_r| + d_in 2^-24 h1_r) + 1e-5,
 h1_r = scale sum_k |x_k| |A_rk|, all in float64; the relative L2 error over all elements stays
 within 5e-3."""
 import numpy as np
@@ -47,7 +48,7 @@ def _assert_lora_close(got, ref, x64, iv, ids, A64, B64, scales, what):
         sc = abs(float(scales[a]))
         h = sc * np.abs(x64[s:e] @ A64[a].T)          # [rows, r]
         h1 = sc * np.abs(x64[s:e]) @ np.abs(A64[a]).T  # sum_k |x_k| |A_rk|
-        bound[s:e] = (2.0 ** -9 * h + d_in * 2.0 ** -24 * h1) @ np.abs(B64[a]).T
+        bound[s:e] = (2.0 ** -8 * h + d_in * 2.0 ** -24 * h1) @ np.abs(B64[a]).T
     bound += ulp_half + 1e-5
     err = np.abs(got - ref)
     assert np.all(np.isfinite(got)), f"{what}: non-finite output"
@@ -86,6 +87,39 @@ def test_lora_against_oracle(rank):
         if a >= 0:
             untouched[s:e] = False
     np.testing.assert_array_equal(host(dy)[untouched], y[untouched])  # no adapter, gaps: bit for bit
+
+
+@pytest.mark.parametrize("rank", [16, 64])
+def test_lora_smallest_dimensions(rank):
+    """d_in 64 and d_out 32 (one chunk each, fewer 32-column blocks than warps), one-row questions
+    and a question whose last tile has a single row."""
+    lengths, d_in, d_out, n_ad = [1, 17, 1, 40], 64, 32, 2
+    iv, T, x, y, A, B, sc = _case(120 + rank, lengths, d_in, d_out, rank, n_ad, gaps=[0, 1, 0, 3], tail=1)
+    ids = [0, 1, 1, 0]
+    status, dy = _run(iv, T, x, y, A, B, sc, ids, rank, d_in, d_out, n_ad)
+    assert status == 0
+    x64, A64, B64 = W.to_float64(x, "bf16"), W.to_float64(A, "bf16"), W.to_float64(B, "bf16")
+    ref = O.lora_apply(W.to_float64(y, "bf16"), x64, iv, ids, A64, B64, sc.astype(np.float64))
+    _assert_lora_close(f64(dy, "bf16"), ref, x64, iv, ids, A64, B64, sc, f"lora small rank {rank}")
+    untouched = np.ones(T, bool)
+    for s, e in iv:
+        untouched[s:e] = False
+    np.testing.assert_array_equal(host(dy)[untouched], y[untouched])
+
+
+def test_lora_most_questions():
+    """4096 questions of 1 to 40 rows (the most a call takes), adapters drawn at random, some
+    questions without one."""
+    rng = np.random.default_rng(130)
+    n, d_in, d_out, rank, n_ad = 4096, 64, 64, 16, 5
+    lengths = rng.integers(1, 41, n).tolist()
+    iv, T, x, y, A, B, sc = _case(131, lengths, d_in, d_out, rank, n_ad)
+    ids = rng.integers(-1, n_ad, n).tolist()
+    status, dy = _run(iv, T, x, y, A, B, sc, ids, rank, d_in, d_out, n_ad)
+    assert status == 0
+    x64, A64, B64 = W.to_float64(x, "bf16"), W.to_float64(A, "bf16"), W.to_float64(B, "bf16")
+    ref = O.lora_apply(W.to_float64(y, "bf16"), x64, iv, ids, A64, B64, sc.astype(np.float64))
+    _assert_lora_close(f64(dy, "bf16"), ref, x64, iv, ids, A64, B64, sc, "lora 4096 questions")
 
 
 def test_lora_qwen25_7b_projection_sampled_rows():

@@ -102,3 +102,26 @@ def test_invalid_temperature_or_uniform_writes_no_token():
     status, tokens = _run(x, "fp32", np.array([1.0, -0.5, 1.0, 1.0], np.float32),
                           np.array([0.1, 0.2, 0.3, 0.4], np.float32), np.array([1, 0, 1, 1], np.uint8))
     assert status == 0 and tokens[1] == -7 and (tokens[[0, 2, 3]] >= 0).all()
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+def test_sample_mass_in_later_segments(dtype):
+    """A 32,000-token vocabulary (the row split over two CTAs) and the Qwen3 one (eight): the
+    probability mass sits in one later part of the row per question (logits raised over a window),
+    uniforms on a grid up to just below 1, so the token comes from every part of the row and from
+    both ends of the cumulative distribution."""
+    rng = np.random.default_rng(42)
+    for vocab in (32000, 151936):
+        n = 48
+        x = rng.standard_normal((n, vocab), dtype=np.float32)
+        for i in range(n):
+            w0 = int(rng.integers(0, vocab - 4096))
+            x[i, w0:w0 + 4096] += 6.0
+        stored = W.f32_to_bf16_bits(x) if dtype == "bf16" else x
+        logits64 = W.to_float64(stored, dtype)
+        temperature = np.array([0.5, 1.0, 1.5, 0.0] * (n // 4), np.float32)
+        uniforms = np.concatenate([(np.arange(n - 2) + 0.5) / (n - 2), [0.0, 0.99999994]]).astype(np.float32)
+        active = np.ones(n, np.uint8)
+        status, tokens = _run(stored, dtype, temperature, uniforms, active)
+        assert status == 0
+        _assert_valid(tokens, logits64, temperature.astype(np.float64), uniforms, active, f"{dtype} vocab {vocab}")
