@@ -174,32 +174,43 @@ __global__ void __launch_bounds__(32 * kLoraWarps) lora_kernel(LoraArgs a) {
     // copies of chunk ci into stage ci % NS (every thread a share of its 16-byte pieces), then
     // one commit group per chunk, empty past the last one so the group count stays uniform;
     // rows past the tile's end are filled with zeros, not read
+    // Thread tid copies the 16-byte column pcol of rows prow + 8u of a stage (a chunk is 128
+    // columns, 16 pieces a row); its source rows are fixed for the tile, so their addresses are
+    // formed once here.  Rows past the tile's end are filled with zeros, not read; columns past
+    // d_in (d_out) in the last chunk are neither copied nor read.
+    static_assert(KC == 128 && 32 * kLoraWarps == 128, "16 pieces a row, 8 rows a pass of the block");
+    constexpr int U1 = (ROWS + R) / 8, U2 = ROWS / 8;
+    const int prow = tid >> 4, pcol = (tid & 15) * 8;
+    const __nv_bfloat16* src1[U1];  // x rows, then A_a rows (column pcol of chunk 0)
+#pragma unroll
+    for (int u = 0; u < U1; ++u) {
+      const int row = prow + 8 * u;
+      src1[u] = row < ROWS ? X + (int64_t)(r0 + (row < rows ? row : 0)) * a.d_in + pcol
+                           : A + (int64_t)(row - ROWS) * a.d_in + pcol;
+    }
+    __nv_bfloat16* ysrc[U2];  // y rows (column pcol of chunk 0): copied in, and written back
+#pragma unroll
+    for (int u = 0; u < U2; ++u) ysrc[u] = Y + (int64_t)(r0 + (prow + 8 * u < rows ? prow + 8 * u : 0)) * a.d_out + pcol;
     auto issue = [&](int ci) {
       if (ci < n_chunks) {
-        const uint32_t st = stages + (uint32_t)(ci % NS) * Cfg::kStage;
+        const uint32_t st = stages + (uint32_t)(ci % NS) * Cfg::kStage + prow * Cfg::kRowB + pcol * 2;
         if (ci < p1) {
-          const int c0 = ci * KC, pr = min(KC, a.d_in - c0) / 8;  // pieces per row
-          for (int e = tid; e < (ROWS + R) * pr; e += blockDim.x) {
-            const int row = e / pr, col = (e - row * pr) * 8;
-            const uint32_t dst = st + row * Cfg::kRowB + col * 2;
-            if (row < ROWS) {
-              const bool v = row < rows;
-              cp_async16(dst, X + (int64_t)(r0 + (v ? row : 0)) * a.d_in + c0 + col, v);
-            } else {
-              cp_async16(dst, A + (int64_t)(row - ROWS) * a.d_in + c0 + col, true);
-            }
+          const int c0 = ci * KC;
+          if (c0 + pcol < a.d_in) {
+#pragma unroll
+            for (int u = 0; u < U1; ++u)
+              cp_async16(st + 8 * u * Cfg::kRowB, src1[u] + c0, prow + 8 * u >= ROWS || prow + 8 * u < rows);
           }
         } else {
-          const int n0 = (ci - p1) * KC, nc = min(KC, a.d_out - n0), pr = nc / 8;
-          for (int e = tid; e < ROWS * pr; e += blockDim.x) {
-            const int row = e / pr, col = (e - row * pr) * 8;
-            const bool v = row < rows;
-            cp_async16(st + row * Cfg::kRowB + col * 2, Y + (int64_t)(r0 + (v ? row : 0)) * a.d_out + n0 + col, v);
+          const int n0 = (ci - p1) * KC, nc = min(KC, a.d_out - n0);
+          if (n0 + pcol < a.d_out) {
+#pragma unroll
+            for (int u = 0; u < U2; ++u) cp_async16(st + 8 * u * Cfg::kRowB, ysrc[u] + n0, prow + 8 * u < rows);
           }
-          for (int e = tid; e < nc * (R / 8); e += blockDim.x) {
-            const int j = e / (R / 8), part = e - j * (R / 8);
-            cp_async16(st + ROWS * Cfg::kRowB + b_pos(j) * Cfg::kBRowB + part * 16,
-                       B + (int64_t)(n0 + j) * R + part * 8, true);
+          const uint32_t bst = stages + (uint32_t)(ci % NS) * Cfg::kStage + ROWS * Cfg::kRowB;
+          for (int e = tid; e < nc * (R / 8); e += 32 * kLoraWarps) {
+            const int j = e / (R / 8), part = e % (R / 8);
+            cp_async16(bst + b_pos(j) * Cfg::kBRowB + part * 16, B + (int64_t)(n0 + j) * R + part * 8, true);
           }
         }
       }
@@ -326,12 +337,12 @@ __global__ void __launch_bounds__(32 * kLoraWarps) lora_kernel(LoraArgs a) {
         }
       }
       __syncthreads();
-      // the chunk's new rows back to y, 16 bytes a thread
-      const int pr = nc / 8;
-      for (int e = tid; e < rows * pr; e += blockDim.x) {
-        const int row = e / pr, col = (e - row * pr) * 8;
-        *reinterpret_cast<uint4*>(Y + (int64_t)(r0 + row) * a.d_out + n0 + col) =
-            lds128(st + row * Cfg::kRowB + col * 2);
+      // the chunk's new rows back to y, the pieces this thread copied in
+      if (n0 + pcol < a.d_out) {
+#pragma unroll
+        for (int u = 0; u < U2; ++u)
+          if (prow + 8 * u < rows)
+            *reinterpret_cast<uint4*>(ysrc[u] + n0) = lds128(st + (prow + 8 * u) * Cfg::kRowB + pcol * 2);
       }
     }
     cp_async_wait<0>();  // only empty groups are left
