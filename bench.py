@@ -609,7 +609,7 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="kev", choices=["kev", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", choices=["step", "decode", "rope"], default=None,
+    ap.add_argument("--only", choices=["step", "decode", "rope", "sampling", "lora"], default=None,
                     help="run only one workload's warm-up and timed loop (for profiling); prints no JSON line")
     args = ap.parse_args(argv)
     if args.warmup < 3:
@@ -676,6 +676,12 @@ def main(argv=None):
 
     if args.only == "decode":
         return _decode_only(args, kev, torch, dev, tdev)
+    if args.only == "sampling":
+        _sampling(kev, torch, tdev, dev, args.steps, args.warmup)
+        return None
+    if args.only == "lora":
+        _lora(kev, torch, tdev, dev, args.steps, args.warmup)
+        return None
     # The timed steps run back to back, each on the next of R full sets of buffers: one cycle
     # touches R x ~170 MB, several times the 129 MB L2, so no step finds its inputs in L2.
     copies = [step_buffers() for _ in range(STEP_COPIES)]
