@@ -37,6 +37,7 @@
  *    code is stored in *dev_status (if dev_status is not NULL) in stream order.
  *    kev_read_status turns it into a kev_status.
  *  - Scale: kev_attn_shape.scale == 0 means 1/sqrt(d).
+ *  - A call takes at most KEV_MAX_QUESTIONS questions (else KEV_ERR_UNSUPPORTED).
  */
 #ifndef KEV_H
 #define KEV_H
@@ -47,6 +48,8 @@
 #ifdef __cplusplus
 extern "C" {
 #endif
+
+#define KEV_MAX_QUESTIONS 4096
 
 typedef struct CUstream_st* kev_stream_t; /* same type as cudaStream_t; NULL = legacy default stream */
 

@@ -38,6 +38,7 @@ KEV_BF16 = 0
 KEV_FP32 = 1
 KEV_PAGE = 128
 KEV_MAX_PAGED_ENTRIES = 16384
+KEV_MAX_QUESTIONS = 4096
 
 STATUS_NAMES = {
     0: "KEV_OK", 1: "KEV_ERR_INVALID_ARG", 2: "KEV_ERR_UNSUPPORTED", 3: "KEV_ERR_INTERVALS",

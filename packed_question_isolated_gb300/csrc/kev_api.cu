@@ -361,7 +361,9 @@ kev_status kev_sample(const void* logits, int32_t n_questions, int32_t vocab, in
                       kev_stream_t stream) {
   if (n_questions < 0 || vocab <= 0) return KEV_ERR_INVALID_ARG;
   if (dtype != KEV_BF16 && dtype != KEV_FP32) return KEV_ERR_UNSUPPORTED;
-  if (n_questions > (1 << 20)) return KEV_ERR_UNSUPPORTED;
+  // every CTA checks every live question's temperature and uniform (so an invalid call writes
+  // no token): n^2 small reads, bounded by the library's question limit
+  if (n_questions > kMaxQuestions) return KEV_ERR_UNSUPPORTED;
   if (vocab % (dtype == KEV_BF16 ? 8 : 4)) return KEV_ERR_UNSUPPORTED;
   if (dev_status && ((uintptr_t)dev_status & 3u)) return KEV_ERR_INVALID_ARG;
   if (n_questions == 0) return KEV_OK;

@@ -226,7 +226,8 @@ cudaError_t launch_aux(const AuxArgs& a, int num_sms, cudaStream_t s);
 // ---------------------------------------------------------------------------------------
 constexpr int kPage = 128;                  // positions per block (= a decode chunk, a prefill tile)
 constexpr int kMaxPagedEntries = 16384;     // n_questions * max_blocks: the validation's hash capacity
-static_assert(kPage == KEV_PAGE && kMaxPagedEntries == KEV_MAX_PAGED_ENTRIES, "kev.h and the kernels agree");
+static_assert(kPage == KEV_PAGE && kMaxPagedEntries == KEV_MAX_PAGED_ENTRIES && kMaxQuestions == KEV_MAX_QUESTIONS,
+              "kev.h and the kernels agree");
 struct PagedCheckArgs {                     // prefill side: the block tables of the questions' lengths
   const kev_interval* intervals;
   const int32_t* block_table;

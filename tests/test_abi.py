@@ -24,6 +24,23 @@ def _declared():
     return sorted(set(re.findall(r"\b(kev_[a-z_]+)\s*\(", text)))
 
 
+def test_header_constants_match_the_binding(lib):
+    """Every integer #define and every kev_status / kev_dtype enumerator of kev.h has the same
+    value in the Python binding (the binding copies them by hand)."""
+    b = lib.binding
+    text = re.sub(r"/\*.*?\*/", "", open(os.path.join(ROOT, "include", "kev.h")).read(), flags=re.S)
+    consts = {}
+    for name, val in re.findall(r"#define\s+(KEV_[A-Z0-9_]+)\s+([0-9]+)\s*$", text, flags=re.M):
+        consts[name] = int(val)
+    for name, val, shift in re.findall(r"#define\s+(KEV_[A-Z0-9_]+)\s+\(([0-9]+)u\s*<<\s*([0-9]+)\)", text):
+        consts[name] = int(val) << int(shift)
+    for name, val in re.findall(r"\b(KEV_[A-Z0-9_]+)\s*=\s*([0-9]+)", text):
+        consts[name] = int(val)
+    assert {"KEV_OK", "KEV_ERR_ADAPTER", "KEV_BF16", "KEV_PAGE", "KEV_MAX_QUESTIONS"} <= set(consts)
+    for name, val in consts.items():
+        assert getattr(b, name) == val, name
+
+
 def test_every_declared_symbol_is_exported(lib):
     so = ctypes.CDLL(lib.library_path())
     declared = _declared()
@@ -153,6 +170,9 @@ def test_sample_host_errors_without_gpu(lib):
     assert lib.kev_sample(0x1000, 2, 128, 7, *args, None, stream=0, check=False) == b.KEV_ERR_UNSUPPORTED
     assert lib.kev_sample(0x1008, 2, 128, "bf16", *args, None, stream=0, check=False) == b.KEV_ERR_INVALID_ARG
     assert lib.kev_sample(None, 0, 128, "bf16", None, None, None, None, None, stream=0, check=False) == b.KEV_OK
+    # more questions than a call takes (the library's limit, the same for every entry point)
+    assert lib.kev_sample(0x1000, b.KEV_MAX_QUESTIONS + 1, 128, "bf16", *args, None, stream=0, check=False) == \
+        b.KEV_ERR_UNSUPPORTED
 
 
 def test_lora_host_errors_without_gpu(lib):
