@@ -63,7 +63,7 @@ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 inline PrefillLayout prefill_layout(int32_t n, int32_t T, int32_t h_q) {
   PrefillLayout L;
   size_t off = align_up(sizeof(PrefillHeader), 256);
-  L.max_tiles = (int64_t)((T + kTileM - 1) / kTileM) + n;
+  L.max_tiles = ((int64_t)T + kTileM - 1) / kTileM + n;  // 64-bit: T may be up to INT32_MAX
   L.max_items = L.max_tiles * (int64_t)h_q;
   L.cu_seqlens = off;
   off = align_up(off + sizeof(int32_t) * (size_t)(n + 1), 256);
@@ -101,7 +101,7 @@ inline int decode_head_block_size(int group) {
 // to 16) per item; the CUDA-core kernel takes blocks of up to 8.
 inline DecodeLayout decode_layout(int32_t n, int32_t cap, int32_t h_q, int32_t h_kv, int32_t d, bool tc) {
   DecodeLayout L;
-  L.max_chunks = (cap + kDecodeChunk - 1) / kDecodeChunk;
+  L.max_chunks = (int32_t)(((int64_t)cap + kDecodeChunk - 1) / kDecodeChunk);
   const int32_t G = h_q / h_kv;
   const int32_t nhb = tc ? 1 : (G + 7) / 8;
   const int32_t GT = tc ? 16 : decode_head_block_size(G);

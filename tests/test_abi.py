@@ -41,6 +41,20 @@ def test_header_constants_match_the_binding(lib):
         assert getattr(b, name) == val, name
 
 
+def test_workspace_sizes_at_the_int32_limit(lib):
+    """Sizes for the largest token count and slot capacity an int32 holds: computed without
+    overflow (monotone in T and cap, and at least the bytes of the work list they hold)."""
+    big = 2 ** 31 - 1
+    shape = lib.make_shape(4, 2, 128, "bf16")
+    s_big = lib.kev_prefill_workspace_size(1, big, shape)
+    s_less = lib.kev_prefill_workspace_size(1, big - 1000, shape)
+    assert s_big >= s_less > 0
+    assert s_big >= 16 * 4 * (big // 128)  # an int4 work item per (query tile, q-head)
+    d_big = lib.kev_decode_workspace_size(8, big, shape)
+    d_less = lib.kev_decode_workspace_size(8, big - 1000, shape)
+    assert d_big >= d_less > 0
+
+
 def test_every_declared_symbol_is_exported(lib):
     so = ctypes.CDLL(lib.library_path())
     declared = _declared()
