@@ -40,7 +40,8 @@ WORKLOAD = ("qwen25_7b_prefill: 8 questions, lengths U{256..2048} seed 2 (T=7921
 DECODE_WORKLOAD = ("qwen3_8b_decode: [64, 8, 2458, 128] bf16 pools, lens U{64..2400} seed 4, 32 of 64 questions "
                    "live, 1 new token each")
 PREFILL3_WORKLOAD = ("qwen3_8b_prefill: 32 questions, lengths clip(rint(exp(N(ln 512, 0.8))), 1, 4096) seed 3 "
-                     "(T=24100), H_q 32, H_kv 8, d 128, bf16, prefill attention alone")
+                     "(T=24100), H_q 32, H_kv 8, d 128, bf16; one call = segment build + prefill attention + slot "
+                     "write into [32, 8, 4096, 128] pools")
 STEP_COPIES = 3           # buffer sets the back-to-back steps cycle through
 DECODE_COPIES = 2
 
@@ -243,7 +244,7 @@ def run_reference(args):
 # GPU arm
 # ---------------------------------------------------------------------------------------
 
-def _stress_decode_graph(kev, torch, dev, tdev):
+def _stress_decode_graph(kev, torch, dev, tdev, tf_peak, hbm_peak):
     """The stress batch: prefill into the slot pools, then its 128-step decode loop with early
     stop (decode + lens advance per step, each step with its own live set and inputs) captured
     once as a CUDA graph and replayed.  L2 is not flushed between the steps of a replay."""
@@ -316,8 +317,10 @@ def _stress_decode_graph(kev, torch, dev, tdev):
     return {"workload": "stress: 256 questions (T=19483), H_q 32, H_kv 8, d 128, bf16, cap 4224; prefill with slot "
                         "write, then 128 decode steps with early stop (116 with live questions)",
             "prefill_tflops": useful / (pre_avg * 1e-3) / 1e12, "prefill_ms": pre_avg,
+            "prefill_frac": useful / (pre_avg * 1e-3) / 1e12 / tf_peak,
             "decode_graph_ms": ms, "decode_steps": steps, "decode_bytes": total_bytes,
-            "decode_gbs": total_bytes / (ms * 1e-3) / 1e9, "launches_per_step": kev.kev_launch_count(4) + 1,
+            "decode_gbs": total_bytes / (ms * 1e-3) / 1e9, "decode_frac": total_bytes / (ms * 1e-3) / 1e9 / hbm_peak,
+            "launches_per_step": kev.kev_launch_count(4) + 1,
             "l2": "not flushed between the steps of a graph replay (L2 may hold part of the working set)"}
 
 
@@ -571,6 +574,63 @@ def _paged_decode(kev, torch, tdev, dev, K, warmup):
     return out
 
 
+def _prefill_qwen3_8b(kev, torch, tdev, dev, K, warmup, tf_peak, peak_src):
+    """The Qwen3-8B-shaped batch (T = 24,100) as the workload states it: prefill + slot write.
+    One call = kev_prefill_attn (segment build, attention, slot write into [32, 8, 4096, 128]
+    pools), back to back over two buffer sets of ~1 GB each (inputs, output, pools), so no call
+    finds its inputs in L2.  Also reported: the attention kernel alone over a prebuilt work list."""
+    w3 = W.qwen3_8b_prefill()
+    N3, T3 = w3.n_questions, w3.total_tokens
+    shape3 = kev.make_shape(w3.h_q, w3.h_kv, w3.d, "bf16")
+    ws3_bytes = kev.kev_prefill_workspace_size(N3, T3, shape3)
+    p3 = []
+    for _ in range(2):
+        c = {"q": tdev(w3.q), "k": tdev(w3.k), "v": tdev(w3.v), "iv": tdev(w3.intervals), "sl": tdev(w3.slot_ids),
+             "out": torch.empty((T3, w3.h_q, w3.d), dtype=torch.bfloat16, device=dev),
+             "pk": torch.zeros((w3.n_slots, w3.h_kv, w3.cap, w3.d), dtype=torch.bfloat16, device=dev),
+             "ws": torch.empty(ws3_bytes, dtype=torch.uint8, device=dev),
+             "st": torch.zeros(1, dtype=torch.int32, device=dev)}
+        c["pv"] = torch.zeros_like(c["pk"])
+        p3.append(c)
+    set_bytes = sum(t.numel() * t.element_size() for t in p3[0].values())
+
+    def call(c):
+        kev.kev_prefill_attn(c["q"], c["k"], c["v"], T3, c["iv"], N3, c["sl"], c["pk"], c["pv"], w3.n_slots, w3.cap,
+                             c["out"], shape3, c["ws"], ws3_bytes, c["st"])
+
+    def attn_only(c):
+        kev.kev_prefill_from_segments(c["q"], c["k"], c["v"], T3, c["iv"], N3, None, None, None, 0, 0, c["out"],
+                                      shape3, c["ws"], ws3_bytes, c["st"])
+
+    for fn in (call, attn_only):
+        for _ in range(warmup):
+            for c in p3:
+                fn(c)
+    torch.cuda.synchronize()
+    assert all(kev.kev_read_status(c["st"]) == 0 for c in p3)
+    timed = {}
+    for name, fn in (("call", call), ("attn", attn_only)):
+        a3, b3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a3.record()
+        for it in range(K):
+            fn(p3[it % 2])
+        b3.record()
+        torch.cuda.synchronize()
+        timed[name] = a3.elapsed_time(b3) / K
+    assert all(kev.kev_read_status(c["st"]) == 0 for c in p3)
+    useful3 = RL.prefill_useful_flops(w3.lengths, w3.h_q, w3.d)
+    tf = useful3 / (timed["call"] * 1e-3) / 1e12
+    tf_attn = useful3 / (timed["attn"] * 1e-3) / 1e12
+    del p3
+    return {"workload": PREFILL3_WORKLOAD, "value": tf, "unit": "TFLOP/s", "ms_per_call": timed["call"],
+            "useful_gflop": useful3 / 1e9,
+            "roofline": {"bound": "tensor", "achieved": tf, "peak": tf_peak, "unit": "TFLOP/s", "frac": tf / tf_peak,
+                         "kernel": "kev_prefill_attn: segment build + attention + slot write",
+                         "peak_source": f"bf16_tflops burst, {peak_src}"},
+            "attention_alone": {"value": tf_attn, "ms_per_launch": timed["attn"], "frac": tf_attn / tf_peak},
+            "l2": f"not flushed; {K} calls back to back over 2 buffer sets of {set_bytes / 1e6:.0f} MB"}
+
+
 def _decode_setup(kev, torch, dev, tdev):
     """The decode workload's buffer sets (DECODE_COPIES of them) and its call."""
     dwl = W.qwen3_8b_decode()
@@ -609,7 +669,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="kev", choices=["kev", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", choices=["step", "decode", "rope", "sampling", "lora"], default=None,
+    ap.add_argument("--only", choices=["step", "decode", "rope", "sampling", "lora", "stress", "prefill3"],
+                    default=None,
                     help="run only one workload's warm-up and timed loop (for profiling); prints no JSON line")
     args = ap.parse_args(argv)
     if args.warmup < 3:
@@ -682,6 +743,12 @@ def main(argv=None):
     if args.only == "lora":
         _lora(kev, torch, tdev, dev, args.steps, args.warmup)
         return None
+    if args.only == "stress":
+        _stress_decode_graph(kev, torch, dev, tdev, 1.0, 1.0)
+        return None
+    if args.only == "prefill3":
+        _prefill_qwen3_8b(kev, torch, tdev, dev, args.steps, args.warmup, 1.0, "")
+        return None
     # The timed steps run back to back, each on the next of R full sets of buffers: one cycle
     # touches R x ~170 MB, several times the 129 MB L2, so no step finds its inputs in L2.
     copies = [step_buffers() for _ in range(STEP_COPIES)]
@@ -733,35 +800,58 @@ def main(argv=None):
     step_bytes = sum(t.numel() * t.element_size() for t in copies[0].values())
 
     # ---- e2e: host buffers, copies inside the timed region ------------------------------
+    # Every step copies its inputs from pinned host memory and its two outputs back.  Three
+    # streams overlap step i's compute with step i+1's host-to-device copies and step i-1's
+    # device-to-host copies; steps alternate between two device buffer sets and two pinned
+    # output sets, and events order each copy after the last use of the buffers it overwrites.
     def pinned(t):
         return t.cpu().pin_memory()
     in_keys = ("q", "k", "v", "iv", "sl", "qn", "kn", "vn", "ln", "act")
-    c0 = copies[0]
-    h_in = [pinned(c0[x]) for x in in_keys]
-    h_out = [torch.empty(c0["out"].shape, dtype=c0["out"].dtype, pin_memory=True),
-             torch.empty(c0["on"].shape, dtype=c0["on"].dtype, pin_memory=True)]
+    h_in = [pinned(copies[0][x]) for x in in_keys]
+    h_outs = [[torch.empty(copies[0]["out"].shape, dtype=copies[0]["out"].dtype, pin_memory=True),
+               torch.empty(copies[0]["on"].shape, dtype=copies[0]["on"].dtype, pin_memory=True)] for _ in range(2)]
     h2d = sum(x.numel() * x.element_size() for x in h_in)
-    d2h = sum(x.numel() * x.element_size() for x in h_out)
+    d2h = sum(x.numel() * x.element_size() for x in h_outs[0])
+    s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    s_comp = torch.cuda.current_stream()
 
-    def e2e_step():
-        for hd, key in zip(h_in, in_keys):
-            c0[key].copy_(hd, non_blocking=True)
-        step(c0)
-        h_out[0].copy_(c0["out"], non_blocking=True)
-        h_out[1].copy_(c0["on"], non_blocking=True)
+    def e2e_run(n_steps):
+        ev_in = [torch.cuda.Event() for _ in range(n_steps)]
+        ev_comp = [torch.cuda.Event() for _ in range(n_steps)]
+        ev_out = [torch.cuda.Event() for _ in range(n_steps)]
+        for i in range(n_steps):
+            c, ho = copies[i % 2], h_outs[i % 2]
+            with torch.cuda.stream(s_in):
+                if i >= 2:
+                    s_in.wait_event(ev_comp[i - 2])  # step i-2 has finished reading this input set
+                for hd, key in zip(h_in, in_keys):
+                    c[key].copy_(hd, non_blocking=True)
+                ev_in[i].record(s_in)
+            s_comp.wait_event(ev_in[i])
+            if i >= 2:
+                s_comp.wait_event(ev_out[i - 2])  # step i-2's outputs are on the host
+            step(c)
+            ev_comp[i].record(s_comp)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev_comp[i])
+                ho[0].copy_(c["out"], non_blocking=True)
+                ho[1].copy_(c["on"], non_blocking=True)
+                ev_out[i].record(s_out)
+        s_comp.wait_stream(s_in)
+        s_comp.wait_stream(s_out)
 
-    for _ in range(args.warmup):
-        e2e_step()
+    e2e_run(args.warmup)
     torch.cuda.synchronize()
+    assert statuses_ok(copies[:2])
     Ke = max(5, K // 2)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
     torch.cuda.synchronize()
     e0.record()
-    for _ in range(Ke):
-        e2e_step()
+    e2e_run(Ke)
     e1.record()
     torch.cuda.synchronize()
+    assert statuses_ok(copies[:2])
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
     e2e_value = aggregate_rate(useful, Ke, world, e2e_ms) / 1e12
 
@@ -797,43 +887,10 @@ def main(argv=None):
     sampling = _sampling(kev, torch, tdev, dev, Kd, args.warmup)
     lora = _lora(kev, torch, tdev, dev, Kd, args.warmup)
 
-    # ---- second prefill workload (Qwen3-8B-shaped batch): measured, not the headline ---------
-    # two buffer sets (each ~490 MB of q, k, v and output) used in turn, launches back to back
-    w3 = W.qwen3_8b_prefill()
-    shape3 = kev.make_shape(w3.h_q, w3.h_kv, w3.d, "bf16")
-    ws3_bytes = kev.kev_prefill_workspace_size(w3.n_questions, w3.total_tokens, shape3)
-    p3 = []
-    for _ in range(2):
-        c = {"q": tdev(w3.q), "k": tdev(w3.k), "v": tdev(w3.v), "iv": tdev(w3.intervals),
-             "out": torch.empty((w3.total_tokens, w3.h_q, w3.d), dtype=torch.bfloat16, device=dev),
-             "ws": torch.empty(ws3_bytes, dtype=torch.uint8, device=dev),
-             "st": torch.zeros(1, dtype=torch.int32, device=dev)}
-        kev.kev_build_segments(c["iv"], w3.n_questions, w3.total_tokens, None, 0, 0, shape3, c["ws"], ws3_bytes,
-                               c["st"])
-        p3.append(c)
+    # ---- second prefill workload (Qwen3-8B-shaped batch) as the workload states it ----------
+    prefill3 = _prefill_qwen3_8b(kev, torch, tdev, dev, max(6, K // 2), args.warmup, tf_peak, peak_src)
 
-    def p3_call(c):
-        kev.kev_prefill_from_segments(c["q"], c["k"], c["v"], w3.total_tokens, c["iv"], w3.n_questions, None, None,
-                                      None, 0, 0, c["out"], shape3, c["ws"], ws3_bytes, c["st"])
-
-    for _ in range(args.warmup):
-        for c in p3:
-            p3_call(c)
-    torch.cuda.synchronize()
-    K3 = max(6, K // 2)
-    a3, b3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a3.record()
-    for it in range(K3):
-        p3_call(p3[it % 2])
-    b3.record()
-    torch.cuda.synchronize()
-    assert all(kev.kev_read_status(c["st"]) == 0 for c in p3)
-    p3_avg = a3.elapsed_time(b3) / K3
-    useful3 = RL.prefill_useful_flops(w3.lengths, w3.h_q, w3.d)
-    p3_tf = useful3 / (p3_avg * 1e-3) / 1e12
-    del p3
-
-    stress = _stress_decode_graph(kev, torch, dev, tdev)
+    stress = _stress_decode_graph(kev, torch, dev, tdev, tf_peak, hbm_peak)
 
     cpu = cpu_fair = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -853,22 +910,22 @@ def main(argv=None):
                               "workspaces) used in turn"),
                        "parallelism": f"replicas x{world} (independent question batches)"},
             "clocks": clocks,
-            "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                    "ms_per_step": e2e_ms / Ke},
-            "gpu_launches": launches_per_step * K,
-            "roofline": {"bound": "tensor", "achieved": achieved, "peak": tf_peak, "unit": "TFLOP/s",
-                         "frac": achieved / tf_peak, "traffic": traffic,
-                         "kernel": "prefill attention (kev_prefill_from_segments)",
-                         "peak_source": f"bf16_tflops burst, {peak_src}", "launch_ms": attn_avg_ms},
             "decode": {"workload": DECODE_WORKLOAD, "value": dec_job_gbs, "unit": "GB/s", "ms_per_step": dec_ms,
                        "l2": (f"not flushed; {Kd} calls back to back over {DECODE_COPIES} pool sets "
                               f"({dec_bytes / 1e6:.0f} MB read per call)"),
                        "roofline": {"bound": "hbm", "achieved": dec_gbs, "peak": hbm_peak, "unit": "GB/s",
                                     "frac": dec_gbs / hbm_peak, "traffic": dec_traffic,
                                     "algorithmic_bytes": dec_bytes, "peak_source": f"hbm_gbs, {peak_src}"}},
-            "prefill_qwen3_8b": {"workload": PREFILL3_WORKLOAD, "value": p3_tf, "unit": "TFLOP/s",
-                                 "ms_per_launch": p3_avg, "useful_gflop": useful3 / 1e9,
-                                 "frac": p3_tf / tf_peak, "peak_source": f"bf16_tflops burst, {peak_src}"},
+            "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "ms_per_step": e2e_ms / Ke,
+                    "overlap": "H2D of step i+1 and D2H of step i-1 on their own streams during step i's compute "
+                               "(two device buffer sets, two pinned output sets)"},
+            "gpu_launches": launches_per_step * K,
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": tf_peak, "unit": "TFLOP/s",
+                         "frac": achieved / tf_peak, "traffic": traffic,
+                         "kernel": "prefill attention (kev_prefill_from_segments)",
+                         "peak_source": f"bf16_tflops burst, {peak_src}", "launch_ms": attn_avg_ms},
+            "prefill_qwen3_8b": prefill3,
             "rope": rope,
             "paged_decode": paged,
             "chunked_prefill": chunked,

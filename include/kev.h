@@ -192,12 +192,17 @@ kev_status kev_decode_attn(const void* q_new, const void* k_new, const void* v_n
  * latency-critical path where cudaMalloc/cudaFree and their device synchronisation are not
  * allowed).  Same arguments, results and errors as kev_decode_attn, minus the workspace.
  * Scratch: a fixed device array of KEV_STATIC_SCRATCH_BYTES inside the library, held by every
- * GPU that loads it until the process exits.  Calls needing more scratch than that
- * (kev_decode_workspace_size(...) > KEV_STATIC_SCRATCH_BYTES) return KEV_ERR_UNSUPPORTED and
- * launch nothing.  The first call on a device looks up the array's device address and clears
- * it (in stream order), so make that first call before any stream capture.  Every call shares
- * the array: calls that overlap on the GPU race on it and give wrong results.  Allocates
- * nothing (no cudaMalloc/cudaFree, no allocating library routine). */
+ * GPU that loads it until the process exits.  The host checks of kev_decode_attn come first
+ * (same codes, same order); then a call needing more scratch than the array holds
+ * (kev_decode_workspace_size(...) > KEV_STATIC_SCRATCH_BYTES) returns KEV_ERR_UNSUPPORTED and
+ * launches nothing.  The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress), so make that first call before any stream capture.  Every call
+ * clears, in stream order and before its kernels, the part of the array that must start at
+ * zero (scheduling words and arrival counters, a few KB): a call that ended in
+ * KEV_ERR_TIMEOUT leaves nothing behind for the next one, unlike a caller workspace, which
+ * must then be zeroed again.  Every call shares the array: calls that overlap on the GPU race
+ * on it and give wrong results.  Allocates nothing (no cudaMalloc/cudaFree, no allocating
+ * library routine). */
 kev_status kev_decode_attn_static(const void* q_new, const void* k_new, const void* v_new,
                                   void* pool_k, void* pool_v, int32_t n_slots, int32_t slot_cap,
                                   const int32_t* slot_ids, const int32_t* lens, const uint8_t* active,

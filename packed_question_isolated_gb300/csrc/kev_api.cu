@@ -90,6 +90,30 @@ SegmentsArgs segments_args(const kev_interval* intervals, int32_t n, int32_t T, 
 
 }  // namespace
 
+// Host checks of kev_decode_attn's arguments other than the workspace, in its order.
+kev_status kev::decode_check_args(const void* q_new, const void* k_new, const void* v_new, const void* pool_k,
+                                  const void* pool_v, int32_t n_slots, int32_t slot_cap, const int32_t* slot_ids,
+                                  const int32_t* lens, const uint8_t* active, int32_t n_questions, const void* out,
+                                  const kev_attn_shape* shape, const int32_t* dev_status) {
+  kev_status st = check_shape(shape);
+  if (st != KEV_OK) return st;
+  if (n_questions < 0 || n_slots <= 0 || slot_cap <= 0) return KEV_ERR_INVALID_ARG;
+  if (n_questions > kMaxQuestions) return KEV_ERR_UNSUPPORTED;
+  if (dev_status && ((uintptr_t)dev_status & 3u)) return KEV_ERR_INVALID_ARG;
+  if (n_questions == 0) return KEV_OK;
+  if (!q_new || !k_new || !v_new || !pool_k || !pool_v || !out || !slot_ids || !lens || !active)
+    return KEV_ERR_INVALID_ARG;
+  if (!aligned16(q_new) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(pool_k) || !aligned16(pool_v) ||
+      !aligned16(out) || ((uintptr_t)slot_ids & 3u) || ((uintptr_t)lens & 3u))
+    return KEV_ERR_INVALID_ARG;
+  return KEV_OK;
+}
+
+// The decode workspace layout of a call with these sizes (valid shape assumed).
+DecodeLayout kev::decode_layout_of(int32_t n_questions, int32_t slot_cap, const kev_attn_shape* shape) {
+  return decode_layout(n_questions, slot_cap, shape->h_q, shape->h_kv, shape->d_h, decode_on_tensor_cores(shape));
+}
+
 extern "C" {
 
 size_t kev_prefill_workspace_size(int32_t n_questions, int32_t total_tokens, const kev_attn_shape* shape) {
@@ -718,20 +742,13 @@ kev_status kev_decode_attn(const void* q_new, const void* k_new, const void* v_n
                            int32_t n_slots, int32_t slot_cap, const int32_t* slot_ids, const int32_t* lens,
                            const uint8_t* active, int32_t n_questions, void* out, const kev_attn_shape* shape,
                            void* workspace, size_t workspace_bytes, int32_t* dev_status, kev_stream_t stream) {
-  kev_status st = check_shape(shape);
+  kev_status st = kev::decode_check_args(q_new, k_new, v_new, pool_k, pool_v, n_slots, slot_cap, slot_ids, lens,
+                                         active, n_questions, out, shape, dev_status);
   if (st != KEV_OK) return st;
-  if (n_questions < 0 || n_slots <= 0 || slot_cap <= 0) return KEV_ERR_INVALID_ARG;
-  if (n_questions > kMaxQuestions) return KEV_ERR_UNSUPPORTED;
-  if (dev_status && ((uintptr_t)dev_status & 3u)) return KEV_ERR_INVALID_ARG;
   if (n_questions == 0) {
     if (dev_status) return from_cuda(cudaMemsetAsync(dev_status, 0, sizeof(int32_t), (cudaStream_t)stream));
     return KEV_OK;
   }
-  if (!q_new || !k_new || !v_new || !pool_k || !pool_v || !out || !slot_ids || !lens || !active)
-    return KEV_ERR_INVALID_ARG;
-  if (!aligned16(q_new) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(pool_k) || !aligned16(pool_v) ||
-      !aligned16(out) || ((uintptr_t)slot_ids & 3u) || ((uintptr_t)lens & 3u))
-    return KEV_ERR_INVALID_ARG;
   const DecodeLayout layout =
       decode_layout(n_questions, slot_cap, shape->h_q, shape->h_kv, shape->d_h, decode_on_tensor_cores(shape));
   if (!workspace || ((uintptr_t)workspace & 255u) || workspace_bytes < layout.total) return KEV_ERR_INVALID_ARG;

@@ -63,6 +63,7 @@ struct DSmem {
 
 struct DBars {
   uint64_t full[kMaxStages];
+  uint64_t stall;  // timeout test hook: nothing ever arrives on it
   int flags;
   int last;
   int abort;
@@ -162,6 +163,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
   if (running < 0) return;
   if (tid == 0) {
     for (int s = 0; s < L::kStages; ++s) mbar_init(&bars->full[s], 1);
+    mbar_init(&bars->stall, 1);
     fence_mbar_init();
   }
   __syncthreads();  // the hash is dead from here on: the stages may be written
@@ -174,7 +176,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
   const int x_end = range_start(blockIdx.x + 1, total, nb);
   volatile int* abort_flag = &bars->abort;
   const volatile int* never = &bars->never;
-  const long long budget = 4000000000ll;
+  const long long budget = a.wait_budget;
 
   // Thread 0 issues the bulk copies of a chunk: K rows, V rows (positions already in the
   // pool) and the item's queries, all counted on the stage's mbarrier.
@@ -233,7 +235,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
         for (int e = 0; e < 4; ++e) o2[g][e] = 0ull;
     }
 
-    const bool landed = mbar_wait(&bars->full[s], round & 1, abort_flag, budget);
+    bool landed = mbar_wait(&bars->full[s], round & 1, abort_flag, budget);
+    // timeout test hook: before its first chunk CTA 0 waits on a barrier nothing arrives on
+    if (a.test_stall && blockIdx.x == 0 && iter == 0) landed = mbar_wait(&bars->stall, 0, abort_flag, budget) && landed;
     if (!named_sync_and(landed)) {
       if (tid == 0) {
         set_status(a.dev_status, ST_TIMEOUT);
@@ -507,9 +511,12 @@ __global__ void advance_kernel(int32_t* lens, const uint8_t* active, int32_t n) 
 }
 
 template <typename T, int D, int GT, int NS>
-cudaError_t launch_stages(const DecodeArgs& a, int num_sms, cudaStream_t s) {
+cudaError_t launch_stages(const DecodeArgs& args, int num_sms, cudaStream_t s) {
   using L = DSmem<D, (int)sizeof(T), GT, NS>;
   static_assert(L::kStages * L::kStageBytes >= 2 * kMaxQuestions * 4, "the validation hash lives in the stages");
+  DecodeArgs a = args;
+  a.wait_budget = wait_budget_cycles();
+  a.test_stall = test_stall_requested();
   const int smem = L::bytes(a.n);
   cudaError_t e = cudaFuncSetAttribute(decode_kernel<T, D, GT, NS>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;

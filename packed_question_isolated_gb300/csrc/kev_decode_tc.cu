@@ -94,6 +94,7 @@ struct TBars {
   uint64_t fixed, s_full[2], s_free[2], p_full[2], o_done[2];
   uint64_t o_full[2], o_free[2], pc_full[2];  // per piece buffer: O^T complete, O^T + info consumed, info written
   uint64_t drain_s, drain_p;
+  uint64_t stall;  // timeout test hook: nothing ever arrives on it
   uint32_t tmem_base;
   int flags, last, abort, never;
   int scan_tmp[11];
@@ -248,6 +249,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
     }
     mbar_init(&bars->drain_s, 1);
     mbar_init(&bars->drain_p, 1);
+    mbar_init(&bars->stall, 1);
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
@@ -289,7 +291,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
       // ---------------------------------------------------------------- TMA producer
       if (lane == 0) {
         uint32_t issued[3] = {0, 0, 0};
-        bool ok = true;
+        // timeout test hook: a wait that runs out (nothing arrives), then the abort path
+        bool ok = !(a.test_stall && blockIdx.x == 0) || mbar_wait(&bars->stall, 0, abort_flag, budget);
         const BatchPlan plan = make_plan(total, gridDim.x);
         int k = 0;  // position in the stage ring
         // the next grab goes out when a batch starts: its round trip hides behind the batch
@@ -783,15 +786,6 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_rows
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-long long wait_budget_cycles() {
-  const char* s = getenv("KEV_TEST_WAIT_LIMIT");
-  if (s && *s) {
-    const long long v = atoll(s);
-    if (v > 0) return v;
-  }
-  return 4000000000ll;
-}
-
 template <int NS, int NH>
 cudaError_t launch_ns(const DecodeArgs& a, int num_sms, cudaStream_t st, const CUtensorMap& mk,
                       const CUtensorMap& mv, const CUtensorMap& mq) {
@@ -801,6 +795,7 @@ cudaError_t launch_ns(const DecodeArgs& a, int num_sms, cudaStream_t st, const C
   if (e != cudaSuccess) return e;
   DTcParams p;
   p.a = a;
+  p.a.test_stall = test_stall_requested();
   p.wait_budget = wait_budget_cycles();
   e = launch_pdl(decode_tc_kernel<NS, NH>, dim3(num_sms), dim3(kThreads), (size_t)smem, st, mk, mv, mq, p);
   if (e != cudaSuccess) return e;

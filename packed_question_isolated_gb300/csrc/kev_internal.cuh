@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <stdint.h>
+#include <stdlib.h>
 
 #include "../../include/kev.h"
 
@@ -59,6 +60,28 @@ struct PrefillLayout {
 };
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Cycle budget of one bounded wait inside a kernel: about two seconds at the top SM clock, or
+// the value of the environment variable KEV_TEST_WAIT_LIMIT (cycles), read at every launch, so
+// that a test can shorten it.
+inline long long wait_budget_cycles() {
+  const char* s = getenv("KEV_TEST_WAIT_LIMIT");
+  if (s && *s) {
+    const long long v = atoll(s);
+    if (v > 0) return v;
+  }
+  return 4000000000ll;
+}
+
+// Test hook of the timeout path: with KEV_TEST_STALL=1 in the environment at launch, CTA 0 of
+// the prefill and decode attention kernels first waits on an mbarrier that nothing ever
+// arrives on.  The wait runs out after the budget above, and the kernel takes its real abort
+// path (status KEV_ERR_TIMEOUT, abort flag, drain of its own copies and MMAs, TMEM freed, exit).
+// Nothing faults, traps or hangs.  Off (0) unless the variable is set.
+inline int test_stall_requested() {
+  const char* s = getenv("KEV_TEST_STALL");
+  return (s && *s == '1') ? 1 : 0;
+}
 
 inline PrefillLayout prefill_layout(int32_t n, int32_t T, int32_t h_q) {
   PrefillLayout L;
@@ -213,6 +236,9 @@ struct DecodeArgs {
   const int32_t* block_table = nullptr;
   int32_t max_blocks = 0;
   int32_t n_blocks = 0;
+  // bounded waits: cycles per wait, and the timeout test hook (both set by the launchers)
+  long long wait_budget = 4000000000ll;
+  int32_t test_stall = 0;
 };
 
 // Host-side launchers (each returns the launch's cudaError_t).
@@ -301,6 +327,12 @@ struct RopeDecodeArgs {
 cudaError_t launch_rope_table(float2* table, int32_t max_pos, int32_t d, double theta, cudaStream_t s);
 cudaError_t launch_rope_prefill(const RopePrefillArgs& a, int num_sms, cudaStream_t s);
 cudaError_t launch_rope_decode(const RopeDecodeArgs& a, cudaStream_t s);
+// kev_api.cu: the host checks of kev_decode_attn other than the workspace, and its workspace layout
+kev_status decode_check_args(const void* q_new, const void* k_new, const void* v_new, const void* pool_k,
+                             const void* pool_v, int32_t n_slots, int32_t slot_cap, const int32_t* slot_ids,
+                             const int32_t* lens, const uint8_t* active, int32_t n_questions, const void* out,
+                             const kev_attn_shape* shape, const int32_t* dev_status);
+DecodeLayout decode_layout_of(int32_t n_questions, int32_t slot_cap, const kev_attn_shape* shape);
 cudaError_t launch_decode(const DecodeArgs& a, int d, kev_dtype dt, int num_sms, cudaStream_t s);     // CUDA cores
 cudaError_t launch_decode_tc(const DecodeArgs& a, int num_sms, cudaStream_t s);                       // bf16, d = 128
 cudaError_t launch_advance(int32_t* lens, const uint8_t* active, int32_t n, cudaStream_t s);

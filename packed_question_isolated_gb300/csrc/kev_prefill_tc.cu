@@ -74,6 +74,7 @@ struct TcParams {
   float scale_log2;  // scale * log2(e)
   int32_t* dev_status;
   long long wait_budget;  // cycles per bounded wait
+  int32_t test_stall;     // timeout test hook: CTA 0's K/V producer first waits on a barrier nothing arrives on
   // chunked prefill: K/V from the slots (the maps tm_k / tm_v are the pools' [rows, D] views)
   const int32_t* prefix_lens;
   const int32_t* slot_ids;
@@ -100,6 +101,7 @@ struct Bars {
   uint64_t s_full[2], p_full[2], o_done[2], o_free[2];
   uint64_t stg_free[4];  // slice q (rows 32q..32q+31) of the output stage has been read by its last store
   uint64_t drain[2];
+  uint64_t stall;  // timeout test hook: nothing ever arrives on it
   uint32_t tmem_base;
   int abort;
   int never;  // stays 0: abort flag for waits that must not give up early
@@ -218,6 +220,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int q = 0; q < 4; ++q) mbar_init(&bars->stg_free[q], 1);
     mbar_init(&bars->drain[0], 1);
     mbar_init(&bars->drain[1], 1);
+    mbar_init(&bars->stall, 1);
     bars->abort = 0;
     bars->never = 0;
     fence_mbar_init();
@@ -248,7 +251,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       uint32_t seq = 0;  // ring sequence: 2 ki is K(ki), 2 ki + 1 is V(ki)
       uint32_t loads[kRingSlots] = {};
-      bool ok = true;
+      // timeout test hook: a wait that runs out (nothing arrives), then the abort path
+      bool ok = !(p.test_stall && blockIdx.x == 0) || mbar_wait(&bars->stall, 0, abort_flag, budget);
       Item x_next = load_work<kChunk>(items, p, blockIdx.x);
       for (int rnd = 0, it = blockIdx.x; it < n_items && ok; it = snake_item(++rnd, blockIdx.x, gridDim.x)) {
         const Item x = x_next;  // loaded one item ahead: its latency hides behind this item
@@ -671,15 +675,6 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, ui
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-long long wait_budget_cycles() {
-  const char* s = getenv("KEV_TEST_WAIT_LIMIT");
-  if (s && *s) {
-    const long long v = atoll(s);
-    if (v > 0) return v;
-  }
-  return 4000000000ll;  // about two seconds at the top SM clock
-}
-
 template <int D>
 cudaError_t launch_tc(const PrefillArgs& a, int num_sms, cudaStream_t s) {
   const bool chunk = a.prefix_lens != nullptr;
@@ -703,6 +698,7 @@ cudaError_t launch_tc(const PrefillArgs& a, int num_sms, cudaStream_t s) {
   p.scale_log2 = a.scale * 1.4426950408889634f;
   p.dev_status = a.dev_status;
   p.wait_budget = wait_budget_cycles();
+  p.test_stall = test_stall_requested();
   p.prefix_lens = a.prefix_lens;
   p.slot_ids = a.slot_ids;
   p.h_kv = a.h_kv;
