@@ -119,10 +119,25 @@ kev_status kev_build_segments(const kev_interval* intervals, int32_t n_questions
  * bf16, whose kernel runs two query tiles that share every K/V tile; 1 for fp32); with
  * two_tiles (bf16, when a group of an odd size leaves one q-head over), that q-head's query
  * tiles starting at q_row_begin and q_row_begin + 128, q_rows being the second tile's rows.
- * Items come longest first.  Returns the item count, or -1 on error.  Writes at most
- * `max_items` items to `items_out` (host int32[4*max_items]). */
+ * Items come longest first.  Returns the item count, or -1 on error (or when the list is in
+ * unit form, below).  Writes at most `max_items` items to `items_out` (host int32[4*max_items]).
+ * This item form is built for fp32, for bf16 with d_h = 64 and for the chunked prefill. */
 int32_t kev_read_work_list(const void* workspace, size_t workspace_bytes, int32_t* items_out,
                            int32_t max_items, kev_stream_t stream);
+
+/* Host copy of the work list in unit form, built by kev_build_segments for bf16 with d_h = 128
+ * (synchronises `stream`): the work of the CTA-pair kernel, whose MMAs are 256 query rows tall,
+ * 128 from each CTA of a pair.  Each unit is 8 int32: {question, kv_head, nkv_A | (nkv_B << 16),
+ * 0, a0, a1, b0, b1}.  A "half" (a0 ... b1) is (m << 8) | h: query tile m of the question (rows
+ * begin + 128 m ...) with q-head kv_head * G + h, or -1 for none.  Tile A is halves a0, a1 (one
+ * per CTA), tile B halves b0, b1; tiles A and B share every K/V tile.  nkv_t is the key tiles
+ * tile t runs: the larger of its halves' m + 1, or 0 when both are -1.  Per question and kv head,
+ * the halves pair the q-heads (2e, 2e+1) of one query tile; with an odd group the last q-head
+ * pairs its tiles m and m + 1 (m even); units take these pairs two by two in order of key-tile
+ * count.  Units come longest first.  Returns the unit count, or -1 on error (or when the list is
+ * in item form).  Writes at most `max_units` units to `units_out` (host int32[8*max_units]). */
+int32_t kev_read_work_units(const void* workspace, size_t workspace_bytes, int32_t* units_out,
+                            int32_t max_units, kev_stream_t stream);
 
 /* Attention over a work list already built in `workspace` by kev_build_segments with the
  * same intervals/slots (step 2 of prefill), plus the slot write when slot_ids != NULL:

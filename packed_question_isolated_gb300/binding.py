@@ -48,7 +48,7 @@ STATUS_NAMES = {
 
 # every symbol include/kev.h declares
 EXPORTED = [
-    "kev_prefill_workspace_size", "kev_build_segments", "kev_read_work_list",
+    "kev_prefill_workspace_size", "kev_build_segments", "kev_read_work_list", "kev_read_work_units",
     "kev_prefill_from_segments", "kev_prefill_attn", "kev_kv_write",
     "kev_decode_workspace_size", "kev_decode_attn", "kev_decode_advance",
     "kev_read_status", "kev_status_string", "kev_launch_count", "kev_decode_attn_static",
@@ -87,6 +87,7 @@ _c = {
     "kev_prefill_workspace_size": _sig("kev_prefill_workspace_size", _Z, _I, _I, _S),
     "kev_build_segments": _sig("kev_build_segments", _I, _P, _I, _I, _P, _I, _I, _S, _P, _Z, _P, _P),
     "kev_read_work_list": _sig("kev_read_work_list", _I, _P, _Z, _P, _I, _P),
+    "kev_read_work_units": _sig("kev_read_work_units", _I, _P, _Z, _P, _I, _P),
     "kev_prefill_from_segments": _sig("kev_prefill_from_segments", _I, _P, _P, _P, _I, _P, _I, _P, _P, _P,
                                       _I, _I, _P, _S, _P, _Z, _P, _P),
     "kev_prefill_attn": _sig("kev_prefill_attn", _I, _P, _P, _P, _I, _P, _I, _P, _P, _P, _I, _I, _P, _S,
@@ -201,6 +202,21 @@ def kev_read_work_list(workspace, workspace_bytes, max_items: int, stream=None):
         raise KevError(KEV_ERR_INVALID_ARG, "kev_read_work_list")
     m = min(n, int(max_items))
     return [tuple(buf[4 * j:4 * j + 4]) for j in range(m)], n
+
+
+def kev_read_work_units(workspace, workspace_bytes, max_units: int, stream=None):
+    """Returns the unit-form work list as (question, kv_head, nkv_a, nkv_b, a0, a1, b0, b1) tuples."""
+    buf = (ctypes.c_int32 * (8 * max(int(max_units), 1)))()
+    n = int(_c["kev_read_work_units"](_ptr(workspace), int(workspace_bytes), buf, int(max_units),
+                                      _stream(stream)))
+    if n < 0:
+        raise KevError(KEV_ERR_INVALID_ARG, "kev_read_work_units")
+    m = min(n, int(max_units))
+    out = []
+    for j in range(m):
+        w = buf[8 * j:8 * j + 8]
+        out.append((w[0], w[1], w[2] & 0xffff, w[2] >> 16, w[4], w[5], w[6], w[7]))
+    return out, n
 
 
 def kev_prefill_from_segments(q, k, v, total_tokens, intervals, n_questions, slot_ids, pool_k, pool_v, n_slots,

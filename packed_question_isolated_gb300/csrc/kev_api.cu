@@ -40,6 +40,15 @@ float effective_scale(const kev_attn_shape* s) {
 
 int elem_size(const kev_attn_shape* s) { return s->dtype == KEV_BF16 ? 2 : 4; }
 
+// bf16 prefill with d = 128 runs on CTA pairs (2-SM MMAs, unit work list); bf16 with d = 64 and the
+// chunked prefill on single CTAs (item work list).
+bool prefill_on_pairs(const kev_attn_shape* s) { return s->dtype == KEV_BF16 && s->d_h == 128; }
+
+cudaError_t launch_prefill(const PrefillArgs& p, const kev_attn_shape* shape, int sms, cudaStream_t s) {
+  if (shape->dtype != KEV_BF16) return launch_prefill_simt(p, shape->d_h, sms, s);
+  return prefill_on_pairs(shape) ? launch_prefill_pair(p, sms, s) : launch_prefill_tc(p, shape->d_h, sms, s);
+}
+
 // bf16 with d = 128 decodes on the tensor cores; fp32 (no TF32) and d = 64 on the CUDA cores.
 bool decode_on_tensor_cores(const kev_attn_shape* s) {
   return s->dtype == KEV_BF16 && s->d_h == 128 && s->h_q / s->h_kv <= kDecodeTcMaxGroup;
@@ -82,6 +91,7 @@ SegmentsArgs segments_args(const kev_interval* intervals, int32_t n, int32_t T, 
   a.group = shape->h_q / shape->h_kv;
   // the tensor-core kernel takes two q-heads of a kv group per item, the fp32 kernel one
   a.heads_per_item = shape->dtype == KEV_BF16 ? 2 : 1;
+  a.units2 = prefill_on_pairs(shape) ? 1 : 0;
   a.ws = static_cast<char*>(ws);
   a.layout = prefill_layout(n, T, shape->h_q);
   a.dev_status = dev_status;
@@ -140,12 +150,30 @@ int32_t kev_read_work_list(const void* workspace, size_t workspace_bytes, int32_
   if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return -1;
   PrefillHeader h;
   if (cudaMemcpy(&h, workspace, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) return -1;
-  if (h.status != ST_OK) return -1;
+  if (h.status != ST_OK || h.format != 0) return -1;
   const PrefillLayout L = prefill_layout(h.n_questions, h.total_tokens, h.h_q);
   if (workspace_bytes < L.total) return -1;
   const int32_t cnt = h.n_items < max_items ? h.n_items : max_items;
   if (cnt > 0 && items_out) {
     if (cudaMemcpy(items_out, static_cast<const char*>(workspace) + L.items, sizeof(int4) * (size_t)cnt,
+                   cudaMemcpyDeviceToHost) != cudaSuccess)
+      return -1;
+  }
+  return h.n_items;
+}
+
+int32_t kev_read_work_units(const void* workspace, size_t workspace_bytes, int32_t* units_out, int32_t max_units,
+                            kev_stream_t stream) {
+  if (!workspace || workspace_bytes < sizeof(PrefillHeader) || max_units < 0) return -1;
+  if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return -1;
+  PrefillHeader h;
+  if (cudaMemcpy(&h, workspace, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) return -1;
+  if (h.status != ST_OK || h.format != 1) return -1;
+  const PrefillLayout L = prefill_layout(h.n_questions, h.total_tokens, h.h_q);
+  if (workspace_bytes < L.total) return -1;
+  const int32_t cnt = h.n_items < max_units ? h.n_items : max_units;
+  if (cnt > 0 && units_out) {
+    if (cudaMemcpy(units_out, static_cast<const char*>(workspace) + L.items, 2 * sizeof(int4) * (size_t)cnt,
                    cudaMemcpyDeviceToHost) != cudaSuccess)
       return -1;
   }
@@ -183,8 +211,7 @@ kev_status kev_prefill_from_segments(const void* q, const void* k, const void* v
   p.ws = static_cast<const char*>(workspace);
   p.layout = layout;
   p.dev_status = dev_status;
-  cudaError_t e = shape->dtype == KEV_BF16 ? launch_prefill_tc(p, shape->d_h, sms, s)
-                                            : launch_prefill_simt(p, shape->d_h, sms, s);
+  cudaError_t e = launch_prefill(p, shape, sms, s);
   if (e != cudaSuccess) return KEV_ERR_CUDA;
 
   AuxArgs x;
@@ -308,8 +335,7 @@ kev_status paged_prefill_tail(const void* q, const void* k, const void* v, int32
     p.ws = static_cast<const char*>(ws);
     p.layout = layout;
     p.dev_status = dev_status;
-    const cudaError_t e = shape->dtype == KEV_BF16 ? launch_prefill_tc(p, shape->d_h, sms, s)
-                                                   : launch_prefill_simt(p, shape->d_h, sms, s);
+    const cudaError_t e = launch_prefill(p, shape, sms, s);
     if (e != cudaSuccess) return KEV_ERR_CUDA;
     attention = T > 0;
   }
@@ -428,6 +454,7 @@ kev_status kev_prefill_chunk(const void* q, const void* k, const void* v, int32_
   SegmentsArgs sa = segments_args(intervals, n_questions, total_tokens, slot_ids, n_slots, slot_cap, shape, workspace,
                                   dev_status);
   sa.prefix_lens = prefix_lens;
+  sa.units2 = 0;  // the chunked prefill runs on single CTAs over the item list
   if (launch_segments(sa, s) != cudaSuccess) return KEV_ERR_CUDA;
   const PrefillLayout layout = prefill_layout(n_questions, total_tokens, shape->h_q);
   // 2. the chunk's K/V rows into the slots (the attention reads them there), gap rows of out

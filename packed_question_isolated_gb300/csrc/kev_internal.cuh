@@ -47,6 +47,7 @@ struct PrefillHeader {
   int32_t n_questions;
   int32_t total_tokens;
   int32_t h_q;
+  int32_t format;       // 0: items (one int4 each); 1: units of the CTA-pair kernel (two int4 each)
 };
 
 struct PrefillLayout {
@@ -87,7 +88,9 @@ inline PrefillLayout prefill_layout(int32_t n, int32_t T, int32_t h_q) {
   PrefillLayout L;
   size_t off = align_up(sizeof(PrefillHeader), 256);
   L.max_tiles = ((int64_t)T + kTileM - 1) / kTileM + n;  // 64-bit: T may be up to INT32_MAX
-  L.max_items = L.max_tiles * (int64_t)h_q;
+  // int4 records: items need at most max_tiles * h_q; CTA-pair units (two int4 each, one per
+  // kv head and pair of pair-tiles) at most h_kv * (max_tiles * ceil(G/2) + n) <= (max_tiles + n) * h_q
+  L.max_items = (L.max_tiles + n) * (int64_t)h_q;
   L.cu_seqlens = off;
   off = align_up(off + sizeof(int32_t) * (size_t)(n + 1), 256);
   L.tiles = off;
@@ -158,7 +161,15 @@ struct SegmentsArgs {
   PrefillLayout layout;
   int32_t* dev_status;  // may be null
   const int32_t* prefix_lens = nullptr;  // chunked prefill: cached positions before each chunk
+  int32_t units2 = 0;  // 1: emit the work units of the CTA-pair kernel instead of items
 };
+
+// Work unit of the CTA-pair prefill kernel (two int4): {question, kv head g, nkv_A | nkv_B << 16,
+// 0}, {s0, s1, s2, s3}.  A "half" s = (m << 8) | h is query tile m (rows m*128.. of the question)
+// of q-head g*G + h, or -1 (empty).  The 256-row MMA tile A is halves s0 (even CTA) and s1 (odd
+// CTA), tile B halves s2 and s3; nkv_t is the key tiles tile t runs (the larger of its halves'
+// m + 1; 0 for an absent tile).
+constexpr int kUnitHeadBits = 8;
 
 struct PrefillArgs {
   const void* q;
@@ -245,6 +256,7 @@ struct DecodeArgs {
 cudaError_t launch_segments(const SegmentsArgs& a, cudaStream_t s);
 cudaError_t launch_prefill_simt(const PrefillArgs& a, int d, int num_sms, cudaStream_t s);  // fp32
 cudaError_t launch_prefill_tc(const PrefillArgs& a, int d, int num_sms, cudaStream_t s);    // bf16
+cudaError_t launch_prefill_pair(const PrefillArgs& a, int num_sms, cudaStream_t s);         // bf16, d = 128
 cudaError_t launch_aux(const AuxArgs& a, int num_sms, cudaStream_t s);
 
 // ---------------------------------------------------------------------------------------

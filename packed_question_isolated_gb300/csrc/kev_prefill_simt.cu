@@ -22,6 +22,10 @@ __global__ void __launch_bounds__(kWarps * 32) prefill_simt_kernel(PrefillArgs a
   __shared__ float q_s[kWarps][D];
   const PrefillHeader* hdr = reinterpret_cast<const PrefillHeader*>(a.ws);
   if (hdr->status != ST_OK) return;
+  if (hdr->format != 0) {  // the work list was built for another kernel (another shape)
+    if (blockIdx.x == 0 && threadIdx.x == 0) set_status(a.dev_status, KEV_ERR_INVALID_ARG);
+    return;
+  }
   const int n_items = hdr->n_items;
   const int4* items = reinterpret_cast<const int4*>(a.ws + a.layout.items);
   const T* __restrict__ Q = static_cast<const T*>(a.q);

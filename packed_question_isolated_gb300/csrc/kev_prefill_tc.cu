@@ -200,6 +200,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   pdl_trigger();
   const PrefillHeader* hdr = reinterpret_cast<const PrefillHeader*>(p.ws);
   if (hdr->status != ST_OK) return;
+  if (hdr->format != 0) {  // the work list was built for another kernel (another shape)
+    if (blockIdx.x == 0 && threadIdx.x == 0) set_status(p.dev_status, KEV_ERR_INVALID_ARG);
+    return;
+  }
   const int n_items = hdr->n_items;
   if ((int)blockIdx.x >= n_items) return;
   const int4* items = reinterpret_cast<const int4*>(p.ws + p.layout.items);

@@ -65,6 +65,139 @@ __device__ int block_exclusive_scan(int v, int* tmp /* [kThreads/32 + 1] */, int
   return r;
 }
 
+// Work units of the CTA-pair prefill kernel.  A question of n query tiles has, in each kv
+// group of G q-heads, the (tile, head) pairs of its causal blocks.  They are grouped into
+// "pair-tiles", the 256-row MMA tiles of a CTA pair: heads (2e, 2e+1) of tile m, whose halves
+// both need key tiles 0..m; with G odd, the last head's tiles m and m+1 (m even) form one
+// pair-tile (its first half does one key step more than it needs, with zero weights), or tile
+// m alone if it is the question's last.  In order of key-tile count, consecutive pair-tiles
+// form a unit (tiles A, B, which share every K/V tile and differ by at most one key tile, two
+// when G = 1); an odd count leaves a last unit with tile B absent.  The enumeration depends
+// only on the question's own length, so a question's arithmetic does not depend on its
+// neighbours.  Rank m (key tiles m + 1) holds E = G/2 pair-tiles, plus one more when G is odd
+// and m is odd or the last rank.
+struct UnitShape {
+  int n, G, E, odd;
+  __device__ UnitShape(int n_, int G_) : n(n_), G(G_), E(G_ >> 1), odd(G_ & 1) {}
+  __device__ int pair_tiles() const { return n * E + odd * ((n + 1) >> 1); }
+  __device__ int units() const { return (pair_tiles() + 1) >> 1; }
+  // pair-tile p (in order of key-tile count): its two halves and key-tile count
+  __device__ void pair_tile(int p, int& h0, int& h1, int& nkv) const {
+    int m, k;
+    if (!odd) {
+      m = p / E;
+      k = p - m * E;
+    } else {
+      const int b = p / (2 * E + 1), r = p - b * (2 * E + 1);
+      m = r < E ? 2 * b : 2 * b + 1;
+      k = r < E ? r : r - E;
+      if (m >= n) {  // the odd head's tile n-1 alone (n odd)
+        m = n - 1;
+        k = E;
+      }
+    }
+    if (k < E) {
+      h0 = (m << kUnitHeadBits) | (2 * k);
+      h1 = (m << kUnitHeadBits) | (2 * k + 1);
+    } else if (m & 1) {  // the odd head's tiles m - 1 and m
+      h0 = ((m - 1) << kUnitHeadBits) | (G - 1);
+      h1 = (m << kUnitHeadBits) | (G - 1);
+    } else {  // the odd head's last tile, alone
+      h0 = (m << kUnitHeadBits) | (G - 1);
+      h1 = -1;
+    }
+    nkv = m + 1;
+  }
+  // unit u: pair-tiles 2u (tile A) and 2u + 1 (tile B, absent past the end)
+  __device__ void unit(int u, int4& w1, int& na, int& nb) const {
+    int a0, a1, b0 = -1, b1 = -1;
+    pair_tile(2 * u, a0, a1, na);
+    nb = 0;
+    if (2 * u + 1 < pair_tiles()) pair_tile(2 * u + 1, b0, b1, nb);
+    w1 = make_int4(a0, a1, b0, b1);
+  }
+};
+
+// One thread per (question, unit), longest first by cost bins; `base` (shared, n + 1 ints)
+// holds the questions' first unit indices.
+__device__ void emit_units(const SegmentsArgs& a, PrefillHeader* hdr, int4* out, int* bin_count, int* bin_cursor,
+                           int n_gaps, int* base, int* scan_tmp) {
+  const int tid = threadIdx.x;
+  const int h_kv = a.h_q / a.group;
+  auto n_tiles = [&](int i) { return (a.intervals[i].end - a.intervals[i].begin + kTileM - 1) / kTileM; };
+  __syncthreads();
+  if (tid < kCostBins) bin_count[tid] = 0;
+  int running = 0;
+  for (int b0 = 0; b0 < a.n; b0 += blockDim.x) {
+    const int i = b0 + tid;
+    const int cnt = i < a.n ? UnitShape(n_tiles(i), a.group).units() : 0;
+    int blk;
+    const int off = block_exclusive_scan(cnt, scan_tmp, &blk);
+    if (i < a.n) base[i] = running + off;
+    running += blk;
+  }
+  const int total = running;  // units per kv head
+  if (tid == 0) base[a.n] = total;
+  __syncthreads();
+  auto question_of = [&](int u) {
+    int lo = 0, hi = a.n;  // base[lo] <= u < base[hi]
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (base[mid] <= u) lo = mid; else hi = mid;
+    }
+    return lo;
+  };
+  // a unit's cost is its key-tile count (tile B's, the larger)
+  for (int u = tid; u < total; u += blockDim.x) {
+    const int i = question_of(u);
+    int4 w1;
+    int na, nb;
+    UnitShape(n_tiles(i), a.group).unit(u - base[i], w1, na, nb);
+    atomicAdd(&bin_count[min(max(na, nb) - 1, kCostBins - 1)], h_kv);
+  }
+  __syncthreads();
+  __shared__ int s_total;
+  if (tid < 32) {  // bins in descending order
+    const int hi = kCostBins - 1 - 2 * tid, lo = hi - 1;
+    const int c_hi = bin_count[hi], c_lo = bin_count[lo];
+    int x = c_hi + c_lo;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, o);
+      if (tid >= o) x += y;
+    }
+    const int b = x - (c_hi + c_lo);
+    bin_cursor[hi] = b;
+    bin_cursor[lo] = b + c_hi;
+    if (tid == 31) s_total = x;
+  }
+  __syncthreads();
+  for (int u = tid; u < total; u += blockDim.x) {
+    const int i = question_of(u);
+    int4 w1;
+    int na, nb;
+    UnitShape(n_tiles(i), a.group).unit(u - base[i], w1, na, nb);
+    const int pos = atomicAdd(&bin_cursor[min(max(na, nb) - 1, kCostBins - 1)], h_kv);
+    for (int g = 0; g < h_kv; ++g) {  // the kv heads of one unit stay adjacent (same query rows)
+      out[2 * (pos + g)] = make_int4(i, g, na | (nb << 16), 0);
+      out[2 * (pos + g) + 1] = w1;
+    }
+  }
+  __syncthreads();
+  if (tid == 0) {
+    hdr->n_items = s_total;
+    hdr->n_tiles = 0;
+    hdr->n_gaps = n_gaps;
+    hdr->status = ST_OK;
+    hdr->sched = 0;
+    hdr->n_questions = a.n;
+    hdr->total_tokens = a.T;
+    hdr->h_q = a.h_q;
+    hdr->format = 1;
+    if (a.dev_status) *a.dev_status = ST_OK;
+  }
+}
+
 __global__ void __launch_bounds__(kThreads) segments_kernel(SegmentsArgs a) {
   __shared__ unsigned long long keys[kMaxQuestions];
   __shared__ int s_flags;  // bit 0 intervals, bit 1 slot range, bit 2 overflow, bit 3 duplicate slot, bit 4 prefix
@@ -236,6 +369,7 @@ __global__ void __launch_bounds__(kThreads) segments_kernel(SegmentsArgs a) {
       hdr->n_questions = n;
       hdr->total_tokens = a.T;
       hdr->h_q = a.h_q;
+      hdr->format = a.units2;
       if (a.dev_status) *a.dev_status = code;
     }
     return;
@@ -252,6 +386,11 @@ __global__ void __launch_bounds__(kThreads) segments_kernel(SegmentsArgs a) {
     total_len += blk_total;
   }
   if (tid == 0) cu[n] = total_len;
+
+  if (a.units2) {  // the CTA-pair kernel's units instead of tiles and items
+    emit_units(a, hdr, items, bin_count, bin_cursor, s_ngaps, reinterpret_cast<int*>(keys), scan_tmp);
+    return;
+  }
 
   // 6. tile histogram over cost bins, then longest-first placement
   // a tile's cost is its number of key tiles: m + 1, plus the cached prefix's tiles
@@ -348,6 +487,7 @@ __global__ void __launch_bounds__(kThreads) segments_kernel(SegmentsArgs a) {
     hdr->n_questions = n;
     hdr->total_tokens = a.T;
     hdr->h_q = a.h_q;
+    hdr->format = 0;
     if (a.dev_status) *a.dev_status = ST_OK;
   }
 }

@@ -169,6 +169,49 @@ def test_work_list_covers_exactly_the_allowed_tiles(h_q, h_kv):
         assert n_two > 0
 
 
+@pytest.mark.parametrize("h_q,h_kv", [(4, 1), (7, 1), (14, 2), (2, 2), (3, 1), (16, 1)])
+def test_work_units_cover_exactly_the_allowed_tiles(h_q, h_kv):
+    """bf16 with d = 128: the CTA-pair kernel's units cover every allowed (head, query, key) entry
+    exactly once; a unit's halves share its kv head; tiles A and B differ by at most one key tile
+    (two for G = 1); units come longest first; and the output matches the oracle."""
+    import packed_question_isolated_gb300 as kev
+    w = W.random_case(98, [300, 1, 0, 129, 128, 257, 640, 1100], h_q, h_kv, 128, "bf16",
+                      gaps=[0, 2, 1, 0, 3, 1, 0, 4], tail=5)
+    run = PrefillRun(w)
+    run.run()
+    assert run.device_status() == 0
+    units, n = kev.kev_read_work_units(run.ws, run.ws_bytes, 100000)
+    assert n == len(units)
+    T = w.total_tokens
+    G = w.h_q // w.h_kv
+    allowed = O.allowed_mask(w.intervals, T)
+    covered = np.zeros((w.h_q, T, T), dtype=np.int32)
+    costs = []
+    for (qi, g, nkv_a, nkv_b, a0, a1, b0, b1) in units:
+        s, e = w.intervals[qi]
+        assert 0 <= g < w.h_kv
+        for nkv_t, halves in ((nkv_a, (a0, a1)), (nkv_b, (b0, b1))):
+            on = [x for x in halves if x >= 0]
+            assert nkv_t == (max((x >> 8) + 1 for x in on) if on else 0)
+            for x in on:
+                m, hl = x >> 8, x & 0xff
+                assert hl < G
+                t0 = s + 128 * m
+                tr = min(128, e - t0)
+                assert tr > 0
+                covered[g * G + hl, t0:t0 + tr, s:t0 + tr] += 1
+        assert nkv_a > 0 and (nkv_b == 0 or 0 <= nkv_b - nkv_a <= (2 if G == 1 else 1))
+        costs.append(max(nkv_a, nkv_b))
+    for h in range(w.h_q):
+        assert (covered[h][allowed] == 1).all(), "allowed entry not covered exactly once"
+        assert (covered[h] <= 1).all()
+    assert costs == sorted(costs, reverse=True), "units are not ordered longest first"
+    with pytest.raises(kev.KevError):
+        kev.kev_read_work_list(run.ws, run.ws_bytes, 10)
+    compare(f64(run.out, w.dtype), _oracle_out(w), w.dtype, "unit-form prefill")
+    _check_pools(run, w)
+
+
 def test_scores_growing_past_the_reference_max():
     """Keys aligned with the queries and growing along the sequence: later key tiles exceed the
     first tile of an item by far more than 2^64 in exp2 (the exact rescaling path)."""
