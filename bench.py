@@ -246,8 +246,9 @@ def run_reference(args):
 
 def _stress_decode_graph(kev, torch, dev, tdev, tf_peak, hbm_peak):
     """The stress batch: prefill into the slot pools, then its 128-step decode loop with early
-    stop (decode + lens advance per step, each step with its own live set and inputs) captured
-    once as a CUDA graph and replayed.  L2 is not flushed between the steps of a replay."""
+    stop (kev_decode_step per step: decode with the lens advance folded in, each step with its own
+    live set and inputs) captured once as a CUDA graph and replayed.  L2 is not flushed between
+    the steps of a replay."""
     import numpy as np
     s = W.stress()
     w = s.prefill
@@ -285,11 +286,10 @@ def _stress_decode_graph(kev, torch, dev, tdev, tf_peak, hbm_peak):
     dws = torch.zeros(dws_bytes, dtype=torch.uint8, device=dev)
     pk0, pv0 = pk.clone(), pv.clone()
 
-    def loop():
+    def loop():  # one fused call per step: decode, then the lens advance folded into its merge kernel
         for t in range(steps):
-            kev.kev_decode_attn(qn[t], kn[t], vn[t], pk, pv, w.n_slots, w.cap, sl, lens, act[t], N, dout, shape, dws,
+            kev.kev_decode_step(qn[t], kn[t], vn[t], pk, pv, w.n_slots, w.cap, sl, lens, act[t], N, dout, shape, dws,
                                 dws_bytes, st)
-            kev.kev_decode_advance(lens, act[t], N)
 
     loop()  # eager pass: first-call work happens outside the capture
     torch.cuda.synchronize()
@@ -320,7 +320,7 @@ def _stress_decode_graph(kev, torch, dev, tdev, tf_peak, hbm_peak):
             "prefill_frac": useful / (pre_avg * 1e-3) / 1e12 / tf_peak,
             "decode_graph_ms": ms, "decode_steps": steps, "decode_bytes": total_bytes,
             "decode_gbs": total_bytes / (ms * 1e-3) / 1e9, "decode_frac": total_bytes / (ms * 1e-3) / 1e9 / hbm_peak,
-            "launches_per_step": kev.kev_launch_count(4) + 1,
+            "launches_per_step": kev.kev_launch_count(15),
             "l2": "not flushed between the steps of a graph replay (L2 may hold part of the working set)"}
 
 

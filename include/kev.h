@@ -29,7 +29,9 @@
  *    q-head h reads kv-head h / (H_q / H_kv) (grouped-query attention).
  *  - Element type: KEV_BF16 (bf16 storage, fp32 accumulation, bf16 output rounded to
  *    nearest even) or KEV_FP32 (fp32 storage and arithmetic, no TF32).
- *    Supported head dims: d in {64, 128}; H_q must be a multiple of H_kv, G = H_q/H_kv <= 16.
+ *    Supported head dims: bf16 d in {64, 128} (tensor cores); fp32 any d that is a multiple of 16
+ *    from 16 to 256 (CUDA cores); the RoPE entry points take d in {64, 128}.  H_q must be a
+ *    multiple of H_kv, G = H_q/H_kv <= 16.
  *  - Errors.  Arguments the host can check (null or misaligned pointers, negative sizes,
  *    unsupported shapes, too small a workspace) are returned at once and nothing is
  *    launched.  Data-dependent errors (intervals, slot ids, lengths) are found on the
@@ -79,7 +81,7 @@ typedef struct {
 typedef struct {
   int32_t h_q;   /* query heads */
   int32_t h_kv;  /* key/value heads; h_q % h_kv == 0 */
-  int32_t d_h;   /* head dimension: 64 or 128 */
+  int32_t d_h;   /* head dimension: bf16 64 or 128; fp32 a multiple of 16 up to 256 */
   int32_t dtype; /* kev_dtype */
   float scale;   /* softmax scale; 0 => 1/sqrt(d_h) */
 } kev_attn_shape;
@@ -227,6 +229,19 @@ kev_status kev_decode_attn_static(const void* q_new, const void* k_new, const vo
 /* lens[i] += (active[i] != 0) for i < n, on the device (no host synchronisation), so a
  * decode loop can be captured in a CUDA graph. */
 kev_status kev_decode_advance(int32_t* lens, const uint8_t* active, int32_t n, kev_stream_t stream);
+
+/* One decode step followed by the lens advance: kev_decode_attn, then lens[i] += 1 for every
+ * live i once the step is complete (and only if the call is valid: on a device error lens is
+ * left as it was).  Same arguments, results and errors as kev_decode_attn; `lens` is read and
+ * then advanced.  On the tensor-core path (bf16, d_h = 128) the advance is folded into the
+ * kernel that merges split pieces, so a step is two launches instead of three; this is the
+ * form to capture in a CUDA graph for a decode loop. */
+kev_status kev_decode_step(const void* q_new, const void* k_new, const void* v_new,
+                           void* pool_k, void* pool_v, int32_t n_slots, int32_t slot_cap,
+                           const int32_t* slot_ids, int32_t* lens, const uint8_t* active,
+                           int32_t n_questions, void* out, const kev_attn_shape* shape,
+                           void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                           kev_stream_t stream);
 
 /* ---------------------------------------------------------------------------------------
  * Per-question temperature sampling
@@ -429,7 +444,8 @@ const char* kev_status_string(kev_status status);
  * 6 = rope_table, 7 = rope_prefill, 8 = rope_decode (1 each), 9 = prefill_attn_paged (4:
  * segments, table check, attention, paged write), 10 = kv_write_paged (3), 11 =
  * decode_attn_paged (2), 12 = prefill_chunk (3: segments, slot write, attention), 13 =
- * sample (1), 14 = lora_apply (1).  -1 for an unknown id. */
+ * sample (1), 14 = lora_apply (1), 15 = decode_step (2: decode + merge on the tensor cores,
+ * decode + advance otherwise).  -1 for an unknown id. */
 int32_t kev_launch_count(int32_t entry_point);
 
 #ifdef __cplusplus

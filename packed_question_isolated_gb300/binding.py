@@ -51,7 +51,7 @@ EXPORTED = [
     "kev_prefill_workspace_size", "kev_build_segments", "kev_read_work_list", "kev_read_work_units",
     "kev_prefill_from_segments", "kev_prefill_attn", "kev_kv_write",
     "kev_decode_workspace_size", "kev_decode_attn", "kev_decode_advance",
-    "kev_read_status", "kev_status_string", "kev_launch_count", "kev_decode_attn_static",
+    "kev_read_status", "kev_status_string", "kev_launch_count", "kev_decode_attn_static", "kev_decode_step",
     "kev_rope_table_size", "kev_rope_table", "kev_rope_prefill", "kev_prefill_attn_rope", "kev_rope_decode",
     "kev_decode_attn_rope", "kev_prefill_attn_paged", "kev_kv_write_paged", "kev_decode_attn_paged",
     "kev_assign_blocks", "kev_prefill_chunk", "kev_sample", "kev_lora_apply",
@@ -99,6 +99,7 @@ _c = {
     "kev_decode_attn_static": _sig("kev_decode_attn_static", _I, _P, _P, _P, _P, _P, _I, _I, _P, _P, _P, _I,
                                    _P, _S, _P, _P),
     "kev_decode_advance": _sig("kev_decode_advance", _I, _P, _P, _I, _P),
+    "kev_decode_step": _sig("kev_decode_step", _I, _P, _P, _P, _P, _P, _I, _I, _P, _P, _P, _I, _P, _S, _P, _Z, _P, _P),
     "kev_read_status": _sig("kev_read_status", _I, _P, _P),
     "kev_status_string": _sig("kev_status_string", ctypes.c_char_p, _I),
     "kev_launch_count": _sig("kev_launch_count", _I, _I),
@@ -274,6 +275,18 @@ def kev_decode_attn_static(q_new, k_new, v_new, pool_k, pool_v, n_slots, slot_ca
                                       int(n_questions), _ptr(out), ctypes.byref(s), _ptr(dev_status),
                                       _stream(stream))
     return _check(st, "kev_decode_attn_static", check)
+
+
+def kev_decode_step(q_new, k_new, v_new, pool_k, pool_v, n_slots, slot_cap, slot_ids, lens, active, n_questions,
+                    out, shape, workspace, workspace_bytes, dev_status=None, stream=None, check=True) -> int:
+    """kev_decode_attn followed by lens[i] += 1 for live i (folded into the merge kernel on the
+    tensor-core path)."""
+    s = _shape(shape)
+    st = _c["kev_decode_step"](_ptr(q_new), _ptr(k_new), _ptr(v_new), _ptr(pool_k), _ptr(pool_v), int(n_slots),
+                               int(slot_cap), _ptr(slot_ids), _ptr(lens), _ptr(active), int(n_questions), _ptr(out),
+                               ctypes.byref(s), _ptr(workspace), int(workspace_bytes), _ptr(dev_status),
+                               _stream(stream))
+    return _check(st, "kev_decode_step", check)
 
 
 def kev_decode_advance(lens, active, n, stream=None, check=True) -> int:

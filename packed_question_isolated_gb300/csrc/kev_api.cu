@@ -13,6 +13,8 @@ namespace {
 
 // kernel launches of the most recent successful kev_decode_attn (2 on the tensor-core path)
 std::atomic<int32_t> g_decode_launches{1};
+// ... and of the most recent successful kev_decode_step (2: decode + merge, or decode + advance)
+std::atomic<int32_t> g_step_launches{2};
 
 bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
@@ -28,11 +30,16 @@ kev_status check_shape(const kev_attn_shape* s) {
   if (s->h_q <= 0 || s->h_kv <= 0) return KEV_ERR_INVALID_ARG;
   if (s->h_q % s->h_kv) return KEV_ERR_UNSUPPORTED;
   if (s->h_q / s->h_kv > 16) return KEV_ERR_UNSUPPORTED;
-  if (s->d_h != 64 && s->d_h != 128) return KEV_ERR_UNSUPPORTED;
   if (s->dtype != KEV_BF16 && s->dtype != KEV_FP32) return KEV_ERR_UNSUPPORTED;
+  // bf16: 64 or 128 (tensor cores); fp32 (CUDA cores): any multiple of 16 up to 256
+  if (s->dtype == KEV_BF16 ? (s->d_h != 64 && s->d_h != 128) : (s->d_h < 16 || s->d_h > 256 || s->d_h % 16))
+    return KEV_ERR_UNSUPPORTED;
   if (!(s->scale >= 0.f) || isinf(s->scale)) return KEV_ERR_INVALID_ARG;
   return KEV_OK;
 }
+
+// The RoPE kernels pair 16-byte chunks of a head's two halves: head dims 64 and 128.
+bool rope_head_dim(const kev_attn_shape* s) { return s->d_h == 64 || s->d_h == 128; }
 
 float effective_scale(const kev_attn_shape* s) {
   return s->scale == 0.f ? 1.0f / sqrtf((float)s->d_h) : s->scale;
@@ -653,6 +660,7 @@ kev_status kev_rope_prefill(void* q, void* k, const void* v, int32_t total_token
                             kev_stream_t stream) {
   kev_status st = check_prefill_common(total_tokens, intervals, n_questions, shape, workspace, workspace_bytes);
   if (st != KEV_OK) return st;
+  if (!rope_head_dim(shape)) return KEV_ERR_UNSUPPORTED;
   if (total_tokens > 0 && (!q || !k || !v || !aligned16(q) || !aligned16(k) || !aligned16(v)))
     return KEV_ERR_INVALID_ARG;
   st = check_slots(slot_ids, pool_k, pool_v, n_slots, slot_cap, n_questions);
@@ -694,6 +702,7 @@ kev_status kev_prefill_attn_rope(void* q, void* k, const void* v, int32_t total_
   // full argument check before the first launch, so an invalid call enqueues nothing
   kev_status st = check_prefill_common(total_tokens, intervals, n_questions, shape, workspace, workspace_bytes);
   if (st != KEV_OK) return st;
+  if (!rope_head_dim(shape)) return KEV_ERR_UNSUPPORTED;
   if (total_tokens > 0 && (!q || !k || !v || !out || !aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)))
     return KEV_ERR_INVALID_ARG;
   st = check_slots(slot_ids, pool_k, pool_v, n_slots, slot_cap, n_questions);
@@ -715,6 +724,7 @@ kev_status kev_rope_decode(void* q_new, void* k_new, const int32_t* lens, const 
                            int32_t max_pos, int32_t* dev_status, kev_stream_t stream) {
   kev_status st = check_shape(shape);
   if (st != KEV_OK) return st;
+  if (!rope_head_dim(shape)) return KEV_ERR_UNSUPPORTED;
   if (n_questions < 0) return KEV_ERR_INVALID_ARG;
   if (n_questions > kMaxQuestions) return KEV_ERR_UNSUPPORTED;
   if (dev_status && ((uintptr_t)dev_status & 3u)) return KEV_ERR_INVALID_ARG;
@@ -765,10 +775,17 @@ size_t kev_decode_workspace_size(int32_t n_questions, int32_t slot_cap, const ke
   return decode_layout(n_questions, slot_cap, shape->h_q, shape->h_kv, shape->d_h, decode_on_tensor_cores(shape)).total;
 }
 
-kev_status kev_decode_attn(const void* q_new, const void* k_new, const void* v_new, void* pool_k, void* pool_v,
-                           int32_t n_slots, int32_t slot_cap, const int32_t* slot_ids, const int32_t* lens,
-                           const uint8_t* active, int32_t n_questions, void* out, const kev_attn_shape* shape,
-                           void* workspace, size_t workspace_bytes, int32_t* dev_status, kev_stream_t stream) {
+}  // extern "C"
+
+namespace {
+// kev_decode_attn, and with `advance` (kev_decode_step) lens[i] += 1 for live i once the step is
+// complete: in the merge kernel on the tensor-core path, by the advance kernel otherwise.
+// `entry` is the launch-count slot of the calling entry point.
+kev_status decode_call(const void* q_new, const void* k_new, const void* v_new, void* pool_k, void* pool_v,
+                       int32_t n_slots, int32_t slot_cap, const int32_t* slot_ids, const int32_t* lens,
+                       const uint8_t* active, int32_t n_questions, void* out, const kev_attn_shape* shape,
+                       void* workspace, size_t workspace_bytes, int32_t* dev_status, kev_stream_t stream,
+                       int32_t* advance, int entry) {
   kev_status st = kev::decode_check_args(q_new, k_new, v_new, pool_k, pool_v, n_slots, slot_cap, slot_ids, lens,
                                          active, n_questions, out, shape, dev_status);
   if (st != KEV_OK) return st;
@@ -801,14 +818,39 @@ kev_status kev_decode_attn(const void* q_new, const void* k_new, const void* v_n
   a.ws = static_cast<char*>(workspace);
   a.layout = layout;
   a.dev_status = dev_status;
-  if (decode_on_tensor_cores(shape)) {  // decode kernel + merge kernel
+  std::atomic<int32_t>& launches = entry == 4 ? g_decode_launches : g_step_launches;
+  if (decode_on_tensor_cores(shape)) {  // decode kernel + merge kernel (which also advances lens)
+    a.advance_lens = advance;
     st = from_cuda(launch_decode_tc(a, sms, (cudaStream_t)stream));
-    if (st == KEV_OK) g_decode_launches.store(2);
+    if (st == KEV_OK) launches.store(2);
     return st;
   }
   st = from_cuda(launch_decode(a, shape->d_h, (kev_dtype)shape->dtype, sms, (cudaStream_t)stream));
-  if (st == KEV_OK) g_decode_launches.store(1);
+  if (st == KEV_OK && advance)  // only if the step was valid: the decode kernels store their code in sched[2]
+    st = from_cuda(launch_advance(advance, active, n_questions, (cudaStream_t)stream,
+                                  reinterpret_cast<const int32_t*>(static_cast<char*>(workspace) + layout.sched) + 2));
+  if (st == KEV_OK) launches.store(advance ? 2 : 1);
   return st;
+}
+}  // namespace
+
+extern "C" {
+
+
+kev_status kev_decode_attn(const void* q_new, const void* k_new, const void* v_new, void* pool_k, void* pool_v,
+                           int32_t n_slots, int32_t slot_cap, const int32_t* slot_ids, const int32_t* lens,
+                           const uint8_t* active, int32_t n_questions, void* out, const kev_attn_shape* shape,
+                           void* workspace, size_t workspace_bytes, int32_t* dev_status, kev_stream_t stream) {
+  return decode_call(q_new, k_new, v_new, pool_k, pool_v, n_slots, slot_cap, slot_ids, lens, active, n_questions, out,
+                     shape, workspace, workspace_bytes, dev_status, stream, nullptr, 4);
+}
+
+kev_status kev_decode_step(const void* q_new, const void* k_new, const void* v_new, void* pool_k, void* pool_v,
+                           int32_t n_slots, int32_t slot_cap, const int32_t* slot_ids, int32_t* lens,
+                           const uint8_t* active, int32_t n_questions, void* out, const kev_attn_shape* shape,
+                           void* workspace, size_t workspace_bytes, int32_t* dev_status, kev_stream_t stream) {
+  return decode_call(q_new, k_new, v_new, pool_k, pool_v, n_slots, slot_cap, slot_ids, lens, active, n_questions, out,
+                     shape, workspace, workspace_bytes, dev_status, stream, lens, 15);
 }
 
 kev_status kev_decode_advance(int32_t* lens, const uint8_t* active, int32_t n, kev_stream_t stream) {
@@ -862,6 +904,7 @@ int32_t kev_launch_count(int32_t entry_point) {
     case 12: return 3;
     case 13: return 1;
     case 14: return 1;
+    case 15: return g_step_launches.load();
   }
   return -1;
 }

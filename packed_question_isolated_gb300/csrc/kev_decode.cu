@@ -159,7 +159,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
     bars->abort = 0;
     bars->never = 0;
   }
-  const int running = dec::prologue<kThreads>(a, n_hblocks, item_base, meta, hash, &bars->flags, bars->scan_tmp);
+  int* sched = reinterpret_cast<int*>(a.ws + a.layout.sched);  // [2]: this call's validation code
+  const int running =
+      dec::prologue<kThreads>(a, n_hblocks, item_base, meta, hash, &bars->flags, bars->scan_tmp, &sched[2]);
   if (running < 0) return;
   if (tid == 0) {
     for (int s = 0; s < L::kStages; ++s) mbar_init(&bars->full[s], 1);
@@ -241,6 +243,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
     if (!named_sync_and(landed)) {
       if (tid == 0) {
         set_status(a.dev_status, ST_TIMEOUT);
+        sched[2] = ST_TIMEOUT;  // a step's lens advance is skipped
         *abort_flag = 1;
       }
       break;
@@ -505,7 +508,102 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
   }
 }
 
-__global__ void advance_kernel(int32_t* lens, const uint8_t* active, int32_t n) {
+// fp32 decode at head dims other than 64 and 128 (any multiple of 16 up to 256): the same
+// validation prologue (nothing is written unless every live question is valid), then one warp
+// per (live question, q-head), the online softmax over positions 0..n in blocks of 32 (lane j
+// scores position j of the block; dims lane, lane + 32, ... for the output), the new position
+// read from k_new / v_new; the first q-head of each kv group writes the new row into the pool.
+// No split over the positions, so no workspace is used beyond the prologue's shared memory.
+constexpr int kSimpleWarps = 8;
+constexpr int kSimpleMaxD = 256;
+
+template <int PER>
+__global__ void __launch_bounds__(kSimpleWarps * 32) decode_simple_kernel(DecodeArgs a, int D) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  __shared__ float q_s[kSimpleWarps][kSimpleMaxD];
+  __shared__ int s_flags;
+  __shared__ int s_scan[kSimpleWarps + 1];
+  const int n = a.n;
+  int* item_base = reinterpret_cast<int*>(smem);
+  int2* meta = reinterpret_cast<int2*>(smem + (size_t)((n + 2) / 2) * 8);
+  int* hash = reinterpret_cast<int*>(smem + (size_t)((n + 2) / 2) * 8 + (size_t)n * 8);
+  int* sched = reinterpret_cast<int*>(a.ws + a.layout.sched);  // [2]: this call's validation code
+  if (dec::prologue<kSimpleWarps * 32>(a, 1, item_base, meta, hash, &s_flags, s_scan, &sched[2]) < 0) return;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const float* Qn = static_cast<const float*>(a.q_new);
+  const float* Kn = static_cast<const float*>(a.k_new);
+  const float* Vn = static_cast<const float*>(a.v_new);
+  float* PK = static_cast<float*>(a.pool_k);
+  float* PV = static_cast<float*>(a.pool_v);
+  float* O = static_cast<float*>(a.out);
+  const int64_t items = (int64_t)n * a.h_q;
+  for (int64_t it = (int64_t)blockIdx.x * kSimpleWarps + warp; it < items; it += (int64_t)gridDim.x * kSimpleWarps) {
+    const int i = (int)(it / a.h_q), h = (int)(it % a.h_q);
+    if (!a.active[i]) continue;
+    const int len = meta[i].x, slot = meta[i].y, g = h / a.group;
+    const float* krow_new = Kn + ((int64_t)i * a.h_kv + g) * D;
+    const float* vrow_new = Vn + ((int64_t)i * a.h_kv + g) * D;
+    const int64_t pool0 = (((int64_t)slot * a.h_kv + g) * a.cap) * D;  // row 0 of the slot, kv head g
+    __syncwarp();
+    for (int c = lane; c < D; c += 32) q_s[warp][c] = Qn[((int64_t)i * a.h_q + h) * D + c];
+    if (h % a.group == 0)  // the new row: appended once per (question, kv head)
+      for (int c = lane; c < D; c += 32) {
+        PK[pool0 + (int64_t)len * D + c] = krow_new[c];
+        PV[pool0 + (int64_t)len * D + c] = vrow_new[c];
+      }
+    __syncwarp();
+    float m = -INFINITY, l = 0.f;
+    float acc[PER];
+#pragma unroll
+    for (int e = 0; e < PER; ++e) acc[e] = 0.f;
+    for (int kb = 0; kb <= len; kb += 32) {
+      const int pos = kb + lane;
+      float sc = -INFINITY;
+      if (pos <= len) {
+        const float* kr = pos < len ? PK + pool0 + (int64_t)pos * D : krow_new;
+        float dot = 0.f;
+#pragma unroll 8
+        for (int c = 0; c < D; ++c) dot = fmaf(q_s[warp][c], kr[c], dot);
+        sc = dot * a.scale;
+      }
+      const float m_new = fmaxf(m, warp_max(sc));
+      const float alpha = expf(m - m_new);  // m = -inf on the first block gives 0
+      const float pw = (pos <= len) ? expf(sc - m_new) : 0.f;
+      l = l * alpha + warp_sum(pw);
+#pragma unroll
+      for (int e = 0; e < PER; ++e) acc[e] *= alpha;
+      const int nk = min(32, len - kb + 1);
+      for (int j = 0; j < nk; ++j) {
+        const float pj = __shfl_sync(0xffffffffu, pw, j);
+        const float* vr = (kb + j < len ? PV + pool0 + (int64_t)(kb + j) * D : vrow_new) + lane;
+#pragma unroll
+        for (int e = 0; e < PER; ++e)
+          if (lane + 32 * e < D) acc[e] = fmaf(pj, vr[32 * e], acc[e]);
+      }
+      m = m_new;
+    }
+    const float inv = 1.f / l;
+    float* orow = O + ((int64_t)i * a.h_q + h) * D + lane;
+#pragma unroll
+    for (int e = 0; e < PER; ++e)
+      if (lane + 32 * e < D) orow[32 * e] = acc[e] * inv;
+  }
+}
+
+cudaError_t launch_decode_simple(const DecodeArgs& a, int d, int num_sms, cudaStream_t s) {
+  if (d < 16 || d > kSimpleMaxD || d % 16) return cudaErrorInvalidValue;
+  int hs = 1;
+  while (hs < 2 * a.n) hs <<= 1;
+  const size_t smem = (size_t)((a.n + 2) / 2) * 8 + (size_t)a.n * 8 + (size_t)hs * 4;
+  auto kern = d <= 64 ? decode_simple_kernel<2> : d <= 128 ? decode_simple_kernel<4> : decode_simple_kernel<8>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  kern<<<num_sms, kSimpleWarps * 32, smem, s>>>(a, d);
+  return cudaGetLastError();
+}
+
+__global__ void advance_kernel(int32_t* lens, const uint8_t* active, int32_t n, const int32_t* code) {
+  if (code && *code != ST_OK) return;  // kev_decode_step after an invalid (or timed-out) step: lens kept
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i < n && active[i]) lens[i] += 1;
 }
@@ -545,13 +643,16 @@ cudaError_t launch_d(const DecodeArgs& a, int num_sms, cudaStream_t s) {
 }  // namespace
 
 cudaError_t launch_decode(const DecodeArgs& a, int d, kev_dtype dt, int num_sms, cudaStream_t s) {
-  if (dt == KEV_FP32) return d == 64 ? launch_d<float, 64>(a, num_sms, s) : launch_d<float, 128>(a, num_sms, s);
+  if (dt == KEV_FP32) {
+    if (d != 64 && d != 128) return launch_decode_simple(a, d, num_sms, s);
+    return d == 64 ? launch_d<float, 64>(a, num_sms, s) : launch_d<float, 128>(a, num_sms, s);
+  }
   return d == 64 ? launch_d<__nv_bfloat16, 64>(a, num_sms, s) : launch_d<__nv_bfloat16, 128>(a, num_sms, s);
 }
 
-cudaError_t launch_advance(int32_t* lens, const uint8_t* active, int32_t n, cudaStream_t s) {
+cudaError_t launch_advance(int32_t* lens, const uint8_t* active, int32_t n, cudaStream_t s, const int32_t* code) {
   if (n <= 0) return cudaSuccess;
-  advance_kernel<<<(n + 255) / 256, 256, 0, s>>>(lens, active, n);
+  advance_kernel<<<(n + 255) / 256, 256, 0, s>>>(lens, active, n, code);
   return cudaGetLastError();
 }
 

@@ -606,7 +606,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
       const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
       const int eid = tid - 224;     // 0..127
       float* partials = reinterpret_cast<float*>(a.ws + a.layout.partials);
-      int* item_xi0 = reinterpret_cast<int*>(a.ws + a.layout.xi0);
+      int2* item_xi0 = reinterpret_cast<int2*>(a.ws + a.layout.xi0);
       constexpr int pstride = kN * (kD + 2);
       bool ok = true;
       for (int pc = 0;; ++pc) {
@@ -648,7 +648,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
             part[kN * kD + kN + eid] = l_sum[eid];
           }
         }
-        if (c_start == 0 && eid == 0) item_xi0[cidx] = xi0;
+        if (c_start == 0 && eid == 0) item_xi0[cidx] = make_int2(xi0, pi.nch);
       }
       if (!ok && lane == 0) raise_timeout(a, bars);
     }
@@ -670,7 +670,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
 }
 
 // Merge of the pieces of every (question, kv head) that the decode kernel split (one CTA per
-// pair, thread r = head dimension r), in a fixed order: piece 0 starts at chunk 0, piece j > 0
+// pair, thread r = head dimension r; the pair's first chunk and chunk count come from the decode
+// kernel through the workspace, so lens is not read here), in a fixed order: piece 0 starts at chunk 0, piece j > 0
 // at the j-th batch boundary of the grab plan after the pair's first chunk.  Online over rounds of pieces whose
 // reference max and sum are gathered into shared memory while the O rows load.  Block 0 also
 // resets the decode kernel's batch counter for the next call.
@@ -682,7 +683,10 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeArgs a) {
   pdl_trigger();
   int* sched = reinterpret_cast<int*>(a.ws + a.layout.sched);
   if (blockIdx.x == 0 && threadIdx.x == 0) sched[0] = 0;
-  if (sched[2] != ST_OK) return;  // invalid call (or timeout): nothing to merge
+  if (sched[2] != ST_OK) return;  // invalid call (or timeout): nothing to merge, lens kept
+  if (a.advance_lens)  // kev_decode_step: the step is complete, so lens moves on (nothing here reads it)
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < a.n; i += gridDim.x * blockDim.x)
+      if (a.active[i]) a.advance_lens[i] += 1;
   BatchPlan plan;
   plan.x1 = sched[1];
   plan.n1 = sched[3];
@@ -690,15 +694,16 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeArgs a) {
   __shared__ float mg_m[128], mg_l[128];
   const int r = threadIdx.x;
   const float* partials = reinterpret_cast<const float*>(a.ws + a.layout.partials);
-  const int* item_xi0 = reinterpret_cast<const int*>(a.ws + a.layout.xi0);
+  const int2* item_xi0 = reinterpret_cast<const int2*>(a.ws + a.layout.xi0);
   constexpr int pstride = kN * (kD + 2);
   constexpr int kRound = 32 / NH > 8 ? 8 : 32 / NH;  // pieces per round (O loads in flight)
   for (int cidx = blockIdx.x; cidx < a.n * a.h_kv; cidx += gridDim.x) {
     const int i = cidx / a.h_kv, g = cidx % a.h_kv;
     // three independent loads in one round trip
-    const int live = a.active[i], len = a.lens[i], xi0 = item_xi0[cidx];
+    const int live = a.active[i];
+    const int2 xc = item_xi0[cidx];  // written by this call's decode kernel for every live pair
+    const int xi0 = xc.x, nch = xc.y;
     if (!live || xi0 < 0) continue;  // dropped, or not a chunk index (never written by a valid call)
-    const int nch = (len + 1 + kC - 1) / kC;
     const int b0 = plan.of(xi0);
     const int np = plan.of(xi0 + nch - 1) - b0 + 1;
     if (np == 1) continue;  // one piece: the decode kernel wrote the output

@@ -107,9 +107,10 @@ inline PrefillLayout prefill_layout(int32_t n, int32_t T, int32_t h_q) {
 // decode workspace
 // ---------------------------------------------------------------------------------------
 struct DecodeLayout {
-  size_t sched;     // int32[8]  tensor-core decode: [0] batch-grab counter (left at zero), [1] [3] [4] grab
-                    // plan, [2] validation code
-  size_t xi0;       // int32[N * H_kv]  tensor-core decode: global index of chunk 0 of each (question, kv head)
+  size_t sched;     // int32[8]  [2] validation code of the call (both paths); tensor-core decode: [0]
+                    // batch-grab counter (left at zero), [1] [3] [4] grab plan
+  size_t xi0;       // int2[N * H_kv]  tensor-core decode: {global index of chunk 0, chunk count} of each
+                    // (question, kv head) (the merge kernel reads these, not lens)
   size_t counters;  // int32[N * H_kv * n_hblocks]  arrivals per (question, kv head, head block); left at zero
   size_t partials;  // float[N * H_kv * n_hblocks * max_chunks * GT * (d + 2)]
   size_t total;
@@ -135,7 +136,7 @@ inline DecodeLayout decode_layout(int32_t n, int32_t cap, int32_t h_q, int32_t h
   L.sched = off;
   off = align_up(off + 8 * sizeof(int32_t), 256);
   L.xi0 = off;
-  off = align_up(off + (tc ? sizeof(int32_t) * (size_t)n * h_kv : 0), 256);
+  off = align_up(off + (tc ? sizeof(int2) * (size_t)n * h_kv : 0), 256);
   L.counters = off;
   off = align_up(off + sizeof(int32_t) * (size_t)n * h_kv * nhb, 256);
   L.partials = off;
@@ -250,6 +251,8 @@ struct DecodeArgs {
   // bounded waits: cycles per wait, and the timeout test hook (both set by the launchers)
   long long wait_budget = 4000000000ll;
   int32_t test_stall = 0;
+  // kev_decode_step: lens itself, advanced (lens[i] += 1 for live i) once the step is complete
+  int32_t* advance_lens = nullptr;
 };
 
 // Host-side launchers (each returns the launch's cudaError_t).
@@ -347,7 +350,9 @@ kev_status decode_check_args(const void* q_new, const void* k_new, const void* v
 DecodeLayout decode_layout_of(int32_t n_questions, int32_t slot_cap, const kev_attn_shape* shape);
 cudaError_t launch_decode(const DecodeArgs& a, int d, kev_dtype dt, int num_sms, cudaStream_t s);     // CUDA cores
 cudaError_t launch_decode_tc(const DecodeArgs& a, int num_sms, cudaStream_t s);                       // bf16, d = 128
-cudaError_t launch_advance(int32_t* lens, const uint8_t* active, int32_t n, cudaStream_t s);
+// lens[i] += 1 for active i; with `code` (a device word), only if *code is ST_OK
+cudaError_t launch_advance(int32_t* lens, const uint8_t* active, int32_t n, cudaStream_t s,
+                           const int32_t* code = nullptr);
 
 // ---------------------------------------------------------------------------------------
 // device helpers

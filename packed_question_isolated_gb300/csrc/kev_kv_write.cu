@@ -58,10 +58,14 @@ __global__ void __launch_bounds__(kAuxThreads) aux_kernel(AuxArgs a) {
   __syncthreads();
 
   if (s_ok && to_pool) {
-    const int vpr = a.row_bytes / 16;  // 16-byte vectors per row of one head (8, 16 or 32)
-    const int upp = 32 / vpr;          // units per warp pass
-    const int lane = threadIdx.x & 31, sub = lane / vpr, v = lane % vpr;
-    const int64_t units = (int64_t)s_cu[a.n] * a.h_kv;
+    // A unit is up to 32 16-byte vectors of one (row, kv head): a row of vpr vectors is `parts`
+    // units; a warp pass copies upp units of lpu lanes each (the other lanes idle).
+    const int vpr = a.row_bytes / 16;
+    const int lpu = vpr < 32 ? vpr : 32;
+    const int upp = 32 / lpu;
+    const int parts = (vpr + 31) / 32;
+    const int lane = threadIdx.x & 31, sub = lane / lpu, v_in = lane % lpu;
+    const int64_t units = (int64_t)s_cu[a.n] * a.h_kv * parts;
     const int64_t per_chunk = (int64_t)upp * kUnroll;
     const int64_t n_chunks = (units + per_chunk - 1) / per_chunk;
     const int warps = gridDim.x * (kAuxThreads / 32);
@@ -76,8 +80,10 @@ __global__ void __launch_bounds__(kAuxThreads) aux_kernel(AuxArgs a) {
       for (int t = 0; t < kUnroll; ++t) {
         const int64_t u = c * per_chunk + t * upp + sub;
         dst[t] = -1;
-        if (u < units) {
-          const int r = (int)(u / a.h_kv), g = (int)(u % a.h_kv);
+        const int v = (int)(u % parts) * 32 + v_in;
+        if (sub < upp && u < units && v < vpr) {
+          const int64_t rg = u / parts;
+          const int r = (int)(rg / a.h_kv), g = (int)(rg % a.h_kv);
           const int i = question_of(s_cu, a.n, r);
           const int j = r - s_cu[i];
           const int2 bs = s_bs[i];

@@ -8,18 +8,19 @@
 //
 // Work: one CTA of 4 warps per item of the segment builder's list (question, 128-row tile,
 // q-head); warp w takes rows w, w+4, ...  Inside a 32-key block lane j owns key j for the
-// score and dims [j*D/32, (j+1)*D/32) for the output accumulator.
+// score and dims j, j+32, j+64, ... (< D) for the output accumulator.  D is any multiple of 16
+// up to 256, taken at run time; PER = ceil(D / 32) is the accumulator's length.
 #include "kev_internal.cuh"
 
 namespace kev {
 namespace {
 
 constexpr int kWarps = 4;
+constexpr int kMaxD = 256;
 
-template <typename T, int D>
-__global__ void __launch_bounds__(kWarps * 32) prefill_simt_kernel(PrefillArgs a) {
-  constexpr int PER = D / 32;
-  __shared__ float q_s[kWarps][D];
+template <typename T, int PER>
+__global__ void __launch_bounds__(kWarps * 32) prefill_simt_kernel(PrefillArgs a, int D) {
+  __shared__ float q_s[kWarps][kMaxD];
   const PrefillHeader* hdr = reinterpret_cast<const PrefillHeader*>(a.ws);
   if (hdr->status != ST_OK) return;
   if (hdr->format != 0) {  // the work list was built for another kernel (another shape)
@@ -67,16 +68,18 @@ __global__ void __launch_bounds__(kWarps * 32) prefill_simt_kernel(PrefillArgs a
         const int nk = min(32, t - kb + 1);
         for (int j = 0; j < nk; ++j) {
           const float pj = __shfl_sync(0xffffffffu, p, j);
-          const T* vr = V + (int64_t)(kb + j) * kv_row + (int64_t)g * D + lane * PER;
+          const T* vr = V + (int64_t)(kb + j) * kv_row + (int64_t)g * D + lane;
 #pragma unroll
-          for (int e = 0; e < PER; ++e) acc[e] = fmaf(pj, to_f32(vr[e]), acc[e]);
+          for (int e = 0; e < PER; ++e)
+            if (lane + 32 * e < D) acc[e] = fmaf(pj, to_f32(vr[32 * e]), acc[e]);
         }
         m = m_new;
       }
       const float inv = 1.f / l;
-      T* orow = O + (int64_t)t * q_row + (int64_t)h * D + lane * PER;
+      T* orow = O + (int64_t)t * q_row + (int64_t)h * D + lane;
 #pragma unroll
-      for (int e = 0; e < PER; ++e) orow[e] = from_f32<T>(acc[e] * inv);
+      for (int e = 0; e < PER; ++e)
+        if (lane + 32 * e < D) orow[32 * e] = from_f32<T>(acc[e] * inv);
     }
   }
 }
@@ -86,9 +89,11 @@ __global__ void __launch_bounds__(kWarps * 32) prefill_simt_kernel(PrefillArgs a
 cudaError_t launch_prefill_simt(const PrefillArgs& a, int d, int num_sms, cudaStream_t s) {
   const int64_t max_items = a.layout.max_items;
   if (max_items == 0) return cudaSuccess;
+  if (d < 16 || d > kMaxD || d % 16) return cudaErrorInvalidValue;
   const int grid = (int)(max_items < (int64_t)num_sms * 16 ? max_items : (int64_t)num_sms * 16);
-  if (d == 64) prefill_simt_kernel<float, 64><<<grid, kWarps * 32, 0, s>>>(a);
-  else prefill_simt_kernel<float, 128><<<grid, kWarps * 32, 0, s>>>(a);
+  if (d <= 64) prefill_simt_kernel<float, 2><<<grid, kWarps * 32, 0, s>>>(a, d);
+  else if (d <= 128) prefill_simt_kernel<float, 4><<<grid, kWarps * 32, 0, s>>>(a, d);
+  else prefill_simt_kernel<float, 8><<<grid, kWarps * 32, 0, s>>>(a, d);
   return cudaGetLastError();
 }
 

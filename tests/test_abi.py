@@ -69,7 +69,7 @@ def test_status_strings_and_launch_counts(lib):
         assert lib.kev_status_string(code) != "unknown status"
     assert lib.kev_status_string(99) == "unknown status"
     assert lib.kev_launch_count(0) == 3 and lib.kev_launch_count(4) == 1 and lib.kev_launch_count(99) == -1
-    assert [lib.kev_launch_count(i) for i in (6, 7, 8, 9, 10, 11, 12, 13, 14)] == [1, 1, 1, 4, 3, 2, 3, 1, 1]
+    assert [lib.kev_launch_count(i) for i in (6, 7, 8, 9, 10, 11, 12, 13, 14, 15)] == [1, 1, 1, 4, 3, 2, 3, 1, 1, 2]
 
 
 def test_workspace_sizes(lib):
@@ -80,6 +80,12 @@ def test_workspace_sizes(lib):
     assert sz >= max_tiles * 28 * 16 + max_tiles * 8 + (n + 1) * 4
     assert lib.kev_prefill_workspace_size(n, T, lib.make_shape(28, 5, 128)) == 0   # H_q % H_kv
     assert lib.kev_prefill_workspace_size(n, T, lib.make_shape(28, 4, 96)) == 0    # d_h
+    # fp32 runs on the CUDA cores at any head dim that is a multiple of 16 up to 256
+    for d in (16, 48, 96, 256):
+        assert lib.kev_prefill_workspace_size(n, T, lib.make_shape(28, 4, d, "fp32")) > 0
+        assert lib.kev_decode_workspace_size(n, 512, lib.make_shape(28, 4, d, "fp32")) > 0
+    for d in (8, 100, 272):
+        assert lib.kev_prefill_workspace_size(n, T, lib.make_shape(28, 4, d, "fp32")) == 0
     assert lib.kev_prefill_workspace_size(5000, T, s) == 0                          # too many questions
     d = lib.kev_decode_workspace_size(64, 2458, lib.make_shape(32, 8, 128))
     assert d >= 64 * 8 * 4 + 64 * 8 * ((2458 + 255) // 256) * 4 * 130 * 4
@@ -112,6 +118,15 @@ def test_rope_table_size_and_host_errors_without_gpu(lib):
     assert lib.kev_rope_table(0x1000, 16, 96, 1e4, stream=0, check=False) == b.KEV_ERR_UNSUPPORTED
     assert lib.kev_rope_table(0x1000, 16, 64, 1.0, stream=0, check=False) == b.KEV_ERR_INVALID_ARG
     assert lib.kev_rope_table(0x1008, 16, 64, 1e4, stream=0, check=False) == b.KEV_ERR_INVALID_ARG
+    # RoPE pairs 16-byte chunks of a head's halves: head dims 64 and 128 only (fp32 attention
+    # itself takes any multiple of 16 up to 256)
+    s96 = lib.make_shape(4, 2, 96, "fp32")
+    assert lib.kev_rope_prefill(0x1000, 0x1000, 0x1000, 10, 0x1000, 1, None, None, None, 0, 0, s96, 0x1000, 16,
+                                0x1000, 1 << 20, None, stream=0, check=False) == b.KEV_ERR_UNSUPPORTED
+    assert lib.kev_prefill_attn_rope(0x1000, 0x1000, 0x1000, 10, 0x1000, 1, None, None, None, 0, 0, 0x1000, s96,
+                                     0x1000, 16, 0x1000, 1 << 20, None, stream=0, check=False) == b.KEV_ERR_UNSUPPORTED
+    assert lib.kev_rope_decode(0x1000, 0x1000, 0x1000, 0x1000, 1, s96, 0x1000, 16, None, stream=0,
+                               check=False) == b.KEV_ERR_UNSUPPORTED
     # no table / misaligned table / bad max_pos are refused before any CUDA call
     assert lib.kev_rope_prefill(0x1000, 0x1000, 0x1000, 10, 0x1000, 1, None, None, None, 0, 0, s, None, 16,
                                 0x1000, 1 << 20, None, stream=0, check=False) == b.KEV_ERR_INVALID_ARG

@@ -82,6 +82,70 @@ def test_random_decode_group_sizes(G):
     assert np.array_equal(first, host(run.out))
 
 
+@pytest.mark.parametrize("d", [16, 96, 256])
+def test_fp32_decode_head_dims_multiple_of_16(d):
+    """fp32 decode at head dims other than 64 and 128 (the one-warp-per-head kernel): appended
+    rows bit-exact, dropped questions untouched, outputs within the fp32 tolerance."""
+    rng = np.random.default_rng(500 + d)
+    h_kv, G, cap, n, n_slots = 2, 3, 300, 7, 9
+    pool_k = rng.standard_normal((n_slots, h_kv, cap, d), dtype=np.float32)
+    pool_v = rng.standard_normal((n_slots, h_kv, cap, d), dtype=np.float32)
+    slot_ids = rng.permutation(n_slots)[:n].astype(np.int32)
+    lens = np.array([0, 1, 31, 32, 33, 299, 150], np.int32)
+    active = np.array([1, 1, 1, 0, 1, 1, 1], np.uint8)
+    q_new = rng.standard_normal((n, h_kv * G, d), dtype=np.float32)
+    k_new = rng.standard_normal((n, h_kv, d), dtype=np.float32)
+    v_new = rng.standard_normal((n, h_kv, d), dtype=np.float32)
+    run = DecodeRun("fp32", h_kv * G, h_kv, d, pool_k, pool_v, slot_ids, lens, active, q_new, k_new, v_new,
+                    cap, n_slots)
+    run.run()
+    assert run.device_status() == 0
+    _check_decode(run, pool_k, pool_v, slot_ids, lens, active, q_new, k_new, v_new, "fp32")
+
+
+@pytest.mark.parametrize("dtype,d", [("bf16", 128), ("fp32", 64), ("fp32", 96)])
+def test_decode_step_equals_decode_then_advance(dtype, d):
+    """kev_decode_step = kev_decode_attn, then lens[i] += 1 for live i (tensor-core path: in the
+    merge kernel); an invalid step writes nothing and leaves lens as it was."""
+    import packed_question_isolated_gb300 as kev
+    rng = np.random.default_rng(600 + d)
+    h_kv, G, cap, n, n_slots = 2, 4, 900, 8, 10
+    f = W.f32_to_bf16_bits if dtype == "bf16" else (lambda x: x)
+    pool_k = f(rng.standard_normal((n_slots, h_kv, cap, d), dtype=np.float32))
+    pool_v = f(rng.standard_normal((n_slots, h_kv, cap, d), dtype=np.float32))
+    slot_ids = rng.permutation(n_slots)[:n].astype(np.int32)
+    lens = np.array([0, 127, 128, 500, 899, 3, 640, 255], np.int32)
+    active = np.array([1, 1, 0, 1, 1, 1, 0, 1], np.uint8)
+    q_new = f(rng.standard_normal((n, h_kv * G, d), dtype=np.float32))
+    k_new = f(rng.standard_normal((n, h_kv, d), dtype=np.float32))
+    v_new = f(rng.standard_normal((n, h_kv, d), dtype=np.float32))
+    ref = DecodeRun(dtype, h_kv * G, h_kv, d, pool_k, pool_v, slot_ids, lens, active, q_new, k_new, v_new, cap,
+                    n_slots)
+    assert ref.run() == 0 and ref.device_status() == 0
+    run = DecodeRun(dtype, h_kv * G, h_kv, d, pool_k, pool_v, slot_ids, lens, active, q_new, k_new, v_new, cap,
+                    n_slots)
+    st = kev.kev_decode_step(run.q_new, run.k_new, run.v_new, run.pool_k, run.pool_v, run.n_slots, run.cap,
+                             run.slot_ids, run.lens, run.active, run.n, run.out, run.shape, run.ws, run.ws_bytes,
+                             run.status)
+    assert st == 0 and run.device_status() == 0
+    assert np.array_equal(host(run.lens), lens + active.astype(np.int32))
+    live = active.astype(bool)
+    assert np.array_equal(host(run.out)[live], host(ref.out)[live])  # the same kernels, the same bits
+    _check_decode(run, pool_k, pool_v, slot_ids, lens, active, q_new, k_new, v_new, dtype)
+    # an invalid step (two live questions on one slot): nothing written, lens kept
+    bad_slots = slot_ids.copy()
+    bad_slots[1] = bad_slots[0]
+    bad = DecodeRun(dtype, h_kv * G, h_kv, d, pool_k, pool_v, bad_slots, lens, active, q_new, k_new, v_new, cap,
+                    n_slots)
+    kev.kev_decode_step(bad.q_new, bad.k_new, bad.v_new, bad.pool_k, bad.pool_v, bad.n_slots, bad.cap,
+                        bad.slot_ids, bad.lens, bad.active, bad.n, bad.out, bad.shape, bad.ws, bad.ws_bytes,
+                        bad.status)
+    assert bad.device_status() == kev.binding.KEV_ERR_SLOT
+    assert np.array_equal(host(bad.lens), lens)
+    assert np.isnan(f64(bad.out, dtype)).all()
+    assert np.array_equal(host(bad.pool_k), pool_k)
+
+
 def _ramp_pools(rng, n_slots, h_kv, cap, d, growth):
     """K rows aligned with a fixed +-1 direction u and growing with position: q = u scores
     position j at growth * j (log2 units, after the 1/sqrt(d) scale), so later chunks exceed

@@ -59,6 +59,21 @@ def test_random_cases_full_parity(case):
     _check_pools(run, w)
 
 
+@pytest.mark.parametrize("d", [16, 48, 96, 256])
+def test_fp32_head_dims_multiple_of_16(d):
+    """fp32 (CUDA cores) at head dims other than 64 and 128: any multiple of 16 up to 256."""
+    w = W.random_case(400 + d, [70, 1, 0, 161, 33], 6, 2, d, "fp32", gaps=[0, 2, 1, 0, 3], tail=2,
+                      permute_slots=True, n_slots=7)
+    run = PrefillRun(w)
+    run.run()
+    assert run.device_status() == 0
+    got = f64(run.out, w.dtype)[:w.total_tokens]
+    compare(got, _oracle_out(w), "fp32", f"fp32 d={d}")
+    seg = O.segment_ids(w.intervals, w.total_tokens)
+    assert (got[seg < 0] == 0).all()
+    _check_pools(run, w)
+
+
 def test_unsorted_interval_order_and_no_slot_write():
     w = W.random_case(77, [90, 300, 12, 150], 8, 2, 128, "bf16", gaps=[3, 0, 2, 0], order=[2, 0, 3, 1])
     run = PrefillRun(w, slots=False)

@@ -4,8 +4,9 @@
 decoded for 128 steps with the seeded early-stop schedule: a question leaves after an EOS
 draw or after its max_new_tokens steps (Kev pipeline article, gsyq.cn, §2.3: a finished
 question takes no further part in attention).  The decode loop runs twice from the same
-post-prefill state: eagerly, and as one captured CUDA graph replay (the form the benchmark
-times), with lens advanced on the device between steps.
+post-prefill state: eagerly (kev_decode_attn, then kev_decode_advance), and as one captured CUDA
+graph replay of kev_decode_step (the advance folded into the step; the form the benchmark times),
+with lens advanced on the device between steps.
 
 Checked against the oracle: every row of every question's prefill output; every live
 question's output at every step of both runs; the final slot contents bit for bit; rows of
@@ -82,11 +83,16 @@ def test_stress_whole_run_eager_and_graph():
     dws = torch.zeros(dws_bytes, dtype=torch.uint8, device="cuda")
     dst = torch.full((1,), -1, dtype=torch.int32, device="cuda")
 
-    def loop(outs):
+    def loop(outs):  # decode, then the lens advance, as two calls
         for t in range(steps):
             kev.kev_decode_attn(qn[t], kn[t], vn[t], pk, pv, w.n_slots, w.cap, sl, lens, act[t], N, outs[t], shape,
                                 dws, dws_bytes, dst)
             kev.kev_decode_advance(lens, act[t], N)
+
+    def loop_fused(outs):  # kev_decode_step: the advance folded into the merge kernel
+        for t in range(steps):
+            kev.kev_decode_step(qn[t], kn[t], vn[t], pk, pv, w.n_slots, w.cap, sl, lens, act[t], N, outs[t], shape,
+                                dws, dws_bytes, dst)
 
     # eager run
     outs_e = torch.full((steps, N, w.h_q, w.d), float("nan"), dtype=torch.bfloat16, device="cuda")
@@ -103,11 +109,11 @@ def test_stress_whole_run_eager_and_graph():
         assert torch.all(pk[w.slot_ids[i], :, tail] == SENT_K) and torch.all(pv[w.slot_ids[i], :, tail] == SENT_V)
     del outs_e
 
-    # graph replay from the same post-prefill state
+    # graph replay of the fused steps, from the same post-prefill state
     outs_g = torch.full((steps, N, w.h_q, w.d), float("nan"), dtype=torch.bfloat16, device="cuda")
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g):
-        loop(outs_g)
+        loop_fused(outs_g)
     pk.copy_(pk_pre)
     pv.copy_(pv_pre)
     lens.copy_(lens0)
