@@ -50,6 +50,12 @@ constexpr uint32_t kTmemCols = 64; // S^T x2 (cols 0, 16) + O^T x2 (cols 32, 48)
 // the exact rescaling path: below it, P < 2^64 and the fp32 sums cannot overflow.
 constexpr float kLog2Guard = 64.f;
 
+// Tensor maps of one call: the K/V pools in boxes of 16 << j rows (j < kBoxSizes), the new queries.
+constexpr int kBoxSizes = 4;
+struct DecodeMaps {
+  CUtensorMap k[kBoxSizes], v[kBoxSizes], q;
+};
+
 struct DTcParams {
   DecodeArgs a;
   long long wait_budget;
@@ -83,7 +89,8 @@ struct TSmem {
   static constexpr int kRed = kP + 2 * kPBytes;          // float red_m[4][16]
   static constexpr int kPiece = kRed + 4 * kN * 4;       // PieceInfo[2]
   static constexpr int kInfo = kPiece + 2 * (int)sizeof(PieceInfo);  // StageInfo[NS]
-  static constexpr int kBar = kInfo + NS * (int)sizeof(StageInfo);
+  static constexpr int kNew = kInfo + NS * (int)sizeof(StageInfo);  // per stage: the new K and V rows
+  static constexpr int kBar = kNew + NS * 2 * kD * 2;
   static constexpr int kBase = kBar + 512;               // int item_base[N+1], then int2 meta[N]
   static __host__ __device__ constexpr int meta_off(int n) { return kBase + ((n + 2) / 2) * 8; }
   static __host__ __device__ constexpr int bytes(int n) { return meta_off(n) + n * 8 + 1024; }
@@ -211,9 +218,7 @@ __device__ __forceinline__ void cursor_next(Cursor& u, const DecodeArgs& a, cons
 }
 
 template <int NS, int NH>
-__global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
-                                                               const __grid_constant__ CUtensorMap tm_v,
-                                                               const __grid_constant__ CUtensorMap tm_q,
+__global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_constant__ DecodeMaps maps,
                                                                const DTcParams prm) {
   using L = TSmem<NS>;
   const DecodeArgs& a = prm.a;
@@ -253,9 +258,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
-    tma_prefetch_desc(&tm_k);
-    tma_prefetch_desc(&tm_v);
-    tma_prefetch_desc(&tm_q);
+    for (int j = 0; j < kBoxSizes; ++j) {
+      tma_prefetch_desc(&maps.k[j]);
+      tma_prefetch_desc(&maps.v[j]);
+    }
+    tma_prefetch_desc(&maps.q);
   }
   if (warp == 1) {
     tmem_alloc(&bars->tmem_base, kTmemCols);
@@ -319,12 +326,27 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
             info[s] = StageInfo{u.i, u.g, u.c, u.nch, u.len, row0, x - u.c, flags};
             unsigned char* st = smem + L::kStage + s * L::kStageBytes;
             const int qrow = u.i * a.h_q + u.g * a.group;
-            mbar_arrive_expect_tx(&bars->full[s], L::kStageBytes);  // release: info[s] is visible with the phase
-            for (int c = 0; c < 2; ++c) {
-              tma_load_2d(st + c * (kC * 128), &tm_k, c * 64, row0, &bars->full[s]);
-              tma_load_2d(st + L::kKBytes + c * (kC * 128), &tm_v, c * 64, row0, &bars->full[s]);
-              tma_load_2d(st + 2 * L::kKBytes + c * (kN * 128), &tm_q, c * 64, qrow, &bars->full[s]);
+            // The chunk that holds position n = len reads only its len - 128 c cached rows, in
+            // one box per 64-column half of the smallest height that covers them (a TMA copy costs
+            // about as much to issue whatever its size); the rows past them are masked, or zeroed
+            // for V, by the fix-ups.  Every other chunk is a whole 128-row tile.
+            const int rows = (flags & kFix) ? u.len - u.c * kC : kC;
+            const int j = rows <= 16 ? 0 : rows <= 32 ? 1 : rows <= 64 ? 2 : 3;
+            const int new_bytes = (flags & kFix) ? 2 * kD * 2 : 0;  // the new K and V rows, for the fix-ups
+            mbar_arrive_expect_tx(&bars->full[s], (rows > 0 ? (16 << j) * 512 : 0) + L::kQBytes + new_bytes);  // release: info[s]
+            if (new_bytes) {
+              const int64_t src = ((int64_t)u.i * a.h_kv + u.g) * kD * 2;
+              unsigned char* nb = smem + L::kNew + s * 2 * kD * 2;
+              bulk_load(nb, static_cast<const unsigned char*>(a.k_new) + src, kD * 2, &bars->full[s]);
+              bulk_load(nb + kD * 2, static_cast<const unsigned char*>(a.v_new) + src, kD * 2, &bars->full[s]);
             }
+            if (rows > 0)
+              for (int c = 0; c < 2; ++c) {
+                tma_load_2d(st + c * (kC * 128), &maps.k[j], c * 64, row0, &bars->full[s]);
+                tma_load_2d(st + L::kKBytes + c * (kC * 128), &maps.v[j], c * 64, row0, &bars->full[s]);
+              }
+            for (int c = 0; c < 2; ++c)
+              tma_load_2d(st + 2 * L::kKBytes + c * (kN * 128), &maps.q, c * 64, qrow, &bars->full[s]);
             ++issued[s];
             cursor_next(u, a, item_base, meta);
           }
@@ -393,6 +415,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
           const int flags = info[s].flags;
           if (flags & kEnd) break;
           const bool first = flags & kFirst;
+          // the chunk that holds position n: its keys past n have P = 0, so only the 16-key steps
+          // up to n run (the fix-ups zero the V rows between n and the end of the last step)
+          const int nk = (flags & kFix) ? (min(kC, info[s].len + 1 - info[s].c * kC) + 15) >> 4 : kC / 16;
           if (!mbar_wait(&bars->p_full[k & 1], (k >> 1) & 1, abort_flag, budget)) { ok = false; break; }
           if (first && pc >= 2 && !mbar_wait(&bars->o_free[pc & 1], ((pc >> 1) - 1) & 1, abort_flag, budget)) {
             ok = false;
@@ -403,6 +428,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
           const uint32_t d_o = tmem + (2 + (pc & 1)) * kN;
 #pragma unroll
           for (int kk = 0; kk < kC / 16; ++kk) {
+            if (kk >= nk) break;
             const uint64_t av = sdesc_sw128(v_addr + kk * 16 * 128, kC * 128, 1024);
             const uint64_t bp =
                 sdesc_sw128(p_addr + (k & 1) * L::kPBytes + (kk >> 2) * (kN * 128) + (kk & 3) * 32, 16, 1024);
@@ -472,22 +498,22 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
 
         if (inf.flags & kFix) {
           // fix-ups of the chunk that holds position n = len: the new K/V row goes into the
-          // swizzled tiles (and, once, into the pool); V rows past it are zeroed (their P is 0,
-          // but stale pool contents could hold NaN bit patterns)
+          // swizzled tiles (and, once, into the pool); V rows past it, up to the end of the last
+          // 16-key PV step, are zeroed (their P is 0, but stale contents could hold NaN bit patterns)
           const int rn = inf.len - p0;
-          const int64_t src = ((int64_t)inf.i * a.h_kv + inf.g) * kD * 2;
           const int64_t dst = ((int64_t)inf.row0 + rn) * kD * 2;  // the new row's pool row
           if (sid < 32) {
             const int ch = sid & 15;  // 16-byte chunk of the 256-byte row
             const bool isv = sid >= 16;
-            const uint4 w = *reinterpret_cast<const uint4*>(
-                static_cast<const unsigned char*>(isv ? a.v_new : a.k_new) + src + ch * 16);
+            // the new rows came with the stage
+            const uint4 w = *reinterpret_cast<const uint4*>(smem + L::kNew + s * 2 * kD * 2 + (isv ? kD * 2 : 0) + ch * 16);
             unsigned char* tile = isv ? vst : kst;
             *reinterpret_cast<uint4*>(tile + (ch >> 3) * (kC * 128) + rn * 128 + (((ch & 7) ^ (rn & 7)) << 4)) = w;
             if (ok)
               *reinterpret_cast<uint4*>(static_cast<unsigned char*>(isv ? a.pool_v : a.pool_k) + dst + ch * 16) = w;
           }
-          for (int e = (nr * 16) + sid; e < kC * 16; e += kQuad) {  // rows nr..127, 16 chunks each
+          const int rows_pv = ((nr + 15) >> 4) << 4;  // rows the PV MMAs read
+          for (int e = (nr * 16) + sid; e < rows_pv * 16; e += kQuad) {  // rows nr..rows_pv-1, 16 chunks each
             const int row = e >> 4, ch = e & 15;
             *reinterpret_cast<uint4*>(vst + (ch >> 3) * (kC * 128) + row * 128 + (ch & 7) * 16) =
                 make_uint4(0, 0, 0, 0);
@@ -792,8 +818,7 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_rows
 }
 
 template <int NS, int NH>
-cudaError_t launch_ns(const DecodeArgs& a, int num_sms, cudaStream_t st, const CUtensorMap& mk,
-                      const CUtensorMap& mv, const CUtensorMap& mq) {
+cudaError_t launch_ns(const DecodeArgs& a, int num_sms, cudaStream_t st, const DecodeMaps& m) {
   const int smem = TSmem<NS>::bytes(a.n);
   cudaError_t e =
       cudaFuncSetAttribute(decode_tc_kernel<NS, NH>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -802,7 +827,7 @@ cudaError_t launch_ns(const DecodeArgs& a, int num_sms, cudaStream_t st, const C
   p.a = a;
   p.a.test_stall = test_stall_requested();
   p.wait_budget = wait_budget_cycles();
-  e = launch_pdl(decode_tc_kernel<NS, NH>, dim3(num_sms), dim3(kThreads), (size_t)smem, st, mk, mv, mq, p);
+  e = launch_pdl(decode_tc_kernel<NS, NH>, dim3(num_sms), dim3(kThreads), (size_t)smem, st, m, p);
   if (e != cudaSuccess) return e;
   // the merge kernel, programmatically dependent on the decode kernel (its launch overlaps the
   // decode kernel's end; its griddepcontrol.wait orders every read after the decode grid)
@@ -810,11 +835,10 @@ cudaError_t launch_ns(const DecodeArgs& a, int num_sms, cudaStream_t st, const C
 }
 
 template <int NH>
-cudaError_t launch_nh(const DecodeArgs& a, int num_sms, cudaStream_t st, const CUtensorMap& mk,
-                      const CUtensorMap& mv, const CUtensorMap& mq) {
+cudaError_t launch_nh(const DecodeArgs& a, int num_sms, cudaStream_t st, const DecodeMaps& m) {
   constexpr int kMaxSmem = 232448;
-  if (TSmem<3>::bytes(a.n) <= kMaxSmem) return launch_ns<3, NH>(a, num_sms, st, mk, mv, mq);
-  return launch_ns<2, NH>(a, num_sms, st, mk, mv, mq);
+  if (TSmem<3>::bytes(a.n) <= kMaxSmem) return launch_ns<3, NH>(a, num_sms, st, m);
+  return launch_ns<2, NH>(a, num_sms, st, m);
 }
 
 }  // namespace
@@ -822,14 +846,15 @@ cudaError_t launch_nh(const DecodeArgs& a, int num_sms, cudaStream_t st, const C
 cudaError_t launch_decode_tc(const DecodeArgs& a, int num_sms, cudaStream_t st) {
   static_assert(kDecodeTcMaxGroup == kN, "one MMA covers the q-heads of a group");
   if (a.group < 1 || a.group > kDecodeTcMaxGroup) return cudaErrorInvalidValue;
-  CUtensorMap mk, mv, mq;
+  DecodeMaps m;
   const uint64_t pool_rows = a.block_table ? (uint64_t)a.n_blocks * a.h_kv * kC : (uint64_t)a.n_slots * a.h_kv * a.cap;
-  if (!make_map(&mk, a.pool_k, pool_rows, kC) || !make_map(&mv, a.pool_v, pool_rows, kC) ||
-      !make_map(&mq, a.q_new, (uint64_t)a.n * a.h_q, kN))
-    return cudaErrorInvalidValue;
-  if (a.group <= 4) return launch_nh<4>(a, num_sms, st, mk, mv, mq);
-  if (a.group <= 8) return launch_nh<8>(a, num_sms, st, mk, mv, mq);
-  return launch_nh<16>(a, num_sms, st, mk, mv, mq);
+  for (int j = 0; j < kBoxSizes; ++j)
+    if (!make_map(&m.k[j], a.pool_k, pool_rows, 16u << j) || !make_map(&m.v[j], a.pool_v, pool_rows, 16u << j))
+      return cudaErrorInvalidValue;
+  if (!make_map(&m.q, a.q_new, (uint64_t)a.n * a.h_q, kN)) return cudaErrorInvalidValue;
+  if (a.group <= 4) return launch_nh<4>(a, num_sms, st, m);
+  if (a.group <= 8) return launch_nh<8>(a, num_sms, st, m);
+  return launch_nh<16>(a, num_sms, st, m);
 }
 
 }  // namespace kev
