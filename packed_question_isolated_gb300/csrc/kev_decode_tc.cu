@@ -13,17 +13,18 @@
 // so the CUDA cores only run the softmax over 128 x 16 scores per chunk and the kernel is a
 // TMA stream of K/V tiles: decode is HBM-bound, and this keeps its instruction count tiny.
 //
-// Roles (224 threads): warp 0 issues the TMA loads (K, V tiles of 128 rows, the 16 query rows)
-// into a ring of stages, records each chunk's position in the stage, and pulls the K/V tiles
-// of the chunk kAhead places ahead into L2, so more of the HBM stream is in flight than the
-// stages alone hold; warp 1 issues the S MMAs, warp 6 the PV MMAs (each on its own thread, so
-// neither waits behind the other; a stage is released when its PV completes); warps 2-5 (one
-// thread per key row for S^T, one thread per head dimension for O^T): the softmax over the
-// group's heads only, with a reference max per piece and per-thread sums, P^T into shared
-// memory, the new K/V row and the zeroing of V rows past the question's length (fix-ups of
-// the chunk that holds position n), and the output / split-K partials.  Consecutive chunks of
-// one (question, kv head) in a CTA accumulate in TMEM; the pieces of one (question, kv head)
-// that different CTAs produce are merged in a fixed order by the CTA that finishes last.
+// Roles (384 threads): warp 0 issues the TMA loads (K, V tiles, the 16 query rows, and for the
+// chunk that holds position n its new K and V rows) into a ring of stages and records each
+// chunk's position in the stage; warp 11 does the fix-ups of that chunk as soon as it lands (the
+// new K/V row into the tiles and, once, into the pool; V rows past n zeroed up to the end of
+// the last 16-key PV step), so they never wait behind the softmax of the chunk before; warp 1
+// issues the S MMAs, warp 6 the PV MMAs (each on its own thread, so neither waits behind the
+// other; a stage is released when its PV completes); warps 2-5 (one thread per key row for S^T):
+// the softmax over the group's heads only, with a reference max per piece and per-thread sums,
+// P^T into shared memory; warps 7-10 (one thread per head dimension of O^T): the output /
+// split-K partials.  Consecutive chunks of one (question, kv head) in a CTA accumulate in TMEM;
+// the pieces of one (question, kv head) that different CTAs produce are merged in a fixed order
+// by a second kernel.
 #include <cuda.h>
 #include <stdlib.h>
 
@@ -42,7 +43,7 @@ constexpr int kN = 16;             // MMA N: q-heads of one group, padded to 16
 constexpr int kC = dec::kChunk;    // 128 keys per chunk
 constexpr int kBatch = 4;          // most consecutive chunks per dynamic grab
 constexpr int kTailPerCta = 0;     // single-chunk grabs at the end, per CTA of the grid (measured: none is best)
-constexpr int kThreads = 352;
+constexpr int kThreads = 384;
 constexpr int kQuad = 128;         // threads of the softmax (warps 2-5) and of the epilogue (warps 7-10)
 constexpr long long kDrainBudget = 4000000000ll;
 constexpr uint32_t kTmemCols = 64; // S^T x2 (cols 0, 16) + O^T x2 (cols 32, 48), 16 cols each
@@ -98,7 +99,7 @@ struct TSmem {
 
 struct TBars {
   uint64_t full[3], empty[3];
-  uint64_t fixed, s_full[2], s_free[2], p_full[2], o_done[2];
+  uint64_t fixed[3], s_full[2], s_free[2], p_full[2], o_done[2];  // fixed: per stage, once per chunk
   uint64_t o_full[2], o_free[2], pc_full[2];  // per piece buffer: O^T complete, O^T + info consumed, info written
   uint64_t drain_s, drain_p;
   uint64_t stall;  // timeout test hook: nothing ever arrives on it
@@ -242,7 +243,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
       mbar_init(&bars->full[s], 1);
       mbar_init(&bars->empty[s], 1);
     }
-    mbar_init(&bars->fixed, kQuad);
+    for (int s = 0; s < NS; ++s) mbar_init(&bars->fixed[s], 32);  // the fix-up warp
     for (int b = 0; b < 2; ++b) {
       mbar_init(&bars->s_full[b], 1);
       mbar_init(&bars->s_free[b], kQuad);
@@ -374,17 +375,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
       // ---------------------------------------------------------------- S issuer
       if (lane == 0) {
         constexpr uint32_t idesc_s = idesc_bf16(128, kN, false, false);  // K (K-major) x Q^T
-        uint32_t fix_cnt = 0;
         bool ok = true;
         for (int k = 0;; ++k) {
           const int s = k % NS, sb = k & 1;
           if (!mbar_wait(&bars->full[s], (k / NS) & 1, abort_flag, budget)) { ok = false; break; }
           const int flags = info[s].flags;
           if (flags & kEnd) break;
-          if (flags & kFix) {  // the new row is written into the tiles first
-            if (!mbar_wait(&bars->fixed, fix_cnt & 1, abort_flag, budget)) { ok = false; break; }
-            ++fix_cnt;
-          }
+          // the new row is written into the tiles first
+          if ((flags & kFix) && !mbar_wait(&bars->fixed[s], (k / NS) & 1, abort_flag, budget)) { ok = false; break; }
           if (k >= 2 && !mbar_wait(&bars->s_free[sb], ((k >> 1) - 1) & 1, abort_flag, budget)) { ok = false; break; }
           tc_fence_after();
           const uint32_t k_addr = smem_u32(smem + L::kStage + s * L::kStageBytes);
@@ -445,6 +443,43 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
         umma_commit(&bars->drain_p);
         mbar_wait(&bars->drain_p, 0, never, kDrainBudget);
       }
+    } else if (warp == 11) {
+      // ---------------------------------------------------------------- fix-up warp
+      // Per chunk, once its stage has landed: for the chunk that holds position n = len, the new
+      // K/V row (it came with the stage) goes into the swizzled tiles and, once, into the pool,
+      // and V rows past it, up to the end of the last 16-key PV step, are zeroed (their P is 0,
+      // but stale contents could hold NaN bit patterns).  fixed[s] completes once per chunk.
+      bool ok = true;
+      for (int k = 0;; ++k) {
+        const int s = k % NS;
+        ok = warp_wait(&bars->full[s], (k / NS) & 1, abort_flag, budget);
+        if (!ok) break;
+        const StageInfo inf = info[s];
+        if (inf.flags & kEnd) break;
+        if (inf.flags & kFix) {
+          unsigned char* kst = smem + L::kStage + s * L::kStageBytes;
+          unsigned char* vst = kst + L::kKBytes;
+          const int p0 = inf.c * kC;
+          const int nr = min(kC, inf.len + 1 - p0);
+          const int rn = inf.len - p0;
+          const int64_t dst = ((int64_t)inf.row0 + rn) * kD * 2;  // the new row's pool row
+          const int ch = lane & 15;  // 16-byte chunk of the 256-byte row
+          const bool isv = lane >= 16;
+          const uint4 w = *reinterpret_cast<const uint4*>(smem + L::kNew + s * 2 * kD * 2 + (isv ? kD * 2 : 0) + ch * 16);
+          unsigned char* tile = isv ? vst : kst;
+          *reinterpret_cast<uint4*>(tile + (ch >> 3) * (kC * 128) + rn * 128 + (((ch & 7) ^ (rn & 7)) << 4)) = w;
+          *reinterpret_cast<uint4*>(static_cast<unsigned char*>(isv ? a.pool_v : a.pool_k) + dst + ch * 16) = w;
+          const int rows_pv = ((nr + 15) >> 4) << 4;  // rows the PV MMAs read
+          for (int e = (nr * 16) + lane; e < rows_pv * 16; e += 32) {  // rows nr..rows_pv-1, 16 chunks each
+            const int row = e >> 4, c16 = e & 15;
+            *reinterpret_cast<uint4*>(vst + (c16 >> 3) * (kC * 128) + row * 128 + (c16 & 7) * 16) =
+                make_uint4(0, 0, 0, 0);
+          }
+          fence_proxy_async_smem();
+        }
+        mbar_arrive(&bars->fixed[s]);
+      }
+      if (!ok && lane == 0) raise_timeout(a, bars);
     } else if (warp <= 5) {
       // ---------------------------------------------------------------- softmax warps 2-5
       const int q4 = warp & 3;                 // TMEM lane quarter of this warp
@@ -493,34 +528,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
         const bool first = inf.flags & kFirst, last = inf.flags & kLast;
         const int p0 = inf.c * kC;
         const int nr = min(kC, inf.len + 1 - p0);  // valid rows, the new one included
-        unsigned char* kst = smem + L::kStage + s * L::kStageBytes;
-        unsigned char* vst = kst + L::kKBytes;
-
-        if (inf.flags & kFix) {
-          // fix-ups of the chunk that holds position n = len: the new K/V row goes into the
-          // swizzled tiles (and, once, into the pool); V rows past it, up to the end of the last
-          // 16-key PV step, are zeroed (their P is 0, but stale contents could hold NaN bit patterns)
-          const int rn = inf.len - p0;
-          const int64_t dst = ((int64_t)inf.row0 + rn) * kD * 2;  // the new row's pool row
-          if (sid < 32) {
-            const int ch = sid & 15;  // 16-byte chunk of the 256-byte row
-            const bool isv = sid >= 16;
-            // the new rows came with the stage
-            const uint4 w = *reinterpret_cast<const uint4*>(smem + L::kNew + s * 2 * kD * 2 + (isv ? kD * 2 : 0) + ch * 16);
-            unsigned char* tile = isv ? vst : kst;
-            *reinterpret_cast<uint4*>(tile + (ch >> 3) * (kC * 128) + rn * 128 + (((ch & 7) ^ (rn & 7)) << 4)) = w;
-            if (ok)
-              *reinterpret_cast<uint4*>(static_cast<unsigned char*>(isv ? a.pool_v : a.pool_k) + dst + ch * 16) = w;
-          }
-          const int rows_pv = ((nr + 15) >> 4) << 4;  // rows the PV MMAs read
-          for (int e = (nr * 16) + sid; e < rows_pv * 16; e += kQuad) {  // rows nr..rows_pv-1, 16 chunks each
-            const int row = e >> 4, ch = e & 15;
-            *reinterpret_cast<uint4*>(vst + (ch >> 3) * (kC * 128) + row * 128 + (ch & 7) * 16) =
-                make_uint4(0, 0, 0, 0);
-          }
-          fence_proxy_async_smem();
-          mbar_arrive(&bars->fixed);
-        }
 
         // scores of this thread's key row for the group's heads
         wait_ok(&bars->s_full[sb], (k >> 1) & 1);
@@ -695,12 +702,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
   pdl_trigger();
 }
 
-// Merge of the pieces of every (question, kv head) that the decode kernel split (one CTA per
-// pair, thread r = head dimension r; the pair's first chunk and chunk count come from the decode
-// kernel through the workspace, so lens is not read here), in a fixed order: piece 0 starts at chunk 0, piece j > 0
-// at the j-th batch boundary of the grab plan after the pair's first chunk.  Online over rounds of pieces whose
-// reference max and sum are gathered into shared memory while the O rows load.  Block 0 also
-// resets the decode kernel's batch counter for the next call.
+// Merge of the pieces of every (question, kv head) that the decode kernel split (thread r =
+// head dimension r; the pair's first chunk and chunk count come from the decode kernel through
+// the workspace, so lens is not read here), in a fixed order: piece 0 starts at chunk 0, piece
+// j > 0 at the j-th batch boundary of the grab plan after the pair's first chunk.  Online over
+// rounds of pieces whose reference max and sum are gathered into shared memory while the O rows
+// load.  Everything that decides a CTA's work -- the call's code and grab plan, the live flag and
+// chunk range of pair blockIdx.x + t * gridDim.x for each thread t, a question's lens for the
+// advance -- is loaded in one round trip; the CTA then merges only its pairs that were split.
+// Block 0 also resets the decode kernel's batch counter for the next call.
 template <int NH>
 __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeArgs a) {
   pdl_wait();  // the decode grid is complete and visible
@@ -708,31 +718,45 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeArgs a) {
   // (the next step's segment builder launches during the merge instead of after it)
   pdl_trigger();
   int* sched = reinterpret_cast<int*>(a.ws + a.layout.sched);
-  if (blockIdx.x == 0 && threadIdx.x == 0) sched[0] = 0;
-  if (sched[2] != ST_OK) return;  // invalid call (or timeout): nothing to merge, lens kept
-  if (a.advance_lens)  // kev_decode_step: the step is complete, so lens moves on (nothing here reads it)
-    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < a.n; i += gridDim.x * blockDim.x)
-      if (a.active[i]) a.advance_lens[i] += 1;
+  const int2* item_xi0 = reinterpret_cast<const int2*>(a.ws + a.layout.xi0);
+  const int r = threadIdx.x;
+  const int n_pairs = a.n * a.h_kv;
+  const int code = sched[2];
   BatchPlan plan;
   plan.x1 = sched[1];
   plan.n1 = sched[3];
   plan.B = sched[4];
+  const int pair = blockIdx.x + r * gridDim.x;  // the grid covers every pair and every question
+  const int live = pair < n_pairs ? a.active[pair / a.h_kv] : 0;
+  const int2 xc = pair < n_pairs ? item_xi0[pair] : make_int2(-1, 0);  // written for every live pair
+  const int qi = blockIdx.x * blockDim.x + r;
+  const bool adv = a.advance_lens && qi < a.n && a.active[qi];
+  const int len = adv ? a.advance_lens[qi] : 0;
+  if (blockIdx.x == 0 && r == 0) sched[0] = 0;
+  if (code != ST_OK) return;  // invalid call (or timeout): nothing to merge, lens kept
+  if (adv) a.advance_lens[qi] = len + 1;  // kev_decode_step: the step is complete, so lens moves on
+
+  __shared__ int s_pair[128], s_xi0[128], s_nch[128], s_n;
+  if (r == 0) s_n = 0;
+  __syncthreads();
+  if (live && xc.x >= 0 && plan.of(xc.x + xc.y - 1) != plan.of(xc.x)) {  // more than one piece
+    const int e = atomicAdd(&s_n, 1);
+    s_pair[e] = pair;
+    s_xi0[e] = xc.x;
+    s_nch[e] = xc.y;
+  }
+  __syncthreads();
+  const int n_split = s_n;
+
   __shared__ float mg_m[128], mg_l[128];
-  const int r = threadIdx.x;
   const float* partials = reinterpret_cast<const float*>(a.ws + a.layout.partials);
-  const int2* item_xi0 = reinterpret_cast<const int2*>(a.ws + a.layout.xi0);
   constexpr int pstride = kN * (kD + 2);
   constexpr int kRound = 32 / NH > 8 ? 8 : 32 / NH;  // pieces per round (O loads in flight)
-  for (int cidx = blockIdx.x; cidx < a.n * a.h_kv; cidx += gridDim.x) {
+  for (int e = 0; e < n_split; ++e) {
+    const int cidx = s_pair[e], xi0 = s_xi0[e], nch = s_nch[e];
     const int i = cidx / a.h_kv, g = cidx % a.h_kv;
-    // three independent loads in one round trip
-    const int live = a.active[i];
-    const int2 xc = item_xi0[cidx];  // written by this call's decode kernel for every live pair
-    const int xi0 = xc.x, nch = xc.y;
-    if (!live || xi0 < 0) continue;  // dropped, or not a chunk index (never written by a valid call)
     const int b0 = plan.of(xi0);
     const int np = plan.of(xi0 + nch - 1) - b0 + 1;
-    if (np == 1) continue;  // one piece: the decode kernel wrote the output
     const float* base = partials + (int64_t)cidx * a.layout.max_chunks * pstride;
     auto piece_off = [&](int j) { return (j == 0 ? 0 : plan.start(b0 + j) - xi0) * pstride; };
     float M[NH], Ls[NH], O[NH];
@@ -831,7 +855,10 @@ cudaError_t launch_ns(const DecodeArgs& a, int num_sms, cudaStream_t st, const D
   if (e != cudaSuccess) return e;
   // the merge kernel, programmatically dependent on the decode kernel (its launch overlaps the
   // decode kernel's end; its griddepcontrol.wait orders every read after the decode grid)
-  return launch_pdl(decode_merge_kernel<NH>, dim3((unsigned)min(a.n * a.h_kv, 8 * num_sms)), dim3(128), 0, st, a);
+  // one pair per thread at most (the CTAs spread the merges), every question covered for the advance
+  const int pairs = a.n * a.h_kv;
+  const int grid = max(min(pairs, 4 * num_sms), max((pairs + 127) / 128, (a.n + 127) / 128));
+  return launch_pdl(decode_merge_kernel<NH>, dim3((unsigned)grid), dim3(128), 0, st, a);
 }
 
 template <int NH>
