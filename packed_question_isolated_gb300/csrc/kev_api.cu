@@ -218,6 +218,17 @@ kev_status kev_prefill_from_segments(const void* q, const void* k, const void* v
   p.ws = static_cast<const char*>(workspace);
   p.layout = layout;
   p.dev_status = dev_status;
+  // the CTA-pair kernel stores the whole K/V tiles into the slots itself; the slot write below
+  // then copies only each question's last, partial tile
+  p.store_tiles = slot_ids != nullptr && total_tokens > 0 && prefill_on_pairs(shape) &&
+                  (int64_t)n_slots * shape->h_kv * slot_cap < ((int64_t)1 << 31);  // TMA row coordinates
+  if (p.store_tiles) {
+    p.slot_ids = slot_ids;
+    p.pool_k = pool_k;
+    p.pool_v = pool_v;
+    p.n_slots = n_slots;
+    p.cap = slot_cap;
+  }
   cudaError_t e = launch_prefill(p, shape, sms, s);
   if (e != cudaSuccess) return KEV_ERR_CUDA;
 
@@ -239,6 +250,7 @@ kev_status kev_prefill_from_segments(const void* q, const void* k, const void* v
   x.ws = static_cast<const char*>(workspace);
   x.layout = layout;
   x.after_attention = total_tokens > 0;  // the attention kernel was launched just before
+  x.tails_only = p.store_tiles;
   return from_cuda(launch_aux(x, sms, s));
 }
 

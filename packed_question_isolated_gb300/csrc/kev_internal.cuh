@@ -195,6 +195,9 @@ struct PrefillArgs {
   const void* pool_v = nullptr;
   int32_t n_slots = 0;
   int32_t cap = 0;
+  // CTA-pair kernel: also store every whole 128-row K/V tile of each question into its slot
+  // (pools, slot_ids and cap above), from the shared-memory copies the attention loads anyway
+  bool store_tiles = false;
 };
 
 struct AuxArgs {  // slot write + zero rows of tokens in no question
@@ -221,6 +224,9 @@ struct AuxArgs {  // slot write + zero rows of tokens in no question
   // launched right after an attention kernel that waited for the segment builder before letting
   // this grid start: run alongside its tail, wait for it at the end
   bool after_attention = false;
+  // the attention kernel stored every whole 128-row tile of each question: copy only the rows of
+  // each question's last, partial tile
+  bool tails_only = false;
 };
 
 struct DecodeArgs {

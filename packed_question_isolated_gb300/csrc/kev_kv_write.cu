@@ -86,6 +86,7 @@ __global__ void __launch_bounds__(kAuxThreads) aux_kernel(AuxArgs a) {
           const int r = (int)(rg / a.h_kv), g = (int)(rg % a.h_kv);
           const int i = question_of(s_cu, a.n, r);
           const int j = r - s_cu[i];
+          if (a.tails_only && j < ((s_cu[i + 1] - s_cu[i]) & ~127)) continue;  // stored by the attention kernel
           const int2 bs = s_bs[i];
           const int64_t src = ((int64_t)(bs.x + j) * a.h_kv + g) * vpr + v;
           if (paged) {  // block of position j (the tables were checked before the attention)

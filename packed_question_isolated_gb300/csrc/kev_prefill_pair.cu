@@ -66,6 +66,13 @@ struct PairParams {
   int32_t* dev_status;
   long long wait_budget;
   int32_t test_stall;
+  // slot write of every whole 128-row K/V tile (store_tiles): pool row of (slot, kv head g,
+  // position j) is (slot * h_kv + g) * cap + j
+  const int32_t* slot_ids;
+  int32_t h_kv;
+  int32_t cap;
+  int32_t n_slots;
+  int32_t store_tiles;
 };
 
 struct Smem {
@@ -112,7 +119,7 @@ struct Half {
   int head, row0, rows, nkv;
 };
 struct Unit {
-  int q, g, seg_begin;
+  int q, g, seg_begin, len;
   int nkv;        // key tiles the unit loads
   int nkv_t[2];   // per MMA tile (0: absent)
   int s[4];       // halves: A even, A odd, B even, B odd
@@ -131,6 +138,7 @@ __device__ __forceinline__ Unit load_unit(const int4* units, const kev_interval*
   x.s[2] = w1.z;
   x.s[3] = w1.w;
   x.seg_begin = iv[x.q].begin;
+  x.len = iv[x.q].end - x.seg_begin;
   return x;
 }
 
@@ -156,6 +164,7 @@ __device__ __forceinline__ int snake(int r, int c, int C) { return r * C + ((r &
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     prefill_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_out,
+                        const __grid_constant__ CUtensorMap tm_pk, const __grid_constant__ CUtensorMap tm_pv,
                         const PairParams p) {
   using L = Smem;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -205,6 +214,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
     tma_prefetch_desc(&tm_out);
+    if (p.store_tiles) {
+      tma_prefetch_desc(&tm_pk);
+      tma_prefetch_desc(&tm_pv);
+    }
   }
   if (warp == kMmaWarp) {  // the same columns in both CTAs
     tmem_alloc_pair(&bars->tmem_base, kTmemCols);
@@ -228,13 +241,38 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // ---------------------------------------------------------------- K/V producer
       // Sequence 2j is K(j) (this CTA's 64 keys), 2j + 1 is V(j) (this CTA's 64 dims).  The even
       // CTA arms each slot's barrier for both CTAs' bytes; the odd CTA's copies complete on it.
+      // With store_tiles, the tiles this CTA holds of every whole 128-row key tile j of a
+      // (question, kv head) also go to the slot pool, once: from the unit with the half of q-head 0
+      // of the group at query tile j, at its key step j.  A slot's tile is stored when its MMAs
+      // are done with it and the slot is about to be refilled (or at the end).
       if (lane == 0) {
         uint32_t seq = 0;
         uint32_t loads[kRingSlots] = {};
+        int pend[kRingSlots];  // pool row of the key tile a slot holds for the slot write, or -1
+        for (int s = 0; s < kRingSlots; ++s) pend[s] = -1;
+        auto flush = [&](int s) {  // slot s: K (even) or V (odd) of this CTA, into the pool
+          unsigned char* src = smem + L::kRing + s * L::kSlot;
+          if (s & 1) {  // all 128 keys, dims [64 rank, 64 rank + 64)
+            tma_store_2d(&tm_pv, src, rank * 64, pend[s]);
+          } else {      // keys [64 rank, 64 rank + 64), all 128 dims
+            tma_store_2d(&tm_pk, src, 0, pend[s] + 64 * rank);
+            tma_store_2d(&tm_pk, src + L::kKSub, 64, pend[s] + 64 * rank);
+          }
+          bulk_commit_group();
+          pend[s] = -1;
+        };
         bool ok = !(p.test_stall && blockIdx.x == 0) || mbar_wait(&bars->stall, 0, abort_flag, budget);
         for (int rnd = 0, u = cid; u < n_units && ok; u = snake(++rnd, cid, ncl)) {
           const Unit x = load_unit(units, p.intervals, u);
+          const int slot = p.store_tiles ? p.slot_ids[x.q] : -1;
           for (int j = 0; j < x.nkv && ok; ++j) {
+            bool store = slot >= 0 && slot < p.n_slots && (j + 1) * kBN <= min(x.len, p.cap);
+            if (store) {
+              bool head0 = false;
+              for (int k = 0; k < 4; ++k)
+                head0 |= x.s[k] >= 0 && (x.s[k] & ((1 << kUnitHeadBits) - 1)) == 0 && (x.s[k] >> kUnitHeadBits) == j;
+              store = head0;
+            }
             for (int is_v = 0; is_v < 2; ++is_v, ++seq) {
               const int s = seq % kRingSlots;
               const uint32_t round = seq / kRingSlots;
@@ -242,6 +280,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 ok = false;
                 break;
               }
+              if (pend[s] >= 0) {  // its MMAs are done: store the old tile, then let the new one in
+                flush(s);
+                bulk_wait_read_all();
+              }
+              pend[s] = store ? (int)(((int64_t)slot * p.h_kv + x.g) * p.cap + j * kBN) : -1;
               if (leader) mbar_arrive_expect_tx(&bars->r_full[s], 2 * L::kSlot);
               unsigned char* dst = smem + L::kRing + s * L::kSlot;
               const uint32_t bar = mapa_rank(smem_u32(&bars->r_full[s]), 0);
@@ -257,6 +300,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
         }
         if (!ok) raise_timeout(p, bars);
+        // the tiles still waiting for the slot write: stored once their MMAs are done
+        for (int s = 0; s < kRingSlots && ok; ++s)
+          if (pend[s] >= 0) {
+            ok = mbar_wait(&bars->r_empty[s], (loads[s] - 1) & 1, abort_flag, budget);
+            if (ok) flush(s);
+          }
+        bulk_wait_all();  // the stores are complete before the CTA leaves
         if (*abort_flag && leader) {  // the copies counted on this CTA's barriers land before it leaves
           for (int s = 0; s < kRingSlots; ++s)
             if (loads[s]) mbar_wait(&bars->r_full[s], (loads[s] - 1) & 1, never, kDrainBudget);
@@ -694,12 +744,20 @@ int max_pairs(int num_sms) {
 
 cudaError_t launch_prefill_pair(const PrefillArgs& a, int num_sms, cudaStream_t s) {
   if (a.T <= 0 || a.layout.max_items == 0) return cudaSuccess;
-  CUtensorMap mq, mk, mv, mo;
+  CUtensorMap mq, mk, mv, mo, mpk, mpv;
   if (!make_map(&mq, a.q, (uint64_t)a.h_q * kD, (uint64_t)a.T, 128) ||
       !make_map(&mo, a.out, (uint64_t)a.h_q * kD, (uint64_t)a.T, 32) ||
       !make_map(&mk, a.k, (uint64_t)a.h_kv * kD, (uint64_t)a.T, 64) ||
       !make_map(&mv, a.v, (uint64_t)a.h_kv * kD, (uint64_t)a.T, 128))
     return cudaErrorInvalidValue;
+  if (a.store_tiles) {  // the pools as [n_slots * H_kv * cap, 128] rows, the boxes of the ring slots
+    const uint64_t rows = (uint64_t)a.n_slots * a.h_kv * a.cap;
+    if (!make_map(&mpk, a.pool_k, kD, rows, 64) || !make_map(&mpv, a.pool_v, kD, rows, 128))
+      return cudaErrorInvalidValue;
+  } else {
+    mpk = mk;  // not used
+    mpv = mv;
+  }
   PairParams p;
   p.ws = const_cast<char*>(a.ws);
   p.layout = a.layout;
@@ -711,6 +769,11 @@ cudaError_t launch_prefill_pair(const PrefillArgs& a, int num_sms, cudaStream_t 
   p.dev_status = a.dev_status;
   p.wait_budget = wait_budget_cycles();
   p.test_stall = test_stall_requested();
+  p.store_tiles = a.store_tiles ? 1 : 0;
+  p.slot_ids = a.slot_ids;
+  p.h_kv = a.h_kv;
+  p.cap = a.cap;
+  p.n_slots = a.n_slots;
   cudaError_t e = cudaFuncSetAttribute(prefill_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        Smem::kLaunchBytes);
   if (e != cudaSuccess) return e;
@@ -727,7 +790,7 @@ cudaError_t launch_prefill_pair(const PrefillArgs& a, int num_sms, cudaStream_t 
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, prefill_pair_kernel, mq, mk, mv, mo, p);
+  return cudaLaunchKernelEx(&cfg, prefill_pair_kernel, mq, mk, mv, mo, mpk, mpv, p);
 }
 
 }  // namespace kev

@@ -118,6 +118,20 @@ struct UnitShape {
   }
 };
 
+// Shared-memory counter add aggregated over a warp: the lanes that pass the same `key` add `v`
+// each with one atomic between them (units mostly share a handful of bins, so per-lane atomics
+// on one word would serialise the warp); returns this lane's old value plus v x its rank among
+// those lanes.  Every lane of the warp calls it; lanes with `valid` false add nothing.
+__device__ __forceinline__ int warp_aggregated_add(int* counters, int key, int v, bool valid) {
+  const int lane = threadIdx.x & 31;
+  const unsigned peers = __match_any_sync(0xffffffffu, valid ? key : -1);
+  const int leader = __ffs(peers) - 1;
+  int old = 0;
+  if (valid && lane == leader) old = atomicAdd(&counters[key], v * __popc(peers));
+  old = __shfl_sync(0xffffffffu, old, leader);
+  return old + v * __popc(peers & ((1u << lane) - 1u));
+}
+
 // One thread per (question, unit), longest first by cost bins; `base` (shared, n + 1 ints)
 // holds the questions' first unit indices.
 __device__ void emit_units(const SegmentsArgs& a, PrefillHeader* hdr, int4* out, int* bin_count, int* bin_cursor,
@@ -147,13 +161,18 @@ __device__ void emit_units(const SegmentsArgs& a, PrefillHeader* hdr, int4* out,
     }
     return lo;
   };
-  // a unit's cost is its key-tile count (tile B's, the larger)
-  for (int u = tid; u < total; u += blockDim.x) {
-    const int i = question_of(u);
-    int4 w1;
-    int na, nb;
-    UnitShape(n_tiles(i), a.group).unit(u - base[i], w1, na, nb);
-    atomicAdd(&bin_count[min(max(na, nb) - 1, kCostBins - 1)], h_kv);
+  // a unit's cost is its key-tile count (tile B's, the larger); the loops run in whole warps
+  for (int u0 = 0; u0 < total; u0 += blockDim.x) {
+    const int u = u0 + tid;
+    int bin = 0;
+    if (u < total) {
+      const int i = question_of(u);
+      int4 w1;
+      int na, nb;
+      UnitShape(n_tiles(i), a.group).unit(u - base[i], w1, na, nb);
+      bin = min(max(na, nb) - 1, kCostBins - 1);
+    }
+    warp_aggregated_add(bin_count, bin, h_kv, u < total);
   }
   __syncthreads();
   __shared__ int s_total;
@@ -172,16 +191,21 @@ __device__ void emit_units(const SegmentsArgs& a, PrefillHeader* hdr, int4* out,
     if (tid == 31) s_total = x;
   }
   __syncthreads();
-  for (int u = tid; u < total; u += blockDim.x) {
-    const int i = question_of(u);
-    int4 w1;
-    int na, nb;
-    UnitShape(n_tiles(i), a.group).unit(u - base[i], w1, na, nb);
-    const int pos = atomicAdd(&bin_cursor[min(max(na, nb) - 1, kCostBins - 1)], h_kv);
-    for (int g = 0; g < h_kv; ++g) {  // the kv heads of one unit stay adjacent (same query rows)
-      out[2 * (pos + g)] = make_int4(i, g, na | (nb << 16), 0);
-      out[2 * (pos + g) + 1] = w1;
+  for (int u0 = 0; u0 < total; u0 += blockDim.x) {
+    const int u = u0 + tid;
+    int i = 0, na = 0, nb = 0, bin = 0;
+    int4 w1 = make_int4(0, 0, 0, 0);
+    if (u < total) {
+      i = question_of(u);
+      UnitShape(n_tiles(i), a.group).unit(u - base[i], w1, na, nb);
+      bin = min(max(na, nb) - 1, kCostBins - 1);
     }
+    const int pos = warp_aggregated_add(bin_cursor, bin, h_kv, u < total);
+    if (u < total)
+      for (int g = 0; g < h_kv; ++g) {  // the kv heads of one unit stay adjacent (same query rows)
+        out[2 * (pos + g)] = make_int4(i, g, na | (nb << 16), 0);
+        out[2 * (pos + g) + 1] = w1;
+      }
   }
   __syncthreads();
   if (tid == 0) {
