@@ -272,35 +272,89 @@ __global__ void __launch_bounds__(kThreads) segments_kernel(SegmentsArgs a) {
   __syncthreads();
 
   if (small) {
-    // 2-4 for a small batch: every non-empty interval against every other one (overlap, and a
-    // slot shared by two non-empty questions), and its rank by (begin, index) places it in
-    // `keys`, begin-sorted; empty intervals sort last
+    // 2-4 for a small batch.  Fast path, the usual layout: the intervals come in index order,
+    // each ending at or before the next one begins -- no overlap, the ranks are the index order
+    // of the non-empty ones, and a shared-memory hash finds a slot two non-empty questions share.
     const bool ranges_ok = (s_flags & 1) == 0;
-    for (int i = tid; i < n; i += blockDim.x) {
-      const int2 me = s_iv[i];
-      if (me.y <= me.x) continue;
-      int rank = 0;
-      bool overlap = false, dup = false;
-      for (int j = 0; j < n; ++j) {
-        const int2 o = s_iv[j];
-        if (j == i || o.y <= o.x) continue;
-        overlap |= (me.x < o.y) && (o.x < me.y);
-        dup |= a.slot_ids != nullptr && s_slot[j] == s_slot[i];
-        rank += (o.x < me.x) || (o.x == me.x && j < i);
-      }
-      if (overlap) atomicOr(&s_flags, 1);
-      if (dup) atomicOr(&s_flags, 8);
-      if (ranges_ok) keys[rank] = ((unsigned long long)(unsigned)me.x << 32) | (unsigned)me.y;
+    __shared__ int s_unordered;
+    if (tid == 0) s_unordered = 0;
+    __syncthreads();
+    for (int i = tid; i + 1 < n; i += blockDim.x) {
+      const int2 me = s_iv[i], nx = s_iv[i + 1];
+      if (!(me.x <= nx.x && me.y <= nx.x)) s_unordered = 1;
     }
     __syncthreads();
-    // the ranks of the non-empty intervals fill keys[0, n_ne); the rest marks the end
-    if (ranges_ok) {
-      int ne = 0;
-      for (int i = tid; i < n; i += blockDim.x) ne += s_iv[i].y > s_iv[i].x;
-      int n_ne;
-      block_exclusive_scan(ne, scan_tmp, &n_ne);
-      for (int i = n_ne + tid; i < n2; i += blockDim.x) keys[i] = ~0ull;
+    if (!s_unordered) {
+      if (a.slot_ids) {
+        int* hash = reinterpret_cast<int*>(keys);  // free until the ranks are written
+        int hs = 1;
+        while (hs < 2 * n) hs <<= 1;
+        for (int j = tid; j < hs; j += blockDim.x) hash[j] = -1;
+        __syncthreads();
+        for (int i = tid; i < n; i += blockDim.x) {
+          if (s_iv[i].y <= s_iv[i].x) continue;
+          const int slot = s_slot[i];
+          unsigned h = ((unsigned)slot * 2654435761u) & (unsigned)(hs - 1);
+          for (int probe = 0; probe < hs; ++probe) {
+            const int prev = atomicCAS(&hash[h], -1, slot);
+            if (prev == -1) break;
+            if (prev == slot) {
+              atomicOr(&s_flags, 8);
+              break;
+            }
+            h = (h + 1) & (unsigned)(hs - 1);
+          }
+        }
+        __syncthreads();
+      }
+      if (ranges_ok) {
+        int running = 0;
+        for (int base = 0; base < n; base += blockDim.x) {
+          const int i = base + tid;
+          const bool ne = i < n && s_iv[i].y > s_iv[i].x;
+          int blk;
+          const int off = block_exclusive_scan(ne ? 1 : 0, scan_tmp, &blk);
+          if (ne) keys[running + off] = ((unsigned long long)(unsigned)s_iv[i].x << 32) | (unsigned)s_iv[i].y;
+          running += blk;
+        }
+        for (int i = running + tid; i < n2; i += blockDim.x) keys[i] = ~0ull;
+        __syncthreads();
+      }
+    } else {
+      // every non-empty interval against every other one (overlap, and a slot shared by two
+      // non-empty questions), and its rank by (begin, index) places it in `keys`, begin-sorted;
+      // empty intervals sort last
+      const bool has_slots = a.slot_ids != nullptr;
+      for (int i = tid; i < n; i += blockDim.x) {
+        const int2 me = s_iv[i];
+        if (me.y <= me.x) continue;
+        const int my_slot = s_slot[i];
+        int rank = 0;
+        bool overlap = false, dup = false;
+        // branch-free and unrolled: the shared-memory loads of several j are in flight at once
+#pragma unroll 8
+        for (int j = 0; j < n; ++j) {
+          const int2 o = s_iv[j];
+          const int so = s_slot[j];
+          const bool other = j != i && o.y > o.x;
+          overlap |= other & (me.x < o.y) & (o.x < me.y);
+          dup |= other & has_slots & (so == my_slot);
+          rank += other & ((o.x < me.x) | ((o.x == me.x) & (j < i)));
+        }
+        if (overlap) atomicOr(&s_flags, 1);
+        if (dup) atomicOr(&s_flags, 8);
+        if (ranges_ok) keys[rank] = ((unsigned long long)(unsigned)me.x << 32) | (unsigned)me.y;
+      }
       __syncthreads();
+      // the ranks of the non-empty intervals fill keys[0, n_ne); the rest marks the end
+      if (ranges_ok) {
+        int ne = 0;
+        for (int i = tid; i < n; i += blockDim.x) ne += s_iv[i].y > s_iv[i].x;
+        int n_ne;
+        block_exclusive_scan(ne, scan_tmp, &n_ne);
+        for (int i = n_ne + tid; i < n2; i += blockDim.x) keys[i] = ~0ull;
+        __syncthreads();
+      }
     }
   } else {
     // 2. overlap: sort non-empty intervals by begin, neighbours must not intersect

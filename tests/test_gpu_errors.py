@@ -24,6 +24,8 @@ PREFILL_BAD = [
     ([[0, 20], [20, 40]], [1, 2], 16),     # longer than the slot
     ([[0, 20], [20, 20]], [1, 1], 64),     # empty question may share a slot: valid
     ([[0, 16], [16, 40]], [2, 0], 24),     # exactly cap: valid
+    ([[20, 40], [0, 20]], [0, 1], 64),     # not in index order: valid
+    ([[24, 40], [0, 20]], [2, 2], 64),     # not in index order, shared slot
 ]
 
 
