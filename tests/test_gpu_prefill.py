@@ -118,6 +118,50 @@ def test_qwen3_8b_config_sampled_rows_and_pools():
     _check_pools(run, w)
 
 
+def test_qwen3_8b_config_every_row_against_oracle():
+    """Every output row of the Qwen3-8B-shaped batch (T = 24,100, questions up to 4096 tokens)
+    against the oracle, one (question, kv group) per job in spawned worker processes."""
+    import multiprocessing as mp
+    import os
+    import prefill_oracle
+    from kev_harness import TOL_BF16_MAX, TOL_BF16_REL_L2
+    w = W.qwen3_8b_prefill()
+    run = PrefillRun(w)
+    run.run()
+    assert run.device_status() == 0
+    out = host(run.out)
+    G = w.h_q // w.h_kv
+    jobs = []
+    for i, (s, e) in enumerate(w.intervals):
+        s, e = int(s), int(e)
+        for g in range(w.h_kv):
+            jobs.append({"i": i, "g": g, "L": e - s, "q": w.q[s:e, g * G:(g + 1) * G], "k": w.k[s:e, g:g + 1],
+                         "v": w.v[s:e, g:g + 1], "gpu_out": out[s:e, g * G:(g + 1) * G]})
+    jobs.sort(key=lambda j: -j["L"])  # the longest start first
+    ctx = mp.get_context("spawn")  # this process already holds a CUDA context
+    saved = {k: os.environ.get(k) for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS")}
+    for k in saved:
+        os.environ[k] = "1"
+    try:
+        with ctx.Pool(max(1, min(32, os.cpu_count() or 1))) as pool:
+            res = pool.map(prefill_oracle.check_group, jobs, chunksize=1)
+    finally:
+        for k, v in saved.items():
+            if v is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = v
+    per_q = {}
+    for r in res:
+        assert r["finite"], f"question {r['i']} group {r['g']}: non-finite output"
+        a = per_q.setdefault(r["i"], [0.0, 0.0, 0.0])
+        a[0], a[1], a[2] = max(a[0], r["max"]), a[1] + r["d2"], a[2] + r["r2"]
+    assert len(per_q) == w.n_questions
+    for i, (mx, d2, r2) in per_q.items():
+        rel = (d2 / r2) ** 0.5 if r2 > 0 else 0.0
+        assert mx <= TOL_BF16_MAX and rel <= TOL_BF16_REL_L2, f"question {i}: max|d| {mx:.3e}, rel L2 {rel:.3e}"
+
+
 def test_deterministic_and_isolated_bitwise():
     """Same call twice gives identical bits; a question's rows do not depend on its neighbours
     or on where it sits in the packed sequence (segment-local tiling)."""
