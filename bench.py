@@ -314,10 +314,19 @@ def _stress_decode_graph(kev, torch, dev, tdev, tf_peak, hbm_peak):
     total_bytes = sum(RL.decode_bytes(s.lens_at(t), s.active_at(t), w.h_q, w.h_kv, w.d, 2) for t in range(steps))
     ms = statistics.mean(reps)
     useful = RL.prefill_useful_flops(w.lengths, w.h_q, w.d)
+    # short questions make this prefill memory-bound: its intensity (useful FLOP per algorithmic
+    # byte: q, k, v read, out and both slot rows written) is below the ridge point peak / bandwidth
+    pre_bytes = RL.prefill_bytes(w.total_tokens, w.h_q, w.h_kv, w.d, 2)
+    intensity = RL.arithmetic_intensity(useful, pre_bytes)
+    ridge = tf_peak * 1e12 / (hbm_peak * 1e9)
     return {"workload": "stress: 256 questions (T=19483), H_q 32, H_kv 8, d 128, bf16, cap 4224; prefill with slot "
                         "write, then 128 decode steps with early stop (116 with live questions)",
             "prefill_tflops": useful / (pre_avg * 1e-3) / 1e12, "prefill_ms": pre_avg,
             "prefill_frac": useful / (pre_avg * 1e-3) / 1e12 / tf_peak,
+            "prefill_bytes": pre_bytes, "prefill_gbs": pre_bytes / (pre_avg * 1e-3) / 1e9,
+            "prefill_intensity_flop_per_byte": intensity, "ridge_flop_per_byte": ridge,
+            "prefill_bound": "hbm" if intensity < ridge else "tensor",
+            "prefill_bound_frac": (RL.ideal_time(useful, pre_bytes, tf_peak * 1e12, hbm_peak * 1e9) * 1e3) / pre_avg,
             "decode_graph_ms": ms, "decode_steps": steps, "decode_bytes": total_bytes,
             "decode_gbs": total_bytes / (ms * 1e-3) / 1e9, "decode_frac": total_bytes / (ms * 1e-3) / 1e9 / hbm_peak,
             "launches_per_step": kev.kev_launch_count(15),

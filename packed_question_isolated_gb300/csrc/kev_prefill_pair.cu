@@ -489,6 +489,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const int nkv = x.nkv_t[t];
       if (nkv == 0) continue;  // tile t absent from this unit: no MMA, nothing to wait for
       const Half h = t ? hb : ha;
+      // rows of this warp all past the question's end (its last query tile): nothing of them is
+      // stored, so their weights are neither computed nor written (their O rows stay garbage)
+      const bool dead = h.rows <= quarter * 32;
       float m_run = -INFINITY, l_run = 0.f;
 
       for (int j = 0; j < nkv; ++j) {
@@ -510,12 +513,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           arrive_leader(cl_p_full);
           continue;
         }
+        if (dead) {
+          tc_fence_before();
+          arrive_leader(cl_p_full);
+          continue;
+        }
+        // On the diagonal tile key k is visible to row r iff k <= r, so the 32-key chunks past
+        // this warp's own (c > quarter) are masked for all its rows: not loaded, their weights
+        // written as zeros without an exponential (the sums and the max are unchanged: those
+        // entries only ever contributed exact zeros and -inf).
+        const int cmax = (j == h.nkv - 1) ? quarter : 3;
         uint32_t sr[4][32];
 #pragma unroll
         for (int c = 0; c < 4; ++c) tmem_ld32(tm_s + c * 32, sr[c]);
 #pragma unroll
         for (int c = 0; c < 4; ++c) tmem_ld_wait(sr[c]);
-        if (j == h.nkv - 1) {  // this half's diagonal tile: key k is visible to row r iff k <= r
+        if (j == h.nkv - 1) {
 #pragma unroll
           for (int c = 0; c < 4; ++c)
 #pragma unroll
@@ -544,6 +557,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
             uint32_t pk[16];
+            if (c > cmax) {
+#pragma unroll
+              for (int e = 0; e < 16; ++e) pk[e] = 0u;
+              tmem_st16(tm_s + c * 16, pk);
+              continue;
+            }
 #pragma unroll
             for (int e = 0; e < 16; ++e) {
               const unsigned long long sv =
