@@ -162,11 +162,13 @@ __global__ void __launch_bounds__(kSampleThreads) sample_kernel(SampleArgs a, in
   // the segment size)
   const int per = ((seg + kSampleThreads - 1) / kSampleThreads + 7) / 8 * 8;
   const int k_lo = min(q_hi, q_lo + tid * per), k_hi = min(q_hi, k_lo + per);
-  // the range's first 32 logits (four vector loads) go out before the checks: reads inside the
-  // row, used only when the call is valid and the question live
-  float f0[32];
+  // the range's first kFirst logits (five vector loads: the whole range of a 151,936-token
+  // vocabulary over 8 CTAs) go out before the checks: reads inside the row, used only when the
+  // call is valid and the question live; longer ranges continue 32 at a time
+  constexpr int kFirst = 40;
+  float f0[kFirst];
 #pragma unroll
-  for (int v = 0; v < 4; ++v) load8<E>(row, k_lo + 8 * v, k_hi, f0 + 8 * v);
+  for (int v = 0; v < kFirst / 8; ++v) load8<E>(row, k_lo + 8 * v, k_hi, f0 + 8 * v);
   bool bad = false;
   for (int j = tid; j < a.n; j += blockDim.x) {
     if (!a.active[j]) continue;
@@ -184,16 +186,17 @@ __global__ void __launch_bounds__(kSampleThreads) sample_kernel(SampleArgs a, in
   if (T == 0.f) {  // greedy: the first maximum
     float best = -INFINITY;
     int bi = V;
-    auto scan = [&](const float (&f)[32], int k0) {
+    auto scan = [&](const auto& f, int k0) {
+      constexpr int N = sizeof(f) / sizeof(float);
 #pragma unroll
-      for (int e = 0; e < 32; ++e)
+      for (int e = 0; e < N; ++e)
         if (f[e] > best) {  // k increases per thread: the first maximum of this thread
           best = f[e];
           bi = k0 + e;
         }
     };
     scan(f0, k_lo);
-    for (int k0 = k_lo + 32; k0 < k_hi; k0 += 32) {
+    for (int k0 = k_lo + kFirst; k0 < k_hi; k0 += 32) {
       float f[32];
 #pragma unroll
       for (int v = 0; v < 4; ++v) load8<E>(row, k0 + 8 * v, k_hi, f + 8 * v);
@@ -245,10 +248,11 @@ __global__ void __launch_bounds__(kSampleThreads) sample_kernel(SampleArgs a, in
   const float inv_t = 1.0f / T;
   // max and sum of exp(z - max) over the range, 32 logits at a time
   float m = -INFINITY, s = 0.f;
-  auto accumulate = [&](float (&f)[32]) {
+  auto accumulate = [&](auto& f) {
+    constexpr int N = sizeof(f) / sizeof(float);
     float bm = -INFINITY;
 #pragma unroll
-    for (int e = 0; e < 32; ++e) {
+    for (int e = 0; e < N; ++e) {
       f[e] *= inv_t;
       bm = fmaxf(bm, f[e]);
     }
@@ -258,11 +262,11 @@ __global__ void __launch_bounds__(kSampleThreads) sample_kernel(SampleArgs a, in
     }
     float add = 0.f;
 #pragma unroll
-    for (int e = 0; e < 32; ++e) add += expf(f[e] - m);  // exp(-inf) = 0 past the range
+    for (int e = 0; e < N; ++e) add += expf(f[e] - m);  // exp(-inf) = 0 past the range
     s += add;
   };
   accumulate(f0);
-  for (int k0 = k_lo + 32; k0 < k_hi; k0 += 32) {
+  for (int k0 = k_lo + kFirst; k0 < k_hi; k0 += 32) {
     float f[32];
 #pragma unroll
     for (int v = 0; v < 4; ++v) load8<E>(row, k0 + 8 * v, k_hi, f + 8 * v);  // four loads in flight
