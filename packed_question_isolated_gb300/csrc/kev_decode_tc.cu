@@ -28,6 +28,8 @@
 #include <cuda.h>
 #include <stdlib.h>
 
+#include <climits>
+
 #include "kev_decode_common.cuh"
 #include "kev_internal.cuh"
 #include "kev_sm100.cuh"
@@ -42,7 +44,12 @@ constexpr int kD = 128;
 constexpr int kN = 16;             // MMA N: q-heads of one group, padded to 16
 constexpr int kC = dec::kChunk;    // 128 keys per chunk
 constexpr int kBatch = 4;          // most consecutive chunks per dynamic grab
-constexpr int kTailPerCta = 0;     // single-chunk grabs at the end, per CTA of the grid (measured: none is best)
+// A call of at most kSmallPerCta chunks per CTA hands out its last kTailPerCta chunks per CTA in
+// grabs of kTailBatch chunks (measured: the 128-step decode of 256 short questions 2.12 -> 1.96 ms;
+// on the 32-question Qwen3-8B decode, ~18 chunks per CTA, any such tail was slower)
+constexpr int kSmallPerCta = 8;
+constexpr int kTailPerCta = 4;
+constexpr int kTailBatch = 2;
 constexpr int kThreads = 384;
 constexpr int kQuad = 128;         // threads of the softmax (warps 2-5) and of the epilogue (warps 7-10)
 constexpr long long kDrainBudget = 4000000000ll;
@@ -176,21 +183,23 @@ __device__ __forceinline__ bool reduce_writer(int lane) {
 }
 
 // The fixed plan of the dynamic grabs: batches of B = kBatch consecutive chunks over [0, x1),
-// then one batch per chunk over [x1, total).  Batch boundaries depend on the chunk index only (not on which CTA grabs what), so
+// then batches of kTailBatch chunks over [x1, total) (on a small call the last kTailPerCta chunks
+// per CTA, else what is left of the B-chunk batches).  Batch boundaries depend on the chunk index only (not on which CTA grabs what), so
 // the pieces, and hence the results, are the same on every run.
 struct BatchPlan {
-  int B, n1, x1, nbat;
-  __device__ int start(int b) const { return b < n1 ? b * B : x1 + (b - n1); }
-  __device__ int end(int b) const { return b < n1 ? (b + 1) * B : x1 + (b - n1) + 1; }
-  __device__ int of(int x) const { return x < x1 ? x / B : n1 + (x - x1); }
+  int B, n1, x1, nbat, total;
+  __device__ int start(int b) const { return b < n1 ? b * B : x1 + (b - n1) * kTailBatch; }
+  __device__ int end(int b) const { return b < n1 ? (b + 1) * B : min(x1 + (b - n1 + 1) * kTailBatch, total); }
+  __device__ int of(int x) const { return x < x1 ? x / B : n1 + (x - x1) / kTailBatch; }
 };
 __device__ __forceinline__ BatchPlan make_plan(int total, int ctas) {
-  const int tail = kTailPerCta * ctas;
+  const int tail = total <= kSmallPerCta * ctas ? kTailPerCta * ctas : 0;
   BatchPlan p;
   p.B = kBatch;  // measured: fixed 4-chunk batches beat a per-call size on small and large decodes
   p.n1 = total > tail ? (total - tail) / p.B : 0;
   p.x1 = p.n1 * p.B;
-  p.nbat = p.n1 + (total - p.x1);
+  p.nbat = p.n1 + (total - p.x1 + kTailBatch - 1) / kTailBatch;
+  p.total = total;
   return p;
 }
 
@@ -726,6 +735,7 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeArgs a) {
   plan.x1 = sched[1];
   plan.n1 = sched[3];
   plan.B = sched[4];
+  plan.total = INT_MAX;  // not needed here (only start and of are)
   const int pair = blockIdx.x + r * gridDim.x;  // the grid covers every pair and every question
   const int live = pair < n_pairs ? a.active[pair / a.h_kv] : 0;
   const int2 xc = pair < n_pairs ? item_xi0[pair] : make_int2(-1, 0);  // written for every live pair
