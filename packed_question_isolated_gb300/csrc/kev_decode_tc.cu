@@ -45,7 +45,7 @@ constexpr int kN = 16;             // MMA N: q-heads of one group, padded to 16
 constexpr int kC = dec::kChunk;    // 128 keys per chunk
 constexpr int kBatch = 4;          // most consecutive chunks per dynamic grab
 // A call of at most kSmallPerCta chunks per CTA hands out its last kTailPerCta chunks per CTA in
-// grabs of kTailBatch chunks (measured: the 128-step decode of 256 short questions 2.12 -> 1.96 ms;
+// grabs of kTailBatch chunks (measured: the 128-step decode of 256 short questions 2.12 -> 1.99 ms;
 // on the 32-question Qwen3-8B decode, ~18 chunks per CTA, any such tail was slower)
 constexpr int kSmallPerCta = 8;
 constexpr int kTailPerCta = 4;
@@ -184,8 +184,9 @@ __device__ __forceinline__ bool reduce_writer(int lane) {
 
 // The fixed plan of the dynamic grabs: batches of B = kBatch consecutive chunks over [0, x1),
 // then batches of kTailBatch chunks over [x1, total) (on a small call the last kTailPerCta chunks
-// per CTA, else what is left of the B-chunk batches).  Batch boundaries depend on the chunk index only (not on which CTA grabs what), so
-// the pieces, and hence the results, are the same on every run.
+// per CTA, else what is left of the B-chunk batches).  Batch boundaries depend on the chunk index
+// only (not on which CTA grabs what), so the pieces, and hence the results, are the same on every
+// run.
 struct BatchPlan {
   int B, n1, x1, nbat, total;
   __device__ int start(int b) const { return b < n1 ? b * B : x1 + (b - n1) * kTailBatch; }
